@@ -1,0 +1,434 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each oracle function is checked here against what the pages and mathematics
+fix: hand-worked examples, closed forms, brute force on tiny inputs, library
+routines (numpy integer matmul, numpy binary32 arithmetic, torch's bf16
+rounding), invariants, error bounds, and the pages' candidate-softmax identity
+("把决策模型推理从 vLLM 换到 Prism", sections 方案 and 实现要点).  No GPU.
+"""
+import json
+import math
+import os
+from fractions import Fraction as Fr
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers --
+def rn32(v) -> float:
+    """Round an exact rational to binary32, nearest-even (normal range and
+    zero only; independent of any float unit)."""
+    v = Fr(v)
+    if v == 0:
+        return 0.0
+    s = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fr(2) ** e > a:
+        e -= 1
+    while Fr(2) ** (e + 1) <= a:
+        e += 1
+    assert e >= -126, "helper covers normal numbers only"
+    ulp = Fr(2) ** (e - 23)
+    m = a / ulp
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    if rem > Fr(1, 2) or (rem == Fr(1, 2) and fl % 2 == 1):
+        fl += 1
+    return s * float(fl * ulp)
+
+
+def rnbf16_bits(v) -> int:
+    """Round an exact rational to bf16 (8 significant bits), nearest-even."""
+    v = Fr(v)
+    if v == 0:
+        return 0
+    s = 0x8000 if v < 0 else 0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fr(2) ** e > a:
+        e -= 1
+    while Fr(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fr(2) ** (e - 7)
+    m = a / ulp
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    if rem > Fr(1, 2) or (rem == Fr(1, 2) and fl % 2 == 1):
+        fl += 1
+    val = float(fl * ulp)
+    return s | int(np.float32(val).view(np.uint32) >> 16)
+
+
+def f32_bits(x) -> int:
+    return int(np.float32(x).view(np.uint32))
+
+
+def bits(x_f32: np.ndarray) -> np.ndarray:
+    return wl.bf16_bits(np.asarray(x_f32, np.float32))
+
+
+# ------------------------------------------------------------ quantiser ----
+def test_quant_hand_worked_examples():
+    cases = json.load(open(os.path.join(GOLDEN, "quant_examples.json")))["cases"]
+    for c in cases:
+        x = np.array([c["x"]], np.float32)
+        assert np.array_equal(wl.bits_to_f32(bits(x)), x), "example must be bf16-exact"
+        inv_s = None if c["inv_s"] is None else np.array(c["inv_s"], np.float32)
+        q, a = oracle.quant_act(bits(x), inv_s)
+        assert q[0].tolist() == c["q"], c["name"]
+        assert f32_bits(a[0]) == int(c["a_scale_bits"], 16), c["name"]
+
+
+def test_quant_scale_closed_form():
+    # a_scale = RN(amax / 127) on exact rationals, for a spread of amax values
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((64, 96)).astype(np.float32)
+         * np.exp2(rng.integers(-20, 20, size=(64, 1))).astype(np.float32))
+    xb = bits(x)
+    q, a = oracle.quant_act(xb, None)
+    xf = wl.bits_to_f32(xb)
+    for m in range(64):
+        amax = float(np.abs(xf[m]).max())
+        assert a[m] == np.float32(rn32(Fr(amax) / 127))
+        inv_a = rn32(Fr(127) / Fr(amax))
+        # every code by exact rationals: rint(RN(xs * inv_a)), ties to even
+        for k in range(0, 96, 7):
+            t = rn32(Fr(float(xf[m, k])) * Fr(inv_a))
+            assert q[m, k] == max(-127, min(127, round(t)))  # Python round: ties to even
+
+
+def test_quant_invariants_and_error_bound():
+    case = wl.make_linear("tiny_m37_k256_n384")
+    q, a = oracle.quant_act(case.x_bits, case.inv_s)
+    xs = wl.bits_to_f32(case.x_bits).astype(np.float64) * case.inv_s.astype(np.float64)
+    assert np.abs(q.astype(np.int32)).max() <= 127
+    for m in range(case.M):
+        amax = np.abs(xs[m]).max()
+        j = int(np.argmax(np.abs(xs[m])))
+        assert abs(int(q[m, j])) == 127
+        assert np.all(np.sign(q[m]) * np.sign(xs[m]) >= 0)
+        # dequantisation error: at most half a step, plus the fp32 roundings
+        step = amax / 127.0
+        err = np.abs(q[m].astype(np.float64) * step - xs[m])
+        assert err.max() <= 0.5 * step * (1 + 1e-5) + 1e-6 * amax
+
+
+def test_quant_power_of_two_equivariance_and_unit_smoothing():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((9, 128)).astype(np.float32)
+    q0, a0 = oracle.quant_act(bits(x), None)
+    q1, a1 = oracle.quant_act(bits(x * np.float32(2.0 ** 9)), None)
+    assert np.array_equal(q0, q1)
+    assert np.array_equal(a1, a0 * np.float32(2.0 ** 9))
+    q2, a2 = oracle.quant_act(bits(x), np.ones(128, np.float32))
+    assert np.array_equal(q0, q2) and np.array_equal(a0, a2)
+    # smoothing by 2^-k on input scaled by 2^k is the identity
+    s = np.exp2(rng.integers(-6, 7, size=128)).astype(np.float32)
+    q3, a3 = oracle.quant_act(bits(x * s), (1.0 / s).astype(np.float32))
+    assert np.array_equal(q0, q3) and np.array_equal(a0, a3)
+
+
+def test_quant_tiny_rows_are_zero():
+    x = np.zeros((2, 32), np.float32)
+    x[1, 5] = np.float32(2.0 ** -125)    # amax below 2^-120: treated as zero
+    q, a = oracle.quant_act(bits(x), None)
+    assert not q.any() and not a.any()
+
+
+def test_quant_matches_library_binary32_arithmetic():
+    # numpy's float32 ufuncs are single IEEE RN operations; np.rint ties to even
+    case = wl.make_linear("tiny_m37_k256_n384")
+    xf = wl.bits_to_f32(case.x_bits)
+    xs = xf * case.inv_s
+    amax = np.abs(xs).max(axis=1)
+    inv_a = np.float32(127.0) / amax
+    qn = np.clip(np.rint(xs * inv_a[:, None]), -127, 127).astype(np.int8)
+    q, a = oracle.quant_act(case.x_bits, case.inv_s)
+    assert np.array_equal(q, qn)
+    assert np.array_equal(a, amax / np.float32(127.0))
+
+
+# ------------------------------------------------------- contraction -------
+def test_gemm_brute_force_tiny():
+    rng = np.random.default_rng(5)
+    for M, N, K in [(1, 1, 1), (2, 3, 16), (5, 4, 64), (3, 5, 33)]:
+        q = rng.integers(-127, 128, size=(M, K), dtype=np.int8)
+        w = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+        acc = oracle.gemm_s32(q, w)
+        for m in range(M):
+            for n in range(N):
+                assert acc[m, n] == sum(int(q[m, k]) * int(w[n, k]) for k in range(K))
+
+
+def test_gemm_sign_patterns_and_extremes():
+    # every sign pattern of 4 extreme terms, plus mixed magnitudes
+    K = 4
+    pats = np.array([[127 if (p >> i) & 1 else -127 for i in range(K)] for p in range(16)], np.int8)
+    acc = oracle.gemm_s32(pats, pats)
+    for i in range(16):
+        for j in range(16):
+            assert acc[i, j] == sum(int(pats[i, k]) * int(pats[j, k]) for k in range(K))
+
+
+def test_gemm_matches_numpy_int64():
+    case = wl.make_linear("tiny_m37_k256_n384")
+    q, _ = oracle.quant_act(case.x_bits, case.inv_s)
+    ref = q.astype(np.int64) @ case.w.astype(np.int64).T
+    assert np.array_equal(oracle.gemm_s32(q, case.w), ref)
+    rng = np.random.default_rng(1)
+    w = wl.draw_weights(rng, (96, 5120), "normal")
+    q2 = rng.integers(-127, 128, size=(12, 5120), dtype=np.int8)
+    assert np.array_equal(oracle.gemm_s32(q2, w), q2.astype(np.int64) @ w.astype(np.int64).T)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 7, 16, 64])
+def test_gemm_split_k_invariant(S):
+    rng = np.random.default_rng(S)
+    q = rng.integers(-127, 128, size=(7, 1040), dtype=np.int8)
+    w = rng.integers(-127, 128, size=(9, 1040), dtype=np.int8)
+    assert np.array_equal(oracle.gemm_s32_splitk(q, w, S), oracle.gemm_s32(q, w))
+
+
+def test_gemm_int32_range_closed_form():
+    K = 133136   # largest multiple of 16 with K * 127^2 < 2^31
+    assert K <= oracle.max_k() == 133144
+    q = np.full((2, K), 127, np.int8)
+    q[1] = -127
+    w = np.full((1, K), 127, np.int8)
+    acc = oracle.gemm_s32(q, w)
+    assert acc[0, 0] == K * 16129 and acc[1, 0] == -K * 16129
+    with pytest.raises(OverflowError):
+        oracle.gemm_s32(np.full((1, 133145), 127, np.int8), np.full((1, 133145), 127, np.int8))
+
+
+# ------------------------------------------------------------- epilogue ----
+def _ep(acc, a, w, r=None):
+    acc = np.array([[acc]], np.int32)
+    rb = None if r is None else np.array([[r]], np.uint16)
+    return int(oracle.epilogue(acc, np.array([a], np.float32), np.array([w], np.float32), rb)[0, 0])
+
+
+def test_epilogue_small_integers_exact():
+    accs = np.arange(-256, 257, dtype=np.int32).reshape(1, -1)
+    out = oracle.epilogue(accs, np.ones(1, np.float32), np.ones(513, np.float32), None)
+    assert np.array_equal(wl.bits_to_f32(out), accs.astype(np.float32))
+
+
+def test_epilogue_zero_acc_returns_residual():
+    rng = np.random.default_rng(2)
+    r = bits(rng.standard_normal((3, 50)).astype(np.float32))
+    out = oracle.epilogue(np.zeros((3, 50), np.int32), np.full(3, 0.01, np.float32),
+                          np.full(50, 0.003, np.float32), r)
+    assert np.array_equal(out, r)
+
+
+def test_epilogue_int_to_float_and_bf16_ties():
+    # int32 -> binary32 is round-to-nearest-even
+    assert _ep(16777217, 1.0, 1.0) == rnbf16_bits(16777216)
+    assert _ep(16777219, 1.0, 1.0) == rnbf16_bits(16777220)
+    # bf16 ties to even: 257/256 lies halfway between 1 and 1 + 2^-7
+    assert _ep(257, 2.0 ** -8, 1.0) == 0x3F80
+    assert _ep(259, 2.0 ** -8, 1.0) == 0x3F82
+    assert _ep(-259, 2.0 ** -8, 1.0) == 0xBF82
+
+
+def test_epilogue_power_of_two_scales_closed_form():
+    rng = np.random.default_rng(9)
+    for acc in rng.integers(-2 ** 28, 2 ** 28, size=200):
+        got = _ep(int(acc), 2.0 ** -7, 2.0 ** -11)
+        assert got == rnbf16_bits(Fr(rn32(int(acc))) / 2 ** 18)
+
+
+def test_epilogue_rounding_order_reading():
+    # Reading: ((acc * a_scale) * w_scale) + residual, each step one binary32
+    # RN operation, no FMA.  The final bf16 rounding hides most binary32
+    # differences, so search (vectorised, numpy binary32) for inputs where the
+    # other orders land on other bf16 values, then check the oracle against
+    # exact-rational evaluation of the stated order on those inputs.
+    rng = np.random.default_rng(4)
+    n = 2_000_000
+    acc = rng.integers(-2 ** 24, 2 ** 24, size=n).astype(np.int32)
+    a = rng.uniform(1e-4, 1e-1, n).astype(np.float32)
+    w = rng.uniform(1e-3, 2e-2, n).astype(np.float32)
+    rb = bits((rng.standard_normal(n) * 64).astype(np.float32))
+    r = wl.bits_to_f32(rb)
+    t1 = acc.astype(np.float32) * a
+    want = wl.bf16_bits((t1 * w) + r)
+    alt = wl.bf16_bits((acc.astype(np.float32) * (a * w)) + r)
+    fma = wl.bf16_bits(((t1.astype(np.float64) * w.astype(np.float64)) + r.astype(np.float64)).astype(np.float32))
+    idx_order = np.nonzero(alt != want)[0][:20]
+    idx_fma = np.nonzero(fma != want)[0][:20]
+    assert idx_order.size > 0 and idx_fma.size > 0
+    for i in np.concatenate([idx_order, idx_fma]):
+        A, S, W, R = int(acc[i]), float(a[i]), float(w[i]), float(r[i])
+        e1 = rn32(Fr(rn32(A)) * Fr(S))
+        e2 = rn32(Fr(e1) * Fr(W))
+        expect = rnbf16_bits(Fr(rn32(Fr(e2) + Fr(R))))
+        other_order = rnbf16_bits(Fr(rn32(Fr(rn32(Fr(rn32(A)) * Fr(rn32(Fr(S) * Fr(W))))) + Fr(R))))
+        fused = rnbf16_bits(Fr(rn32(Fr(e1) * Fr(W) + Fr(R))))
+        assert expect != other_order or expect != fused
+        assert _ep(A, S, W, int(rb[i])) == expect
+
+
+def test_epilogue_matches_library_ops():
+    import torch
+    rng = np.random.default_rng(6)
+    acc = rng.integers(-2 ** 27, 2 ** 27, size=(17, 40)).astype(np.int32)
+    a = rng.uniform(1e-3, 1e-1, 17).astype(np.float32)
+    w = rng.uniform(1e-3, 2e-2, 40).astype(np.float32)
+    r = bits(rng.standard_normal((17, 40)).astype(np.float32))
+    t = ((acc.astype(np.float32) * a[:, None]) * w[None, :]) + wl.bits_to_f32(r)
+    ref = torch.from_numpy(t).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.epilogue(acc, a, w, r), ref)
+    t0 = (acc.astype(np.float32) * a[:, None]) * w[None, :]
+    ref0 = torch.from_numpy(t0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.epilogue(acc, a, w, None), ref0)
+
+
+def test_linear_batch_invariance():
+    case = wl.make_linear("tiny_m37_k256_n384")
+    q, a = oracle.quant_act(case.x_bits, case.inv_s)
+    out, acc = oracle.w8a8_linear(q, a, case.w, case.w_scale, case.residual_bits)
+    perm = np.random.default_rng(0).permutation(case.M)
+    qp, ap = oracle.quant_act(case.x_bits[perm], case.inv_s)
+    outp, _ = oracle.w8a8_linear(qp, ap, case.w, case.w_scale, case.residual_bits[perm])
+    assert np.array_equal(outp, out[perm])
+    for m in (0, 17, 36):
+        q1, a1 = oracle.quant_act(case.x_bits[m:m + 1], case.inv_s)
+        o1, _ = oracle.w8a8_linear(q1, a1, case.w, case.w_scale, case.residual_bits[m:m + 1])
+        assert np.array_equal(o1[0], out[m])
+
+
+# ------------------------------------------------------------------ exp ----
+def test_exp_exact_points_and_underflow():
+    assert oracle.exp(np.array([0.0], np.float32))[0] == np.float32(1.0)
+    y = oracle.exp(np.array([-88.0, -100.0, -1e30], np.float32))
+    assert np.all(y == 0.0)
+
+
+def test_exp_error_bound_two_ulp():
+    xs = np.concatenate([np.linspace(-87.0, 0.0, 400_001, dtype=np.float32),
+                         -np.abs(np.random.default_rng(0).standard_normal(100_000).astype(np.float32)) * 10,
+                         np.float32(-np.logspace(-30, 0, 2000))])
+    y = oracle.exp(xs).astype(np.float64)
+    ref = np.exp(xs.astype(np.float64))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    err = np.abs(y - ref) / ulp
+    assert err.max() <= 2.0, float(err.max())
+
+
+# ------------------------------------------------------------- read-out ----
+def _full_logits(h_bits, inv_s, W, lm_scale):
+    q, a = oracle.quant_act(h_bits, inv_s)
+    acc = oracle.gemm_s32(q, W)
+    return (acc.astype(np.float32) * a[:, None]) * lm_scale[None, :]
+
+
+def test_readout_identity_on_subvocabulary():
+    # The pages' identity: softmax over the candidate logits equals the
+    # full-vocabulary softmax gathered on the candidates and renormalised.
+    case = wl.make_readout("identity_p16_v32000", P=6)
+    W = case.lm_head_full()
+    rc, logits, probs = oracle.candidate_readout(case.h_bits, None, W, case.lm_scale,
+                                                 case.cand_offsets, case.cand_ids)
+    assert rc == 0
+    full = _full_logits(case.h_bits, None, W, case.lm_scale).astype(np.float64)
+    for p in range(case.P):
+        b, e = case.cand_offsets[p], case.cand_offsets[p + 1]
+        ids = case.cand_ids[b:e]
+        z = full[p] - full[p].max()
+        sm = np.exp(z) / np.exp(z).sum()
+        ren = sm[ids] / sm[ids].sum()
+        assert np.array_equal(logits[b:e], full[p, ids].astype(np.float32))
+        d = np.abs(probs[b:e] - ren)
+        # 1e-6 relative to the position's probability vector (its largest entry)
+        assert d.max() <= 1e-6 * ren.max(), (p, probs[b:e], ren)
+        # per element: binary32 error of (logit - max) grows with its magnitude
+        x = (logits[b:e].astype(np.float64) - logits[b:e].max())
+        bound = (np.abs(x) + (e - b) + 4) * 2.0 ** -23 * ren
+        assert np.all(d <= bound + 1e-38), (p, d, bound)
+
+
+def test_readout_single_candidate_and_ties():
+    rng = np.random.default_rng(12)
+    K = 256
+    W = rng.integers(-127, 128, size=(20, K), dtype=np.int8)
+    W[5] = W[3]
+    W[9] = W[3]
+    W[11] = W[3]
+    sc = np.full(20, 0.01, np.float32)
+    h = bits(rng.standard_normal((2, K)).astype(np.float32))
+    off = np.array([0, 1, 5], np.int32)
+    ids = np.array([7, 3, 5, 9, 11], np.int32)
+    rc, logits, probs = oracle.candidate_readout(h, None, W, sc, off, ids)
+    assert rc == 0
+    assert probs[0] == np.float32(1.0)
+    assert np.all(logits[1:] == logits[1]) and np.all(probs[1:] == np.float32(0.25))
+
+
+def test_readout_rejects_bad_candidates():
+    rng = np.random.default_rng(13)
+    K, V = 64, 30
+    W = rng.integers(-127, 128, size=(V, K), dtype=np.int8)
+    sc = np.full(V, 0.01, np.float32)
+    h = bits(rng.standard_normal((4, K)).astype(np.float32))
+    off = np.array([0, 2, 4, 6, 8], np.int32)
+    ids = np.array([1, 2, 3, 3, 4, 30, 5, 6], np.int32)   # dup in p1, out-of-range in p2
+    rc, logits, probs = oracle.candidate_readout(h, None, W, sc, off, ids)
+    assert rc < 0
+    assert np.isnan(probs[2:6]).all() and np.isfinite(probs[[0, 1, 6, 7]]).all()
+    off2 = np.array([0, 0, 2], np.int32)                  # an empty position
+    rc, _, probs = oracle.candidate_readout(h[:2], None, W, sc, off2, ids[:2])
+    assert rc == -2 and np.isfinite(probs).all()
+    off3 = np.array([0, 65], np.int32)                    # over the cap
+    ids3 = np.arange(65, dtype=np.int32) % V
+    rc, _, _ = oracle.candidate_readout(h[:1], None, np.concatenate([W, W, W]),
+                                        np.concatenate([sc, sc, sc]), off3, np.arange(65, dtype=np.int32))
+    assert rc == -2
+
+
+def test_readout_probs_sum_and_logit_consistency():
+    case = wl.make_readout("readout_p192_v248000", P=24)
+    uniq = np.unique(case.cand_ids)
+    rows = case.lm_rows(uniq)
+    remap = np.searchsorted(uniq, case.cand_ids).astype(np.int32)
+    rc, logits, probs = oracle.candidate_readout(case.h_bits, None, rows, case.lm_scale[uniq],
+                                                 case.cand_offsets, remap)
+    assert rc == 0
+    for p in range(case.P):
+        b, e = case.cand_offsets[p], case.cand_offsets[p + 1]
+        assert abs(float(probs[b:e].astype(np.float64).sum()) - 1.0) <= (e - b + 1) * 2 ** -23
+        full = _full_logits(case.h_bits[p:p + 1], None, rows[remap[b:e]], case.lm_scale[case.cand_ids[b:e]])
+        assert np.array_equal(full[0], logits[b:e])
+
+
+def test_readout_softmax_arithmetic_exact_rationals():
+    # Given the (pinned) logits and exp, the read-out's last steps are
+    # binary32 RN: x = logit - max, s = e_1 + e_2 + ... in candidate order,
+    # prob = e_i / s.  Check every bit against exact rationals.
+    case = wl.make_readout("readout_p192_v248000", P=12)
+    uniq = np.unique(case.cand_ids)
+    rows = case.lm_rows(uniq)
+    remap = np.searchsorted(uniq, case.cand_ids).astype(np.int32)
+    rc, logits, probs = oracle.candidate_readout(case.h_bits, None, rows, case.lm_scale[uniq],
+                                                 case.cand_offsets, remap)
+    assert rc == 0
+    for p in range(case.P):
+        b, e = case.cand_offsets[p], case.cand_offsets[p + 1]
+        lg = [float(v) for v in logits[b:e]]
+        mx = max(lg)
+        xs = [rn32(Fr(v) - Fr(mx)) for v in lg]
+        ev = [float(v) for v in oracle.exp(np.array(xs, np.float32))]
+        s = Fr(0)
+        for v in ev:
+            s = Fr(rn32(s + Fr(v))) if v or s else s
+        for i, v in enumerate(ev):
+            want = rn32(Fr(v) / s) if v else 0.0
+            assert probs[b + i] == np.float32(want), (p, i)
