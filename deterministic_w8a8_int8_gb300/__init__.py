@@ -1,0 +1,226 @@
+"""Batch-invariant W8A8 int8 linear layer and candidate read-out for GB300.
+
+Thin Python binding over the C ABI of ``libprism.so`` (see ``include/prism.h``):
+argument marshalling only.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and the import
+of any compute entry point fails loudly when the library has not been built
+(``deterministic_w8a8_int8_gb300.build.build()``).
+
+PyTorch is used for device memory and the current CUDA stream only.
+
+Entry points (same names as the C ABI):
+  prism_quant_act(x, inv_s)                      -> (q, a_scale)
+  prism_w8a8_linear(q, a_scale, w, w_scale, ...) -> out
+  prism_candidate_readout(hidden, ...)           -> (logits, probs)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libprism.so")
+
+PRISM_OK = 0
+PRISM_ERR_INVALID_ARG = -1
+PRISM_ERR_ALIGNMENT = -2
+PRISM_ERR_UNSUPPORTED = -3
+PRISM_ERR_WORKSPACE = -4
+PRISM_ERR_CUDA = -5
+PRISM_MAX_K = 133144
+PRISM_MAX_SPLIT_K = 64
+PRISM_MAX_CANDIDATES = 64
+PRISM_MAX_READOUT_K = 65536
+PRISM_DEV_ERR_OFFSETS = 1
+PRISM_DEV_ERR_COUNT = 2
+PRISM_DEV_ERR_ID_RANGE = 4
+PRISM_DEV_ERR_DUPLICATE = 8
+
+# (restype, argtypes) of every symbol the header declares
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "prism_quant_act": (_I32, [_P, _I64, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "prism_w8a8_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "prism_w8a8_linear": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _P, _I64, _P,
+                                 _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "prism_candidate_readout": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _P, _P,
+                                       _I64, _I64, _P, _P, _P, _P]),
+    "prism_status_string": (ctypes.c_char_p, [_I32]),
+    "prism_version": (_I32, []),
+    "prism_w8a8_kernel_kind": (_I32, [_I64, _I64, _I64]),
+    "prism_w8a8_auto_split": (_I32, [_I64, _I64, _I64]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PrismError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libprism.so.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"libprism.so is not built at {LIB_PATH}; run "
+                    "deterministic_w8a8_int8_gb300.build.build() (needs nvcc)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().prism_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PRISM_OK:
+        raise PrismError(fn, status)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _require(t, dtype, name, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    if ndim == 2 and t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous")
+    if ndim == 1 and t.numel() > 1 and t.stride(0) != 1:
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prism_w8a8_workspace_bytes(M: int, N: int, K: int, split_k: int = 0) -> int:
+    return int(lib().prism_w8a8_workspace_bytes(M, N, K, split_k))
+
+
+def prism_w8a8_kernel_kind(M: int, N: int, K: int) -> int:
+    return int(lib().prism_w8a8_kernel_kind(M, N, K))
+
+
+def prism_w8a8_auto_split(M: int, N: int, K: int) -> int:
+    return int(lib().prism_w8a8_auto_split(M, N, K))
+
+
+def prism_version() -> int:
+    return int(lib().prism_version())
+
+
+def prism_quant_act(x, inv_s=None, q=None, a_scale=None, stream=None):
+    """Per-token quantisation of bf16 ``x`` [M, K] -> (int8 q [M, K], float32 a_scale [M])."""
+    import torch
+    _require(x, torch.bfloat16, "x", 2)
+    M, K = x.shape
+    if inv_s is not None:
+        _require(inv_s, torch.float32, "inv_s", 1)
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if a_scale is None:
+        a_scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _require(q, torch.int8, "q", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    st = lib().prism_quant_act(_ptr(x), x.stride(0), _ptr(inv_s), M, K, _ptr(q), q.stride(0),
+                               _ptr(a_scale), _stream(stream))
+    _check("prism_quant_act", st)
+    return q, a_scale
+
+
+def new_workspace(M: int, N: int, K: int, split_k: int = 0, device=None):
+    """A zeroed workspace for prism_w8a8_linear (None when none is needed)."""
+    import torch
+    n = prism_w8a8_workspace_bytes(M, N, K, split_k)
+    if n == 0:
+        return None
+    return torch.zeros((n,), dtype=torch.uint8, device=device)
+
+
+def prism_w8a8_linear(q, a_scale, w, w_scale, residual=None, out=None, acc_out=None,
+                      split_k: int = 0, workspace=None, stream=None):
+    """out[M, N] (bf16) = epilogue(q @ w^T) with exact int32 accumulation.
+
+    ``residual`` may be ``out`` itself (in-place residual add).  ``workspace``
+    must be a zeroed uint8 tensor of at least prism_w8a8_workspace_bytes bytes
+    when split-K is in use; one is allocated (and zeroed) per call when None."""
+    import torch
+    _require(q, torch.int8, "q", 2)
+    _require(w, torch.int8, "w", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    _require(w_scale, torch.float32, "w_scale", 1)
+    M, K = q.shape
+    N = w.shape[0]
+    if w.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if residual is not None:
+        _require(residual, torch.bfloat16, "residual", 2)
+        if tuple(residual.shape) != (M, N):
+            raise ValueError("residual shape")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
+    _require(out, torch.bfloat16, "out", 2)
+    if acc_out is not None:
+        _require(acc_out, torch.int32, "acc_out", 2)
+        if not acc_out.is_contiguous() or tuple(acc_out.shape) != (M, N):
+            raise ValueError("acc_out must be a contiguous [M, N] int32 tensor")
+    if workspace is None:
+        workspace = new_workspace(M, N, K, split_k, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().prism_w8a8_linear(
+        _ptr(q), q.stride(0), _ptr(a_scale), _ptr(w), w.stride(0), _ptr(w_scale),
+        _ptr(residual), 0 if residual is None else residual.stride(0), _ptr(out), out.stride(0),
+        _ptr(acc_out), M, N, K, int(split_k), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("prism_w8a8_linear", st)
+    return out
+
+
+def prism_candidate_readout(hidden, inv_s, lm_head, lm_scale, cand_offsets, cand_ids,
+                            logits=None, probs=None, err=None, stream=None):
+    """Candidate-restricted read-out -> (logits float32 [T], probs float32 [T])."""
+    import torch
+    _require(hidden, torch.bfloat16, "hidden", 2)
+    _require(lm_head, torch.int8, "lm_head", 2)
+    _require(lm_scale, torch.float32, "lm_scale", 1)
+    _require(cand_offsets, torch.int32, "cand_offsets", 1)
+    _require(cand_ids, torch.int32, "cand_ids", 1)
+    if inv_s is not None:
+        _require(inv_s, torch.float32, "inv_s", 1)
+    P, K = hidden.shape
+    V = lm_head.shape[0]
+    T = cand_ids.numel()
+    if lm_head.shape[1] != K or cand_offsets.numel() != P + 1:
+        raise ValueError("shape mismatch")
+    if logits is None:
+        logits = torch.empty((T,), dtype=torch.float32, device=hidden.device)
+    if probs is None:
+        probs = torch.empty((T,), dtype=torch.float32, device=hidden.device)
+    st = lib().prism_candidate_readout(
+        _ptr(hidden), hidden.stride(0), _ptr(inv_s), _ptr(lm_head), lm_head.stride(0),
+        _ptr(lm_scale), V, K, _ptr(cand_offsets), _ptr(cand_ids), P, T, _ptr(logits),
+        _ptr(probs), _ptr(err), _stream(stream))
+    _check("prism_candidate_readout", st)
+    return logits, probs

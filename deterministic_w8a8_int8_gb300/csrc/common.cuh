@@ -1,0 +1,126 @@
+// common.cuh -- device helpers shared by the libprism kernels (sm_103a).
+//
+// Every floating-point step that decides a stored value is written with an
+// explicit round-to-nearest-even intrinsic (__fmul_rn, __fadd_rn, __fdiv_rn,
+// __int2float_rn, __float2int_rn) so that the compiler can neither contract
+// it into a fused multiply-add nor reorder it.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "prism.h"
+
+namespace prism {
+
+// ----------------------------------------------------------------- bf16 ---
+__device__ __forceinline__ float bf16_lo(uint32_t pair) {
+  return __uint_as_float(pair << 16);
+}
+__device__ __forceinline__ float bf16_hi(uint32_t pair) {
+  return __uint_as_float(pair & 0xffff0000u);
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+// binary32 -> bf16, round to nearest even (finite values; NaN -> quiet NaN).
+__device__ __forceinline__ uint32_t float_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+// The epilogue of the W8A8 linear: ((float(acc) * a) * w) [+ r], each step
+// one binary32 RN operation, then bf16 round-to-nearest-even.
+__device__ __forceinline__ uint32_t epilogue_bf16(int32_t acc, float a, float w) {
+  float t = __int2float_rn(acc);
+  t = __fmul_rn(t, a);
+  t = __fmul_rn(t, w);
+  return float_to_bf16_rne(t);
+}
+__device__ __forceinline__ uint32_t epilogue_bf16_res(int32_t acc, float a, float w, float r) {
+  float t = __int2float_rn(acc);
+  t = __fmul_rn(t, a);
+  t = __fmul_rn(t, w);
+  t = __fadd_rn(t, r);
+  return float_to_bf16_rne(t);
+}
+
+// ------------------------------------------------------ cp.async / ldmatrix
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// 16-byte asynchronous copy global -> shared; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x32 s8, row) * B(32x8 s8, col) + C, exact int32.
+__device__ __forceinline__ void mma_s8_16832(int32_t (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Streaming 16-byte global load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream_16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute
+// is per device context).  Thread-safe; idempotent.
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+}  // namespace prism
+
+// Internal launchers (one per kernel family), defined in their .cu files.
+namespace prism {
+cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K,
+                             int8_t* q, int64_t ldq, float* a_scale, cudaStream_t stream);
+
+struct LinearArgs {
+  const int8_t* q;
+  int64_t ldq;
+  const float* a_scale;
+  const int8_t* w;
+  int64_t ldw;
+  const float* w_scale;
+  const uint16_t* residual;
+  int64_t ldr;
+  uint16_t* out;
+  int64_t ldo;
+  int32_t* acc_out;
+  int64_t M, N, K;
+  int split;
+  int32_t* ws_acc;      // [M, N] int32, zero between calls (split > 1)
+  uint32_t* ws_count;   // [tiles] arrival counters, zero between calls
+};
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
+int linear_kernel_kind(int64_t M, int64_t N, int64_t K);
+int linear_auto_split(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream);
+
+cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const int8_t* W,
+                           int64_t ldw, const float* lm_scale, int64_t V, int64_t K,
+                           const int32_t* off, const int32_t* ids, int64_t P, int64_t T,
+                           float* logits, float* probs, uint32_t* err, cudaStream_t stream);
+}  // namespace prism

@@ -1,0 +1,163 @@
+// prism_abi.cu -- the extern "C" boundary of libprism.so: host-side argument
+// checks (returned as prism_status before anything is enqueued) and dispatch
+// to the kernel launchers.  See include/prism.h for the contract.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace prism {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_attr_mutex;
+struct AttrEntry {
+  const void* kernel;
+  int bytes;
+};
+AttrEntry g_attr[kMaxDevices][8];
+int g_attr_n[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  for (int i = 0; i < g_attr_n[dev]; ++i)
+    if (g_attr[dev][i].kernel == kernel && g_attr[dev][i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (g_attr_n[dev] < 8) g_attr[dev][g_attr_n[dev]++] = AttrEntry{kernel, bytes};
+  return cudaSuccess;
+}
+
+}  // namespace prism
+
+using prism::aligned;
+
+extern "C" {
+
+int prism_version(void) { return 100; }
+
+const char* prism_status_string(int status) {
+  switch (status) {
+    case PRISM_OK: return "ok";
+    case PRISM_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad stride)";
+    case PRISM_ERR_ALIGNMENT: return "misaligned pointer or stride, or K not a multiple of 16";
+    case PRISM_ERR_UNSUPPORTED: return "unsupported size (K, split_k or candidate count beyond the limits)";
+    case PRISM_ERR_WORKSPACE: return "workspace missing or too small";
+    case PRISM_ERR_CUDA: return "CUDA launch or runtime error";
+    default: return "unknown status";
+  }
+}
+
+int prism_quant_act(const void* x_bf16, int64_t ldx, const float* inv_smooth, int64_t M, int64_t K,
+                    int8_t* q, int64_t ldq, float* a_scale, void* cuda_stream) {
+  if (M < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (M == 0) return PRISM_OK;
+  if (x_bf16 == nullptr || q == nullptr || a_scale == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldx < K || ldq < K) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+  if (ldx % 8 != 0 || ldq % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(a_scale, 4)) return PRISM_ERR_ALIGNMENT;
+  if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
+  if (M > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  cudaError_t e = prism::launch_quant_act(x_bf16, ldx, inv_smooth, M, K, q, ldq, a_scale,
+                                          static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+}
+
+int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K) { return prism::linear_kernel_kind(M, N, K); }
+
+int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K) { return prism::linear_auto_split(M, N, K); }
+
+size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+  if (M <= 0 || N <= 0 || K <= 0 || split_k < 0 || split_k > PRISM_MAX_SPLIT_K) return 0;
+  const int s = split_k == 0 ? prism::linear_auto_split(M, N, K) : split_k;
+  return prism::linear_workspace_bytes(M, N, K, s);
+}
+
+int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
+                      const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16,
+                      int64_t ldo, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (M < 0 || N < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (split_k < 0) return PRISM_ERR_INVALID_ARG;
+  if (split_k > PRISM_MAX_SPLIT_K) return PRISM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return PRISM_OK;
+  if (q == nullptr || a_scale == nullptr || w == nullptr || w_scale == nullptr || out_bf16 == nullptr)
+    return PRISM_ERR_INVALID_ARG;
+  if (ldq < K || ldw < K || ldo < N || (residual_bf16 != nullptr && ldr < N)) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+  if (ldq % 16 != 0 || ldw % 16 != 0 || ldo % 8 != 0) return PRISM_ERR_ALIGNMENT;
+  if (residual_bf16 != nullptr && ldr % 8 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(out_bf16, 16) || !aligned(a_scale, 4) ||
+      !aligned(w_scale, 4))
+    return PRISM_ERR_ALIGNMENT;
+  if (residual_bf16 != nullptr && !aligned(residual_bf16, 16)) return PRISM_ERR_ALIGNMENT;
+  if (acc_out != nullptr && !aligned(acc_out, 4)) return PRISM_ERR_ALIGNMENT;
+  if (M > 65535LL * 128 || N > (1LL << 31) * 64) return PRISM_ERR_UNSUPPORTED;
+
+  const int split = split_k == 0 ? prism::linear_auto_split(M, N, K) : split_k;
+  const size_t need = prism::linear_workspace_bytes(M, N, K, split);
+  prism::LinearArgs a{};
+  a.q = q;
+  a.ldq = ldq;
+  a.a_scale = a_scale;
+  a.w = w;
+  a.ldw = ldw;
+  a.w_scale = w_scale;
+  a.residual = static_cast<const uint16_t*>(residual_bf16);
+  a.ldr = ldr;
+  a.out = static_cast<uint16_t*>(out_bf16);
+  a.ldo = ldo;
+  a.acc_out = acc_out;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.split = split;
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need) return PRISM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PRISM_ERR_ALIGNMENT;
+    const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~static_cast<size_t>(255);
+    a.ws_acc = static_cast<int32_t*>(workspace);
+    a.ws_count = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + acc_bytes);
+  }
+  cudaError_t e = prism::launch_linear(a, static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+}
+
+int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* inv_smooth,
+                            const int8_t* lm_head, int64_t ldw, const float* lm_scale, int64_t V,
+                            int64_t K, const int32_t* cand_offsets, const int32_t* cand_ids, int64_t P,
+                            int64_t T, float* logits, float* probs, uint32_t* dev_error_word,
+                            void* cuda_stream) {
+  if (P < 0 || T < 0 || V <= 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (P == 0) return T == 0 ? PRISM_OK : PRISM_ERR_INVALID_ARG;
+  if (hidden_bf16 == nullptr || lm_head == nullptr || lm_scale == nullptr || cand_offsets == nullptr ||
+      logits == nullptr || probs == nullptr)
+    return PRISM_ERR_INVALID_ARG;
+  if (T > 0 && cand_ids == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldh < K || ldw < K) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_READOUT_K || T > P * PRISM_MAX_CANDIDATES || V > (1LL << 31) - 1)
+    return PRISM_ERR_UNSUPPORTED;
+  if (ldh % 8 != 0 || ldw % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(hidden_bf16, 16) || !aligned(lm_head, 16) || !aligned(lm_scale, 4) ||
+      !aligned(cand_offsets, 4) || !aligned(cand_ids, 4) || !aligned(logits, 4) || !aligned(probs, 4))
+    return PRISM_ERR_ALIGNMENT;
+  if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
+  if (dev_error_word != nullptr && !aligned(dev_error_word, 4)) return PRISM_ERR_ALIGNMENT;
+  if (P > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  cudaError_t e = prism::launch_readout(hidden_bf16, ldh, inv_smooth, lm_head, ldw, lm_scale, V, K,
+                                        cand_offsets, cand_ids, P, T, logits, probs, dev_error_word,
+                                        static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// quant_act.cu -- per-token activation quantisation with the SmoothQuant
+// divisor folded in (StartLux-Prism, "Compute shared evidence once").
+//
+//   xs_k    = x_k * inv_s_k                      binary32 RN
+//   amax    = max_k |xs_k|                       exact (order free)
+//   q_k     = clamp(rint_even(xs_k * RN(127/amax)), -127, 127)
+//   a_scale = RN(amax / 127);  amax < 2^-120  =>  q = 0, a_scale = 0
+//
+// HBM-bound: each row is read once from DRAM (3 bytes per element in and
+// out, plus 4 bytes of scale per row).  A team of TEAM threads owns one row:
+// pass 1 streams the row with 16-byte loads and keeps the smoothed values in
+// registers while they fit (CACHE vectors of 8 per thread), reduces amax with
+// warp shuffles, pass 2 quantises from registers (or re-reads the row from L2
+// when it is longer than the cache) and stores 8-byte int8 vectors.
+#include "common.cuh"
+
+namespace prism {
+namespace {
+
+constexpr int kBlock = 256;
+
+struct Vec8 {
+  float v[8];
+};
+
+__device__ __forceinline__ Vec8 load_smoothed(const uint16_t* __restrict__ xr,
+                                              const float* __restrict__ inv_s, int64_t k0) {
+  const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + k0));
+  Vec8 r;
+  r.v[0] = bf16_lo(xv.x);
+  r.v[1] = bf16_hi(xv.x);
+  r.v[2] = bf16_lo(xv.y);
+  r.v[3] = bf16_hi(xv.y);
+  r.v[4] = bf16_lo(xv.z);
+  r.v[5] = bf16_hi(xv.z);
+  r.v[6] = bf16_lo(xv.w);
+  r.v[7] = bf16_hi(xv.w);
+  if (inv_s != nullptr) {
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(inv_s + k0));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(inv_s + k0 + 4));
+    r.v[0] = __fmul_rn(r.v[0], s0.x);
+    r.v[1] = __fmul_rn(r.v[1], s0.y);
+    r.v[2] = __fmul_rn(r.v[2], s0.z);
+    r.v[3] = __fmul_rn(r.v[3], s0.w);
+    r.v[4] = __fmul_rn(r.v[4], s1.x);
+    r.v[5] = __fmul_rn(r.v[5], s1.y);
+    r.v[6] = __fmul_rn(r.v[6], s1.z);
+    r.v[7] = __fmul_rn(r.v[7], s1.w);
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float inv_a) {
+  int qa = max(-127, min(127, __float2int_rn(__fmul_rn(a, inv_a))));
+  int qb = max(-127, min(127, __float2int_rn(__fmul_rn(b, inv_a))));
+  int qc = max(-127, min(127, __float2int_rn(__fmul_rn(c, inv_a))));
+  int qd = max(-127, min(127, __float2int_rn(__fmul_rn(d, inv_a))));
+  return (static_cast<uint32_t>(qa) & 0xffu) | ((static_cast<uint32_t>(qb) & 0xffu) << 8) |
+         ((static_cast<uint32_t>(qc) & 0xffu) << 16) | ((static_cast<uint32_t>(qd) & 0xffu) << 24);
+}
+
+__device__ __forceinline__ float vmaxabs(const Vec8& r, float m) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(r.v[i]));
+  return m;
+}
+
+template <int TEAM, int CACHE>
+__global__ void __launch_bounds__(kBlock)
+    quant_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, const float* __restrict__ inv_s,
+                     int64_t M, int64_t K, int8_t* __restrict__ q, int64_t ldq,
+                     float* __restrict__ a_scale) {
+  constexpr int kRows = kBlock / TEAM;
+  constexpr int kWarpsPerTeam = TEAM / 32;
+  __shared__ float red[kBlock / 32];
+  const int team = threadIdx.x / TEAM;
+  const int lt = threadIdx.x % TEAM;
+  const int64_t m = static_cast<int64_t>(blockIdx.x) * kRows + team;
+  const bool active = m < M;
+  const uint16_t* xr = x + (active ? m : 0) * ldx;
+  const int64_t nvec = K >> 3;
+
+  Vec8 cache[CACHE];
+  float amax = 0.0f;
+  if (active) {
+#pragma unroll
+    for (int c = 0; c < CACHE; ++c) {
+      const int64_t v = lt + static_cast<int64_t>(c) * TEAM;
+      if (v < nvec) {
+        cache[c] = load_smoothed(xr, inv_s, v * 8);
+        amax = vmaxabs(cache[c], amax);
+      }
+    }
+    for (int64_t v = lt + static_cast<int64_t>(CACHE) * TEAM; v < nvec; v += TEAM)
+      amax = vmaxabs(load_smoothed(xr, inv_s, v * 8), amax);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (kWarpsPerTeam > 1) {
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    const int w0 = team * kWarpsPerTeam;
+#pragma unroll
+    for (int i = 0; i < kWarpsPerTeam; ++i) amax = fmaxf(amax, red[w0 + i]);
+  }
+  if (!active) return;
+
+  int8_t* qr = q + m * ldq;
+  const bool zero_row = !(amax >= 0x1p-120f);
+  const float inv_a = zero_row ? 0.0f : __fdiv_rn(127.0f, amax);
+  if (lt == 0) a_scale[m] = zero_row ? 0.0f : __fdiv_rn(amax, 127.0f);
+
+#pragma unroll
+  for (int c = 0; c < CACHE; ++c) {
+    const int64_t v = lt + static_cast<int64_t>(c) * TEAM;
+    if (v < nvec) {
+      const Vec8& r = cache[c];
+      uint2 o;
+      o.x = quant4(r.v[0], r.v[1], r.v[2], r.v[3], inv_a);
+      o.y = quant4(r.v[4], r.v[5], r.v[6], r.v[7], inv_a);
+      *reinterpret_cast<uint2*>(qr + v * 8) = o;
+    }
+  }
+  for (int64_t v = lt + static_cast<int64_t>(CACHE) * TEAM; v < nvec; v += TEAM) {
+    const Vec8 r = load_smoothed(xr, inv_s, v * 8);
+    uint2 o;
+    o.x = quant4(r.v[0], r.v[1], r.v[2], r.v[3], inv_a);
+    o.y = quant4(r.v[4], r.v[5], r.v[6], r.v[7], inv_a);
+    *reinterpret_cast<uint2*>(qr + v * 8) = o;
+  }
+}
+
+template <int TEAM, int CACHE>
+cudaError_t launch_team(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K,
+                        int8_t* q, int64_t ldq, float* a_scale, cudaStream_t stream) {
+  constexpr int kRows = kBlock / TEAM;
+  const int64_t blocks = (M + kRows - 1) / kRows;
+  quant_act_kernel<TEAM, CACHE><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
+      static_cast<const uint16_t*>(x), ldx, inv_s, M, K, q, ldq, a_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K,
+                             int8_t* q, int64_t ldq, float* a_scale, cudaStream_t stream) {
+  // Team size grows with K so that a row fits the team's register cache
+  // (TEAM * CACHE * 8 elements); longer rows re-read their tail from L2.
+  if (K <= 32 * 8 * 4) return launch_team<32, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
+  if (K <= 64 * 8 * 4) return launch_team<64, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
+  if (K <= 128 * 8 * 4) return launch_team<128, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
+  return launch_team<256, 9>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
+}
+
+}  // namespace prism

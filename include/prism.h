@@ -1,0 +1,188 @@
+/*
+ * prism.h -- C ABI of the batch-invariant W8A8 linear layer and the
+ * candidate-restricted read-out (libprism.so, sm_103a).
+ *
+ * The operations follow "StartLux-Prism: Fast, exact inference for
+ * StartLux-Decision models on NVIDIA GPUs" and its companion post
+ * "把决策模型推理从 vLLM 换到 Prism":
+ *   - activations are quantised per token after SmoothQuant smoothing
+ *     (StartLux-Prism, section "Compute shared evidence once");
+ *   - int8 products accumulate exactly in int32, split-K partial sums stay
+ *     integers, and the result is scaled and added to the residual in a
+ *     fixed rounding sequence (section "Bitwise consistency is not lossless
+ *     quantization");
+ *   - the output layer scores only each answer position's candidates and
+ *     normalises within that set (post, sections 方案 and 实现要点), with a
+ *     hard cap on the candidate count (section 复盘).
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller owns every buffer.  The library never allocates,
+ *     frees or retains a pointer after the call returns.
+ *   - Memory: every array argument is a DEVICE pointer on the current CUDA
+ *     device (for example a torch tensor's data_ptr()).  Scalars are passed
+ *     by value.  Strides ("ld*") are in elements and describe row-major
+ *     matrices whose rows are contiguous.
+ *   - Asynchrony: work is enqueued on `cuda_stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and the call returns without synchronising.
+ *   - Errors: argument errors are detected on the host and returned before
+ *     anything is enqueued.  PRISM_ERR_CUDA means the launch itself failed.
+ *     Errors that only the device can see (bad candidate lists) are OR-ed
+ *     into a caller-provided device error word; no kernel traps or asserts.
+ *   - Determinism: every output row depends only on its own input row, the
+ *     weights and the scales.  It is bit-identical for any batch size, batch
+ *     composition, row order, split-K setting and internal tile choice.
+ *   - Numerics (readings where the pages give no formula):
+ *       quantiser  xs = x * inv_s (binary32 RN); amax = max |xs|;
+ *                  q = clamp(rint_even(xs * RN(127/amax)), -127, 127);
+ *                  a_scale = RN(amax / 127); rows with amax < 2^-120 give
+ *                  q = 0, a_scale = 0.
+ *       epilogue   y = bf16_rne(((float(acc) * a_scale[m]) * w_scale[n])
+ *                               + residual[m,n]), one binary32 RN operation
+ *                  per step, no fused multiply-add.
+ *       read-out   logit = (float(acc) * a_scale[p]) * lm_scale[c] (binary32),
+ *                  prob  = e_c / (e_1 + ... + e_n) summed in list order, with
+ *                  e_c = exp(logit_c - max) from a Cody-Waite reduction and a
+ *                  degree-7 Taylor polynomial in binary32 RN operations.
+ */
+#ifndef PRISM_H_
+#define PRISM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PRISM_OK = 0,
+  PRISM_ERR_INVALID_ARG = -1, /* NULL pointer, negative size, bad stride  */
+  PRISM_ERR_ALIGNMENT = -2,   /* pointer or stride not 16-byte aligned,
+                                 K not a multiple of 16                      */
+  PRISM_ERR_UNSUPPORTED = -3, /* K above PRISM_MAX_K, split_k above
+                                 PRISM_MAX_SPLIT_K, T above P * 64, ...      */
+  PRISM_ERR_WORKSPACE = -4,   /* workspace missing or too small             */
+  PRISM_ERR_CUDA = -5         /* a CUDA launch or runtime call failed       */
+} prism_status;
+
+/* Largest K for which every int32 accumulator is exact: K * 127 * 127 must
+ * not exceed 2^31 - 1.  With K a multiple of 16 the usable maximum is 133136. */
+#define PRISM_MAX_K 133144
+/* Largest split-K factor accepted by prism_w8a8_linear. */
+#define PRISM_MAX_SPLIT_K 64
+/* Hard cap on candidates per answer position (post, section 复盘). */
+#define PRISM_MAX_CANDIDATES 64
+/* Largest hidden size accepted by the read-out (its quantised row is staged
+ * on chip). */
+#define PRISM_MAX_READOUT_K 65536
+
+/* Bits OR-ed into the read-out's device error word. */
+#define PRISM_DEV_ERR_OFFSETS   1u /* offsets outside [0, T] or decreasing    */
+#define PRISM_DEV_ERR_COUNT     2u /* count outside [1, PRISM_MAX_CANDIDATES] */
+#define PRISM_DEV_ERR_ID_RANGE  4u /* candidate id outside [0, V)             */
+#define PRISM_DEV_ERR_DUPLICATE 8u /* the same id twice in one position       */
+
+/*
+ * prism_quant_act -- per-token activation quantisation with SmoothQuant
+ * smoothing folded in (StartLux-Prism, "Compute shared evidence once").
+ *
+ *   x_bf16      [M, K] bf16, row stride ldx (ldx % 8 == 0, 16-byte aligned)
+ *   inv_smooth  [K] float32 = 1/s_k, or NULL for no smoothing (16-byte aligned)
+ *   q           [M, K] int8 out, row stride ldq (ldq % 16 == 0, 16-byte aligned)
+ *   a_scale     [M] float32 out (4-byte aligned)
+ *   M >= 0 (M == 0 enqueues nothing), 16 <= K <= PRISM_MAX_K, K % 16 == 0.
+ * Inputs must be finite and x * inv_s must not overflow.
+ */
+int prism_quant_act(const void *x_bf16, int64_t ldx, const float *inv_smooth,
+                    int64_t M, int64_t K, int8_t *q, int64_t ldq,
+                    float *a_scale, void *cuda_stream);
+
+/*
+ * Bytes of workspace prism_w8a8_linear needs for this shape and split-K
+ * setting (split_k = 0 means the automatic choice, as in the linear call).
+ * Returns 0 when no workspace is needed (split-K of 1).
+ */
+size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+/*
+ * prism_w8a8_linear -- out = epilogue(q @ w^T) with exact int32 accumulation
+ * (StartLux-Prism, "Bitwise consistency is not lossless quantization").
+ *
+ *   q, ldq         [M, K] int8 activations (prism_quant_act's output)
+ *   a_scale        [M] float32 per-token scales
+ *   w, ldw         [N, K] int8 weights, K contiguous (nn.Linear layout)
+ *   w_scale        [N] float32 per-output-channel scales
+ *   residual, ldr  [M, N] bf16 or NULL; may be the same buffer as out
+ *   out, ldo       [M, N] bf16 output
+ *   acc_out        [M, N] int32 dense (stride N) copy of the accumulator, or
+ *                  NULL (a debugging aid; costs 4*M*N bytes of writes)
+ *   split_k        0 = automatic, else 1..PRISM_MAX_SPLIT_K.  The K range is
+ *                  cut into split_k pieces whose int32 partial sums are added
+ *                  as integers; the result does not depend on split_k.
+ *   workspace      device memory of at least
+ *                  prism_w8a8_workspace_bytes(M, N, K, split_k) bytes, 256-byte
+ *                  aligned, ZEROED by the caller before its first use.  Every
+ *                  call leaves it zeroed again, so one zeroing serves all later
+ *                  calls.  Calls sharing a workspace must not overlap in time
+ *                  (use one stream, or one workspace per stream).  May be NULL
+ *                  when the required size is 0.
+ * Alignment: q, w, residual, out 16-byte aligned; ldq, ldw % 16 == 0;
+ * ldr, ldo % 8 == 0; K % 16 == 0.  M == 0 or N == 0 enqueues nothing.
+ */
+int prism_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
+                      const int8_t *w, int64_t ldw, const float *w_scale,
+                      const void *residual_bf16, int64_t ldr, void *out_bf16,
+                      int64_t ldo, int32_t *acc_out, int64_t M, int64_t N,
+                      int64_t K, int split_k, void *workspace,
+                      size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * prism_candidate_readout -- logits and probabilities for the candidate
+ * tokens of each answer position only; the softmax runs over the candidates
+ * (post "把决策模型推理从 vLLM 换到 Prism", sections 方案 and 实现要点: equal to
+ * the full-vocabulary softmax renormalised on the candidates).
+ *
+ *   hidden_bf16, ldh  [P, K] bf16 final hidden states (ldh % 8 == 0)
+ *   inv_smooth        [K] float32 or NULL
+ *   lm_head, ldw      [V, K] int8 LM head (ldw % 16 == 0), lm_scale [V] float32
+ *   cand_offsets      [P+1] int32 CSR offsets, cand_offsets[0] = 0,
+ *                     cand_offsets[P] = T
+ *   cand_ids          [T] int32 token ids, distinct within a position,
+ *                     1..PRISM_MAX_CANDIDATES per position
+ *   logits, probs     [T] float32 out, in CSR order
+ *   dev_error_word    device uint32: PRISM_DEV_ERR_* bits are OR-ed into it
+ *                     for invalid positions, whose outputs are set to NaN.
+ *                     The caller clears it.  May be NULL (errors then only
+ *                     show as NaN outputs).
+ *   P >= 0 (P == 0 enqueues nothing), T <= P * PRISM_MAX_CANDIDATES,
+ *   16 <= K <= PRISM_MAX_READOUT_K, K % 16 == 0.
+ */
+int prism_candidate_readout(const void *hidden_bf16, int64_t ldh,
+                            const float *inv_smooth, const int8_t *lm_head,
+                            int64_t ldw, const float *lm_scale, int64_t V,
+                            int64_t K, const int32_t *cand_offsets,
+                            const int32_t *cand_ids, int64_t P, int64_t T,
+                            float *logits, float *probs,
+                            uint32_t *dev_error_word, void *cuda_stream);
+
+/* Human-readable text for a prism_status value (static storage). */
+const char *prism_status_string(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int prism_version(void);
+
+/*
+ * Which contraction kernel prism_w8a8_linear would launch for this shape:
+ * 0 = none (empty), 1 = tensor-core tile kernel (mma.sync s8),
+ * 2 = weight-streaming kernel for few rows.  For tests and benchmarks.
+ */
+int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K);
+
+/* The split-K factor an automatic (split_k = 0) call would use. */
+int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRISM_H_ */

@@ -1,0 +1,149 @@
+"""Host-side tests of the C ABI: the library builds and loads, exports every
+function include/prism.h declares, and rejects bad arguments with the right
+status before anything is enqueued.  No GPU: every call below fails argument
+validation by construction (the pointers are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from deterministic_w8a8_int8_gb300 import build
+    build.build()
+    import deterministic_w8a8_int8_gb300 as p
+    return p.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(prism_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(L):
+    import deterministic_w8a8_int8_gb300 as p
+    names = declared_functions()
+    assert {"prism_quant_act", "prism_w8a8_linear", "prism_candidate_readout"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in p.SIGNATURES, f"binding lacks {n}"
+
+
+def test_header_constants_match_binding():
+    import deterministic_w8a8_int8_gb300 as p
+    src = open(os.path.join(ROOT, "include", "prism.h")).read()
+    for name in ("PRISM_MAX_K", "PRISM_MAX_SPLIT_K", "PRISM_MAX_CANDIDATES", "PRISM_MAX_READOUT_K"):
+        v = int(re.search(rf"#define {name} (\d+)", src).group(1))
+        assert getattr(p, name) == v
+    for name, v in re.findall(r"(PRISM_ERR_\w+) = (-?\d+)", src):
+        assert getattr(p, name) == int(v)
+    for name, v in re.findall(r"#define (PRISM_DEV_ERR_\w+)\s+(\d+)u", src):
+        assert getattr(p, name) == int(v)
+
+
+def test_status_strings(L):
+    for s in range(-5, 1):
+        assert L.prism_status_string(s)
+    assert L.prism_version() >= 100
+
+
+A = 0x10000  # a 256-byte-aligned fake address; never dereferenced below
+
+
+def quant(L, x=A, ldx=64, s=None, M=4, K=64, q=A, ldq=64, a=A):
+    return L.prism_quant_act(x, ldx, s, M, K, q, ldq, a, None)
+
+
+def test_quant_act_validation(L):
+    assert quant(L, M=0) == 0                       # empty: nothing to do
+    assert quant(L, M=-1) == -1
+    assert quant(L, K=0) == -1
+    assert quant(L, x=None) == -1
+    assert quant(L, q=None) == -1
+    assert quant(L, a=None) == -1
+    assert quant(L, ldx=32) == -1                   # ldx < K
+    assert quant(L, K=72, ldx=80, ldq=80) == -2     # K % 16
+    assert quant(L, ldx=68, ldq=64) == -2           # ldx % 8
+    assert quant(L, ldq=72) == -2                   # ldq % 16
+    assert quant(L, x=A + 8) == -2
+    assert quant(L, q=A + 4) == -2
+    assert quant(L, a=A + 2) == -2
+    assert quant(L, s=A + 4) == -2
+    K = 133152                                      # multiple of 16 above the int32 bound
+    assert quant(L, K=K, ldx=K, ldq=K) == -3
+
+
+def lin(L, M=64, N=64, K=64, split=1, ws=None, wsb=0, q=A, w=A, out=A, res=None, ldr=0,
+        ldq=None, ldw=None, ldo=None, a=A, ws_=A, acc=None):
+    ldq = K if ldq is None else ldq
+    ldw = K if ldw is None else ldw
+    ldo = N if ldo is None else ldo
+    return L.prism_w8a8_linear(q, ldq, a, w, ldw, ws_, res, ldr, out, ldo, acc, M, N, K, split,
+                               ws, wsb, None)
+
+
+def test_linear_validation(L):
+    assert lin(L, M=0) == 0 and lin(L, N=0) == 0
+    assert lin(L, M=-1) == -1 and lin(L, K=0) == -1
+    assert lin(L, split=-1) == -1
+    assert lin(L, split=65) == -3
+    assert lin(L, q=None) == -1 and lin(L, w=None) == -1 and lin(L, out=None) == -1
+    assert lin(L, a=None) == -1 and lin(L, ws_=None) == -1
+    assert lin(L, ldq=32) == -1 and lin(L, ldo=32) == -1
+    assert lin(L, res=A, ldr=32) == -1
+    assert lin(L, K=72, ldq=80, ldw=80) == -2
+    assert lin(L, ldq=72) == -2 and lin(L, ldw=72) == -2 and lin(L, ldo=68) == -2
+    assert lin(L, res=A, ldr=68) == -2
+    assert lin(L, q=A + 8) == -2 and lin(L, w=A + 8) == -2 and lin(L, out=A + 4) == -2
+    assert lin(L, res=A + 4, ldr=64) == -2 and lin(L, a=A + 2) == -2
+    assert lin(L, acc=A + 2) == -2
+    K = 133152
+    assert lin(L, K=K) == -3
+    # split-K needs a workspace of the advertised size, 256-byte aligned
+    need = L.prism_w8a8_workspace_bytes(64, 64, 4096, 4)
+    assert need >= 64 * 64 * 4
+    assert lin(L, K=4096, split=4) == -4
+    assert lin(L, K=4096, split=4, ws=A, wsb=need - 1) == -4
+    assert lin(L, K=4096, split=4, ws=A + 16, wsb=need) == -2
+
+
+def test_workspace_and_dispatch_queries(L):
+    assert L.prism_w8a8_workspace_bytes(64, 64, 64, 1) == 0
+    assert L.prism_w8a8_workspace_bytes(0, 64, 64, 4) == 0
+    assert L.prism_w8a8_workspace_bytes(64, 64, 64, 65) == 0
+    for M, N, K in [(1, 5120, 17408), (304, 5120, 5120), (2048, 34816, 5120), (37, 384, 256)]:
+        s = L.prism_w8a8_auto_split(M, N, K)
+        assert 1 <= s <= 64
+        assert L.prism_w8a8_workspace_bytes(M, N, K, 0) == L.prism_w8a8_workspace_bytes(M, N, K, s)
+        assert L.prism_w8a8_kernel_kind(M, N, K) in (1, 2)
+    assert L.prism_w8a8_kernel_kind(0, 5, 16) == 0
+
+
+def ro(L, P=4, T=8, V=100, K=64, h=A, ldh=64, s=None, W=A, ldw=64, sc=A, off=A, ids=A,
+       lg=A, pr=A, err=None):
+    return L.prism_candidate_readout(h, ldh, s, W, ldw, sc, V, K, off, ids, P, T, lg, pr, err, None)
+
+
+def test_readout_validation(L):
+    assert ro(L, P=0, T=0) == 0
+    assert ro(L, P=0, T=3) == -1
+    assert ro(L, P=-1) == -1 and ro(L, V=0) == -1 and ro(L, K=0) == -1
+    assert ro(L, h=None) == -1 and ro(L, W=None) == -1 and ro(L, sc=None) == -1
+    assert ro(L, off=None) == -1 and ro(L, ids=None) == -1
+    assert ro(L, lg=None) == -1 and ro(L, pr=None) == -1
+    assert ro(L, ldh=32) == -1 and ro(L, ldw=32) == -1
+    assert ro(L, K=72, ldh=80, ldw=80) == -2
+    assert ro(L, T=4 * 64 + 1) == -3                # beyond the per-position cap
+    assert ro(L, K=65536 + 16, ldh=65552, ldw=65552) == -3
+    assert ro(L, ldh=68) == -2 and ro(L, ldw=72) == -2
+    assert ro(L, h=A + 8) == -2 and ro(L, W=A + 8) == -2 and ro(L, off=A + 2) == -2
+    assert ro(L, s=A + 4) == -2 and ro(L, err=A + 2) == -2

@@ -1,0 +1,193 @@
+"""GPU parity of prism_w8a8_linear against the CPU oracle, and the layer's
+invariances: int32 accumulators and bf16 outputs bit-exact; identical bits
+for every split-K factor, batch size, batch composition and row order
+(StartLux-Prism, "Bitwise consistency is not lossless quantization")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests.gpu_util import dev, dev_bf16, host, host_bits, padded
+
+import deterministic_w8a8_int8_gb300 as prism
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_linear(q, a, w, ws, res=None, split=0, acc=True, out=None):
+    M, N = q.shape[0], w.shape[0]
+    acc_t = torch.empty((M, N), dtype=torch.int32, device="cuda") if acc else None
+    out = prism.prism_w8a8_linear(q, a, w, ws, residual=res, out=out, acc_out=acc_t, split_k=split)
+    torch.cuda.synchronize()
+    return out, acc_t
+
+
+def random_problem(M, N, K, seed, residual=True):
+    rng = np.random.default_rng(seed)
+    xb = wl.bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    w = wl.draw_weights(rng, (N, K), "normal")
+    w_scale = rng.uniform(0.001, 0.02, N).astype(np.float32)
+    rb = wl.bf16_bits(rng.standard_normal((M, N), dtype=np.float32)) if residual else None
+    return xb, w, w_scale, rb
+
+
+def oracle_full(xb, inv_s, w, w_scale, rb):
+    q, a = oracle.quant_act(xb, inv_s)
+    out, acc = oracle.w8a8_linear(q, a, w, w_scale, rb)
+    return q, a, out, acc
+
+
+def test_tiny_config_end_to_end(cuda_device):
+    c = wl.make_linear("tiny_m37_k256_n384")
+    qo, ao, outo, acco = oracle_full(c.x_bits, c.inv_s, c.w, c.w_scale, c.residual_bits)
+    q, a = prism.prism_quant_act(dev_bf16(c.x_bits), dev(c.inv_s))
+    assert np.array_equal(host(q), qo) and np.array_equal(host(a), ao)
+    w, ws, r = dev(c.w), dev(c.w_scale), dev_bf16(c.residual_bits)
+    out, acc = gpu_linear(q, a, w, ws, r)
+    assert np.array_equal(host(acc), acco)
+    assert np.array_equal(host_bits(out), outo)
+    # the same rows run one at a time give the same bits
+    for m in range(c.M):
+        q1, a1 = prism.prism_quant_act(dev_bf16(c.x_bits[m:m + 1]), dev(c.inv_s))
+        o1, _ = gpu_linear(q1, a1, w, ws, r[m:m + 1], acc=False)
+        assert np.array_equal(host_bits(o1)[0], outo[m]), m
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 16), (3, 130, 48), (129, 384, 256), (37, 131, 64),
+                                   (130, 257, 528), (255, 136, 1040), (1, 1, 16)])
+@pytest.mark.parametrize("residual", [True, False])
+def test_ragged_shapes(cuda_device, M, N, K, residual):
+    xb, w, w_scale, rb = random_problem(M, N, K, M * 131 + N * 7 + K, residual)
+    _, _, outo, acco = oracle_full(xb, None, w, w_scale, rb)
+    q, a = prism.prism_quant_act(dev_bf16(xb))
+    ld = (N + 7) // 8 * 8 + 8
+    r = None
+    if residual:
+        r = padded(M, N, ld, torch.bfloat16)
+        r.copy_(dev_bf16(rb))
+    out = padded(M, N, ld, torch.bfloat16)
+    out, acc = gpu_linear(q, a, dev(w), dev(w_scale), r, out=out)
+    assert np.array_equal(host(acc), acco)
+    assert np.array_equal(host_bits(out), outo)
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 4, 7, 8, 16, 33, 64])
+def test_split_k_bit_identical(cuda_device, split):
+    M, N, K = 70, 520, 2064
+    xb, w, w_scale, rb = random_problem(M, N, K, 17)
+    _, _, outo, acco = oracle_full(xb, None, w, w_scale, rb)
+    q, a = prism.prism_quant_act(dev_bf16(xb))
+    out, acc = gpu_linear(q, a, dev(w), dev(w_scale), dev_bf16(rb), split=split)
+    assert np.array_equal(host(acc), acco)
+    assert np.array_equal(host_bits(out), outo)
+
+
+def test_split_k_workspace_reuse_stays_zero(cuda_device):
+    M, N, K = 40, 300, 4096
+    xb, w, w_scale, rb = random_problem(M, N, K, 23)
+    _, _, outo, _ = oracle_full(xb, None, w, w_scale, rb)
+    q, a = prism.prism_quant_act(dev_bf16(xb))
+    ws_buf = prism.new_workspace(M, N, K, 8, "cuda")
+    W, S, R = dev(w), dev(w_scale), dev_bf16(rb)
+    for _ in range(3):
+        out = prism.prism_w8a8_linear(q, a, W, S, residual=R, split_k=8, workspace=ws_buf)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(out), outo)
+        assert int(ws_buf.count_nonzero()) == 0
+
+
+def test_in_place_residual(cuda_device):
+    M, N, K = 50, 264, 512
+    xb, w, w_scale, rb = random_problem(M, N, K, 5)
+    _, _, outo, _ = oracle_full(xb, None, w, w_scale, rb)
+    q, a = prism.prism_quant_act(dev_bf16(xb))
+    for split in (1, 4):
+        buf = dev_bf16(rb)
+        prism.prism_w8a8_linear(q, a, dev(w), dev(w_scale), residual=buf, out=buf, split_k=split)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(buf), outo)
+
+
+def test_int32_extremes_at_max_k(cuda_device):
+    K = 133136
+    q = np.full((3, K), 127, np.int8)
+    q[1] = -127
+    q[2, ::2] = -127
+    w = np.full((16, K), 127, np.int8)
+    w[1::2] = -127
+    a = np.ones(3, np.float32)
+    ws = np.full(16, 1.0, np.float32)
+    outo, acco = oracle.w8a8_linear(q, a, w, ws, None)
+    assert acco[0, 0] == K * 16129
+    for split in (1, 5, 16):
+        out, acc = gpu_linear(dev(q), dev(a), dev(w), dev(ws), None, split=split)
+        assert np.array_equal(host(acc), acco)
+        assert np.array_equal(host_bits(out), outo)
+
+
+def test_batch_composition_and_row_order(cuda_device):
+    M, N, K = 96, 640, 1024
+    xb, w, w_scale, rb = random_problem(M, N, K, 31)
+    W, S = dev(w), dev(w_scale)
+    q, a = prism.prism_quant_act(dev_bf16(xb))
+    base, _ = gpu_linear(q, a, W, S, dev_bf16(rb), acc=False)
+    base = host_bits(base)
+    perm = np.random.default_rng(0).permutation(M)
+    qp, ap = prism.prism_quant_act(dev_bf16(xb[perm]))
+    o, _ = gpu_linear(qp, ap, W, S, dev_bf16(rb[perm]), acc=False)
+    assert np.array_equal(host_bits(o), base[perm])
+    # unrelated extra rows added to the batch change nothing
+    xe, _, _, re_ = random_problem(300, N, K, 99)
+    xa = np.concatenate([xe[:150], xb, xe[150:]])
+    ra = np.concatenate([re_[:150], rb, re_[150:]])
+    qa, aa = prism.prism_quant_act(dev_bf16(xa))
+    o, _ = gpu_linear(qa, aa, W, S, dev_bf16(ra), acc=False)
+    assert np.array_equal(host_bits(o)[150:150 + M], base)
+
+
+def test_decode_rows_invariant_across_m_and_split(cuda_device):
+    c = wl.make_linear("decode_m64_k17408_n5120")
+    W, S = dev(c.w), dev(c.w_scale)
+    inv = dev(c.inv_s)
+    ref = None
+    for M in wl.DECODE_M:
+        q, a = prism.prism_quant_act(dev_bf16(c.x_bits[:M]), inv)
+        R = dev_bf16(c.residual_bits[:M])
+        for split in wl.DECODE_SPLITS:
+            o, _ = gpu_linear(q, a, W, S, R, split=split, acc=False)
+            o = host_bits(o)
+            if ref is None:
+                ref = {}
+            for m in range(M):
+                if m in ref:
+                    assert np.array_equal(o[m], ref[m]), (M, split, m)
+                else:
+                    ref[m] = o[m]
+    # and the rows match the oracle on sampled output channels
+    cols = np.random.default_rng(1).choice(c.N, 384, replace=False)
+    qo, ao = oracle.quant_act(c.x_bits, c.inv_s)
+    outo, _ = oracle.w8a8_linear(qo, ao, c.w[cols], c.w_scale[cols], c.residual_bits[:, cols])
+    got = np.stack([ref[m] for m in range(64)])
+    assert np.array_equal(got[:, cols], outo)
+
+
+@pytest.mark.parametrize("name", ["forest_qkv_m304_k5120_n15360", "forest_oproj_m304_k5120_n5120",
+                                  "load_gateup_m2048_k5120_n34816", "load_down_m2048_k17408_n5120",
+                                  "long_m8192_k5120_n5120"])
+def test_full_size_sampled_parity(cuda_device, name):
+    """Full-size call in the benchmark's launch configuration (automatic
+    split-K); sampled rows and output channels checked against the oracle,
+    which computes them one by one."""
+    c = wl.make_linear(name)
+    q, a = prism.prism_quant_act(dev_bf16(c.x_bits), dev(c.inv_s))
+    R = None if c.residual_bits is None else dev_bf16(c.residual_bits)
+    out, _ = gpu_linear(q, a, dev(c.w), dev(c.w_scale), R, acc=False)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, c.M - 1], rng.choice(c.M, 6, replace=False)]))
+    cols = np.unique(np.concatenate([[0, c.N - 1], rng.choice(c.N, 250, replace=False)]))
+    qo, ao = oracle.quant_act(c.x_bits[rows], c.inv_s)
+    assert np.array_equal(host(q)[rows], qo) and np.array_equal(host(a)[rows], ao)
+    rr = None if c.residual_bits is None else c.residual_bits[rows][:, cols]
+    outo, _ = oracle.w8a8_linear(qo, ao, c.w[cols], c.w_scale[cols], rr)
+    assert np.array_equal(host_bits(out)[rows][:, cols], outo)

@@ -52,8 +52,11 @@ def draw_weights(rng: np.random.Generator, shape, dist: str) -> np.ndarray:
     if dist == "uniform":
         return rng.integers(-127, 128, size=shape, dtype=np.int8)
     if dist == "normal":
-        g = rng.standard_normal(shape, dtype=np.float32) * np.float32(40.0)
-        return np.clip(np.rint(g), -127, 127).astype(np.int8)
+        g = rng.standard_normal(shape, dtype=np.float32)
+        g *= np.float32(40.0)
+        np.rint(g, out=g)
+        np.clip(g, -127, 127, out=g)
+        return g.astype(np.int8)
     raise ValueError(dist)
 
 
