@@ -14,10 +14,10 @@ size 5120.  One step is one pass of the whole hot path:
 The metric is int8 tensor operations per second (2*M*N*K per linear plus the
 read-out's candidate dot products) over the whole step.
 
-Timing: W warm-up steps, then exactly K steps captured as one CUDA graph and
-replayed once between CUDA events (device-resident inputs).  Three weight
+Timing: W warm-up steps, then exactly K steps of direct C-ABI launches on one
+stream between CUDA events (device-resident inputs).  Three weight
 sets are rotated so every weight byte comes from HBM (3 x 105 MB > 2 x L2).
-CUDA events around every QKV launch (inside the graph) give the dominant
+CUDA events around every QKV launch give the dominant
 kernel's average duration for the roofline.  nvidia-smi samples SM clocks
 during the timed region.  The e2e figure repeats the step through the Python
 binding with the step's inputs copied from pinned host memory and the
@@ -203,7 +203,7 @@ def run_cpu_baseline(work: Workload, budget_s: float = 12.0):
     import oracle
     cores = host_cores()
     oracle.set_threads(cores)
-    rows = sample_rows(32)
+    rows = sample_rows(96)
     t0 = time.perf_counter()
     ops, outs = cpu_oracle_step(work, rows)
     dt = time.perf_counter() - t0
@@ -310,54 +310,58 @@ def run_gpu(args):
     hid = H[ANSWER_ROWS[0]::16]
     assert hid.shape[0] == len(ANSWER_ROWS)
 
+    import ctypes
+    L = prism.lib()
+    vp = lambda x: ctypes.c_void_p(x.data_ptr()) if x is not None else None
+    stream = torch.cuda.Stream(device=dev)
+    st = ctypes.c_void_p(stream.cuda_stream)
+    wsq_b = 0 if ws_q is None else ws_q.numel()
+    wso_b = 0 if ws_o is None else ws_o.numel()
+    Nq, No, T_ = work.qkv.N, work.o.N, int(T)
+
+    def calls_for(s):
+        """The five C-ABI calls of one step, arguments marshalled once."""
+        return [
+            (L.prism_quant_act, (vp(X), K, vp(s["iq"]), M, K, vp(q1), K, vp(a1), st)),
+            (L.prism_w8a8_linear, (vp(q1), K, vp(a1), vp(s["wq"]), K, vp(s["sq"]), None, 0, vp(Y), Nq,
+                                   None, M, Nq, K, 0, vp(ws_q), wsq_b, st)),
+            (L.prism_quant_act, (vp(Xo), K, vp(s["io"]), M, K, vp(q2), K, vp(a2), st)),
+            (L.prism_w8a8_linear, (vp(q2), K, vp(a2), vp(s["wo"]), K, vp(s["so"]), vp(Res), No, vp(H), No,
+                                   None, M, No, K, 0, vp(ws_o), wso_b, st)),
+            (L.prism_candidate_readout, (vp(hid), hid.stride(0), None, vp(lm_head), K, vp(lm_scale),
+                                         wl.VOCAB, K, vp(off), vp(ids), len(ANSWER_ROWS), T_, vp(logits),
+                                         vp(probs), vp(err), st)),
+        ]
+
+    rot_calls = [calls_for(s) for s in sets]
+
     def step(i, ev=None):
-        s = sets[i % N_ROTATE]
-        prism.prism_quant_act(X, s["iq"], q=q1, a_scale=a1)
-        if ev is not None:
-            ev[0].record()
-        prism.prism_w8a8_linear(q1, a1, s["wq"], s["sq"], out=Y, workspace=ws_q)
-        if ev is not None:
-            ev[1].record()
-        prism.prism_quant_act(Xo, s["io"], q=q2, a_scale=a2)
-        prism.prism_w8a8_linear(q2, a2, s["wo"], s["so"], residual=Res, out=H, workspace=ws_o)
-        prism.prism_candidate_readout(hid, None, lm_head, lm_scale, off, ids, logits=logits,
-                                      probs=probs, err=err)
+        for j, (fn, a) in enumerate(rot_calls[i % N_ROTATE]):
+            if ev is not None and j == 1:
+                ev[0].record(stream)
+            rc = fn(*a)
+            if rc != 0:
+                raise RuntimeError(f"{fn.__name__} failed with status {rc}")
+            if ev is not None and j == 1:
+                ev[1].record(stream)
 
     launches_per_step = 5
-    stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, N_ROTATE)):
-            step(i)
+    for i in range(max(args.warmup, N_ROTATE)):
+        step(i)
     torch.cuda.synchronize()
 
-    use_graph = not args.no_graph
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    graph = None
-    if use_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(args.steps):
-                step(i, evs[i])
-        torch.cuda.synchronize()
-        # warm the graph itself (first replay uploads it)
-        graph.replay()
-        torch.cuda.synchronize()
-
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            start.record()
-            if use_graph:
-                graph.replay()
-            else:
-                for i in range(args.steps):
-                    step(i, evs[i])
-            end.record()
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -387,12 +391,18 @@ def run_gpu(args):
     d2h = hlog.numel() * 4 + hpro.numel() * 4
 
     def e2e_step(i):
+        sset = sets[i % N_ROTATE]
         X.copy_(hX, non_blocking=True)
         Xo.copy_(hXo, non_blocking=True)
         Res.copy_(hRes, non_blocking=True)
         off.copy_(hoff, non_blocking=True)
         ids.copy_(hids, non_blocking=True)
-        step(i)
+        prism.prism_quant_act(X, sset["iq"], q=q1, a_scale=a1)
+        prism.prism_w8a8_linear(q1, a1, sset["wq"], sset["sq"], out=Y, workspace=ws_q)
+        prism.prism_quant_act(Xo, sset["io"], q=q2, a_scale=a2)
+        prism.prism_w8a8_linear(q2, a2, sset["wo"], sset["so"], residual=Res, out=H, workspace=ws_o)
+        prism.prism_candidate_readout(hid, None, lm_head, lm_scale, off, ids, logits=logits,
+                                      probs=probs, err=err)
         hlog.copy_(logits, non_blocking=True)
         hpro.copy_(probs, non_blocking=True)
 
@@ -439,7 +449,7 @@ def run_gpu(args):
                    "global_batch_rows": M * world, "split_k": {"qkv": split_q, "o_proj": split_o},
                    "l2": f"inputs larger than L2: {N_ROTATE} rotated weight sets "
                          f"({N_ROTATE * (work.qkv.N + work.o.N) * K / 1e6:.0f} MB) + 1.27 GB LM head",
-                   "graph": use_graph,
+                   "launch": "direct C-ABI calls, arguments marshalled once",
                    "step_gbs": work.bytes * args.steps * world / secs / 1e9},
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -473,7 +483,6 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-graph", action="store_true", help="launch steps directly instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -111,6 +111,7 @@ struct LinearArgs {
   int32_t* acc_out;
   int64_t M, N, K;
   int split;
+  int pair_io;          // 1: out/residual rows allow 4-byte bf16 pairs
   int32_t* ws_acc;      // [M, N] int32, zero between calls (split > 1)
   uint32_t* ws_count;   // [tiles] arrival counters, zero between calls
 };

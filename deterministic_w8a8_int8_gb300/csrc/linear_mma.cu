@@ -40,6 +40,21 @@ __device__ __forceinline__ void store_pair(const LinearArgs& a, int64_t row, int
                                            int32_t v1) {
   const float as = __ldg(a.a_scale + row);
   const bool two = col + 1 < a.N;
+  if (!a.pair_io) {  // odd row strides or 2-byte-aligned bases: element stores
+    const float as1 = __ldg(a.a_scale + row);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if (e == 1 && !two) break;
+      const int32_t v = e ? v1 : v0;
+      const float ws1 = __ldg(a.w_scale + col + e);
+      const uint32_t o = a.residual != nullptr
+                             ? epilogue_bf16_res(v, as1, ws1, bf16_bits_to_float(a.residual[row * a.ldr + col + e]))
+                             : epilogue_bf16(v, as1, ws1);
+      a.out[row * a.ldo + col + e] = static_cast<uint16_t>(o);
+      if (a.acc_out != nullptr) a.acc_out[row * a.N + col + e] = v;
+    }
+    return;
+  }
   const float w0 = __ldg(a.w_scale + col);
   const float w1 = two ? __ldg(a.w_scale + col + 1) : 0.0f;
   uint32_t o0, o1 = 0;

@@ -94,12 +94,11 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
   if (ldq < K || ldw < K || ldo < N || (residual_bf16 != nullptr && ldr < N)) return PRISM_ERR_INVALID_ARG;
   if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
   if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
-  if (ldq % 16 != 0 || ldw % 16 != 0 || ldo % 8 != 0) return PRISM_ERR_ALIGNMENT;
-  if (residual_bf16 != nullptr && ldr % 8 != 0) return PRISM_ERR_ALIGNMENT;
-  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(out_bf16, 16) || !aligned(a_scale, 4) ||
+  if (ldq % 16 != 0 || ldw % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(out_bf16, 2) || !aligned(a_scale, 4) ||
       !aligned(w_scale, 4))
     return PRISM_ERR_ALIGNMENT;
-  if (residual_bf16 != nullptr && !aligned(residual_bf16, 16)) return PRISM_ERR_ALIGNMENT;
+  if (residual_bf16 != nullptr && !aligned(residual_bf16, 2)) return PRISM_ERR_ALIGNMENT;
   if (acc_out != nullptr && !aligned(acc_out, 4)) return PRISM_ERR_ALIGNMENT;
   if (M > 65535LL * 128 || N > (1LL << 31) * 64) return PRISM_ERR_UNSUPPORTED;
 
@@ -121,6 +120,8 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
   a.N = N;
   a.K = K;
   a.split = split;
+  a.pair_io = aligned(out_bf16, 4) && ldo % 2 == 0 &&
+              (residual_bf16 == nullptr || (aligned(residual_bf16, 4) && ldr % 2 == 0));
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need) return PRISM_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return PRISM_ERR_ALIGNMENT;

@@ -126,8 +126,10 @@ size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
  *                  calls.  Calls sharing a workspace must not overlap in time
  *                  (use one stream, or one workspace per stream).  May be NULL
  *                  when the required size is 0.
- * Alignment: q, w, residual, out 16-byte aligned; ldq, ldw % 16 == 0;
- * ldr, ldo % 8 == 0; K % 16 == 0.  M == 0 or N == 0 enqueues nothing.
+ * Alignment: q, w 16-byte aligned with ldq, ldw % 16 == 0 and K % 16 == 0;
+ * residual and out need only bf16 (2-byte) alignment and any ldr, ldo >= N
+ * (even strides on 4-byte-aligned bases take a faster paired store).
+ * M == 0 or N == 0 enqueues nothing.
  */
 int prism_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
                       const int8_t *w, int64_t ldw, const float *w_scale,

@@ -101,10 +101,9 @@ def test_linear_validation(L):
     assert lin(L, ldq=32) == -1 and lin(L, ldo=32) == -1
     assert lin(L, res=A, ldr=32) == -1
     assert lin(L, K=72, ldq=80, ldw=80) == -2
-    assert lin(L, ldq=72) == -2 and lin(L, ldw=72) == -2 and lin(L, ldo=68) == -2
-    assert lin(L, res=A, ldr=68) == -2
-    assert lin(L, q=A + 8) == -2 and lin(L, w=A + 8) == -2 and lin(L, out=A + 4) == -2
-    assert lin(L, res=A + 4, ldr=64) == -2 and lin(L, a=A + 2) == -2
+    assert lin(L, ldq=72) == -2 and lin(L, ldw=72) == -2
+    assert lin(L, q=A + 8) == -2 and lin(L, w=A + 8) == -2 and lin(L, out=A + 1) == -2
+    assert lin(L, res=A + 1, ldr=64) == -2 and lin(L, a=A + 2) == -2
     assert lin(L, acc=A + 2) == -2
     K = 133152
     assert lin(L, K=K) == -3

@@ -57,11 +57,12 @@ def test_tiny_config_end_to_end(cuda_device):
 @pytest.mark.parametrize("M,N,K", [(1, 8, 16), (3, 130, 48), (129, 384, 256), (37, 131, 64),
                                    (130, 257, 528), (255, 136, 1040), (1, 1, 16)])
 @pytest.mark.parametrize("residual", [True, False])
-def test_ragged_shapes(cuda_device, M, N, K, residual):
+@pytest.mark.parametrize("ld_pad", [8, 1])
+def test_ragged_shapes(cuda_device, M, N, K, residual, ld_pad):
     xb, w, w_scale, rb = random_problem(M, N, K, M * 131 + N * 7 + K, residual)
     _, _, outo, acco = oracle_full(xb, None, w, w_scale, rb)
     q, a = prism.prism_quant_act(dev_bf16(xb))
-    ld = (N + 7) // 8 * 8 + 8
+    ld = (N + 7) // 8 * 8 + 8 if ld_pad == 8 else N + 1
     r = None
     if residual:
         r = padded(M, N, ld, torch.bfloat16)
