@@ -32,6 +32,7 @@ PRISM_MAX_K = 133144
 PRISM_MAX_SPLIT_K = 64
 PRISM_MAX_CANDIDATES = 64
 PRISM_MAX_READOUT_K = 65536
+PRISM_NOALLOC_SCRATCH_BYTES = 8388608
 PRISM_DEV_ERR_OFFSETS = 1
 PRISM_DEV_ERR_COUNT = 2
 PRISM_DEV_ERR_ID_RANGE = 4
@@ -44,6 +45,8 @@ SIGNATURES = {
     "prism_w8a8_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
     "prism_w8a8_linear": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _P, _I64, _P,
                                  _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "prism_w8a8_linear_noalloc": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _P, _I64, _P,
+                                         _I64, _I64, _I64, _I32, _P]),
     "prism_candidate_readout": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _P, _P,
                                        _I64, _I64, _P, _P, _P, _P]),
     "prism_status_string": (ctypes.c_char_p, [_I32]),
@@ -195,6 +198,33 @@ def prism_w8a8_linear(q, a_scale, w, w_scale, residual=None, out=None, acc_out=N
         _ptr(residual), 0 if residual is None else residual.stride(0), _ptr(out), out.stride(0),
         _ptr(acc_out), M, N, K, int(split_k), _ptr(workspace), ws_bytes, _stream(stream))
     _check("prism_w8a8_linear", st)
+    return out
+
+
+def prism_w8a8_linear_noalloc(q, a_scale, w, w_scale, residual=None, out=None, acc_out=None,
+                              split_k: int = 0, stream=None):
+    """prism_w8a8_linear for callers that cannot supply scratch memory: split-K
+    scratch comes from a fixed array inside the library (see include/prism.h
+    for its size limit and the rule that overlapping calls must not share it)."""
+    import torch
+    _require(q, torch.int8, "q", 2)
+    _require(w, torch.int8, "w", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    _require(w_scale, torch.float32, "w_scale", 1)
+    M, K = q.shape
+    N = w.shape[0]
+    if w.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if residual is not None:
+        _require(residual, torch.bfloat16, "residual", 2)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
+    _require(out, torch.bfloat16, "out", 2)
+    st = lib().prism_w8a8_linear_noalloc(
+        _ptr(q), q.stride(0), _ptr(a_scale), _ptr(w), w.stride(0), _ptr(w_scale),
+        _ptr(residual), 0 if residual is None else residual.stride(0), _ptr(out), out.stride(0),
+        _ptr(acc_out), M, N, K, int(split_k), _stream(stream))
+    _check("prism_w8a8_linear_noalloc", st)
     return out
 
 

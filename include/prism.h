@@ -138,6 +138,40 @@ int prism_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
                       int64_t K, int split_k, void *workspace,
                       size_t workspace_bytes, void *cuda_stream);
 
+/* Size of the fixed scratch array compiled into libprism.so for
+ * prism_w8a8_linear_noalloc.  Every GPU that loads the library reserves it
+ * until the process exits. */
+#define PRISM_NOALLOC_SCRATCH_BYTES 8388608
+
+/*
+ * prism_w8a8_linear_noalloc -- prism_w8a8_linear without a workspace argument.
+ * The pages describe no such call; it exists for callers that cannot provide
+ * device scratch memory: a plugin host that hands the library only its own
+ * input and output buffers, a latency-critical loop that must not call
+ * cudaMalloc (which can synchronise the whole device), or a process whose
+ * device memory budget is fixed up front.
+ *
+ * Arguments, layouts, alignment and results are exactly those of
+ * prism_w8a8_linear (bit-identical outputs), minus workspace and
+ * workspace_bytes.  Split-K scratch comes from a fixed array of
+ * PRISM_NOALLOC_SCRATCH_BYTES inside the library; the call allocates nothing.
+ *   - Shapes whose split-K scratch exceeds that size (about 4*M*N bytes when
+ *     split_k > 1; split_k = 1 needs none) return PRISM_ERR_UNSUPPORTED and
+ *     enqueue nothing.
+ *   - All calls on one device share the array.  Each call zeroes the part it
+ *     uses on its own stream before computing, but calls that overlap on the
+ *     GPU (other streams, unordered host threads) race on it: order them on
+ *     one stream.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ */
+int prism_w8a8_linear_noalloc(const int8_t *q, int64_t ldq, const float *a_scale,
+                              const int8_t *w, int64_t ldw, const float *w_scale,
+                              const void *residual_bf16, int64_t ldr,
+                              void *out_bf16, int64_t ldo, int32_t *acc_out,
+                              int64_t M, int64_t N, int64_t K, int split_k,
+                              void *cuda_stream);
+
 /*
  * prism_candidate_readout -- logits and probabilities for the candidate
  * tokens of each answer position only; the softmax runs over the candidates
