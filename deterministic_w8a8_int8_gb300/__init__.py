@@ -53,6 +53,7 @@ SIGNATURES = {
     "prism_version": (_I32, []),
     "prism_w8a8_kernel_kind": (_I32, [_I64, _I64, _I64]),
     "prism_w8a8_auto_split": (_I32, [_I64, _I64, _I64]),
+    "prism_device_status": (_I32, [_P]),
 }
 
 _lock = threading.Lock()
@@ -129,6 +130,13 @@ def prism_w8a8_kernel_kind(M: int, N: int, K: int) -> int:
 
 def prism_w8a8_auto_split(M: int, N: int, K: int) -> int:
     return int(lib().prism_w8a8_auto_split(M, N, K))
+
+
+def prism_device_status() -> int:
+    """Device error bits raised since the last query (0 = none); synchronous."""
+    v = ctypes.c_uint32(0)
+    _check("prism_device_status", lib().prism_device_status(ctypes.byref(v)))
+    return int(v.value)
 
 
 def prism_version() -> int:

@@ -116,9 +116,15 @@ struct LinearArgs {
   uint32_t* ws_count;   // [tiles] arrival counters, zero between calls
 };
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
+// Dispatch between the two contraction kernels (linear_tc.cu): the tcgen05
+// kernel by default; PRISM_LINEAR_PATH=mma selects the mma.sync s8 kernel.
 int linear_kernel_kind(int64_t M, int64_t N, int64_t K);
 int linear_auto_split(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream);
+int mma_auto_split(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream);
+// Sticky device error bits raised by kernels (bounded waits that expired).
+cudaError_t read_and_clear_kernel_error(uint32_t* out);
 
 cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const int8_t* W,
                            int64_t ldw, const float* lm_scale, int64_t V, int64_t K,

@@ -236,13 +236,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 }  // namespace
 
-int linear_kernel_kind(int64_t M, int64_t N, int64_t K) {
-  (void)K;
-  if (M <= 0 || N <= 0) return 0;
-  return 1;
-}
-
-int linear_auto_split(int64_t M, int64_t N, int64_t K) {
+int mma_auto_split(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0) return 1;
   const int64_t tiles = cdiv(M, kBM) * cdiv(N, kBN);
   const int64_t ktiles = cdiv(K, kBK);
@@ -260,7 +254,7 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
   return align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 4) + align256(tiles * 4);
 }
 
-cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream) {
+cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(linear_mma_kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(cdiv(a.N, kBN)), static_cast<unsigned>(cdiv(a.M, kBM)),

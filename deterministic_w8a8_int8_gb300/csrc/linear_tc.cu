@@ -1,0 +1,597 @@
+// linear_tc.cu -- W8A8 linear on the 5th-generation tensor cores (tcgen05).
+//
+// acc[m,n] = sum_k q[m,k] * w[n,k], exact int32, then the fixed-order
+// epilogue y = bf16_rne(((float(acc) * a_scale[m]) * w_scale[n]) + r[m,n])
+// (StartLux-Prism, "Bitwise consistency is not lossless quantization").
+//
+// sm_103a has no integer tcgen05 MMA, and its legacy int8 mma.sync pipe is
+// slow, so the contraction runs on the f16 tensor pipe with exact arithmetic:
+//   * every int8 value is exactly representable in f16 (11-bit significand);
+//   * every product |q*w| <= 127*127 = 16129 is exact in the fp32 accumulator;
+//   * a chunk of at most 1024 K-elements keeps every partial sum of products
+//     below 1024 * 16129 < 2^24, so each fp32 partial is an exact integer no
+//     matter in which order the tensor core adds the terms.
+// The fp32 accumulator D lives in tensor memory (TMEM).  After each chunk the
+// drain warps read D, convert it to int32 (exact) and add it into a second
+// TMEM region I holding the int32 running sum; integer addition makes the
+// result independent of chunking, tiling and split-K.
+//
+// CTA roles (416 threads, one CTA per SM):
+//   warps 0-3   drain + epilogue; warp w owns TMEM lanes 32w..32w+31 (one
+//               A-tile row per thread);
+//   warp 4      TMEM allocator; lane 0 issues every tcgen05.mma;
+//   warps 5-12  converters: 16-byte global loads of int8 A/B rows (a register
+//               ring two stages ahead), exact int8->f16 widening, stores into
+//               128-byte-swizzled K-major shared-memory tiles.
+// Pipeline: 4 shared-memory stages of 64 K-elements (A 128 rows, B up to 256
+// rows, f16).  mbarriers: full[s] (256 converter arrivals), empty[s] and
+// acc_full (tcgen05.commit), acc_empty (128 drain arrivals).  Every wait is
+// bounded by a 2-second global-timer limit; on expiry the CTA records
+// kDevErrTimeout in the library's device error word and winds down.
+//
+// Two orientations:
+//   normal (many rows)  A = q rows (tokens, 128 per tile), B = w rows
+//                       (256 output channels per tile);
+//   swapped (few rows)  A = w rows (128 channels), B = q rows (the tokens, one
+//                       piece of up to 256), so small batches still fill the
+//                       128-row MMA.
+// Split-K reuses the integer-atomic / last-arriver protocol of the workspace.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace prism {
+
+__device__ uint32_t g_kernel_error = 0;
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBM = 128;                  // A rows per tile = TMEM lanes
+constexpr int kBNMax = 256;               // max B rows per tile = MMA N
+constexpr int kBK = 64;                   // K elements per stage (128 B of f16 per row)
+constexpr int kChunkStages = 16;          // 16 * 64 = 1024 K per exact fp32 chunk
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kDrainThreads = 128;
+constexpr int kThreads = kDrainThreads + 32 + kConvThreads;  // 416
+constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
+constexpr int kStageB = kBNMax * 128;     // bytes of one f16 B stage
+constexpr int kBarBytes = 256;
+constexpr int kSmemBytes = 1024 + kStages * (kStageA + kStageB) + kBarBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColD = 0;             // fp32 chunk accumulator
+constexpr uint32_t kColI = 256;           // int32 running sum
+constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kConvThreads;  // 6 x 16 B per stage
+constexpr int kPrefetch = 2;              // register ring depth (stages)
+constexpr uint32_t kDevErrTimeout = 1u;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+struct TcParams {
+  LinearArgs a;
+  int swap;      // 0 normal, 1 swapped
+  int bpiece;    // B rows per tile (multiple of 32, <= 256)
+  int vec_io;    // 16-byte vector epilogue loads/stores allowed (normal orientation)
+};
+
+// ------------------------------------------------------------ PTX helpers --
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: true when the phase completed; false on timeout or when
+// another thread of the CTA has already given up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(&g_kernel_error, kDevErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (stride between atoms = 1024 B), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused here), 16 B
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;             // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: f16 x f16 -> f32, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_f16_f32(int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+// Exact int8 -> f16 widening of 4 packed bytes: bias to u = b + 128 in
+// [1, 255], place each byte under the f16 pattern of 1024 (0x6400 | u is the
+// f16 of 1024 + u), subtract 1152 (0x6480) exactly.
+__device__ __forceinline__ void widen4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = x ^ 0x80808080u;
+  uint32_t p0, p1;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(p0) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(p1) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(p0), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(p1), "r"(0x64806480u));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// --------------------------------------------------------------- epilogue --
+__device__ __forceinline__ void emit(const LinearArgs& a, int64_t m, int64_t n, int32_t v) {
+  const float as = __ldg(a.a_scale + m);
+  const float ws = __ldg(a.w_scale + n);
+  const uint32_t o = a.residual != nullptr ? epilogue_bf16_res(v, as, ws, bf16_bits_to_float(a.residual[m * a.ldr + n]))
+                                           : epilogue_bf16(v, as, ws);
+  a.out[m * a.ldo + n] = static_cast<uint16_t>(o);
+  if (a.acc_out != nullptr) a.acc_out[m * a.N + n] = v;
+}
+
+// 32 consecutive output channels n0..n0+31 of row m (normal orientation).
+__device__ __forceinline__ void emit_row32(const TcParams& p, int64_t m, int64_t n0, const int32_t (&v)[32]) {
+  const LinearArgs& a = p.a;
+  if (m >= a.M) return;
+  if (p.vec_io && n0 + 32 <= a.N) {
+    const float as = __ldg(a.a_scale + m);
+    uint32_t r[16];
+    if (a.residual != nullptr) {
+      const uint4* rp = reinterpret_cast<const uint4*>(a.residual + m * a.ldr + n0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 t = rp[i];
+        r[4 * i] = t.x;
+        r[4 * i + 1] = t.y;
+        r[4 * i + 2] = t.z;
+        r[4 * i + 3] = t.w;
+      }
+    }
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 w4 = __ldg(reinterpret_cast<const float4*>(a.w_scale + n0) + i);
+      const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int j = 0; j < 4; j += 2) {
+        const int e = 4 * i + j;
+        uint32_t lo, hi;
+        if (a.residual != nullptr) {
+          lo = epilogue_bf16_res(v[e], as, wv[j], bf16_lo(r[e >> 1]));
+          hi = epilogue_bf16_res(v[e + 1], as, wv[j + 1], bf16_hi(r[e >> 1]));
+        } else {
+          lo = epilogue_bf16(v[e], as, wv[j]);
+          hi = epilogue_bf16(v[e + 1], as, wv[j + 1]);
+        }
+        o[e >> 1] = lo | (hi << 16);
+      }
+    }
+    uint4* op = reinterpret_cast<uint4*>(a.out + m * a.ldo + n0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) op[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    if (a.acc_out != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a.acc_out[m * a.N + n0 + j] = v[j];
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (n0 + j < a.N) emit(a, m, n0 + j, v[j]);
+}
+
+// ------------------------------------------------------------------ kernel --
+__global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const LinearArgs& a = p.a;
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  const uint32_t sA = base;                                   // kStages x kStageA
+  const uint32_t sB = base + kStages * kStageA;               // kStages x kStageB
+  const uint32_t bars = sB + kStages * kStageB;
+  uint8_t* bar_ptr = smem + (bars - base);
+  const uint32_t bar_full = bars;                             // kStages x 8 B
+  const uint32_t bar_empty = bars + 8 * kStages;
+  const uint32_t bar_acc_full = bars + 16 * kStages;
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  const uint32_t bar_done = bar_acc_full + 16;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_ptr + 16 * kStages + 24);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bar_ptr + 16 * kStages + 28);
+  int* s_last = reinterpret_cast<int*>(bar_ptr + 16 * kStages + 32);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // tile coordinates
+  const int64_t rows_a = p.swap ? a.N : a.M;
+  const int64_t rows_b = p.swap ? a.M : a.N;
+  const int8_t* Am = p.swap ? a.w : a.q;
+  const int8_t* Bm = p.swap ? a.q : a.w;
+  const int64_t lda = p.swap ? a.ldw : a.ldq;
+  const int64_t ldb = p.swap ? a.ldq : a.ldw;
+  const int64_t a0 = static_cast<int64_t>(blockIdx.x) * kBM;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.y) * p.bpiece;
+  const int64_t b_left = rows_b - b0;
+  const int64_t b_round = (b_left + 31) & ~static_cast<int64_t>(31);
+  const int bn = static_cast<int>(b_round < p.bpiece ? b_round : p.bpiece);
+  const int64_t ktiles = (a.K + kBK - 1) / kBK;
+  const int64_t per = (ktiles + a.split - 1) / a.split;
+  const int64_t kt0 = static_cast<int64_t>(blockIdx.z) * per;
+  const int64_t kt1 = kt0 + per < ktiles ? kt0 + per : ktiles;
+  const int nk = kt1 > kt0 ? static_cast<int>(kt1 - kt0) : 0;
+  const int nchunks = (nk + kChunkStages - 1) / kChunkStages;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, kConvThreads);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, kDrainThreads);
+    mbar_init(bar_done, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 4) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp < 4) {
+    // ======================= drain + epilogue (128 threads) =================
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int64_t arow = a0 + warp * 32 + lane;  // this thread's A-tile row
+    const int ncb = bn / 32;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_acc_full, c & 1, s_abort));
+      if (!ok) break;
+      tc_fence_after();
+      const bool last = c == nchunks - 1;
+      for (int cb = 0; cb < ncb; ++cb) {
+        uint32_t d[32], iv[32];
+        tmem_ld32(tmem + lane_base + kColD + cb * 32, d);
+        if (c > 0) tmem_ld32(tmem + lane_base + kColI + cb * 32, iv);
+        tmem_wait_ld();
+        int32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          v[j] = (c > 0 ? static_cast<int32_t>(iv[j]) : 0) + __float2int_rn(__uint_as_float(d[j]));
+        if (!last) {
+          uint32_t u[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) u[j] = static_cast<uint32_t>(v[j]);
+          tmem_st32(tmem + lane_base + kColI + cb * 32, u);
+        } else if (a.split == 1) {
+          if (!p.swap) {
+            emit_row32(p, arow, b0 + cb * 32, v);
+          } else if (arow < a.N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int64_t m = b0 + cb * 32 + j;
+              if (m < a.M) emit(a, m, arow, v[j]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t m = p.swap ? b0 + cb * 32 + j : arow;
+            const int64_t n = p.swap ? arow : b0 + cb * 32 + j;
+            if (m < a.M && n < a.N) atomicAdd(a.ws_acc + m * a.N + n, v[j]);
+          }
+        }
+      }
+      if (!last) {
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_acc_empty);
+      }
+    }
+    if (a.split > 1) {
+      // integer split-K: the last CTA to finish this tile applies the epilogue
+      __threadfence();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
+      if (tid == 0) *s_last = (atomicAdd(a.ws_count + tile, 1u) == static_cast<unsigned>(a.split - 1));
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (*s_last) {
+        __threadfence();
+        for (int cb = 0; cb < ncb; ++cb) {
+          for (int j = 0; j < 32; ++j) {
+            const int64_t m = p.swap ? b0 + cb * 32 + j : arow;
+            const int64_t n = p.swap ? arow : b0 + cb * 32 + j;
+            if (m < a.M && n < a.N) {
+              int32_t* wp = a.ws_acc + m * a.N + n;
+              const int32_t v = __ldcg(wp);
+              __stcg(wp, 0);
+              emit(a, m, n, v);
+            }
+          }
+        }
+        if (tid == 0) a.ws_count[tile] = 0u;
+      }
+    }
+  } else if (warp == 4) {
+    // ======================= MMA issuer (one thread) =========================
+    if (lane == 0 && nk > 0) {
+      const uint32_t idesc = idesc_f16_f32(bn);
+      for (int it = 0; it < nk; ++it) {
+        const int s = it % kStages;
+        const int cpos = it % kChunkStages;
+        if (cpos == 0 && it > 0) {
+          if (!mbar_wait(bar_acc_empty, ((it / kChunkStages) - 1) & 1, s_abort)) break;
+          tc_fence_after();
+        }
+        if (!mbar_wait(bar_full + 8 * s, (it / kStages) & 1, s_abort)) break;
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(sA + s * kStageA);
+        const uint64_t bd = smem_desc_sw128(sB + s * kStageB);
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          tc_mma(tmem + kColD, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
+        tc_commit(bar_empty + 8 * s);
+        if (cpos == kChunkStages - 1 || it == nk - 1) tc_commit(bar_acc_full);
+      }
+      // every MMA issued above has completed before TMEM is released
+      tc_commit(bar_done);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(bar_done, 0)) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          atomicOr(&g_kernel_error, kDevErrTimeout);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ======================= converters (256 threads) ========================
+    const int ct = tid - (kDrainThreads + 32);
+    const int segs = (kBM + bn) * 4;  // 16-byte int8 segments per stage
+    uint4 ring[kPrefetch][kSegPerThread];
+
+    auto load_stage = [&](int it, uint4 (&buf)[kSegPerThread]) {
+      const int64_t kb = (kt0 + it) * kBK;
+#pragma unroll
+      for (int i = 0; i < kSegPerThread; ++i) {
+        const int g = ct + i * kConvThreads;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (g < segs) {
+          const int r = g >> 2;
+          const int64_t k = kb + (g & 3) * 16;
+          if (r < kBM) {
+            const int64_t row = a0 + r;
+            if (row < rows_a && k < a.K) v = ld_stream_16(Am + row * lda + k);
+          } else {
+            const int64_t row = b0 + (r - kBM);
+            if (row < rows_b && k < a.K) v = ld_stream_16(Bm + row * ldb + k);
+          }
+        }
+        buf[i] = v;
+      }
+    };
+    auto store_stage = [&](int s, const uint4 (&buf)[kSegPerThread]) {
+#pragma unroll
+      for (int i = 0; i < kSegPerThread; ++i) {
+        const int g = ct + i * kConvThreads;
+        if (g < segs) {
+          const int r = g >> 2;
+          const int seg = g & 3;
+          const uint32_t tile = r < kBM ? sA + s * kStageA : sB + s * kStageB;
+          const int rr = r < kBM ? r : r - kBM;
+          const uint32_t row_addr = tile + rr * 128;
+          uint32_t w[8];
+          widen4(buf[i].x, w[0], w[1]);
+          widen4(buf[i].y, w[2], w[3]);
+          widen4(buf[i].z, w[4], w[5]);
+          widen4(buf[i].w, w[6], w[7]);
+          const int c0 = (2 * seg) ^ (rr & 7);
+          const int c1 = (2 * seg + 1) ^ (rr & 7);
+          st_shared_v4(row_addr + c0 * 16, w[0], w[1], w[2], w[3]);
+          st_shared_v4(row_addr + c1 * 16, w[4], w[5], w[6], w[7]);
+        }
+      }
+    };
+
+#pragma unroll
+    for (int pf = 0; pf < kPrefetch; ++pf)
+      if (pf < nk) load_stage(pf, ring[pf]);
+    bool ok = true;
+    for (int it0 = 0; it0 < nk && ok; it0 += kPrefetch) {
+#pragma unroll
+      for (int pf = 0; pf < kPrefetch; ++pf) {
+        const int it = it0 + pf;
+        if (it < nk && ok) {
+          const int s = it % kStages;
+          if (!mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort)) {
+            ok = false;
+          } else {
+            store_stage(s, ring[pf]);
+            fence_proxy_async();
+            mbar_arrive(bar_full + 8 * s);
+            if (it + kPrefetch < nk) load_stage(it + kPrefetch, ring[pf]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every role has finished its (bounded) work
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+inline int64_t cdiv(int64_t x, int64_t y) { return (x + y - 1) / y; }
+
+}  // namespace
+
+// Plan for the tensor-core path: orientation, B-piece width and the automatic
+// split.  Few rows (M < 512) use the swapped orientation with the tokens as
+// the MMA's N side; otherwise tokens fill the 128-row side.
+struct TcPlan {
+  int swap;
+  int bpiece;
+  int64_t grid_x, grid_y;
+};
+
+static TcPlan tc_plan(int64_t M, int64_t N) {
+  TcPlan pl{};
+  pl.swap = M < 512 ? 1 : 0;
+  if (pl.swap) {
+    pl.bpiece = 256;
+    pl.grid_x = cdiv(N, kBM);
+    pl.grid_y = cdiv(M, 256);
+  } else {
+    pl.bpiece = 256;
+    pl.grid_x = cdiv(M, kBM);
+    pl.grid_y = cdiv(N, 256);
+  }
+  return pl;
+}
+
+static int tc_auto_split(int64_t M, int64_t N, int64_t K) {
+  const TcPlan pl = tc_plan(M, N);
+  const int64_t tiles = pl.grid_x * pl.grid_y;
+  const int64_t kchunks = cdiv(K, kBK * kChunkStages);
+  if (tiles >= 120) return 1;
+  int64_t s = std::max<int64_t>(1, 152 / tiles);
+  s = std::min<int64_t>(s, std::max<int64_t>(1, cdiv(K, kBK) / 8));
+  (void)kchunks;
+  return static_cast<int>(std::min<int64_t>(s, 16));
+}
+
+static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(linear_tc_kernel), kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const TcPlan pl = tc_plan(a.M, a.N);
+  TcParams p{};
+  p.a = a;
+  p.swap = pl.swap;
+  p.bpiece = pl.bpiece;
+  const uintptr_t ob = reinterpret_cast<uintptr_t>(a.out), rb = reinterpret_cast<uintptr_t>(a.residual);
+  const uintptr_t wb = reinterpret_cast<uintptr_t>(a.w_scale);
+  p.vec_io = (ob % 16 == 0) && (a.ldo % 8 == 0) && (wb % 16 == 0) &&
+             (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
+  dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y), static_cast<unsigned>(a.split));
+  linear_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// PRISM_LINEAR_PATH=mma routes the linear to the mma.sync s8 kernel (a
+// diagnostic for cross-checking the two contraction kernels); read per call.
+static bool use_mma_path() {
+  const char* s = std::getenv("PRISM_LINEAR_PATH");
+  return s != nullptr && std::strcmp(s, "mma") == 0;
+}
+
+int linear_kernel_kind(int64_t M, int64_t N, int64_t K) {
+  (void)K;
+  if (M <= 0 || N <= 0) return 0;
+  if (use_mma_path()) return 1;
+  return tc_plan(M, N).swap ? 3 : 2;
+}
+
+int linear_auto_split(int64_t M, int64_t N, int64_t K) {
+  return use_mma_path() ? mma_auto_split(M, N, K) : tc_auto_split(M, N, K);
+}
+
+cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream) {
+  return use_mma_path() ? launch_linear_mma(a, stream) : launch_linear_tc(a, stream);
+}
+
+cudaError_t read_and_clear_kernel_error(uint32_t* out) {
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_kernel_error, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_kernel_error, &zero, sizeof zero);
+  }
+  *out = v;
+  return e;
+}
+
+}  // namespace prism

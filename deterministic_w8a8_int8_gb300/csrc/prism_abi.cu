@@ -73,6 +73,11 @@ int prism_quant_act(const void* x_bf16, int64_t ldx, const float* inv_smooth, in
 
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K) { return prism::linear_kernel_kind(M, N, K); }
 
+int prism_device_status(uint32_t* flags) {
+  if (flags == nullptr) return PRISM_ERR_INVALID_ARG;
+  return prism::read_and_clear_kernel_error(flags) == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+}
+
 int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K) { return prism::linear_auto_split(M, N, K); }
 
 size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {

@@ -209,13 +209,22 @@ int prism_version(void);
 
 /*
  * Which contraction kernel prism_w8a8_linear would launch for this shape:
- * 0 = none (empty), 1 = tensor-core tile kernel (mma.sync s8),
- * 2 = weight-streaming kernel for few rows.  For tests and benchmarks.
+ * 0 = none (empty); 1 = warp-level mma.sync s8 kernel; 2 = tcgen05 kernel,
+ * tokens on the 128-row MMA side; 3 = tcgen05 kernel, output channels on the
+ * 128-row side and tokens on the N side (few rows).  The tcgen05 kernel is the
+ * default; setting the environment variable PRISM_LINEAR_PATH=mma selects
+ * the mma.sync kernel (a diagnostic; results are bit-identical).
  */
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K);
 
 /* The split-K factor an automatic (split_k = 0) call would use. */
 int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K);
+
+/* Device error bits (PRISM_DEVSTATUS_*) raised by kernels since the last
+ * query, then cleared.  Synchronous: waits for all work on the device.
+ * A nonzero value means some output of that period is invalid. */
+#define PRISM_DEVSTATUS_WAIT_TIMEOUT 1u /* a bounded on-chip wait expired */
+int prism_device_status(uint32_t *flags);
 
 #ifdef __cplusplus
 }

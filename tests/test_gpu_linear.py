@@ -192,3 +192,62 @@ def test_full_size_sampled_parity(cuda_device, name):
     rr = None if c.residual_bits is None else c.residual_bits[rows][:, cols]
     outo, _ = oracle.w8a8_linear(qo, ao, c.w[cols], c.w_scale[cols], rr)
     assert np.array_equal(host_bits(out)[rows][:, cols], outo)
+
+
+def _with_path(path, fn):
+    import os
+    old = os.environ.get("PRISM_LINEAR_PATH")
+    if path == "mma":
+        os.environ["PRISM_LINEAR_PATH"] = "mma"
+    else:
+        os.environ.pop("PRISM_LINEAR_PATH", None)
+    try:
+        return fn()
+    finally:
+        if old is None:
+            os.environ.pop("PRISM_LINEAR_PATH", None)
+        else:
+            os.environ["PRISM_LINEAR_PATH"] = old
+
+
+@pytest.mark.parametrize("M", [5, 130, 600])
+def test_tensor_core_chunks_exact_at_2_pow_24(cuda_device, M):
+    """Every fp32 chunk of <= 1024 products stays an exact integer: all
+    +-127 operands (chunk partials up to 1024 * 16129 = 16,516,096) and single
+    +-1 terms next to near-2^24 partials must come out exact."""
+    K = 4096 + 1024 + 64
+    rng = np.random.default_rng(M)
+    q = np.full((M, K), 127, np.int8)
+    q[1::3] = -127
+    q[2::3, 1023::1024] = 1          # a unit term at the end of every chunk
+    N = 264
+    w = np.where(rng.random((N, K)) < 0.5, 127, -127).astype(np.int8)
+    w[0] = 127
+    w[1] = -127
+    w[2, 1023::1024] = -1
+    w[3, ::2] = 1
+    a = np.ones(M, np.float32)
+    ws = np.ones(N, np.float32)
+    outo, acco = oracle.w8a8_linear(q, a, w, ws, None)
+    assert abs(int(acco[0, 0])) == 127 * 127 * K
+    for split in (1, 3):
+        out, acc = gpu_linear(dev(q), dev(a), dev(w), dev(ws), None, split=split)
+        assert np.array_equal(host(acc), acco)
+        assert np.array_equal(host_bits(out), outo)
+    assert prism.prism_device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(37, 384, 256), (304, 512, 5120), (600, 520, 2064), (64, 1024, 17408)])
+def test_contraction_kernels_agree(cuda_device, M, N, K):
+    """The tcgen05 kernel and the mma.sync s8 kernel give identical bits."""
+    xb, w, w_scale, rb = random_problem(M, N, K, 41 + M)
+    q, a = prism.prism_quant_act(dev_bf16(xb))
+    W, S, R = dev(w), dev(w_scale), dev_bf16(rb)
+    kinds = {p: _with_path(p, lambda: prism.prism_w8a8_kernel_kind(M, N, K)) for p in ("tc", "mma")}
+    assert kinds["mma"] == 1 and kinds["tc"] in (2, 3)
+    outs = {p: _with_path(p, lambda: gpu_linear(q, a, W, S, R)) for p in ("tc", "mma")}
+    assert torch.equal(outs["tc"][1], outs["mma"][1])
+    assert torch.equal(outs["tc"][0].view(torch.int16), outs["mma"][0].view(torch.int16))
+    _, _, outo, _ = oracle_full(xb, None, w, w_scale, rb)
+    assert np.array_equal(host_bits(outs["tc"][0]), outo)
+    assert prism.prism_device_status() == 0
