@@ -477,6 +477,63 @@ def run_gpu(args):
     return 0
 
 
+def run_kernel(args):
+    """Time one contraction call type alone on a named workload case (for
+    per-kernel numbers and focused ncu captures).  Rotates enough weight copies
+    that every launch reads its weights from HBM."""
+    import ctypes
+    import torch
+
+    import deterministic_w8a8_int8_gb300 as prism
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    L = prism.lib()
+    c = wl.make_linear(args.case)
+    M, K, N = c.M, c.K, c.N
+    rows = M if args.rows is None else args.rows
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x = torch.from_numpy(c.x_bits[:rows].view(np.int16)).view(torch.bfloat16).to(dev)
+    inv = t(c.inv_s)
+    q = torch.empty((rows, K), dtype=torch.int8, device=dev)
+    a = torch.empty((rows,), dtype=torch.float32, device=dev)
+    prism.prism_quant_act(x, inv, q=q, a_scale=a)
+    wbytes = N * K
+    n_rot = max(1, int(np.ceil(3 * 129e6 / wbytes)))
+    Ws = [t(c.w) for _ in range(n_rot)]
+    S = t(c.w_scale)
+    R = None if c.residual_bits is None else torch.from_numpy(c.residual_bits[:rows].view(np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
+    split = args.split if args.split is not None else prism.prism_w8a8_auto_split(rows, N, K)
+    ws = prism.new_workspace(rows, N, K, split, dev)
+    stream = torch.cuda.Stream(device=dev)
+    st = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda z: None if z is None else ctypes.c_void_p(z.data_ptr())
+    calls = [(vp(q), K, vp(a), vp(W), K, vp(S), vp(R), N, vp(out), N, None, rows, N, K, split, vp(ws),
+              0 if ws is None else ws.numel(), st) for W in Ws]
+    for i in range(args.warmup):
+        assert L.prism_w8a8_linear(*calls[i % n_rot]) == 0
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        assert L.prism_w8a8_linear(*calls[i % n_rot]) == 0
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+    avg = statistics.mean(us)
+    ops = 2 * rows * N * K
+    byts = rows * K + N * K + 4 * N + 4 * rows + 2 * rows * N * (2 if R is not None else 1)
+    hbm, bf16, src = load_peaks()
+    print(json.dumps({"kernel": "prism_w8a8_linear", "case": args.case, "M": rows, "N": N, "K": K,
+                      "split": split, "kind": prism.prism_w8a8_kernel_kind(rows, N, K),
+                      "avg_us": avg, "min_us": min(us), "tflops": ops / avg / 1e6,
+                      "frac_bf16_peak": ops / avg / 1e6 / bf16, "gbs": byts / avg / 1e3,
+                      "frac_hbm": byts / avg / 1e3 / hbm, "weight_copies": n_rot,
+                      "status": prism.prism_device_status()}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -484,11 +541,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["linear"], help="time one call type alone on --case")
+    ap.add_argument("--case", default="forest_qkv_m304_k5120_n15360", choices=sorted(wl.LINEAR_CONFIGS))
+    ap.add_argument("--rows", type=int, default=None, help="use the first ROWS token rows of --case")
+    ap.add_argument("--split", type=int, default=None, help="split-K for --kernel (default automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel:
+        return run_kernel(args)
     return run_gpu(args)
 
 

@@ -54,6 +54,7 @@ SIGNATURES = {
     "prism_w8a8_kernel_kind": (_I32, [_I64, _I64, _I64]),
     "prism_w8a8_auto_split": (_I32, [_I64, _I64, _I64]),
     "prism_device_status": (_I32, [_P]),
+    "prism_last_cuda_error": (_I32, [ctypes.c_char_p, _SZ]),
 }
 
 _lock = threading.Lock()
@@ -63,7 +64,12 @@ _lib = None
 class PrismError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} failed: {status} ({status_string(status)})")
+        detail = ""
+        if status == PRISM_ERR_CUDA:
+            buf = ctypes.create_string_buffer(256)
+            code = lib().prism_last_cuda_error(buf, 256)
+            detail = f"; CUDA error {code}: {buf.value.decode(errors='replace')}"
+        super().__init__(f"{fn} failed: {status} ({status_string(status)}{detail})")
 
 
 def lib() -> ctypes.CDLL:

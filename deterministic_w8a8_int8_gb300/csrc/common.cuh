@@ -90,6 +90,9 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
 // is per device context).  Thread-safe; idempotent.
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);
 
+// Remember a failed CUDA call for prism_last_cuda_error; map to a status.
+int record_cuda(cudaError_t e);
+
 }  // namespace prism
 
 // Internal launchers (one per kernel family), defined in their .cu files.

@@ -107,11 +107,13 @@ extern "C" int prism_w8a8_linear_noalloc(const int8_t* q, int64_t ldq, const flo
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   if (need > 0) {
     void* scratch = nullptr;
-    if (prism::scratch_for_current_device(&scratch) != cudaSuccess) return PRISM_ERR_CUDA;
-    if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return PRISM_ERR_CUDA;
+    const int st = prism::record_cuda(prism::scratch_for_current_device(&scratch));
+    if (st != PRISM_OK) return st;
+    const int st2 = prism::record_cuda(cudaMemsetAsync(scratch, 0, need, stream));
+    if (st2 != PRISM_OK) return st2;
     const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~static_cast<size_t>(255);
     a.ws_acc = static_cast<int32_t*>(scratch);
     a.ws_count = reinterpret_cast<uint32_t*>(static_cast<char*>(scratch) + acc_bytes);
   }
-  return prism::launch_linear(a, stream) == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+  return prism::record_cuda(prism::launch_linear(a, stream));
 }

@@ -16,16 +16,17 @@
 // TMEM region I holding the int32 running sum; integer addition makes the
 // result independent of chunking, tiling and split-K.
 //
-// CTA roles (416 threads, one CTA per SM):
+// CTA roles (544 threads, one CTA per SM):
 //   warps 0-3   drain + epilogue; warp w owns TMEM lanes 32w..32w+31 (one
 //               A-tile row per thread);
 //   warp 4      TMEM allocator; lane 0 issues every tcgen05.mma;
-//   warps 5-12  converters: 16-byte global loads of int8 A/B rows (a register
-//               ring two stages ahead), exact int8->f16 widening, stores into
+//   warps 5-16  converters: 16-byte global loads of int8 A/B rows (a register
+//               ring three stages ahead), exact int8->f16 widening, stores into
 //               128-byte-swizzled K-major shared-memory tiles.
 // Pipeline: 4 shared-memory stages of 64 K-elements (A 128 rows, B up to 256
-// rows, f16).  mbarriers: full[s] (256 converter arrivals), empty[s] and
-// acc_full (tcgen05.commit), acc_empty (128 drain arrivals).  Every wait is
+// rows, f16, stored back to back in one stage).  mbarriers: full[s] (one arrival per converter warp), empty[s]
+// and acc_full (tcgen05.commit), acc_empty (one arrival per drain warp); one
+// lane per warp polls a barrier and shares the result with its warp.  Every wait is
 // bounded by a 2-second global-timer limit; on expiry the CTA records
 // kDevErrTimeout in the library's device error word and winds down.
 //
@@ -37,6 +38,7 @@
 //                       128-row MMA.
 // Split-K reuses the integer-atomic / last-arriver protocol of the workspace.
 #include <algorithm>
+#include <climits>
 #include <cstdlib>
 #include <cstring>
 
@@ -53,19 +55,21 @@ constexpr int kBM = 128;                  // A rows per tile = TMEM lanes
 constexpr int kBNMax = 256;               // max B rows per tile = MMA N
 constexpr int kBK = 64;                   // K elements per stage (128 B of f16 per row)
 constexpr int kChunkStages = 16;          // 16 * 64 = 1024 K per exact fp32 chunk
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 12;   // 17 warps in all (at most 96 registers each)
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kDrainThreads = 128;
-constexpr int kThreads = kDrainThreads + 32 + kConvThreads;  // 416
+constexpr int kThreads = kDrainThreads + 32 + kConvThreads;  // 544
 constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
 constexpr int kStageB = kBNMax * 128;     // bytes of one f16 B stage
+constexpr int kStageBytes = kStageA + kStageB;  // one stage: A tile then B tile
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = 1024 + kStages * (kStageA + kStageB) + kBarBytes;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;             // fp32 chunk accumulator
 constexpr uint32_t kColI = 256;           // int32 running sum
-constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kConvThreads;  // 6 x 16 B per stage
-constexpr int kPrefetch = 2;              // register ring depth (stages)
+constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kConvThreads;  // 4 x 16 B per stage
+static_assert((kBM * 4 + kBNMax * 4) % kConvThreads == 0 && kConvThreads % 4 == 0, "segment layout");
+constexpr int kPrefetch = 3;              // register ring depth (stages)
 constexpr uint32_t kDevErrTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -135,25 +139,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -201,55 +198,78 @@ __device__ __forceinline__ void emit(const LinearArgs& a, int64_t m, int64_t n, 
   if (a.acc_out != nullptr) a.acc_out[m * a.N + n] = v;
 }
 
-// 32 consecutive output channels n0..n0+31 of row m (normal orientation).
-__device__ __forceinline__ void emit_row32(const TcParams& p, int64_t m, int64_t n0, const int32_t (&v)[32]) {
+// Coalesced tile output.  The final int32 tile sits in shared memory as
+// T[rows_out][cols_out] (row stride cols_out + 4 words, so the per-row writes
+// of the drain threads hit distinct banks).  Each of the 128 drain threads
+// then owns groups of 4 consecutive columns, a warp covering contiguous
+// column ranges of one row, so global loads and stores are coalesced.
+//   mode 0: epilogue to bf16 out (+ residual, + acc_out)
+//   mode 1: integer atomics of the tile into the split-K workspace
+//   mode 2: read the finished sum back from the workspace (and re-zero it),
+//           then the epilogue
+__device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, int rows_out, int cols_out,
+                                         int64_t m0, int64_t n0, int mode, int t) {
   const LinearArgs& a = p.a;
-  if (m >= a.M) return;
-  if (p.vec_io && n0 + 32 <= a.N) {
-    const float as = __ldg(a.a_scale + m);
-    uint32_t r[16];
-    if (a.residual != nullptr) {
-      const uint4* rp = reinterpret_cast<const uint4*>(a.residual + m * a.ldr + n0);
+  const int stride = cols_out + 4;
+  const int groups = cols_out / 4;                 // 4-column groups per row
+  const int per_row = groups < 32 ? groups : 32;   // threads on one row
+  const int rows_per_pass = kDrainThreads / per_row;
+  const int g0 = t % per_row;
+  for (int r = t / per_row; r < rows_out; r += rows_per_pass) {
+    const int64_t rr = r;
+    for (int g = g0; g < groups; g += per_row) {
+      const int c = 4 * g;
+      // global coordinates of the 4 elements: along n (normal) or along n
+      // with a fixed m (swap): in both layouts the tile row is one token m
+      const int64_t m = m0 + rr;
+      const int64_t n = n0 + c;
+      if (m >= a.M) continue;
+      int32_t v[4];
+      const uint4 tv = *reinterpret_cast<const uint4*>(T + r * stride + c);
+      v[0] = static_cast<int32_t>(tv.x);
+      v[1] = static_cast<int32_t>(tv.y);
+      v[2] = static_cast<int32_t>(tv.z);
+      v[3] = static_cast<int32_t>(tv.w);
+      const bool full = n + 4 <= a.N;
+      if (mode == 1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 t = rp[i];
-        r[4 * i] = t.x;
-        r[4 * i + 1] = t.y;
-        r[4 * i + 2] = t.z;
-        r[4 * i + 3] = t.w;
+        for (int j = 0; j < 4; ++j)
+          if (n + j < a.N) atomicAdd(a.ws_acc + m * a.N + n + j, v[j]);
+        continue;
       }
-    }
-    uint32_t o[16];
+      if (mode == 2) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 w4 = __ldg(reinterpret_cast<const float4*>(a.w_scale + n0) + i);
-      const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-      for (int j = 0; j < 4; j += 2) {
-        const int e = 4 * i + j;
-        uint32_t lo, hi;
+        for (int j = 0; j < 4; ++j)
+          if (n + j < a.N) {
+            int32_t* wp = a.ws_acc + m * a.N + n + j;
+            v[j] = __ldcg(wp);
+            __stcg(wp, 0);
+          }
+      }
+      if (p.vec_io && full) {
+        const float as = __ldg(a.a_scale + m);
+        const float4 w4 = __ldg(reinterpret_cast<const float4*>(a.w_scale + n));
+        uint32_t o0, o1;
         if (a.residual != nullptr) {
-          lo = epilogue_bf16_res(v[e], as, wv[j], bf16_lo(r[e >> 1]));
-          hi = epilogue_bf16_res(v[e + 1], as, wv[j + 1], bf16_hi(r[e >> 1]));
+          const uint2 rv = *reinterpret_cast<const uint2*>(a.residual + m * a.ldr + n);
+          o0 = epilogue_bf16_res(v[0], as, w4.x, bf16_lo(rv.x)) | (epilogue_bf16_res(v[1], as, w4.y, bf16_hi(rv.x)) << 16);
+          o1 = epilogue_bf16_res(v[2], as, w4.z, bf16_lo(rv.y)) | (epilogue_bf16_res(v[3], as, w4.w, bf16_hi(rv.y)) << 16);
         } else {
-          lo = epilogue_bf16(v[e], as, wv[j]);
-          hi = epilogue_bf16(v[e + 1], as, wv[j + 1]);
+          o0 = epilogue_bf16(v[0], as, w4.x) | (epilogue_bf16(v[1], as, w4.y) << 16);
+          o1 = epilogue_bf16(v[2], as, w4.z) | (epilogue_bf16(v[3], as, w4.w) << 16);
         }
-        o[e >> 1] = lo | (hi << 16);
+        *reinterpret_cast<uint2*>(a.out + m * a.ldo + n) = make_uint2(o0, o1);
+        if (a.acc_out != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a.acc_out[m * a.N + n + j] = v[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (n + j < a.N) emit(a, m, n + j, v[j]);
       }
     }
-    uint4* op = reinterpret_cast<uint4*>(a.out + m * a.ldo + n0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) op[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-    if (a.acc_out != nullptr) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) a.acc_out[m * a.N + n0 + j] = v[j];
-    }
-    return;
   }
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    if (n0 + j < a.N) emit(a, m, n0 + j, v[j]);
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -259,9 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const uint32_t sA = base;                                   // kStages x kStageA
-  const uint32_t sB = base + kStages * kStageA;               // kStages x kStageB
-  const uint32_t bars = sB + kStages * kStageB;
+  const uint32_t sStage = base;                               // kStages x (A tile | B tile)
+  const uint32_t bars = sStage + kStages * kStageBytes;
   uint8_t* bar_ptr = smem + (bars - base);
   const uint32_t bar_full = bars;                             // kStages x 8 B
   const uint32_t bar_empty = bars + 8 * kStages;
@@ -297,11 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full + 8 * s, kConvThreads);
+      mbar_init(bar_full + 8 * s, kConvWarps);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, kDrainThreads);
+    mbar_init(bar_acc_empty, kDrainThreads / 32);
     mbar_init(bar_done, 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -320,75 +339,76 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
   if (warp < 4) {
     // ======================= drain + epilogue (128 threads) =================
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const int64_t arow = a0 + warp * 32 + lane;  // this thread's A-tile row
-    const int ncb = bn / 32;
+    const int ncb = bn / 16;  // 16-column rounds; loads of round r+1 overlap work on round r
+    uint32_t* T = reinterpret_cast<uint32_t*>(smem);
+    const int tl = warp * 32 + lane;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_acc_full, c & 1, s_abort));
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_acc_full, c & 1, s_abort) : false, 0);
       if (!ok) break;
       tc_fence_after();
       const bool last = c == nchunks - 1;
-      for (int cb = 0; cb < ncb; ++cb) {
-        uint32_t d[32], iv[32];
-        tmem_ld32(tmem + lane_base + kColD + cb * 32, d);
-        if (c > 0) tmem_ld32(tmem + lane_base + kColI + cb * 32, iv);
-        tmem_wait_ld();
-        int32_t v[32];
+      const bool has_i = c > 0;
+      uint32_t d[2][16], iv[2][16];
+      auto issue = [&](int cb, int buf) {
+        tmem_ld16(tmem + lane_base + kColD + cb * 16, d[buf]);
+        if (has_i) tmem_ld16(tmem + lane_base + kColI + cb * 16, iv[buf]);
+      };
+      auto finish = [&](int cb, int buf) {
+        uint32_t* v = d[buf];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          v[j] = (c > 0 ? static_cast<int32_t>(iv[j]) : 0) + __float2int_rn(__uint_as_float(d[j]));
+        for (int j = 0; j < 16; ++j)
+          v[j] = static_cast<uint32_t>((has_i ? static_cast<int32_t>(iv[buf][j]) : 0) +
+                                       __float2int_rn(__uint_as_float(v[j])));
         if (!last) {
-          uint32_t u[32];
+          tmem_st16(tmem + lane_base + kColI + cb * 16, d[buf]);
+        } else if (!p.swap) {
+          // stage the final int32 values as T[token][channel]
+          uint4* dst = reinterpret_cast<uint4*>(T + tl * (bn + 4) + cb * 16);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) u[j] = static_cast<uint32_t>(v[j]);
-          tmem_st32(tmem + lane_base + kColI + cb * 32, u);
-        } else if (a.split == 1) {
-          if (!p.swap) {
-            emit_row32(p, arow, b0 + cb * 32, v);
-          } else if (arow < a.N) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int64_t m = b0 + cb * 32 + j;
-              if (m < a.M) emit(a, m, arow, v[j]);
-            }
-          }
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t m = p.swap ? b0 + cb * 32 + j : arow;
-            const int64_t n = p.swap ? arow : b0 + cb * 32 + j;
-            if (m < a.M && n < a.N) atomicAdd(a.ws_acc + m * a.N + n, v[j]);
-          }
+          for (int j = 0; j < 16; ++j) T[(cb * 16 + j) * (kBM + 4) + tl] = v[j];
+        }
+      };
+      issue(0, 0);
+      for (int cb = 0; cb < ncb; cb += 2) {
+        tmem_wait_ld();
+        if (cb + 1 < ncb) issue(cb + 1, 1);
+        finish(cb, 0);
+        if (cb + 1 < ncb) {
+          tmem_wait_ld();
+          if (cb + 2 < ncb) issue(cb + 2, 0);
+          finish(cb + 1, 1);
         }
       }
       if (!last) {
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_acc_empty);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acc_empty);
       }
     }
+    // ---- coalesced output of the staged tile
+    const int rows_out = p.swap ? bn : kBM;
+    const int cols_out = p.swap ? kBM : bn;
+    const int64_t om = p.swap ? b0 : a0;   // first token of the tile
+    const int64_t on = p.swap ? a0 : b0;   // first channel of the tile
+    const int t = tl;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (ok && nchunks > 0) tile_out(p, T, rows_out, cols_out, om, on, a.split == 1 ? 0 : 1, t);
     if (a.split > 1) {
       // integer split-K: the last CTA to finish this tile applies the epilogue
       __threadfence();
       asm volatile("bar.sync 1, 128;" ::: "memory");
       const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
-      if (tid == 0) *s_last = (atomicAdd(a.ws_count + tile, 1u) == static_cast<unsigned>(a.split - 1));
+      if (t == 0) *s_last = (atomicAdd(a.ws_count + tile, 1u) == static_cast<unsigned>(a.split - 1));
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (*s_last) {
         __threadfence();
-        for (int cb = 0; cb < ncb; ++cb) {
-          for (int j = 0; j < 32; ++j) {
-            const int64_t m = p.swap ? b0 + cb * 32 + j : arow;
-            const int64_t n = p.swap ? arow : b0 + cb * 32 + j;
-            if (m < a.M && n < a.N) {
-              int32_t* wp = a.ws_acc + m * a.N + n;
-              const int32_t v = __ldcg(wp);
-              __stcg(wp, 0);
-              emit(a, m, n, v);
-            }
-          }
-        }
-        if (tid == 0) a.ws_count[tile] = 0u;
+        tile_out(p, T, rows_out, cols_out, om, on, 2, t);
+        if (t == 0) a.ws_count[tile] = 0u;
       }
     }
   } else if (warp == 4) {
@@ -404,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
         }
         if (!mbar_wait(bar_full + 8 * s, (it / kStages) & 1, s_abort)) break;
         tc_fence_after();
-        const uint64_t ad = smem_desc_sw128(sA + s * kStageA);
-        const uint64_t bd = smem_desc_sw128(sB + s * kStageB);
+        const uint64_t ad = smem_desc_sw128(sStage + s * kStageBytes);
+        const uint64_t bd = smem_desc_sw128(sStage + s * kStageBytes + kStageA);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
           tc_mma(tmem + kColD, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
@@ -424,50 +444,50 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
     }
     __syncwarp();
   } else {
-    // ======================= converters (256 threads) ========================
+    // ======================= converters (384 threads) ========================
+    // Segment i of this thread is 16 bytes of K at row (ct / 4) + 96 i of the
+    // stacked [A rows | B rows] tile, column offset 16 (ct % 4); rows and
+    // offsets are fixed for the whole tile, only the K offset moves.
     const int ct = tid - (kDrainThreads + 32);
-    const int segs = (kBM + bn) * 4;  // 16-byte int8 segments per stage
+    const int seg = ct & 3;
+    const int64_t segk = seg * 16;
+    const int8_t* gp[kSegPerThread];
+    uint32_t so[kSegPerThread];
+#pragma unroll
+    for (int i = 0; i < kSegPerThread; ++i) {
+      const int r = (ct >> 2) + i * (kConvThreads / 4);
+      const bool is_a = r < kBM;
+      const int rr = is_a ? r : r - kBM;
+      const int64_t row = is_a ? a0 + rr : b0 + rr;
+      const bool in_tile = is_a || rr < bn;
+      const bool valid = in_tile && row < (is_a ? rows_a : rows_b);
+      gp[i] = valid ? (is_a ? Am + row * lda : Bm + row * ldb) + segk : nullptr;
+      so[i] = in_tile ? (is_a ? 0u : static_cast<uint32_t>(kStageA)) + rr * 128 +
+                            static_cast<uint32_t>(((2 * seg) ^ (rr & 7)) * 16)
+                      : 0xFFFFFFFFu;
+    }
     uint4 ring[kPrefetch][kSegPerThread];
 
     auto load_stage = [&](int it, uint4 (&buf)[kSegPerThread]) {
       const int64_t kb = (kt0 + it) * kBK;
+      const bool kin = kb + segk < a.K;
 #pragma unroll
-      for (int i = 0; i < kSegPerThread; ++i) {
-        const int g = ct + i * kConvThreads;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (g < segs) {
-          const int r = g >> 2;
-          const int64_t k = kb + (g & 3) * 16;
-          if (r < kBM) {
-            const int64_t row = a0 + r;
-            if (row < rows_a && k < a.K) v = ld_stream_16(Am + row * lda + k);
-          } else {
-            const int64_t row = b0 + (r - kBM);
-            if (row < rows_b && k < a.K) v = ld_stream_16(Bm + row * ldb + k);
-          }
-        }
-        buf[i] = v;
-      }
+      for (int i = 0; i < kSegPerThread; ++i)
+        buf[i] = (gp[i] != nullptr && kin) ? ld_stream_16(gp[i] + kb) : make_uint4(0u, 0u, 0u, 0u);
     };
     auto store_stage = [&](int s, const uint4 (&buf)[kSegPerThread]) {
+      const uint32_t st_base = sStage + s * kStageBytes;
 #pragma unroll
       for (int i = 0; i < kSegPerThread; ++i) {
-        const int g = ct + i * kConvThreads;
-        if (g < segs) {
-          const int r = g >> 2;
-          const int seg = g & 3;
-          const uint32_t tile = r < kBM ? sA + s * kStageA : sB + s * kStageB;
-          const int rr = r < kBM ? r : r - kBM;
-          const uint32_t row_addr = tile + rr * 128;
+        if (so[i] != 0xFFFFFFFFu) {
           uint32_t w[8];
           widen4(buf[i].x, w[0], w[1]);
           widen4(buf[i].y, w[2], w[3]);
           widen4(buf[i].z, w[4], w[5]);
           widen4(buf[i].w, w[6], w[7]);
-          const int c0 = (2 * seg) ^ (rr & 7);
-          const int c1 = (2 * seg + 1) ^ (rr & 7);
-          st_shared_v4(row_addr + c0 * 16, w[0], w[1], w[2], w[3]);
-          st_shared_v4(row_addr + c1 * 16, w[4], w[5], w[6], w[7]);
+          const uint32_t addr = st_base + so[i];
+          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          st_shared_v4(addr ^ 16u, w[4], w[5], w[6], w[7]);
         }
       }
     };
@@ -482,12 +502,13 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
         const int it = it0 + pf;
         if (it < nk && ok) {
           const int s = it % kStages;
-          if (!mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort)) {
-            ok = false;
-          } else {
+          ok = __shfl_sync(0xffffffffu,
+                           lane == 0 ? mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort) : false, 0);
+          if (ok) {
             store_stage(s, ring[pf]);
             fence_proxy_async();
-            mbar_arrive(bar_full + 8 * s);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_full + 8 * s);
             if (it + kPrefetch < nk) load_stage(it + kPrefetch, ring[pf]);
           }
         }
@@ -532,15 +553,31 @@ static TcPlan tc_plan(int64_t M, int64_t N) {
   return pl;
 }
 
+// Split-K choice, only when the full-width tiles do not fill one wave of the
+// 152 SMs: minimise (waves of full-width CTAs) x (K per split + a fixed
+// per-CTA cost of about one 1024-K chunk).  Short token pieces of the swapped
+// orientation fill the gaps left by the full-width CTAs.
 static int tc_auto_split(int64_t M, int64_t N, int64_t K) {
+  constexpr int64_t kSMs = 152;
+  constexpr int64_t kCtaCost = 1024;
   const TcPlan pl = tc_plan(M, N);
-  const int64_t tiles = pl.grid_x * pl.grid_y;
-  const int64_t kchunks = cdiv(K, kBK * kChunkStages);
-  if (tiles >= 120) return 1;
-  int64_t s = std::max<int64_t>(1, 152 / tiles);
-  s = std::min<int64_t>(s, std::max<int64_t>(1, cdiv(K, kBK) / 8));
-  (void)kchunks;
-  return static_cast<int>(std::min<int64_t>(s, 16));
+  const int64_t b_rows = pl.swap ? M : N;
+  const int64_t full_pieces = b_rows / pl.bpiece > 0 ? b_rows / pl.bpiece : 1;
+  const int64_t long_tiles = pl.grid_x * full_pieces;
+  const int64_t kstages = cdiv(K, kBK);
+  if (long_tiles >= kSMs) return 1;  // a full wave already; integer atomics would cost more
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int sk = 1; sk <= 16; ++sk) {
+    if (sk > 1 && cdiv(kstages, sk) < 8) break;  // keep at least 512 K per split
+    const int64_t waves = cdiv(long_tiles * sk, kSMs);
+    const int64_t cost = waves * (cdiv(K, sk) + kCtaCost);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = sk;
+    }
+  }
+  return best;
 }
 
 static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {

@@ -7,6 +7,13 @@
 
 namespace prism {
 
+thread_local int g_last_cuda_error = 0;
+
+int record_cuda(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda_error = static_cast<int>(e);
+  return e == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+}
+
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_attr_mutex;
@@ -42,6 +49,18 @@ extern "C" {
 
 int prism_version(void) { return 100; }
 
+int prism_last_cuda_error(char* buf, size_t buf_bytes) {
+  const int e = prism::g_last_cuda_error;
+  prism::g_last_cuda_error = 0;
+  if (buf != nullptr && buf_bytes > 0) {
+    const char* msg = e == 0 ? "no error" : cudaGetErrorString(static_cast<cudaError_t>(e));
+    size_t i = 0;
+    for (; i + 1 < buf_bytes && msg[i] != '\0'; ++i) buf[i] = msg[i];
+    buf[i] = '\0';
+  }
+  return e;
+}
+
 const char* prism_status_string(int status) {
   switch (status) {
     case PRISM_OK: return "ok";
@@ -66,16 +85,15 @@ int prism_quant_act(const void* x_bf16, int64_t ldx, const float* inv_smooth, in
   if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(a_scale, 4)) return PRISM_ERR_ALIGNMENT;
   if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
   if (M > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
-  cudaError_t e = prism::launch_quant_act(x_bf16, ldx, inv_smooth, M, K, q, ldq, a_scale,
-                                          static_cast<cudaStream_t>(cuda_stream));
-  return e == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+  return prism::record_cuda(prism::launch_quant_act(x_bf16, ldx, inv_smooth, M, K, q, ldq, a_scale,
+                                                     static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K) { return prism::linear_kernel_kind(M, N, K); }
 
 int prism_device_status(uint32_t* flags) {
   if (flags == nullptr) return PRISM_ERR_INVALID_ARG;
-  return prism::read_and_clear_kernel_error(flags) == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+  return prism::record_cuda(prism::read_and_clear_kernel_error(flags));
 }
 
 int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K) { return prism::linear_auto_split(M, N, K); }
@@ -134,8 +152,7 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
     a.ws_acc = static_cast<int32_t*>(workspace);
     a.ws_count = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + acc_bytes);
   }
-  cudaError_t e = prism::launch_linear(a, static_cast<cudaStream_t>(cuda_stream));
-  return e == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+  return prism::record_cuda(prism::launch_linear(a, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* inv_smooth,
@@ -160,10 +177,9 @@ int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* i
   if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
   if (dev_error_word != nullptr && !aligned(dev_error_word, 4)) return PRISM_ERR_ALIGNMENT;
   if (P > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
-  cudaError_t e = prism::launch_readout(hidden_bf16, ldh, inv_smooth, lm_head, ldw, lm_scale, V, K,
-                                        cand_offsets, cand_ids, P, T, logits, probs, dev_error_word,
-                                        static_cast<cudaStream_t>(cuda_stream));
-  return e == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+  return prism::record_cuda(prism::launch_readout(hidden_bf16, ldh, inv_smooth, lm_head, ldw, lm_scale, V,
+                                                   K, cand_offsets, cand_ids, P, T, logits, probs,
+                                                   dev_error_word, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 }  // extern "C"

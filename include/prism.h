@@ -207,6 +207,11 @@ const char *prism_status_string(int status);
 /* Library version as major * 10000 + minor * 100 + patch. */
 int prism_version(void);
 
+/* The cudaError_t code behind the calling thread's most recent
+ * PRISM_ERR_CUDA (0 if none), then cleared; its text is copied into buf
+ * (NUL-terminated, truncated to buf_bytes) when buf is not NULL. */
+int prism_last_cuda_error(char *buf, size_t buf_bytes);
+
 /*
  * Which contraction kernel prism_w8a8_linear would launch for this shape:
  * 0 = none (empty); 1 = warp-level mma.sync s8 kernel; 2 = tcgen05 kernel,
