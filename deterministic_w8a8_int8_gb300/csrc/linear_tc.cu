@@ -202,11 +202,16 @@ __device__ __forceinline__ void emit(const LinearArgs& a, int64_t m, int64_t n, 
 // T[rows_out][cols_out] (row stride cols_out + 4 words, so the per-row writes
 // of the drain threads hit distinct banks).  Each of the 128 drain threads
 // then owns groups of 4 consecutive columns, a warp covering contiguous
-// column ranges of one row, so global loads and stores are coalesced.
+// column ranges of one row, so global loads and stores are coalesced.  The
+// residual and scale loads of kRowBatch rows are issued before any of them is
+// used, so they overlap instead of paying one memory latency each.
 //   mode 0: epilogue to bf16 out (+ residual, + acc_out)
 //   mode 1: integer atomics of the tile into the split-K workspace
 //   mode 2: read the finished sum back from the workspace (and re-zero it),
 //           then the epilogue
+constexpr int kRowBatch = 4;
+constexpr int kMaxGroupsPerThread = kBNMax / 4 / 32;   // 2
+
 __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, int rows_out, int cols_out,
                                          int64_t m0, int64_t n0, int mode, int t) {
   const LinearArgs& a = p.a;
@@ -214,59 +219,138 @@ __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, i
   const int groups = cols_out / 4;                 // 4-column groups per row
   const int per_row = groups < 32 ? groups : 32;   // threads on one row
   const int rows_per_pass = kDrainThreads / per_row;
+  const int gpt = groups / per_row;                // groups per thread per row (1 or 2)
   const int g0 = t % per_row;
-  for (int r = t / per_row; r < rows_out; r += rows_per_pass) {
-    const int64_t rr = r;
-    for (int g = g0; g < groups; g += per_row) {
-      const int c = 4 * g;
-      // global coordinates of the 4 elements: along n (normal) or along n
-      // with a fixed m (swap): in both layouts the tile row is one token m
-      const int64_t m = m0 + rr;
-      const int64_t n = n0 + c;
-      if (m >= a.M) continue;
-      int32_t v[4];
-      const uint4 tv = *reinterpret_cast<const uint4*>(T + r * stride + c);
-      v[0] = static_cast<int32_t>(tv.x);
-      v[1] = static_cast<int32_t>(tv.y);
-      v[2] = static_cast<int32_t>(tv.z);
-      v[3] = static_cast<int32_t>(tv.w);
-      const bool full = n + 4 <= a.N;
-      if (mode == 1) {
+  const bool has_res = a.residual != nullptr;
+
+  if (mode == 2) {
+    // split-K read-back: copy the finished integer sums into this thread's
+    // own entries of the staged tile (re-zeroing the workspace), kRowBatch rows
+    // of loads in flight, then run the ordinary epilogue from the tile
+    uint32_t* Tw = const_cast<uint32_t*>(T);
+    const bool vec = (a.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.ws_acc) & 15) == 0);
+    for (int rb = t / per_row; rb < rows_out; rb += rows_per_pass * kRowBatch) {
+      int4 wv[kRowBatch][kMaxGroupsPerThread];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (n + j < a.N) atomicAdd(a.ws_acc + m * a.N + n + j, v[j]);
-        continue;
-      }
-      if (mode == 2) {
+      for (int b = 0; b < kRowBatch; ++b) {
+        const int r = rb + b * rows_per_pass;
+        const int64_t m = m0 + r;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (n + j < a.N) {
-            int32_t* wp = a.ws_acc + m * a.N + n + j;
-            v[j] = __ldcg(wp);
-            __stcg(wp, 0);
+        for (int q = 0; q < kMaxGroupsPerThread; ++q) {
+          const int64_t n = n0 + 4 * (g0 + q * per_row);
+          wv[b][q] = make_int4(0, 0, 0, 0);
+          if (r < rows_out && m < a.M && q < gpt) {
+            int32_t* wp = a.ws_acc + m * a.N + n;
+            if (vec && n + 4 <= a.N) {
+              wv[b][q] = __ldcg(reinterpret_cast<const int4*>(wp));
+            } else {
+              wv[b][q].x = n < a.N ? __ldcg(wp) : 0;
+              wv[b][q].y = n + 1 < a.N ? __ldcg(wp + 1) : 0;
+              wv[b][q].z = n + 2 < a.N ? __ldcg(wp + 2) : 0;
+              wv[b][q].w = n + 3 < a.N ? __ldcg(wp + 3) : 0;
+            }
           }
+        }
       }
-      if (p.vec_io && full) {
-        const float as = __ldg(a.a_scale + m);
-        const float4 w4 = __ldg(reinterpret_cast<const float4*>(a.w_scale + n));
-        uint32_t o0, o1;
-        if (a.residual != nullptr) {
-          const uint2 rv = *reinterpret_cast<const uint2*>(a.residual + m * a.ldr + n);
-          o0 = epilogue_bf16_res(v[0], as, w4.x, bf16_lo(rv.x)) | (epilogue_bf16_res(v[1], as, w4.y, bf16_hi(rv.x)) << 16);
-          o1 = epilogue_bf16_res(v[2], as, w4.z, bf16_lo(rv.y)) | (epilogue_bf16_res(v[3], as, w4.w, bf16_hi(rv.y)) << 16);
+#pragma unroll
+      for (int b = 0; b < kRowBatch; ++b) {
+        const int r = rb + b * rows_per_pass;
+        const int64_t m = m0 + r;
+#pragma unroll
+        for (int q = 0; q < kMaxGroupsPerThread; ++q) {
+          const int c = 4 * (g0 + q * per_row);
+          const int64_t n = n0 + c;
+          if (r < rows_out && m < a.M && q < gpt) {
+            *reinterpret_cast<int4*>(Tw + r * stride + c) = wv[b][q];
+            int32_t* wp = a.ws_acc + m * a.N + n;
+            if (vec && n + 4 <= a.N) {
+              __stcg(reinterpret_cast<int4*>(wp), make_int4(0, 0, 0, 0));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (n + j < a.N) __stcg(wp + j, 0);
+            }
+          }
+        }
+      }
+    }
+    mode = 0;
+  }
+
+  float4 wsv[kMaxGroupsPerThread];
+#pragma unroll
+  for (int q = 0; q < kMaxGroupsPerThread; ++q) {
+    const int64_t n = n0 + 4 * (g0 + q * per_row);
+    wsv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mode != 1 && q < gpt && p.vec_io && n + 4 <= a.N)
+      wsv[q] = __ldg(reinterpret_cast<const float4*>(a.w_scale + n));
+  }
+
+  for (int rb = t / per_row; rb < rows_out; rb += rows_per_pass * kRowBatch) {
+    uint2 rv[kRowBatch][kMaxGroupsPerThread];
+    float as[kRowBatch];
+    // ---- issue every load of the batch
+#pragma unroll
+    for (int b = 0; b < kRowBatch; ++b) {
+      const int r = rb + b * rows_per_pass;
+      const int64_t m = m0 + r;
+      const bool row_ok = r < rows_out && m < a.M;
+      as[b] = (mode != 1 && row_ok) ? __ldg(a.a_scale + m) : 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxGroupsPerThread; ++q) {
+        const int c = 4 * (g0 + q * per_row);
+        const int64_t n = n0 + c;
+        const bool ok = row_ok && q < gpt;
+        rv[b][q] = make_uint2(0u, 0u);
+        if (ok && mode != 1 && has_res && p.vec_io && n + 4 <= a.N)
+          rv[b][q] = *reinterpret_cast<const uint2*>(a.residual + m * a.ldr + n);
+      }
+    }
+    // ---- use them
+#pragma unroll
+    for (int b = 0; b < kRowBatch; ++b) {
+      const int r = rb + b * rows_per_pass;
+      const int64_t m = m0 + r;
+      if (r >= rows_out || m >= a.M) continue;
+#pragma unroll
+      for (int q = 0; q < kMaxGroupsPerThread; ++q) {
+        if (q >= gpt) continue;
+        const int c = 4 * (g0 + q * per_row);
+        const int64_t n = n0 + c;
+        int32_t vv[4];
+        const uint4 tv = *reinterpret_cast<const uint4*>(T + r * stride + c);  // read at use time
+        vv[0] = static_cast<int32_t>(tv.x);
+        vv[1] = static_cast<int32_t>(tv.y);
+        vv[2] = static_cast<int32_t>(tv.z);
+        vv[3] = static_cast<int32_t>(tv.w);
+        if (mode == 1) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (n + j < a.N) atomicAdd(a.ws_acc + m * a.N + n + j, vv[j]);
+          continue;
+        }
+        if (p.vec_io && n + 4 <= a.N) {
+          const float4 w4 = wsv[q];
+          uint32_t o0, o1;
+          if (has_res) {
+            o0 = epilogue_bf16_res(vv[0], as[b], w4.x, bf16_lo(rv[b][q].x)) |
+                 (epilogue_bf16_res(vv[1], as[b], w4.y, bf16_hi(rv[b][q].x)) << 16);
+            o1 = epilogue_bf16_res(vv[2], as[b], w4.z, bf16_lo(rv[b][q].y)) |
+                 (epilogue_bf16_res(vv[3], as[b], w4.w, bf16_hi(rv[b][q].y)) << 16);
+          } else {
+            o0 = epilogue_bf16(vv[0], as[b], w4.x) | (epilogue_bf16(vv[1], as[b], w4.y) << 16);
+            o1 = epilogue_bf16(vv[2], as[b], w4.z) | (epilogue_bf16(vv[3], as[b], w4.w) << 16);
+          }
+          *reinterpret_cast<uint2*>(a.out + m * a.ldo + n) = make_uint2(o0, o1);
+          if (a.acc_out != nullptr) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a.acc_out[m * a.N + n + j] = vv[j];
+          }
         } else {
-          o0 = epilogue_bf16(v[0], as, w4.x) | (epilogue_bf16(v[1], as, w4.y) << 16);
-          o1 = epilogue_bf16(v[2], as, w4.z) | (epilogue_bf16(v[3], as, w4.w) << 16);
-        }
-        *reinterpret_cast<uint2*>(a.out + m * a.ldo + n) = make_uint2(o0, o1);
-        if (a.acc_out != nullptr) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) a.acc_out[m * a.N + n + j] = v[j];
+          for (int j = 0; j < 4; ++j)
+            if (n + j < a.N) emit(a, m, n + j, vv[j]);
         }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (n + j < a.N) emit(a, m, n + j, v[j]);
       }
     }
   }
