@@ -16,19 +16,22 @@
 // TMEM region I holding the int32 running sum; integer addition makes the
 // result independent of chunking, tiling and split-K.
 //
-// CTA roles (544 threads, one CTA per SM):
-//   warps 0-3   drain + epilogue; warp w owns TMEM lanes 32w..32w+31 (one
-//               A-tile row per thread);
-//   warp 4      TMEM allocator; lane 0 issues every tcgen05.mma;
-//   warps 5-16  converters: 16-byte global loads of int8 A/B rows (a register
-//               ring three stages ahead), exact int8->f16 widening, stores into
-//               128-byte-swizzled K-major shared-memory tiles.
+// CTA roles (544 threads = 17 warps, one CTA per SM):
+//   warp 4        TMEM allocator; lane 0 issues every tcgen05.mma;
+//   16 workers    (the other warps, four per TMEM lane quadrant) do all the
+//                 rest: 16-byte global loads of the int8 A/B rows into a
+//                 register ring three stages ahead, exact int8->f16
+//                 widening into 128-byte-swizzled K-major shared-memory tiles;
+//                 at each 1024-K chunk boundary each warp drains its quarter
+//                 of its quadrant's accumulator columns; at the end all 512
+//                 threads write the tile out.
 // Pipeline: 4 shared-memory stages of 64 K-elements (A 128 rows, B up to 256
-// rows, f16, stored back to back in one stage).  mbarriers: full[s] (one arrival per converter warp), empty[s]
-// and acc_full (tcgen05.commit), acc_empty (one arrival per drain warp); one
-// lane per warp polls a barrier and shares the result with its warp.  Every wait is
-// bounded by a 2-second global-timer limit; on expiry the CTA records
-// kDevErrTimeout in the library's device error word and winds down.
+// rows, f16, stored back to back in one stage).  mbarriers: full[s] and
+// acc_empty (one arrival per worker warp), empty[s] and acc_full
+// (tcgen05.commit); one lane per warp polls a barrier and shares the result
+// with its warp.  Every wait is bounded by a 2-second global-timer limit; on
+// expiry the CTA records kDevErrTimeout in the library's device error word
+// and winds down.
 //
 // Two orientations:
 //   normal (many rows)  A = q rows (tokens, 128 per tile), B = w rows
@@ -55,10 +58,10 @@ constexpr int kBM = 128;                  // A rows per tile = TMEM lanes
 constexpr int kBNMax = 256;               // max B rows per tile = MMA N
 constexpr int kBK = 64;                   // K elements per stage (128 B of f16 per row)
 constexpr int kChunkStages = 16;          // 16 * 64 = 1024 K per exact fp32 chunk
-constexpr int kConvWarps = 12;   // 17 warps in all (at most 96 registers each)
-constexpr int kConvThreads = kConvWarps * 32;
-constexpr int kDrainThreads = 128;
-constexpr int kThreads = kDrainThreads + 32 + kConvThreads;  // 544
+constexpr int kWorkerWarps = 16;          // convert, drain and write out; 4 per TMEM lane quadrant
+constexpr int kWorkers = kWorkerWarps * 32;
+constexpr int kMmaWarp = 4;               // TMEM allocator + MMA issuer
+constexpr int kThreads = kWorkers + 32;   // 544: 17 warps, at most 96 registers each
 constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
 constexpr int kStageB = kBNMax * 128;     // bytes of one f16 B stage
 constexpr int kStageBytes = kStageA + kStageB;  // one stage: A tile then B tile
@@ -67,8 +70,8 @@ constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;             // fp32 chunk accumulator
 constexpr uint32_t kColI = 256;           // int32 running sum
-constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kConvThreads;  // 4 x 16 B per stage
-static_assert((kBM * 4 + kBNMax * 4) % kConvThreads == 0 && kConvThreads % 4 == 0, "segment layout");
+constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kWorkers;  // 3 x 16 B per stage
+static_assert((kBM * 4 + kBNMax * 4) % kWorkers == 0 && kWorkers / 4 == kBM, "segment layout");
 constexpr int kPrefetch = 3;              // register ring depth (stages)
 constexpr uint32_t kDevErrTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -200,7 +203,7 @@ __device__ __forceinline__ void emit(const LinearArgs& a, int64_t m, int64_t n, 
 
 // Coalesced tile output.  The final int32 tile sits in shared memory as
 // T[rows_out][cols_out] (row stride cols_out + 4 words, so the per-row writes
-// of the drain threads hit distinct banks).  Each of the 128 drain threads
+// of the drain threads hit distinct banks).  Each participating thread
 // then owns groups of 4 consecutive columns, a warp covering contiguous
 // column ranges of one row, so global loads and stores are coalesced.  The
 // residual and scale loads of kRowBatch rows are issued before any of them is
@@ -213,12 +216,12 @@ constexpr int kRowBatch = 4;
 constexpr int kMaxGroupsPerThread = kBNMax / 4 / 32;   // 2
 
 __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, int rows_out, int cols_out,
-                                         int64_t m0, int64_t n0, int mode, int t) {
+                                         int64_t m0, int64_t n0, int mode, int t, int nthreads) {
   const LinearArgs& a = p.a;
   const int stride = cols_out + 4;
   const int groups = cols_out / 4;                 // 4-column groups per row
   const int per_row = groups < 32 ? groups : 32;   // threads on one row
-  const int rows_per_pass = kDrainThreads / per_row;
+  const int rows_per_pass = nthreads / per_row;
   const int gpt = groups / per_row;                // groups per thread per row (1 or 2)
   const int g0 = t % per_row;
   const bool has_res = a.residual != nullptr;
@@ -400,16 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full + 8 * s, kConvWarps);
+      mbar_init(bar_full + 8 * s, kWorkerWarps);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, kDrainThreads / 32);
+    mbar_init(bar_acc_empty, kWorkerWarps);
     mbar_init(bar_done, 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
                  "r"(kTmemCols)
                  : "memory");
@@ -420,82 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp < 4) {
-    // ======================= drain + epilogue (128 threads) =================
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const int ncb = bn / 16;  // 16-column rounds; loads of round r+1 overlap work on round r
-    uint32_t* T = reinterpret_cast<uint32_t*>(smem);
-    const int tl = warp * 32 + lane;
-    bool ok = true;
-    for (int c = 0; c < nchunks && ok; ++c) {
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_acc_full, c & 1, s_abort) : false, 0);
-      if (!ok) break;
-      tc_fence_after();
-      const bool last = c == nchunks - 1;
-      const bool has_i = c > 0;
-      uint32_t d[2][16], iv[2][16];
-      auto issue = [&](int cb, int buf) {
-        tmem_ld16(tmem + lane_base + kColD + cb * 16, d[buf]);
-        if (has_i) tmem_ld16(tmem + lane_base + kColI + cb * 16, iv[buf]);
-      };
-      auto finish = [&](int cb, int buf) {
-        uint32_t* v = d[buf];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          v[j] = static_cast<uint32_t>((has_i ? static_cast<int32_t>(iv[buf][j]) : 0) +
-                                       __float2int_rn(__uint_as_float(v[j])));
-        if (!last) {
-          tmem_st16(tmem + lane_base + kColI + cb * 16, d[buf]);
-        } else if (!p.swap) {
-          // stage the final int32 values as T[token][channel]
-          uint4* dst = reinterpret_cast<uint4*>(T + tl * (bn + 4) + cb * 16);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) T[(cb * 16 + j) * (kBM + 4) + tl] = v[j];
-        }
-      };
-      issue(0, 0);
-      for (int cb = 0; cb < ncb; cb += 2) {
-        tmem_wait_ld();
-        if (cb + 1 < ncb) issue(cb + 1, 1);
-        finish(cb, 0);
-        if (cb + 1 < ncb) {
-          tmem_wait_ld();
-          if (cb + 2 < ncb) issue(cb + 2, 0);
-          finish(cb + 1, 1);
-        }
-      }
-      if (!last) {
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_acc_empty);
-      }
-    }
-    // ---- coalesced output of the staged tile
-    const int rows_out = p.swap ? bn : kBM;
-    const int cols_out = p.swap ? kBM : bn;
-    const int64_t om = p.swap ? b0 : a0;   // first token of the tile
-    const int64_t on = p.swap ? a0 : b0;   // first channel of the tile
-    const int t = tl;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ok && nchunks > 0) tile_out(p, T, rows_out, cols_out, om, on, a.split == 1 ? 0 : 1, t);
-    if (a.split > 1) {
-      // integer split-K: the last CTA to finish this tile applies the epilogue
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
-      if (t == 0) *s_last = (atomicAdd(a.ws_count + tile, 1u) == static_cast<unsigned>(a.split - 1));
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (*s_last) {
-        __threadfence();
-        tile_out(p, T, rows_out, cols_out, om, on, 2, t);
-        if (t == 0) a.ws_count[tile] = 0u;
-      }
-    }
-  } else if (warp == 4) {
+  if (warp == kMmaWarp) {
     // ======================= MMA issuer (one thread) =========================
     if (lane == 0 && nk > 0) {
       const uint32_t idesc = idesc_f16_f32(bn);
@@ -528,18 +456,26 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
     }
     __syncwarp();
   } else {
-    // ======================= converters (384 threads) ========================
-    // Segment i of this thread is 16 bytes of K at row (ct / 4) + 96 i of the
-    // stacked [A rows | B rows] tile, column offset 16 (ct % 4); rows and
-    // offsets are fixed for the whole tile, only the K offset moves.
-    const int ct = tid - (kDrainThreads + 32);
-    const int seg = ct & 3;
+    // ======================= workers (16 warps) ===============================
+    // Conversion: worker thread wt owns 16-byte segment (wt % 4) of rows
+    // wt / 4, wt / 4 + 128 and wt / 4 + 256 of the stacked [A | B] tile; rows
+    // and shared-memory offsets are fixed for the tile, only K moves.
+    // Drain: warp w reads TMEM lanes 32 (w % 4) .. +31; the four warps of a
+    // quadrant take 16-column rounds j, j + 4, j + 8, ... of the accumulator.
+    const int wi = warp < kMmaWarp ? warp : warp - 1;   // worker index 0..15
+    const int wt = wi * 32 + lane;
+    const int quad = warp & 3;
+    const int slice = warp < kMmaWarp ? 0 : (warp - 1) / 4;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int trow = quad * 32 + lane;                    // this thread's TMEM lane
+    uint32_t* T = reinterpret_cast<uint32_t*>(smem);
+    const int seg = wt & 3;
     const int64_t segk = seg * 16;
     const int8_t* gp[kSegPerThread];
     uint32_t so[kSegPerThread];
 #pragma unroll
     for (int i = 0; i < kSegPerThread; ++i) {
-      const int r = (ct >> 2) + i * (kConvThreads / 4);
+      const int r = (wt >> 2) + i * kBM;
       const bool is_a = r < kBM;
       const int rr = is_a ? r : r - kBM;
       const int64_t row = is_a ? a0 + rr : b0 + rr;
@@ -575,16 +511,60 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
         }
       }
     };
+    // Drain this warp's share of chunk c: I += int(D) (or, for the last
+    // chunk, stage the final values as T[token][channel]).
+    auto drain = [&](int c, bool last) -> bool {
+      const bool got = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_acc_full, c & 1, s_abort) : false, 0);
+      if (!got) return false;
+      tc_fence_after();
+      const int rounds = bn / 16;
+      for (int cb = slice; cb < rounds; cb += 4) {
+        uint32_t d[16], iv[16];
+        tmem_ld16(tmem + lane_base + kColD + cb * 16, d);
+        if (c > 0) tmem_ld16(tmem + lane_base + kColI + cb * 16, iv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          d[j] = static_cast<uint32_t>((c > 0 ? static_cast<int32_t>(iv[j]) : 0) +
+                                       __float2int_rn(__uint_as_float(d[j])));
+        if (!last) {
+          tmem_st16(tmem + lane_base + kColI + cb * 16, d);
+        } else if (!p.swap) {
+          uint4* dst = reinterpret_cast<uint4*>(T + trow * (bn + 4) + cb * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) T[(cb * 16 + j) * (kBM + 4) + trow] = d[j];
+        }
+      }
+      if (!last) {
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acc_empty);
+      }
+      return true;
+    };
 
 #pragma unroll
     for (int pf = 0; pf < kPrefetch; ++pf)
       if (pf < nk) load_stage(pf, ring[pf]);
     bool ok = true;
+    int next_drain = 0;  // next intermediate chunk to drain
     for (int it0 = 0; it0 < nk && ok; it0 += kPrefetch) {
 #pragma unroll
       for (int pf = 0; pf < kPrefetch; ++pf) {
         const int it = it0 + pf;
         if (it < nk && ok) {
+          // chunk c's last MMA completes exactly when stage it - kStages is
+          // released, so drain it here, after the next chunk's first stages
+          // have been prepared
+          if (next_drain < nchunks - 1 && it == (next_drain + 1) * kChunkStages + kStages - 1) {
+            ok = drain(next_drain, false);
+            ++next_drain;
+            if (!ok) break;
+          }
           const int s = it % kStages;
           ok = __shfl_sync(0xffffffffu,
                            lane == 0 ? mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort) : false, 0);
@@ -598,12 +578,35 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
         }
       }
     }
+    while (ok && next_drain < nchunks - 1) ok = drain(next_drain++, false);
+    if (ok && nchunks > 0) ok = drain(nchunks - 1, true);
+
+    // ---- coalesced output of the staged tile by all 512 workers
+    const int rows_out = p.swap ? bn : kBM;
+    const int cols_out = p.swap ? kBM : bn;
+    const int64_t om = p.swap ? b0 : a0;   // first token of the tile
+    const int64_t on = p.swap ? a0 : b0;   // first channel of the tile
+    asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+    if (ok && nchunks > 0) tile_out(p, T, rows_out, cols_out, om, on, a.split == 1 ? 0 : 1, wt, kWorkers);
+    if (a.split > 1) {
+      // integer split-K: the last CTA to finish this tile applies the epilogue
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+      const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
+      if (wt == 0) *s_last = (atomicAdd(a.ws_count + tile, 1u) == static_cast<unsigned>(a.split - 1));
+      asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+      if (*s_last) {
+        __threadfence();
+        tile_out(p, T, rows_out, cols_out, om, on, 2, wt, kWorkers);
+        if (wt == 0) a.ws_count[tile] = 0u;
+      }
+    }
   }
 
   // ---- teardown: every role has finished its (bounded) work
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
@@ -615,7 +618,8 @@ inline int64_t cdiv(int64_t x, int64_t y) { return (x + y - 1) / y; }
 
 // Plan for the tensor-core path: orientation, B-piece width and the automatic
 // split.  Few rows (M < 512) use the swapped orientation with the tokens as
-// the MMA's N side; otherwise tokens fill the 128-row side.
+// the MMA's N side (in equal pieces of at most 256); otherwise tokens fill the
+// 128-row side.
 struct TcPlan {
   int swap;
   int bpiece;
@@ -626,9 +630,12 @@ static TcPlan tc_plan(int64_t M, int64_t N) {
   TcPlan pl{};
   pl.swap = M < 512 ? 1 : 0;
   if (pl.swap) {
-    pl.bpiece = 256;
+    // tokens split into equal pieces (multiples of 32, at most 256) so that no
+    // narrow leftover piece piles up on a few SMs
+    const int64_t pieces = cdiv(M, kBNMax);
+    pl.bpiece = static_cast<int>(cdiv(cdiv(M, pieces), 32) * 32);
     pl.grid_x = cdiv(N, kBM);
-    pl.grid_y = cdiv(M, 256);
+    pl.grid_y = cdiv(M, pl.bpiece);
   } else {
     pl.bpiece = 256;
     pl.grid_x = cdiv(M, kBM);
