@@ -16,22 +16,21 @@
 // TMEM region I holding the int32 running sum; integer addition makes the
 // result independent of chunking, tiling and split-K.
 //
-// CTA roles (544 threads = 17 warps, one CTA per SM):
+// CTA roles (576 threads = 18 warps, one CTA per SM):
+//   warp 17       lane 0 streams the raw int8 A and B tiles into a 3-deep
+//                 shared-memory staging ring with 2-D TMA loads;
 //   warp 4        TMEM allocator; lane 0 issues every tcgen05.mma;
 //   16 workers    (the other warps, four per TMEM lane quadrant) do all the
-//                 rest: 16-byte global loads of the int8 A/B rows into a
-//                 register ring three stages ahead, exact int8->f16
-//                 widening into 128-byte-swizzled K-major shared-memory tiles;
-//                 at each 1024-K chunk boundary each warp drains its quarter
-//                 of its quadrant's accumulator columns; at the end all 512
-//                 threads write the tile out.
-// Pipeline: 4 shared-memory stages of 64 K-elements (A 128 rows, B up to 256
-// rows, f16, stored back to back in one stage).  mbarriers: full[s] and
-// acc_empty (one arrival per worker warp), empty[s] and acc_full
-// (tcgen05.commit); one lane per warp polls a barrier and shares the result
-// with its warp.  Every wait is bounded by a 2-second global-timer limit; on
-// expiry the CTA records kDevErrTimeout in the library's device error word
-// and winds down.
+//                 rest: exact int8->f16 widening from the staging ring into
+//                 128-byte-swizzled K-major f16 tiles (3 stages); at each
+//                 1024-K chunk boundary each warp drains its quarter of its
+//                 quadrant's accumulator columns; at the end all 512 threads
+//                 write the tile out.
+// mbarriers: s8_full (TMA transaction count), s8_empty, full and acc_empty
+// (one arrival per worker warp), empty and acc_full (tcgen05.commit); one
+// lane per warp polls a barrier and shares the result with its warp.  Every
+// wait is bounded by a 2-second global-timer limit; on expiry the CTA records
+// kDevErrTimeout in the library's device error word and winds down.
 //
 // Two orientations:
 //   normal (many rows)  A = q rows (tokens, 128 per tile), B = w rows
@@ -45,6 +44,9 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace prism {
@@ -53,7 +55,7 @@ __device__ uint32_t g_kernel_error = 0;
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;               // f16 operand stages read by the MMA
 constexpr int kBM = 128;                  // A rows per tile = TMEM lanes
 constexpr int kBNMax = 256;               // max B rows per tile = MMA N
 constexpr int kBK = 64;                   // K elements per stage (128 B of f16 per row)
@@ -61,18 +63,21 @@ constexpr int kChunkStages = 16;          // 16 * 64 = 1024 K per exact fp32 chu
 constexpr int kWorkerWarps = 16;          // convert, drain and write out; 4 per TMEM lane quadrant
 constexpr int kWorkers = kWorkerWarps * 32;
 constexpr int kMmaWarp = 4;               // TMEM allocator + MMA issuer
-constexpr int kThreads = kWorkers + 32;   // 544: 17 warps, at most 96 registers each
+constexpr int kTmaWarp = 17;              // lane 0 issues the TMA loads
+constexpr int kThreads = kWorkers + 64;   // 576: 18 warps, at most 96 registers each
+constexpr int kS8Stages = 3;              // int8 staging stages filled by TMA
+constexpr int kS8A = kBM * kBK;           // bytes of one int8 A box (128 rows x 64)
+constexpr int kS8Bytes = kS8A + kBNMax * kBK;  // one int8 stage: A box then B box
 constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
 constexpr int kStageB = kBNMax * 128;     // bytes of one f16 B stage
 constexpr int kStageBytes = kStageA + kStageB;  // one stage: A tile then B tile
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kS8Stages * kS8Bytes + kBarBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;             // fp32 chunk accumulator
 constexpr uint32_t kColI = 256;           // int32 running sum
 constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kWorkers;  // 3 x 16 B per stage
 static_assert((kBM * 4 + kBNMax * 4) % kWorkers == 0 && kWorkers / 4 == kBM, "segment layout");
-constexpr int kPrefetch = 3;              // register ring depth (stages)
 constexpr uint32_t kDevErrTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -185,6 +190,23 @@ __device__ __forceinline__ void widen4(uint32_t x, uint32_t& lo, uint32_t& hi) {
   asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(p1) : "r"(u), "r"(0x64646464u));
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(p0), "r"(0x64806480u));
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(p1), "r"(0x64806480u));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// 2-D TMA tile load (x = K byte offset, a multiple of 64; y = first row).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -360,35 +382,36 @@ __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, i
 }
 
 // ------------------------------------------------------------------ kernel --
-__global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ uint8_t smem_raw[];
   const LinearArgs& a = p.a;
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const uint32_t sStage = base;                               // kStages x (A tile | B tile)
-  const uint32_t bars = sStage + kStages * kStageBytes;
+  const uint32_t sStage = base;                               // kStages x (A tile | B tile), f16
+  const uint32_t sS8 = sStage + kStages * kStageBytes;         // kS8Stages x (A box | B box), int8
+  const uint32_t bars = sS8 + kS8Stages * kS8Bytes;
   uint8_t* bar_ptr = smem + (bars - base);
   const uint32_t bar_full = bars;                             // kStages x 8 B
   const uint32_t bar_empty = bars + 8 * kStages;
-  const uint32_t bar_acc_full = bars + 16 * kStages;
+  const uint32_t bar_s8_full = bars + 16 * kStages;           // kS8Stages x 8 B
+  const uint32_t bar_s8_empty = bar_s8_full + 8 * kS8Stages;
+  const uint32_t bar_acc_full = bar_s8_empty + 8 * kS8Stages;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_done = bar_acc_full + 16;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_ptr + 16 * kStages + 24);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bar_ptr + 16 * kStages + 28);
-  int* s_last = reinterpret_cast<int*>(bar_ptr + 16 * kStages + 32);
+  uint8_t* scalars = bar_ptr + (bar_done + 8 - bars);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(scalars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(scalars + 4);
+  int* s_last = reinterpret_cast<int*>(scalars + 8);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
   // tile coordinates
-  const int64_t rows_a = p.swap ? a.N : a.M;
   const int64_t rows_b = p.swap ? a.M : a.N;
-  const int8_t* Am = p.swap ? a.w : a.q;
-  const int8_t* Bm = p.swap ? a.q : a.w;
-  const int64_t lda = p.swap ? a.ldw : a.ldq;
-  const int64_t ldb = p.swap ? a.ldq : a.ldw;
   const int64_t a0 = static_cast<int64_t>(blockIdx.x) * kBM;
   const int64_t b0 = static_cast<int64_t>(blockIdx.y) * p.bpiece;
   const int64_t b_left = rows_b - b0;
@@ -405,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, kWorkerWarps);
       mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int j = 0; j < kS8Stages; ++j) {
+      mbar_init(bar_s8_full + 8 * j, 1);
+      mbar_init(bar_s8_empty + 8 * j, kWorkerWarps);
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, kWorkerWarps);
@@ -455,6 +482,21 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
       }
     }
     __syncwarp();
+  } else if (warp == kTmaWarp) {
+    // ======================= TMA producer (one thread) ========================
+    if (lane == 0 && nk > 0) {
+      const uint32_t tx = static_cast<uint32_t>(kS8A + kBK * p.bpiece);
+      for (int it = 0; it < nk; ++it) {
+        const int j = it % kS8Stages;
+        if (!mbar_wait(bar_s8_empty + 8 * j, ((it / kS8Stages) & 1) ^ 1, s_abort)) break;
+        const uint32_t dst = sS8 + j * kS8Bytes;
+        const int32_t x = static_cast<int32_t>((kt0 + it) * kBK);
+        mbar_expect_tx(bar_s8_full + 8 * j, tx);
+        tma_load_2d(dst, &tmA, x, static_cast<int32_t>(a0), bar_s8_full + 8 * j);
+        tma_load_2d(dst + kS8A, &tmB, x, static_cast<int32_t>(b0), bar_s8_full + 8 * j);
+      }
+    }
+    __syncwarp();
   } else {
     // ======================= workers (16 warps) ===============================
     // Conversion: worker thread wt owns 16-byte segment (wt % 4) of rows
@@ -470,31 +512,21 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
     const int trow = quad * 32 + lane;                    // this thread's TMEM lane
     uint32_t* T = reinterpret_cast<uint32_t*>(smem);
     const int seg = wt & 3;
-    const int64_t segk = seg * 16;
-    const int8_t* gp[kSegPerThread];
+    // per segment: offset of its 16 int8 bytes in a staging stage, and of its
+    // first 16-byte f16 chunk in an operand stage (the second is that ^ 16)
+    uint32_t lo8[kSegPerThread];
     uint32_t so[kSegPerThread];
 #pragma unroll
     for (int i = 0; i < kSegPerThread; ++i) {
       const int r = (wt >> 2) + i * kBM;
       const bool is_a = r < kBM;
       const int rr = is_a ? r : r - kBM;
-      const int64_t row = is_a ? a0 + rr : b0 + rr;
       const bool in_tile = is_a || rr < bn;
-      const bool valid = in_tile && row < (is_a ? rows_a : rows_b);
-      gp[i] = valid ? (is_a ? Am + row * lda : Bm + row * ldb) + segk : nullptr;
+      lo8[i] = (is_a ? 0u : static_cast<uint32_t>(kS8A)) + rr * kBK + seg * 16;
       so[i] = in_tile ? (is_a ? 0u : static_cast<uint32_t>(kStageA)) + rr * 128 +
                             static_cast<uint32_t>(((2 * seg) ^ (rr & 7)) * 16)
                       : 0xFFFFFFFFu;
     }
-    uint4 ring[kPrefetch][kSegPerThread];
-
-    auto load_stage = [&](int it, uint4 (&buf)[kSegPerThread]) {
-      const int64_t kb = (kt0 + it) * kBK;
-      const bool kin = kb + segk < a.K;
-#pragma unroll
-      for (int i = 0; i < kSegPerThread; ++i)
-        buf[i] = (gp[i] != nullptr && kin) ? ld_stream_16(gp[i] + kb) : make_uint4(0u, 0u, 0u, 0u);
-    };
     auto store_stage = [&](int s, const uint4 (&buf)[kSegPerThread]) {
       const uint32_t st_base = sStage + s * kStageBytes;
 #pragma unroll
@@ -547,36 +579,35 @@ __global__ void __launch_bounds__(kThreads, 1) linear_tc_kernel(const TcParams p
       return true;
     };
 
-#pragma unroll
-    for (int pf = 0; pf < kPrefetch; ++pf)
-      if (pf < nk) load_stage(pf, ring[pf]);
     bool ok = true;
     int next_drain = 0;  // next intermediate chunk to drain
-    for (int it0 = 0; it0 < nk && ok; it0 += kPrefetch) {
-#pragma unroll
-      for (int pf = 0; pf < kPrefetch; ++pf) {
-        const int it = it0 + pf;
-        if (it < nk && ok) {
-          // chunk c's last MMA completes exactly when stage it - kStages is
-          // released, so drain it here, after the next chunk's first stages
-          // have been prepared
-          if (next_drain < nchunks - 1 && it == (next_drain + 1) * kChunkStages + kStages - 1) {
-            ok = drain(next_drain, false);
-            ++next_drain;
-            if (!ok) break;
-          }
-          const int s = it % kStages;
-          ok = __shfl_sync(0xffffffffu,
-                           lane == 0 ? mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort) : false, 0);
-          if (ok) {
-            store_stage(s, ring[pf]);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full + 8 * s);
-            if (it + kPrefetch < nk) load_stage(it + kPrefetch, ring[pf]);
-          }
-        }
+    for (int it = 0; it < nk && ok; ++it) {
+      // chunk c's last MMA completes exactly when stage it - kStages is
+      // released, so drain it here, after the next chunk's first stages have
+      // been prepared
+      if (next_drain < nchunks - 1 && it == (next_drain + 1) * kChunkStages + kStages - 1) {
+        ok = drain(next_drain, false);
+        ++next_drain;
+        if (!ok) break;
       }
+      const int j = it % kS8Stages;
+      ok = __shfl_sync(0xffffffffu,
+                       lane == 0 ? mbar_wait(bar_s8_full + 8 * j, (it / kS8Stages) & 1, s_abort) : false, 0);
+      if (!ok) break;
+      uint4 buf[kSegPerThread];
+      const uint32_t s8 = sS8 + j * kS8Bytes;
+#pragma unroll
+      for (int i = 0; i < kSegPerThread; ++i) buf[i] = ld_shared_v4(s8 + lo8[i]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);   // the staging slot may be refilled
+      const int s = it % kStages;
+      ok = __shfl_sync(0xffffffffu,
+                       lane == 0 ? mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort) : false, 0);
+      if (!ok) break;
+      store_stage(s, buf);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_full + 8 * s);
     }
     while (ok && next_drain < nchunks - 1) ok = drain(next_drain++, false);
     if (ok && nchunks > 0) ok = drain(nchunks - 1, true);
@@ -671,6 +702,38 @@ static int tc_auto_split(int64_t M, int64_t N, int64_t K) {
   return best;
 }
 
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    tried = true;
+  }
+  return fn;
+}
+
+// Row-major int8 [rows, K] matrix with row stride ld bytes, read in boxes of
+// 64 K-bytes x box_rows rows; out-of-range rows and K read as zero.
+static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int64_t K, int64_t ld, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(linear_tc_kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -683,8 +746,15 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const uintptr_t wb = reinterpret_cast<uintptr_t>(a.w_scale);
   p.vec_io = (ob % 16 == 0) && (a.ldo % 8 == 0) && (wb % 16 == 0) &&
              (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
+  CUtensorMap tmA, tmB;
+  const int8_t* Am = pl.swap ? a.w : a.q;
+  const int8_t* Bm = pl.swap ? a.q : a.w;
+  e = make_map(&tmA, Am, pl.swap ? a.N : a.M, a.K, pl.swap ? a.ldw : a.ldq, kBM);
+  if (e != cudaSuccess) return e;
+  e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece);
+  if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y), static_cast<unsigned>(a.split));
-  linear_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  linear_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tmA, tmB);
   return cudaGetLastError();
 }
 
