@@ -17,12 +17,14 @@
 // result independent of chunking, tiling and split-K.
 //
 // CTA roles (576 threads = 18 warps, one CTA per SM):
-//   warp 17       lane 0 streams the raw int8 A and B tiles into a 3-deep
-//                 shared-memory staging ring with 2-D TMA loads;
+//   warp 17       lane 0 streams the raw int8 A and B tiles into a
+//                 shared-memory staging ring (3 to 8 stages, as many as fit
+//                 72 KB for the tile's width) with 2-D TMA loads;
 //   warp 4        TMEM allocator; lane 0 issues every tcgen05.mma;
 //   16 workers    (the other warps, four per TMEM lane quadrant) do all the
 //                 rest: exact int8->f16 widening from the staging ring into
-//                 128-byte-swizzled K-major f16 tiles (3 stages); at each
+//                 128-byte-swizzled K-major f16 tiles (3 to 8 stages in
+//                 144 KB); at each
 //                 1024-K chunk boundary each warp drains its quarter of its
 //                 quadrant's accumulator columns; at the end all 512 threads
 //                 write the tile out.
@@ -55,7 +57,7 @@ __device__ uint32_t g_kernel_error = 0;
 
 namespace {
 
-constexpr int kStages = 3;               // f16 operand stages read by the MMA
+constexpr int kMaxStages = 8;            // f16 operand / int8 staging stages (runtime count)
 constexpr int kBM = 128;                  // A rows per tile = TMEM lanes
 constexpr int kBNMax = 256;               // max B rows per tile = MMA N
 constexpr int kBK = 64;                   // K elements per stage (128 B of f16 per row)
@@ -65,19 +67,19 @@ constexpr int kWorkers = kWorkerWarps * 32;
 constexpr int kMmaWarp = 4;               // TMEM allocator + MMA issuer
 constexpr int kTmaWarp = 17;              // lane 0 issues the TMA loads
 constexpr int kThreads = kWorkers + 64;   // 576: 18 warps, at most 96 registers each
-constexpr int kS8Stages = 3;              // int8 staging stages filled by TMA
 constexpr int kS8A = kBM * kBK;           // bytes of one int8 A box (128 rows x 64)
-constexpr int kS8Bytes = kS8A + kBNMax * kBK;  // one int8 stage: A box then B box
 constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
 constexpr int kStageB = kBNMax * 128;     // bytes of one f16 B stage
-constexpr int kStageBytes = kStageA + kStageB;  // one stage: A tile then B tile
-constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kS8Stages * kS8Bytes + kBarBytes;
+constexpr int kF16Region = 3 * (kStageA + kStageB);   // 144 KB of f16 operand stages
+constexpr int kS8Region = 3 * (kBM + kBNMax) * kBK;   // 72 KB of int8 staging
+constexpr int kBarBytes = 512;
+constexpr int kSmemBytes = 1024 + kF16Region + kS8Region + kBarBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;             // fp32 chunk accumulator
 constexpr uint32_t kColI = 256;           // int32 running sum
 constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kWorkers;  // 3 x 16 B per stage
 static_assert((kBM * 4 + kBNMax * 4) % kWorkers == 0 && kWorkers / 4 == kBM, "segment layout");
+static_assert((kChunkStages & (kChunkStages - 1)) == 0, "chunk stages must be a power of two");
 constexpr uint32_t kDevErrTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -86,6 +88,8 @@ struct TcParams {
   int swap;      // 0 normal, 1 swapped
   int bpiece;    // B rows per tile (multiple of 32, <= 256)
   int vec_io;    // 16-byte vector epilogue loads/stores allowed (normal orientation)
+  int nst;       // f16 operand stages, each (128 + bpiece) x 128 bytes
+  int nst8;      // int8 staging stages, each (128 + bpiece) x 64 bytes
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -390,15 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const uint32_t sStage = base;                               // kStages x (A tile | B tile), f16
-  const uint32_t sS8 = sStage + kStages * kStageBytes;         // kS8Stages x (A box | B box), int8
-  const uint32_t bars = sS8 + kS8Stages * kS8Bytes;
+  const int nst = p.nst, nst8 = p.nst8;
+  const uint32_t kStageBytes = static_cast<uint32_t>((kBM + p.bpiece) * 128);
+  const uint32_t kS8Bytes = static_cast<uint32_t>((kBM + p.bpiece) * kBK);
+  const uint32_t sStage = base;                               // nst x (A tile | B tile), f16
+  const uint32_t sS8 = sStage + kF16Region;                   // nst8 x (A box | B box), int8
+  const uint32_t bars = sS8 + kS8Region;
   uint8_t* bar_ptr = smem + (bars - base);
-  const uint32_t bar_full = bars;                             // kStages x 8 B
-  const uint32_t bar_empty = bars + 8 * kStages;
-  const uint32_t bar_s8_full = bars + 16 * kStages;           // kS8Stages x 8 B
-  const uint32_t bar_s8_empty = bar_s8_full + 8 * kS8Stages;
-  const uint32_t bar_acc_full = bar_s8_empty + 8 * kS8Stages;
+  const uint32_t bar_full = bars;                             // kMaxStages x 8 B each
+  const uint32_t bar_empty = bars + 8 * kMaxStages;
+  const uint32_t bar_s8_full = bars + 16 * kMaxStages;
+  const uint32_t bar_s8_empty = bars + 24 * kMaxStages;
+  const uint32_t bar_acc_full = bars + 32 * kMaxStages;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_done = bar_acc_full + 16;
   uint8_t* scalars = bar_ptr + (bar_done + 8 - bars);
@@ -425,11 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nchunks = (nk + kChunkStages - 1) / kChunkStages;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(bar_full + 8 * s, kWorkerWarps);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int j = 0; j < kS8Stages; ++j) {
+    for (int j = 0; j < nst8; ++j) {
       mbar_init(bar_s8_full + 8 * j, 1);
       mbar_init(bar_s8_empty + 8 * j, kWorkerWarps);
     }
@@ -454,14 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= MMA issuer (one thread) =========================
     if (lane == 0 && nk > 0) {
       const uint32_t idesc = idesc_f16_f32(bn);
+      int s = 0;
+      uint32_t ph = 0;  // stage slot and its phase parity, advanced incrementally
       for (int it = 0; it < nk; ++it) {
-        const int s = it % kStages;
-        const int cpos = it % kChunkStages;
+        const int cpos = it & (kChunkStages - 1);
         if (cpos == 0 && it > 0) {
           if (!mbar_wait(bar_acc_empty, ((it / kChunkStages) - 1) & 1, s_abort)) break;
           tc_fence_after();
         }
-        if (!mbar_wait(bar_full + 8 * s, (it / kStages) & 1, s_abort)) break;
+        if (!mbar_wait(bar_full + 8 * s, ph, s_abort)) break;
         tc_fence_after();
         const uint64_t ad = smem_desc_sw128(sStage + s * kStageBytes);
         const uint64_t bd = smem_desc_sw128(sStage + s * kStageBytes + kStageA);
@@ -470,6 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma(tmem + kColD, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
         tc_commit(bar_empty + 8 * s);
         if (cpos == kChunkStages - 1 || it == nk - 1) tc_commit(bar_acc_full);
+        if (++s == nst) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       // every MMA issued above has completed before TMEM is released
       tc_commit(bar_done);
@@ -486,14 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= TMA producer (one thread) ========================
     if (lane == 0 && nk > 0) {
       const uint32_t tx = static_cast<uint32_t>(kS8A + kBK * p.bpiece);
+      int j = 0;
+      uint32_t ph = 0;
       for (int it = 0; it < nk; ++it) {
-        const int j = it % kS8Stages;
-        if (!mbar_wait(bar_s8_empty + 8 * j, ((it / kS8Stages) & 1) ^ 1, s_abort)) break;
+        if (!mbar_wait(bar_s8_empty + 8 * j, ph ^ 1u, s_abort)) break;
         const uint32_t dst = sS8 + j * kS8Bytes;
         const int32_t x = static_cast<int32_t>((kt0 + it) * kBK);
         mbar_expect_tx(bar_s8_full + 8 * j, tx);
         tma_load_2d(dst, &tmA, x, static_cast<int32_t>(a0), bar_s8_full + 8 * j);
         tma_load_2d(dst + kS8A, &tmB, x, static_cast<int32_t>(b0), bar_s8_full + 8 * j);
+        if (++j == nst8) {
+          j = 0;
+          ph ^= 1u;
+        }
       }
     }
     __syncwarp();
@@ -581,33 +598,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool ok = true;
     int next_drain = 0;  // next intermediate chunk to drain
+    int next_trigger = kChunkStages + nst - 1;
+    int j = 0, s = 0;
+    uint32_t ph8 = 0, ph = 0;  // staging / operand slots and phase parities
     for (int it = 0; it < nk && ok; ++it) {
-      // chunk c's last MMA completes exactly when stage it - kStages is
+      // chunk c's last MMA completes exactly when stage it - nst is
       // released, so drain it here, after the next chunk's first stages have
       // been prepared
-      if (next_drain < nchunks - 1 && it == (next_drain + 1) * kChunkStages + kStages - 1) {
+      if (next_drain < nchunks - 1 && it == next_trigger) {
         ok = drain(next_drain, false);
         ++next_drain;
+        next_trigger += kChunkStages;
         if (!ok) break;
       }
-      const int j = it % kS8Stages;
-      ok = __shfl_sync(0xffffffffu,
-                       lane == 0 ? mbar_wait(bar_s8_full + 8 * j, (it / kS8Stages) & 1, s_abort) : false, 0);
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_s8_full + 8 * j, ph8, s_abort) : false, 0);
       if (!ok) break;
       uint4 buf[kSegPerThread];
       const uint32_t s8 = sS8 + j * kS8Bytes;
 #pragma unroll
-      for (int i = 0; i < kSegPerThread; ++i) buf[i] = ld_shared_v4(s8 + lo8[i]);
+      for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
+        buf[i] = so[i] != 0xFFFFFFFFu ? ld_shared_v4(s8 + lo8[i]) : make_uint4(0u, 0u, 0u, 0u);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);   // the staging slot may be refilled
-      const int s = it % kStages;
-      ok = __shfl_sync(0xffffffffu,
-                       lane == 0 ? mbar_wait(bar_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort) : false, 0);
+      if (++j == nst8) {
+        j = 0;
+        ph8 ^= 1u;
+      }
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_empty + 8 * s, ph ^ 1u, s_abort) : false, 0);
       if (!ok) break;
       store_stage(s, buf);
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_full + 8 * s);
+      if (++s == nst) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     while (ok && next_drain < nchunks - 1) ok = drain(next_drain++, false);
     if (ok && nchunks > 0) ok = drain(nchunks - 1, true);
@@ -746,6 +772,8 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const uintptr_t wb = reinterpret_cast<uintptr_t>(a.w_scale);
   p.vec_io = (ob % 16 == 0) && (a.ldo % 8 == 0) && (wb % 16 == 0) &&
              (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
+  p.nst = std::min(kMaxStages, kF16Region / ((kBM + pl.bpiece) * 128));
+  p.nst8 = std::min(kMaxStages, kS8Region / ((kBM + pl.bpiece) * kBK));
   CUtensorMap tmA, tmB;
   const int8_t* Am = pl.swap ? a.w : a.q;
   const int8_t* Bm = pl.swap ? a.q : a.w;
