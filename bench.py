@@ -430,7 +430,7 @@ def run_gpu(args):
     hbm_gbs, bf16_tflops, peak_src = load_peaks()
     qkv_avg_s = statistics.mean(qkv_ms) / 1e3
     achieved = work.ops_linear_qkv / qkv_avg_s / 1e12
-    traffic = kernel_traffic("linear_mma.cu", "linear_qkv_m304_k5120_n15360")
+    traffic = kernel_traffic("linear_tc.cu", "linear_qkv_m304_k5120_n15360")
     roofline = {"kernel": "prism_w8a8_linear (QKV, M=304 K=5120 N=15360)", "bound": "tensor",
                 "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
                 "frac": achieved / bf16_tflops, "traffic": traffic,
