@@ -92,6 +92,24 @@ class Workload:
         self.bytes = self.bytes_qkv + self.bytes_o + self.bytes_quant + self.bytes_readout
 
 
+def reduce_max(value: float, device) -> float:
+    """Max of ``value`` over all ranks of the default process group (the value
+    itself when no group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(ops_per_step: float, steps: int, world: int, t_ms: float) -> float:
+    """Whole-job TOPS: every rank runs ``steps`` steps of its own bucket; the
+    job time is the slowest rank's."""
+    return ops_per_step * steps * world / (t_ms / 1e3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -370,13 +388,9 @@ def run_gpu(args):
     if int(err.item()) != 0:
         raise RuntimeError(f"read-out device error word {int(err.item())}")
 
-    t_max = elapsed_ms
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = reduce_max(elapsed_ms, dev)
     secs = t_max / 1e3
-    value = work.ops * args.steps * world / secs / 1e12
+    value = weak_scaling_value(work.ops, args.steps, world, t_max)
 
     # ---- end to end through the binding, host buffers, copies inside timing
     pin = lambda a: a.pin_memory()
@@ -419,12 +433,8 @@ def run_gpu(args):
             e2e_step(i)
         e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = work.ops * args.steps * world / (e2e_ms / 1e3) / 1e12
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dev)
+    e2e_value = weak_scaling_value(work.ops, args.steps, world, e2e_ms)
 
     # ---- roofline of the dominant kernel (the QKV linear)
     hbm_gbs, bf16_tflops, peak_src = load_peaks()
