@@ -18,13 +18,12 @@
 //
 // CTA roles (576 threads = 18 warps, one CTA per SM):
 //   warp 17       lane 0 streams the raw int8 A and B tiles into a
-//                 shared-memory staging ring (3 to 8 stages, as many as fit
-//                 72 KB for the tile's width) with 2-D TMA loads;
+//                 shared-memory staging ring (3 stages at width 256, up to 8
+//                 for narrow tiles) with 2-D TMA loads;
 //   warp 4        TMEM allocator; lane 0 issues every tcgen05.mma;
 //   16 workers    (the other warps, four per TMEM lane quadrant) do all the
 //                 rest: exact int8->f16 widening from the staging ring into
-//                 128-byte-swizzled K-major f16 tiles (3 to 8 stages in
-//                 144 KB); at each
+//                 128-byte-swizzled K-major f16 tiles (3 stages); at each
 //                 1024-K chunk boundary each warp drains its quarter of its
 //                 quadrant's accumulator columns; at the end all 512 threads
 //                 write the tile out.
@@ -69,11 +68,12 @@ constexpr int kTmaWarp = 17;              // lane 0 issues the TMA loads
 constexpr int kThreads = kWorkers + 64;   // 576: 18 warps, at most 96 registers each
 constexpr int kS8A = kBM * kBK;           // bytes of one int8 A box (128 rows x 64)
 constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
-constexpr int kStageB = kBNMax * 128;     // bytes of one f16 B stage
-constexpr int kF16Region = 3 * (kStageA + kStageB);   // 144 KB of f16 operand stages
-constexpr int kS8Region = 3 * (kBM + kBNMax) * kBK;   // 72 KB of int8 staging
+// One 216 KB region holds both rings: f16 operand stages first, then int8
+// staging stages (the int8 ring gets whatever the f16 ring leaves, so that
+// enough TMA loads are in flight to cover their latency).
+constexpr int kRingRegion = 216 * 1024;
 constexpr int kBarBytes = 512;
-constexpr int kSmemBytes = 1024 + kF16Region + kS8Region + kBarBytes;
+constexpr int kSmemBytes = 1024 + kRingRegion + kBarBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;             // fp32 chunk accumulator
 constexpr uint32_t kColI = 256;           // int32 running sum
@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t kStageBytes = static_cast<uint32_t>((kBM + p.bpiece) * 128);
   const uint32_t kS8Bytes = static_cast<uint32_t>((kBM + p.bpiece) * kBK);
   const uint32_t sStage = base;                               // nst x (A tile | B tile), f16
-  const uint32_t sS8 = sStage + kF16Region;                   // nst8 x (A box | B box), int8
-  const uint32_t bars = sS8 + kS8Region;
+  const uint32_t sS8 = sStage + nst * kStageBytes;            // nst8 x (A box | B box), int8
+  const uint32_t bars = base + kRingRegion;
   uint8_t* bar_ptr = smem + (bars - base);
   const uint32_t bar_full = bars;                             // kMaxStages x 8 B each
   const uint32_t bar_empty = bars + 8 * kMaxStages;
@@ -618,18 +618,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
         buf[i] = so[i] != 0xFFFFFFFFu ? ld_shared_v4(s8 + lo8[i]) : make_uint4(0u, 0u, 0u, 0u);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);   // the staging slot may be refilled
-      if (++j == nst8) {
-        j = 0;
-        ph8 ^= 1u;
-      }
       ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_empty + 8 * s, ph ^ 1u, s_abort) : false, 0);
       if (!ok) break;
       store_stage(s, buf);
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_full + 8 * s);
+      if (lane == 0) {
+        mbar_arrive(bar_full + 8 * s);
+        // released only now: every value read from the staging slot has been
+        // consumed by the widening, so a TMA refill cannot overtake a load
+        mbar_arrive(bar_s8_empty + 8 * j);
+      }
+      if (++j == nst8) {
+        j = 0;
+        ph8 ^= 1u;
+      }
       if (++s == nst) {
         s = 0;
         ph ^= 1u;
@@ -772,8 +775,8 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const uintptr_t wb = reinterpret_cast<uintptr_t>(a.w_scale);
   p.vec_io = (ob % 16 == 0) && (a.ldo % 8 == 0) && (wb % 16 == 0) &&
              (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
-  p.nst = std::min(kMaxStages, kF16Region / ((kBM + pl.bpiece) * 128));
-  p.nst8 = std::min(kMaxStages, kS8Region / ((kBM + pl.bpiece) * kBK));
+  p.nst = 3;
+  p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * (kBM + pl.bpiece) * 128) / ((kBM + pl.bpiece) * kBK));
   CUtensorMap tmA, tmB;
   const int8_t* Am = pl.swap ? a.w : a.q;
   const int8_t* Bm = pl.swap ? a.q : a.w;
