@@ -544,6 +544,107 @@ def run_kernel(args):
     return 0
 
 
+def graph_time_us(calls, reps: int = 5):
+    """Mean device time per call of the no-argument launch callables in
+    ``calls``: they are captured back to back in one CUDA graph (so host
+    marshalling is not timed) and the graph is replayed ``reps`` times."""
+    import torch
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for c in calls:          # warm: per-device attributes, lazy module loading
+            c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
+
+
+def run_kernel_quant(args):
+    """Time prism_quant_act alone on the activations of --case (HBM-bound)."""
+    import torch
+
+    import deterministic_w8a8_int8_gb300 as prism
+
+    dev = torch.device("cuda", 0)
+    c = wl.make_linear(args.case)
+    rows = c.M if args.rows is None else args.rows
+    K = c.K
+    n_rot = max(1, int(np.ceil(3 * 129e6 / (rows * K * 3))))
+    xs = [torch.from_numpy(c.x_bits[:rows].view(np.int16)).view(torch.bfloat16).to(dev) for _ in range(n_rot)]
+    inv = torch.from_numpy(c.inv_s).to(dev)
+    qs = [torch.empty((rows, K), dtype=torch.int8, device=dev) for _ in range(n_rot)]
+    a = torch.empty((rows,), dtype=torch.float32, device=dev)
+    calls = [lambda i=i: prism.prism_quant_act(xs[i % n_rot], inv, q=qs[i % n_rot], a_scale=a)
+             for i in range(max(args.steps, n_rot))]
+    avg = graph_time_us(calls)
+    byts = 3 * rows * K + 4 * rows + 4 * K
+    hbm, _, _ = load_peaks()
+    print(json.dumps({"kernel": "prism_quant_act", "case": args.case, "M": rows, "K": K, "avg_us": avg,
+                      "gbs": byts / avg / 1e3, "frac_hbm": byts / avg / 1e3 / hbm,
+                      "timing": "CUDA graph of back-to-back calls, %d activation copies" % n_rot}), flush=True)
+    return 0
+
+
+def run_kernel_readout(args):
+    """Time prism_candidate_readout alone: P answer positions of a 248,000 x
+    5120 LM head (several head copies rotated so gathers come from HBM)."""
+    import torch
+
+    import deterministic_w8a8_int8_gb300 as prism
+
+    dev = torch.device("cuda", 0)
+    P = 192 if args.rows is None else args.rows
+    case = wl.readout_case("readout", P=P, K=wl.HIDDEN, V=wl.VOCAB, seed=7)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    heads = []
+    uniq = np.unique(case.cand_ids)
+    rows = torch.from_numpy(case.lm_rows(uniq)).to(dev)
+    for _ in range(2):
+        W = torch.randint(-127, 128, (case.V, case.K), dtype=torch.int8, device=dev, generator=g)
+        W[torch.from_numpy(uniq.astype(np.int64)).to(dev)] = rows
+        heads.append(W)
+    # candidate lists rotated through independent id sets, enough of them that
+    # the rows all calls gather (about 5.8 MB per call at P=192) exceed L2
+    n_sets = max(8, int(np.ceil(2 * 129e6 / (P * 6 * (wl.HIDDEN + 4)))))
+    sets = []
+    for r in range(n_sets):
+        cs = wl.readout_case("readout", P=P, K=wl.HIDDEN, V=wl.VOCAB, seed=100 + r)
+        sets.append((torch.from_numpy(cs.h_bits.view(np.int16)).view(torch.bfloat16).to(dev),
+                     torch.from_numpy(cs.cand_offsets).to(dev), torch.from_numpy(cs.cand_ids).to(dev),
+                     cs.cand_ids.size))
+    ls = torch.from_numpy(case.lm_scale).to(dev)
+    Tmax = max(x[3] for x in sets)
+    lg = torch.empty((Tmax,), dtype=torch.float32, device=dev)
+    pr = torch.empty((Tmax,), dtype=torch.float32, device=dev)
+
+    def call(i):
+        h, off, ids, T = sets[i % n_sets]
+        prism.prism_candidate_readout(h, None, heads[i % 2], ls, off, ids, logits=lg[:T], probs=pr[:T])
+
+    avg = graph_time_us([lambda i=i: call(i) for i in range(max(args.steps, 2 * n_sets))])
+    T = statistics.mean(x[3] for x in sets)
+    K = case.K
+    byts = 2 * P * K + T * (K + 4) + 4 * (P + 1) + 4 * T + 8 * T
+    hbm, _, _ = load_peaks()
+    print(json.dumps({"kernel": "prism_candidate_readout", "P": P, "T_avg": T, "K": K, "avg_us": avg,
+                      "gbs": byts / avg / 1e3, "frac_hbm": byts / avg / 1e3 / hbm,
+                      "timing": "CUDA graph of back-to-back calls, %d candidate sets x 2 heads" % n_sets}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -551,7 +652,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["linear"], help="time one call type alone on --case")
+    ap.add_argument("--kernel", choices=["linear", "quant", "readout"], help="time one call type alone")
     ap.add_argument("--case", default="forest_qkv_m304_k5120_n15360", choices=sorted(wl.LINEAR_CONFIGS))
     ap.add_argument("--rows", type=int, default=None, help="use the first ROWS token rows of --case")
     ap.add_argument("--split", type=int, default=None, help="split-K for --kernel (default automatic)")
@@ -560,6 +661,10 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel == "quant":
+        return run_kernel_quant(args)
+    if args.kernel == "readout":
+        return run_kernel_readout(args)
     if args.kernel:
         return run_kernel(args)
     return run_gpu(args)

@@ -251,3 +251,24 @@ def test_contraction_kernels_agree(cuda_device, M, N, K):
     _, _, outo, _ = oracle_full(xb, None, w, w_scale, rb)
     assert np.array_equal(host_bits(outs["tc"][0]), outo)
     assert prism.prism_device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(600, 512, 4096), (64, 512, 3072), (304, 520, 5120), (1000, 300, 2048)])
+def test_repeated_runs_bit_identical(cuda_device, M, N, K):
+    """Twenty back-to-back calls (different pipeline timings each time) must
+    all give the oracle's bits: a race between the staging, widening and MMA
+    stages would show up as an intermittent mismatch."""
+    rng = np.random.default_rng(M + N + K)
+    q = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    w = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    acco = oracle.gemm_s32(q, w)
+    Q, W = dev(q), dev(w)
+    a = torch.ones(M, device="cuda")
+    s = torch.ones(N, device="cuda")
+    accs = [torch.empty((M, N), dtype=torch.int32, device="cuda") for _ in range(20)]
+    for acc in accs:
+        prism.prism_w8a8_linear(Q, a, W, s, acc_out=acc, split_k=1)
+    torch.cuda.synchronize()
+    for acc in accs:
+        assert np.array_equal(host(acc), acco)
+    assert prism.prism_device_status() == 0
