@@ -14,7 +14,10 @@
 // The fp32 accumulator D lives in tensor memory (TMEM).  After each chunk the
 // drain warps read D, convert it to int32 (exact) and add it into a second
 // TMEM region I holding the int32 running sum; integer addition makes the
-// result independent of chunking, tiling and split-K.
+// result independent of chunking, tiling and split-K.  Where three tile widths
+// fit the 512 TMEM columns (tiles of at most 160 B rows), D is double-buffered:
+// chunk c accumulates in D[c % 2] while the workers drain D[(c - 1) % 2], so
+// the tensor pipe does not wait for the drain.
 //
 // CTA roles (576 threads = 18 warps, one CTA per SM):
 //   warp 17       lane 0 streams the raw int8 A and B tiles into a
@@ -28,8 +31,9 @@
 //                 quadrant's accumulator columns; at the end all 512 threads
 //                 write the tile out.
 // mbarriers: s8_full (TMA transaction count), s8_empty, full and acc_empty
-// (one arrival per worker warp), empty and acc_full (tcgen05.commit); one
-// lane per warp polls a barrier and shares the result with its warp.  Every
+// (one arrival per worker warp), empty and acc_full (tcgen05.commit).  Worker
+// warps wait with all 32 lanes polling and agreeing on the outcome, so a warp
+// never splits around a single polling lane.  Every
 // wait is bounded by a 2-second global-timer limit; on expiry the CTA records
 // kDevErrTimeout in the library's device error word and winds down.
 //
@@ -73,10 +77,11 @@ constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
 // enough TMA loads are in flight to cover their latency).
 constexpr int kRingRegion = 216 * 1024;
 constexpr int kBarBytes = 512;
-constexpr int kSmemBytes = 1024 + kRingRegion + kBarBytes;
+constexpr int kScaleBytes = 2 * kBNMax * 4;   // the tile's a_scale and w_scale values
+constexpr int kSmemBytes = 1024 + kRingRegion + kBarBytes + kScaleBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD = 0;             // fp32 chunk accumulator
-constexpr uint32_t kColI = 256;           // int32 running sum
+constexpr uint32_t kColD = 0;             // fp32 chunk accumulator (single-buffered layout)
+constexpr uint32_t kColI = 256;           // int32 running sum (single-buffered layout)
 constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kWorkers;  // 3 x 16 B per stage
 static_assert((kBM * 4 + kBNMax * 4) % kWorkers == 0 && kWorkers / 4 == kBM, "segment layout");
 static_assert((kChunkStages & (kChunkStages - 1)) == 0, "chunk stages must be a power of two");
@@ -129,6 +134,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       }
     }
   }
+}
+// The same wait made by every lane of a warp: all lanes poll (one broadcast
+// shared-memory read per poll) and the warp agrees on the outcome, so the warp
+// never splits around a single polling lane.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -207,14 +218,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+// 16-byte shared-memory load when pred holds, else zeros (predicated, no branch).
+__device__ __forceinline__ uint4 ld_shared_v4_if(uint32_t addr, bool pred) {
   uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %5, 0;\n mov.u32 %0, 0;\n mov.u32 %1, 0;\n mov.u32 %2, 0;\n mov.u32 %3, 0;\n"
+      " @p ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n}\n"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(addr), "r"(static_cast<uint32_t>(pred)));
   return v;
 }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+// 16-byte shared-memory store when pred holds (predicated, no branch).
+__device__ __forceinline__ void st_shared_v4_if(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                bool pred) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %5, 0;\n @p st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n}\n" ::"r"(addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(static_cast<uint32_t>(pred))
+      : "memory");
 }
 
 // --------------------------------------------------------------- epilogue --
@@ -241,8 +261,11 @@ __device__ __forceinline__ void emit(const LinearArgs& a, int64_t m, int64_t n, 
 constexpr int kRowBatch = 4;
 constexpr int kMaxGroupsPerThread = kBNMax / 4 / 32;   // 2
 
-__device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, int rows_out, int cols_out,
-                                         int64_t m0, int64_t n0, int mode, int t, int nthreads) {
+// s_as[r] / s_ws[c]: a_scale of the tile's token r and w_scale of its channel
+// c, copied into shared memory when the CTA started.
+__device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, const float* s_as,
+                                         const float* s_ws, int rows_out, int cols_out, int64_t m0,
+                                         int64_t n0, int mode, int t, int nthreads) {
   const LinearArgs& a = p.a;
   const int stride = cols_out + 4;
   const int groups = cols_out / 4;                 // 4-column groups per row
@@ -312,7 +335,7 @@ __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, i
     const int64_t n = n0 + 4 * (g0 + q * per_row);
     wsv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (mode != 1 && q < gpt && p.vec_io && n + 4 <= a.N)
-      wsv[q] = __ldg(reinterpret_cast<const float4*>(a.w_scale + n));
+      wsv[q] = *reinterpret_cast<const float4*>(s_ws + 4 * (g0 + q * per_row));
   }
 
   for (int rb = t / per_row; rb < rows_out; rb += rows_per_pass * kRowBatch) {
@@ -324,7 +347,7 @@ __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, i
       const int r = rb + b * rows_per_pass;
       const int64_t m = m0 + r;
       const bool row_ok = r < rows_out && m < a.M;
-      as[b] = (mode != 1 && row_ok) ? __ldg(a.a_scale + m) : 0.f;
+      as[b] = (mode != 1 && row_ok) ? s_as[r] : 0.f;
 #pragma unroll
       for (int q = 0; q < kMaxGroupsPerThread; ++q) {
         const int c = 4 * (g0 + q * per_row);
@@ -405,13 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_empty = bars + 8 * kMaxStages;
   const uint32_t bar_s8_full = bars + 16 * kMaxStages;
   const uint32_t bar_s8_empty = bars + 24 * kMaxStages;
-  const uint32_t bar_acc_full = bars + 32 * kMaxStages;
-  const uint32_t bar_acc_empty = bar_acc_full + 8;
-  const uint32_t bar_done = bar_acc_full + 16;
+  const uint32_t bar_acc_full = bars + 32 * kMaxStages;      // 2 x 8 B: one per D buffer
+  const uint32_t bar_acc_empty = bar_acc_full + 16;           // 2 x 8 B
+  const uint32_t bar_done = bar_acc_full + 32;
   uint8_t* scalars = bar_ptr + (bar_done + 8 - bars);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(scalars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(scalars + 4);
   int* s_last = reinterpret_cast<int*>(scalars + 8);
+  float* s_as = reinterpret_cast<float*>(bar_ptr + kBarBytes);   // kBNMax token scales
+  float* s_ws = s_as + kBNMax;                                    // kBNMax channel scales
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -430,6 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t kt1 = kt0 + per < ktiles ? kt0 + per : ktiles;
   const int nk = kt1 > kt0 ? static_cast<int>(kt1 - kt0) : 0;
   const int nchunks = (nk + kChunkStages - 1) / kChunkStages;
+  // TMEM layout: double-buffered D[0] | D[1] | I when three widths fit, else D | I
+  const bool dbuf = 3 * p.bpiece <= static_cast<int>(kTmemCols);
+  const uint32_t col_i = dbuf ? 2u * static_cast<uint32_t>(p.bpiece) : kColI;
 
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -440,8 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_s8_full + 8 * j, 1);
       mbar_init(bar_s8_empty + 8 * j, kWorkerWarps);
     }
-    mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, kWorkerWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_acc_full + 8 * b, 1);
+      mbar_init(bar_acc_empty + 8 * b, kWorkerWarps);
+    }
     mbar_init(bar_done, 1);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -463,11 +493,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_f16_f32(bn);
       int s = 0;
       uint32_t ph = 0;  // stage slot and its phase parity, advanced incrementally
+      int c = -1;       // current chunk
+      uint32_t dcol = kColD, dbar = 0;
       for (int it = 0; it < nk; ++it) {
         const int cpos = it & (kChunkStages - 1);
-        if (cpos == 0 && it > 0) {
-          if (!mbar_wait(bar_acc_empty, ((it / kChunkStages) - 1) & 1, s_abort)) break;
-          tc_fence_after();
+        if (cpos == 0) {
+          // chunk c reuses the D buffer of chunk c - 2 (double-buffered) or
+          // c - 1: wait until the workers have drained it
+          ++c;
+          const int prev = c - (dbuf ? 2 : 1);
+          dbar = dbuf ? static_cast<uint32_t>(c & 1) : 0u;
+          dcol = dbuf && (c & 1) ? static_cast<uint32_t>(p.bpiece) : kColD;
+          if (prev >= 0) {
+            const uint32_t use = static_cast<uint32_t>(dbuf ? prev >> 1 : prev);
+            if (!mbar_wait(bar_acc_empty + 8 * dbar, use & 1u, s_abort)) break;
+            tc_fence_after();
+          }
         }
         if (!mbar_wait(bar_full + 8 * s, ph, s_abort)) break;
         tc_fence_after();
@@ -475,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = smem_desc_sw128(sStage + s * kStageBytes + kStageA);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
-          tc_mma(tmem + kColD, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
+          tc_mma(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
         tc_commit(bar_empty + 8 * s);
-        if (cpos == kChunkStages - 1 || it == nk - 1) tc_commit(bar_acc_full);
+        if (cpos == kChunkStages - 1 || it == nk - 1) tc_commit(bar_acc_full + 8 * dbar);
         if (++s == nst) {
           s = 0;
           ph ^= 1u;
@@ -528,6 +569,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int trow = quad * 32 + lane;                    // this thread's TMEM lane
     uint32_t* T = reinterpret_cast<uint32_t*>(smem);
+    {
+      // the epilogue's scales, read now so that their memory latency overlaps
+      // the first TMA loads instead of the tile's output; the residual tile is
+      // prefetched into L2 for the same reason
+      const int64_t tok0 = p.swap ? b0 : a0, ch0 = p.swap ? a0 : b0;
+      const int ntok = p.swap ? bn : kBM, nch = p.swap ? kBM : bn;
+      if (wt < kBNMax) {
+        const int64_t m = tok0 + wt;
+        s_as[wt] = wt < ntok && m < a.M ? __ldg(a.a_scale + m) : 0.f;
+      } else {
+        const int i = wt - kBNMax;
+        const int64_t n = ch0 + i;
+        s_ws[i] = i < nch && n < a.N ? __ldg(a.w_scale + n) : 0.f;
+      }
+      if (a.residual != nullptr) {
+        const int lines = (nch * 2 + 127) / 128;  // 128-byte lines per token row
+        for (int l = wt; l < ntok * lines; l += kWorkers) {
+          const int r = l / lines;
+          const int64_t m = tok0 + r, n = ch0 + (l - r * lines) * 64;
+          if (m < a.M && n < a.N)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.residual + m * a.ldr + n));
+        }
+      }
+    }
     const int seg = wt & 3;
     // per segment: offset of its 16 int8 bytes in a staging stage, and of its
     // first 16-byte f16 chunk in an operand stage (the second is that ^ 16)
@@ -548,36 +613,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st_base = sStage + s * kStageBytes;
 #pragma unroll
       for (int i = 0; i < kSegPerThread; ++i) {
-        if (so[i] != 0xFFFFFFFFu) {
-          uint32_t w[8];
-          widen4(buf[i].x, w[0], w[1]);
-          widen4(buf[i].y, w[2], w[3]);
-          widen4(buf[i].z, w[4], w[5]);
-          widen4(buf[i].w, w[6], w[7]);
-          const uint32_t addr = st_base + so[i];
-          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-          st_shared_v4(addr ^ 16u, w[4], w[5], w[6], w[7]);
-        }
+        uint32_t w[8];
+        widen4(buf[i].x, w[0], w[1]);
+        widen4(buf[i].y, w[2], w[3]);
+        widen4(buf[i].z, w[4], w[5]);
+        widen4(buf[i].w, w[6], w[7]);
+        const bool valid = so[i] != 0xFFFFFFFFu;   // rows beyond the tile lie outside the stage
+        const uint32_t addr = st_base + (valid ? so[i] : 0u);
+        st_shared_v4_if(addr, w[0], w[1], w[2], w[3], valid);
+        st_shared_v4_if(addr ^ 16u, w[4], w[5], w[6], w[7], valid);
       }
     };
     // Drain this warp's share of chunk c: I += int(D) (or, for the last
     // chunk, stage the final values as T[token][channel]).
     auto drain = [&](int c, bool last) -> bool {
-      const bool got = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_acc_full, c & 1, s_abort) : false, 0);
+      const uint32_t dbar = dbuf ? static_cast<uint32_t>(c & 1) : 0u;
+      const uint32_t use = static_cast<uint32_t>(dbuf ? c >> 1 : c);
+      const uint32_t dcol = dbuf && (c & 1) ? static_cast<uint32_t>(p.bpiece) : kColD;
+      const bool got = mbar_wait_warp(bar_acc_full + 8 * dbar, use & 1u, s_abort);
       if (!got) return false;
       tc_fence_after();
       const int rounds = bn / 16;
       for (int cb = slice; cb < rounds; cb += 4) {
         uint32_t d[16], iv[16];
-        tmem_ld16(tmem + lane_base + kColD + cb * 16, d);
-        if (c > 0) tmem_ld16(tmem + lane_base + kColI + cb * 16, iv);
+        tmem_ld16(tmem + lane_base + dcol + cb * 16, d);
+        if (c > 0) tmem_ld16(tmem + lane_base + col_i + cb * 16, iv);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           d[j] = static_cast<uint32_t>((c > 0 ? static_cast<int32_t>(iv[j]) : 0) +
                                        __float2int_rn(__uint_as_float(d[j])));
         if (!last) {
-          tmem_st16(tmem + lane_base + kColI + cb * 16, d);
+          tmem_st16(tmem + lane_base + col_i + cb * 16, d);
         } else if (!p.swap) {
           uint4* dst = reinterpret_cast<uint4*>(T + trow * (bn + 4) + cb * 16);
 #pragma unroll
@@ -591,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_acc_empty);
+        if (lane == 0) mbar_arrive(bar_acc_empty + 8 * dbar);
       }
       return true;
     };
@@ -611,24 +678,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         next_trigger += kChunkStages;
         if (!ok) break;
       }
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_s8_full + 8 * j, ph8, s_abort) : false, 0);
+      ok = mbar_wait_warp(bar_s8_full + 8 * j, ph8, s_abort);
       if (!ok) break;
       uint4 buf[kSegPerThread];
       const uint32_t s8 = sS8 + j * kS8Bytes;
 #pragma unroll
       for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
-        buf[i] = so[i] != 0xFFFFFFFFu ? ld_shared_v4(s8 + lo8[i]) : make_uint4(0u, 0u, 0u, 0u);
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_empty + 8 * s, ph ^ 1u, s_abort) : false, 0);
+        buf[i] = ld_shared_v4_if(s8 + lo8[i], so[i] != 0xFFFFFFFFu);
+      ok = mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, s_abort);
       if (!ok) break;
       store_stage(s, buf);
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_full + 8 * s);
-        // released only now: every value read from the staging slot has been
-        // consumed by the widening, so a TMA refill cannot overtake a load
-        mbar_arrive(bar_s8_empty + 8 * j);
-      }
+      if (lane == 0) mbar_arrive(bar_full + 8 * s);
+      // released only now: every value read from the staging slot has been
+      // consumed by the widening, so a TMA refill cannot overtake a load
+      if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);
       if (++j == nst8) {
         j = 0;
         ph8 ^= 1u;
@@ -647,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t om = p.swap ? b0 : a0;   // first token of the tile
     const int64_t on = p.swap ? a0 : b0;   // first channel of the tile
     asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-    if (ok && nchunks > 0) tile_out(p, T, rows_out, cols_out, om, on, a.split == 1 ? 0 : 1, wt, kWorkers);
+    if (ok && nchunks > 0) tile_out(p, T, s_as, s_ws, rows_out, cols_out, om, on, a.split == 1 ? 0 : 1, wt, kWorkers);
     if (a.split > 1) {
       // integer split-K: the last CTA to finish this tile applies the epilogue
       __threadfence();
@@ -657,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
       if (*s_last) {
         __threadfence();
-        tile_out(p, T, rows_out, cols_out, om, on, 2, wt, kWorkers);
+        tile_out(p, T, s_as, s_ws, rows_out, cols_out, om, on, 2, wt, kWorkers);
         if (wt == 0) a.ws_count[tile] = 0u;
       }
     }
