@@ -261,6 +261,63 @@ __device__ __forceinline__ void emit(const LinearArgs& a, int64_t m, int64_t n, 
 constexpr int kRowBatch = 4;
 constexpr int kMaxGroupsPerThread = kBNMax / 4 / 32;   // 2
 
+// Epilogue of a tile whose channel width is 128 (kWide false) or 256 (true)
+// and lies wholly inside N, with vector I/O and no int32 dump: warp w writes
+// token rows w, w + 16, ... (a warp-uniform row test, no per-element
+// branches), lane l channels 4l..4l+3 (and 128 + 4l.. when wide); the lane's
+// w_scale values stay in registers and the residuals of kB rows are loaded
+// before any of them is used.
+template <bool kRes, bool kWide>
+__device__ __forceinline__ void tile_out_fast(const TcParams& p, const uint32_t* T, const float* s_as,
+                                              const float* s_ws, int rows_valid, int cols_out, int64_t m0,
+                                              int64_t n0, int t) {
+  const LinearArgs& a = p.a;
+  constexpr int kB = 4;
+  const int stride = cols_out + 4;
+  const int w = t >> 5, l = t & 31;
+  const float4 ws0 = reinterpret_cast<const float4*>(s_ws)[l];
+  const float4 ws1 = kWide ? reinterpret_cast<const float4*>(s_ws)[l + 32] : make_float4(0.f, 0.f, 0.f, 0.f);
+  uint16_t* out0 = a.out + m0 * a.ldo + n0 + 4 * l;
+  const uint16_t* res0 = kRes ? a.residual + m0 * a.ldr + n0 + 4 * l : nullptr;
+  for (int rb = w; rb < rows_valid; rb += 16 * kB) {
+    uint2 rv[kB][2];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int r = rb + 16 * b;
+      rv[b][0] = rv[b][1] = make_uint2(0u, 0u);
+      if (kRes && r < rows_valid) {
+        rv[b][0] = *reinterpret_cast<const uint2*>(res0 + r * a.ldr);
+        if (kWide) rv[b][1] = *reinterpret_cast<const uint2*>(res0 + r * a.ldr + 128);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int r = rb + 16 * b;
+      if (r < rows_valid) {
+        const float as = s_as[r];
+#pragma unroll
+        for (int h = 0; h < (kWide ? 2 : 1); ++h) {
+          const uint4 tv = *reinterpret_cast<const uint4*>(T + r * stride + 4 * l + 128 * h);
+          const float4 w4 = h == 0 ? ws0 : ws1;
+          uint32_t o0, o1;
+          if (kRes) {
+            o0 = epilogue_bf16_res(static_cast<int32_t>(tv.x), as, w4.x, bf16_lo(rv[b][h].x)) |
+                 (epilogue_bf16_res(static_cast<int32_t>(tv.y), as, w4.y, bf16_hi(rv[b][h].x)) << 16);
+            o1 = epilogue_bf16_res(static_cast<int32_t>(tv.z), as, w4.z, bf16_lo(rv[b][h].y)) |
+                 (epilogue_bf16_res(static_cast<int32_t>(tv.w), as, w4.w, bf16_hi(rv[b][h].y)) << 16);
+          } else {
+            o0 = epilogue_bf16(static_cast<int32_t>(tv.x), as, w4.x) |
+                 (epilogue_bf16(static_cast<int32_t>(tv.y), as, w4.y) << 16);
+            o1 = epilogue_bf16(static_cast<int32_t>(tv.z), as, w4.z) |
+                 (epilogue_bf16(static_cast<int32_t>(tv.w), as, w4.w) << 16);
+          }
+          *reinterpret_cast<uint2*>(out0 + r * a.ldo + 128 * h) = make_uint2(o0, o1);
+        }
+      }
+    }
+  }
+}
+
 // s_as[r] / s_ws[c]: a_scale of the tile's token r and w_scale of its channel
 // c, copied into shared memory when the CTA started.
 __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, const float* s_as,
@@ -327,6 +384,20 @@ __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, c
       }
     }
     mode = 0;
+  }
+
+  if (mode == 0 && p.vec_io && a.acc_out == nullptr && (cols_out == 128 || cols_out == 256) &&
+      n0 + cols_out <= a.N && nthreads == 512) {
+    const int rows_valid = static_cast<int>(a.M - m0 < rows_out ? a.M - m0 : rows_out);
+    const bool res = a.residual != nullptr;
+    if (cols_out == 256) {
+      if (res) tile_out_fast<true, true>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
+      else tile_out_fast<false, true>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
+    } else {
+      if (res) tile_out_fast<true, false>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
+      else tile_out_fast<false, false>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
+    }
+    return;
   }
 
   float4 wsv[kMaxGroupsPerThread];
