@@ -113,12 +113,18 @@ struct LinearArgs {
   int64_t ldo;
   int32_t* acc_out;
   int64_t M, N, K;
-  int split;
+  int split;            // 0: automatic schedule; >= 1: explicit split-K
   int pair_io;          // 1: out/residual rows allow 4-byte bf16 pairs
-  int32_t* ws_acc;      // [M, N] int32, zero between calls (split > 1)
-  uint32_t* ws_count;   // [tiles] arrival counters, zero between calls
+  void* ws;             // caller's workspace (256-byte aligned) or null
+  size_t ws_bytes;      // its size
+  int32_t* ws_acc;      // split-K > 1: [M, N] int32, zero between calls (set by the launcher)
+  uint32_t* ws_count;   // split-K > 1: [tiles] arrival counters, zero between calls
 };
+// Workspace bytes a call needs (split 0 = the automatic schedule).
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
+// Leading bytes of the workspace that must be zero when a call starts, for a
+// workspace of cap bytes (SIZE_MAX: the call cannot run within cap).
+size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, size_t cap);
 // Dispatch between the two contraction kernels (linear_tc.cu): the tcgen05
 // kernel by default; PRISM_LINEAR_PATH=mma selects the mma.sync s8 kernel.
 int linear_kernel_kind(int64_t M, int64_t N, int64_t K);

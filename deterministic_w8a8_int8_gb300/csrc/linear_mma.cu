@@ -247,13 +247,6 @@ int mma_auto_split(int64_t M, int64_t N, int64_t K) {
   return static_cast<int>(std::max<int64_t>(1, s));
 }
 
-size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
-  (void)K;
-  if (split <= 1 || M <= 0 || N <= 0) return 0;
-  const size_t tiles = static_cast<size_t>(cdiv(M, kBM) * cdiv(N, kBN));
-  return align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 4) + align256(tiles * 4);
-}
-
 cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(linear_mma_kernel), kSmemBytes);
   if (e != cudaSuccess) return e;

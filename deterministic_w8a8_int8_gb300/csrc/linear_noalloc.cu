@@ -23,6 +23,7 @@
 //   - The device address of the array is looked up once per device, by the
 //     first call made while that device is current (cudaGetSymbolAddress).
 //     Make that first call before any stream capture begins.
+#include <cstdint>
 #include <mutex>
 
 #include "common.cuh"
@@ -82,9 +83,10 @@ extern "C" int prism_w8a8_linear_noalloc(const int8_t* q, int64_t ldq, const flo
   if (acc_out != nullptr && !aligned_to(acc_out, 4)) return PRISM_ERR_ALIGNMENT;
   if (M > 65535LL * 128) return PRISM_ERR_UNSUPPORTED;
 
-  const int split = split_k == 0 ? prism::linear_auto_split(M, N, K) : split_k;
-  const size_t need = prism::linear_workspace_bytes(M, N, K, split);
-  if (need > static_cast<size_t>(PRISM_NOALLOC_SCRATCH_BYTES)) return PRISM_ERR_UNSUPPORTED;
+  // bytes of the scratch array that must be zero for this call (the automatic
+  // schedule falls back to whole tiles when its partial sums do not fit)
+  const size_t zero = prism::linear_workspace_zero_bytes(M, N, K, split_k, PRISM_NOALLOC_SCRATCH_BYTES);
+  if (zero == SIZE_MAX) return PRISM_ERR_UNSUPPORTED;
 
   prism::LinearArgs a{};
   a.q = q;
@@ -101,19 +103,18 @@ extern "C" int prism_w8a8_linear_noalloc(const int8_t* q, int64_t ldq, const flo
   a.M = M;
   a.N = N;
   a.K = K;
-  a.split = split;
+  a.split = split_k;
   a.pair_io = aligned_to(out_bf16, 4) && ldo % 2 == 0 &&
               (residual_bf16 == nullptr || (aligned_to(residual_bf16, 4) && ldr % 2 == 0));
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  if (need > 0) {
+  if (zero > 0) {
     void* scratch = nullptr;
     const int st = prism::record_cuda(prism::scratch_for_current_device(&scratch));
     if (st != PRISM_OK) return st;
-    const int st2 = prism::record_cuda(cudaMemsetAsync(scratch, 0, need, stream));
+    const int st2 = prism::record_cuda(cudaMemsetAsync(scratch, 0, zero, stream));
     if (st2 != PRISM_OK) return st2;
-    const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~static_cast<size_t>(255);
-    a.ws_acc = static_cast<int32_t*>(scratch);
-    a.ws_count = reinterpret_cast<uint32_t*>(static_cast<char*>(scratch) + acc_bytes);
+    a.ws = scratch;
+    a.ws_bytes = PRISM_NOALLOC_SCRATCH_BYTES;
   }
   return prism::record_cuda(prism::launch_linear(a, stream));
 }

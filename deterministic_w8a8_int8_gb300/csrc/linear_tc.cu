@@ -46,6 +46,7 @@
 // Split-K reuses the integer-atomic / last-arriver protocol of the workspace.
 #include <algorithm>
 #include <climits>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 
@@ -92,9 +93,18 @@ struct TcParams {
   LinearArgs a;
   int swap;      // 0 normal, 1 swapped
   int bpiece;    // B rows per tile (multiple of 32, <= 256)
-  int vec_io;    // 16-byte vector epilogue loads/stores allowed (normal orientation)
+  int vec_io;    // vector epilogue loads/stores allowed (16-byte aligned out/residual, ldo/ldr % 8 == 0)
   int nst;       // f16 operand stages, each (128 + bpiece) x 128 bytes
   int nst8;      // int8 staging stages, each (128 + bpiece) x 64 bytes
+  int sched;     // 0: one tile (K piece) per CTA; 1: balanced schedule (see get_item)
+  int gx;        // A blocks of 128 rows (tile index = ty * gx + tx)
+  int T;         // tiles
+  int S;         // K stages of 64
+  int W;         // balanced schedule: rounds of whole tiles per CTA
+  int R;         // balanced schedule: tiles whose K units are shared out
+  uint32_t* cnt;   // balanced schedule: arrival counters of the shared tiles (zero between calls)
+  int32_t* slots;  // balanced schedule: 2 partial tiles per CTA
+  int slot_elems;  // int32 elements of one slot (128 * bpiece)
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -334,53 +344,29 @@ __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, c
 
   if (mode == 2) {
     // split-K read-back: copy the finished integer sums into this thread's
-    // own entries of the staged tile (re-zeroing the workspace), kRowBatch rows
-    // of loads in flight, then run the ordinary epilogue from the tile
+    // own entries of the staged tile (re-zeroing the workspace), one row at a
+    // time (this path is rare; it keeps few registers live), then run the
+    // ordinary epilogue from the tile
     uint32_t* Tw = const_cast<uint32_t*>(T);
     const bool vec = (a.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.ws_acc) & 15) == 0);
-    for (int rb = t / per_row; rb < rows_out; rb += rows_per_pass * kRowBatch) {
-      int4 wv[kRowBatch][kMaxGroupsPerThread];
-#pragma unroll
-      for (int b = 0; b < kRowBatch; ++b) {
-        const int r = rb + b * rows_per_pass;
-        const int64_t m = m0 + r;
-#pragma unroll
-        for (int q = 0; q < kMaxGroupsPerThread; ++q) {
-          const int64_t n = n0 + 4 * (g0 + q * per_row);
-          wv[b][q] = make_int4(0, 0, 0, 0);
-          if (r < rows_out && m < a.M && q < gpt) {
-            int32_t* wp = a.ws_acc + m * a.N + n;
-            if (vec && n + 4 <= a.N) {
-              wv[b][q] = __ldcg(reinterpret_cast<const int4*>(wp));
-            } else {
-              wv[b][q].x = n < a.N ? __ldcg(wp) : 0;
-              wv[b][q].y = n + 1 < a.N ? __ldcg(wp + 1) : 0;
-              wv[b][q].z = n + 2 < a.N ? __ldcg(wp + 2) : 0;
-              wv[b][q].w = n + 3 < a.N ? __ldcg(wp + 3) : 0;
-            }
-          }
+    for (int r = t / per_row; r < rows_out; r += rows_per_pass) {
+      const int64_t m = m0 + r;
+      if (m >= a.M) continue;
+      for (int q = 0; q < gpt; ++q) {
+        const int c = 4 * (g0 + q * per_row);
+        const int64_t n = n0 + c;
+        int32_t* wp = a.ws_acc + m * a.N + n;
+        int4 v = make_int4(0, 0, 0, 0);
+        if (vec && n + 4 <= a.N) {
+          v = __ldcg(reinterpret_cast<const int4*>(wp));
+          __stcg(reinterpret_cast<int4*>(wp), make_int4(0, 0, 0, 0));
+        } else {
+          if (n < a.N) { v.x = __ldcg(wp); __stcg(wp, 0); }
+          if (n + 1 < a.N) { v.y = __ldcg(wp + 1); __stcg(wp + 1, 0); }
+          if (n + 2 < a.N) { v.z = __ldcg(wp + 2); __stcg(wp + 2, 0); }
+          if (n + 3 < a.N) { v.w = __ldcg(wp + 3); __stcg(wp + 3, 0); }
         }
-      }
-#pragma unroll
-      for (int b = 0; b < kRowBatch; ++b) {
-        const int r = rb + b * rows_per_pass;
-        const int64_t m = m0 + r;
-#pragma unroll
-        for (int q = 0; q < kMaxGroupsPerThread; ++q) {
-          const int c = 4 * (g0 + q * per_row);
-          const int64_t n = n0 + c;
-          if (r < rows_out && m < a.M && q < gpt) {
-            *reinterpret_cast<int4*>(Tw + r * stride + c) = wv[b][q];
-            int32_t* wp = a.ws_acc + m * a.N + n;
-            if (vec && n + 4 <= a.N) {
-              __stcg(reinterpret_cast<int4*>(wp), make_int4(0, 0, 0, 0));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (n + j < a.N) __stcg(wp + j, 0);
-            }
-          }
-        }
+        *reinterpret_cast<int4*>(Tw + r * stride + c) = v;
       }
     }
     mode = 0;
@@ -479,9 +465,111 @@ __device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, c
   }
 }
 
+// The atomic split-K output modes (1: add the tile into the workspace, 2:
+// read the finished sum back, then the epilogue).
+__device__ __forceinline__ void tile_out_split(const TcParams& p, const uint32_t* T, const float* s_as,
+                                            const float* s_ws, int rows_out, int cols_out, int64_t m0,
+                                            int64_t n0, int mode, int t) {
+  tile_out(p, T, s_as, s_ws, rows_out, cols_out, m0, n0, mode, t, kWorkers);
+}
+
 // ------------------------------------------------------------------ kernel --
+// One unit of work of a CTA: output tile (tx, ty) -- A block tx of 128 rows,
+// B piece ty of bpiece rows -- over the K stages [k0, k1) of 64.
+//   kind 0: the whole K range; the epilogue is applied directly.
+//   kind 1: one of a.split equal K pieces (explicit split-K): int32 atomics
+//           into the workspace tile; the last piece's CTA applies the epilogue.
+//   kind 2: a K range of a tile that the balanced schedule shares between
+//           CTAs: the partial int32 tile goes to this CTA's slot; the last CTA
+//           to finish the tile adds the other slots and applies the epilogue.
+struct Item {
+  int tx, ty, k0, k1, kind, tile, slot;
+};
+
+// Work item n of this CTA; every role of the CTA walks the same list.
+//   sched 0: one item: tile (blockIdx.x, blockIdx.y), K piece blockIdx.z of
+//            a.split.
+//   sched 1 (balanced, G = gridDim.x CTAs): CTA b first takes whole tiles
+//            b, b + G, ... (W rounds, indices below T), then the K units
+//            [b U / G, (b + 1) U / G) of the last R tiles, U = R * S units of
+//            64 K and shared tile st covering units [st S, (st + 1) S).
+__device__ __forceinline__ bool get_item(const TcParams& p, int n, Item& it) {
+  if (p.sched == 0) {
+    if (n > 0) return false;
+    const int per = (p.S + p.a.split - 1) / p.a.split;
+    it.tx = static_cast<int>(blockIdx.x);
+    it.ty = static_cast<int>(blockIdx.y);
+    const int k0 = static_cast<int>(blockIdx.z) * per;
+    it.k0 = k0 < p.S ? k0 : p.S;
+    it.k1 = it.k0 + per < p.S ? it.k0 + per : p.S;
+    it.kind = p.a.split > 1 ? 1 : 0;
+    it.tile = it.ty * p.gx + it.tx;
+    it.slot = 0;
+    return true;
+  }
+  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  if (n < p.W) {
+    const int t = n * G + b;
+    if (t >= p.T) return false;
+    it.tx = t % p.gx;
+    it.ty = t / p.gx;
+    it.k0 = 0;
+    it.k1 = p.S;
+    it.kind = 0;
+    it.tile = t;
+    it.slot = 0;
+    return true;
+  }
+  if (p.R == 0) return false;
+  // U * G < 2^31: R < 304, S <= 2081 (K <= 133144) and G <= 152
+  const int j = n - p.W;
+  const int U = p.R * p.S;
+  const int u0 = b * U / G, u1 = (b + 1) * U / G;
+  const int st = u0 / p.S + j;
+  const int ts = st * p.S;
+  if (u0 >= u1 || ts >= u1) return false;
+  const int t = p.W * G + st;
+  it.tx = t % p.gx;
+  it.ty = t / p.gx;
+  it.k0 = (u0 > ts ? u0 : ts) - ts;
+  it.k1 = (u1 < ts + p.S ? u1 : ts + p.S) - ts;
+  it.kind = (it.k0 == 0 && it.k1 == p.S) ? 0 : 2;
+  it.tile = st;
+  it.slot = 2 * b + (j == 0 ? 0 : 1);  // a CTA's partial items are its first and its last
+  return true;
+}
+
+// CTAs bf..bl of the balanced schedule whose K ranges meet shared tile st
+// (the CTA holding unit u is floor(((u + 1) G - 1) / U)), and the slot CTA
+// c used for it.
+__device__ __forceinline__ void shared_tile_ctas(const TcParams& p, int st, int& bf, int& bl) {
+  const int G = static_cast<int>(gridDim.x);
+  const int U = p.R * p.S;
+  bf = ((st * p.S + 1) * G - 1) / U;
+  bl = ((st * p.S + p.S) * G - 1) / U;
+}
+__device__ __forceinline__ int shared_tile_slot(const TcParams& p, int st, int c) {
+  const int U = p.R * p.S;
+  const int first = (c * U / static_cast<int>(gridDim.x)) / p.S;  // first shared tile of CTA c
+  return 2 * c + (st == first ? 0 : 1);
+}
+
+// Worker wt's share of an item's epilogue scales: a_scale of token wt of the
+// tile (wt < 256) or w_scale of channel wt - 256 (0 beyond the tile or matrix).
+__device__ __forceinline__ float item_scale(const TcParams& p, const Item& itm, int bn, int wt) {
+  const LinearArgs& a = p.a;
+  const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
+  if (wt < kBNMax) {
+    const int64_t m = (p.swap ? b0 : a0) + wt;
+    return wt < (p.swap ? bn : kBM) && m < a.M ? __ldg(a.a_scale + m) : 0.f;
+  }
+  const int i = wt - kBNMax;
+  const int64_t n = (p.swap ? a0 : b0) + i;
+  return i < (p.swap ? kBM : bn) && n < a.N ? __ldg(a.w_scale + n) : 0.f;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    linear_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA,
+    linear_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ uint8_t smem_raw[];
   const LinearArgs& a = p.a;
@@ -512,23 +600,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-
-  // tile coordinates
-  const int64_t rows_b = p.swap ? a.M : a.N;
-  const int64_t a0 = static_cast<int64_t>(blockIdx.x) * kBM;
-  const int64_t b0 = static_cast<int64_t>(blockIdx.y) * p.bpiece;
-  const int64_t b_left = rows_b - b0;
-  const int64_t b_round = (b_left + 31) & ~static_cast<int64_t>(31);
-  const int bn = static_cast<int>(b_round < p.bpiece ? b_round : p.bpiece);
-  const int64_t ktiles = (a.K + kBK - 1) / kBK;
-  const int64_t per = (ktiles + a.split - 1) / a.split;
-  const int64_t kt0 = static_cast<int64_t>(blockIdx.z) * per;
-  const int64_t kt1 = kt0 + per < ktiles ? kt0 + per : ktiles;
-  const int nk = kt1 > kt0 ? static_cast<int>(kt1 - kt0) : 0;
-  const int nchunks = (nk + kChunkStages - 1) / kChunkStages;
   // TMEM layout: double-buffered D[0] | D[1] | I when three widths fit, else D | I
   const bool dbuf = 3 * p.bpiece <= static_cast<int>(kTmemCols);
   const uint32_t col_i = dbuf ? 2u * static_cast<uint32_t>(p.bpiece) : kColI;
+  // B rows of piece ty that exist, rounded up to 32 (the MMA's N)
+  auto tile_width = [&](int ty) -> int {
+    const int64_t left = (p.swap ? a.M : a.N) - static_cast<int64_t>(ty) * p.bpiece;
+    const int64_t rnd = (left + 31) & ~static_cast<int64_t>(31);
+    return static_cast<int>(rnd < p.bpiece ? rnd : p.bpiece);
+  };
 
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -560,68 +640,90 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kMmaWarp) {
     // ======================= MMA issuer (one thread) =========================
-    if (lane == 0 && nk > 0) {
-      const uint32_t idesc = idesc_f16_f32(bn);
+    if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;  // stage slot and its phase parity, advanced incrementally
-      int c = -1;       // current chunk
+      int c = -1;       // chunk counter over all items
       uint32_t dcol = kColD, dbar = 0;
-      for (int it = 0; it < nk; ++it) {
-        const int cpos = it & (kChunkStages - 1);
-        if (cpos == 0) {
-          // chunk c reuses the D buffer of chunk c - 2 (double-buffered) or
-          // c - 1: wait until the workers have drained it
-          ++c;
-          const int prev = c - (dbuf ? 2 : 1);
-          dbar = dbuf ? static_cast<uint32_t>(c & 1) : 0u;
-          dcol = dbuf && (c & 1) ? static_cast<uint32_t>(p.bpiece) : kColD;
-          if (prev >= 0) {
-            const uint32_t use = static_cast<uint32_t>(dbuf ? prev >> 1 : prev);
-            if (!mbar_wait(bar_acc_empty + 8 * dbar, use & 1u, s_abort)) break;
-            tc_fence_after();
+      bool ok = true, issued = false;
+      Item itm;
+      for (int n = 0; ok && get_item(p, n, itm); ++n) {
+        const int nk = itm.k1 - itm.k0;
+        const uint32_t idesc = idesc_f16_f32(tile_width(itm.ty));
+        for (int it = 0; it < nk; ++it) {
+          const int cpos = it & (kChunkStages - 1);
+          if (cpos == 0) {
+            // chunk c reuses the D buffer of chunk c - 2 (double-buffered) or
+            // c - 1: wait until the workers have drained it
+            ++c;
+            const int prev = c - (dbuf ? 2 : 1);
+            dbar = dbuf ? static_cast<uint32_t>(c & 1) : 0u;
+            dcol = dbuf && (c & 1) ? static_cast<uint32_t>(p.bpiece) : kColD;
+            if (prev >= 0) {
+              const uint32_t use = static_cast<uint32_t>(dbuf ? prev >> 1 : prev);
+              if (!mbar_wait(bar_acc_empty + 8 * dbar, use & 1u, s_abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+          }
+          if (!mbar_wait(bar_full + 8 * s, ph, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(sStage + s * kStageBytes);
+          const uint64_t bd = smem_desc_sw128(sStage + s * kStageBytes + kStageA);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
+          issued = true;
+          tc_commit(bar_empty + 8 * s);
+          if (cpos == kChunkStages - 1 || it == nk - 1) tc_commit(bar_acc_full + 8 * dbar);
+          if (++s == nst) {
+            s = 0;
+            ph ^= 1u;
           }
         }
-        if (!mbar_wait(bar_full + 8 * s, ph, s_abort)) break;
-        tc_fence_after();
-        const uint64_t ad = smem_desc_sw128(sStage + s * kStageBytes);
-        const uint64_t bd = smem_desc_sw128(sStage + s * kStageBytes + kStageA);
-#pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          tc_mma(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
-        tc_commit(bar_empty + 8 * s);
-        if (cpos == kChunkStages - 1 || it == nk - 1) tc_commit(bar_acc_full + 8 * dbar);
-        if (++s == nst) {
-          s = 0;
-          ph ^= 1u;
-        }
       }
-      // every MMA issued above has completed before TMEM is released
-      tc_commit(bar_done);
-      const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(bar_done, 0)) {
-        if (globaltimer() - t0 > kWaitLimitNs) {
-          atomicOr(&g_kernel_error, kDevErrTimeout);
-          break;
+      if (issued) {
+        // every MMA issued above has completed before TMEM is released
+        tc_commit(bar_done);
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(bar_done, 0)) {
+          if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(&g_kernel_error, kDevErrTimeout);
+            break;
+          }
         }
       }
     }
     __syncwarp();
   } else if (warp == kTmaWarp) {
     // ======================= TMA producer (one thread) ========================
-    if (lane == 0 && nk > 0) {
+    if (lane == 0) {
       const uint32_t tx = static_cast<uint32_t>(kS8A + kBK * p.bpiece);
       int j = 0;
       uint32_t ph = 0;
-      for (int it = 0; it < nk; ++it) {
-        if (!mbar_wait(bar_s8_empty + 8 * j, ph ^ 1u, s_abort)) break;
-        const uint32_t dst = sS8 + j * kS8Bytes;
-        const int32_t x = static_cast<int32_t>((kt0 + it) * kBK);
-        mbar_expect_tx(bar_s8_full + 8 * j, tx);
-        tma_load_2d(dst, &tmA, x, static_cast<int32_t>(a0), bar_s8_full + 8 * j);
-        tma_load_2d(dst + kS8A, &tmB, x, static_cast<int32_t>(b0), bar_s8_full + 8 * j);
-        if (++j == nst8) {
-          j = 0;
-          ph ^= 1u;
+      bool ok = true;
+      Item itm;
+      for (int n = 0; ok && get_item(p, n, itm); ++n) {
+        const int32_t ya = itm.tx * kBM, yb = itm.ty * p.bpiece;
+        for (int it = itm.k0; it < itm.k1; ++it) {
+          if (!mbar_wait(bar_s8_empty + 8 * j, ph ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sS8 + j * kS8Bytes;
+          const int32_t x = it * kBK;
+          mbar_expect_tx(bar_s8_full + 8 * j, tx);
+          tma_load_2d(dst, &tmA, x, ya, bar_s8_full + 8 * j);
+          tma_load_2d(dst + kS8A, &tmB, x, yb, bar_s8_full + 8 * j);
+          if (++j == nst8) {
+            j = 0;
+            ph ^= 1u;
+          }
         }
       }
     }
@@ -629,10 +731,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ======================= workers (16 warps) ===============================
     // Conversion: worker thread wt owns 16-byte segment (wt % 4) of rows
-    // wt / 4, wt / 4 + 128 and wt / 4 + 256 of the stacked [A | B] tile; rows
-    // and shared-memory offsets are fixed for the tile, only K moves.
+    // wt / 4, wt / 4 + 128 and wt / 4 + 256 of the stacked [A | B] tile; the
+    // shared-memory offsets are fixed, only K moves.
     // Drain: warp w reads TMEM lanes 32 (w % 4) .. +31; the four warps of a
     // quadrant take 16-column rounds j, j + 4, j + 8, ... of the accumulator.
+    // Every worker passes the same sequence of named barriers whatever
+    // happens (a timed-out wait only skips work), so none can be left waiting.
     const int wi = warp < kMmaWarp ? warp : warp - 1;   // worker index 0..15
     const int wt = wi * 32 + lane;
     const int quad = warp & 3;
@@ -640,45 +744,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int trow = quad * 32 + lane;                    // this thread's TMEM lane
     uint32_t* T = reinterpret_cast<uint32_t*>(smem);
-    {
-      // the epilogue's scales, read now so that their memory latency overlaps
-      // the first TMA loads instead of the tile's output; the residual tile is
-      // prefetched into L2 for the same reason
-      const int64_t tok0 = p.swap ? b0 : a0, ch0 = p.swap ? a0 : b0;
-      const int ntok = p.swap ? bn : kBM, nch = p.swap ? kBM : bn;
-      if (wt < kBNMax) {
-        const int64_t m = tok0 + wt;
-        s_as[wt] = wt < ntok && m < a.M ? __ldg(a.a_scale + m) : 0.f;
-      } else {
-        const int i = wt - kBNMax;
-        const int64_t n = ch0 + i;
-        s_ws[i] = i < nch && n < a.N ? __ldg(a.w_scale + n) : 0.f;
-      }
-      if (a.residual != nullptr) {
-        const int lines = (nch * 2 + 127) / 128;  // 128-byte lines per token row
-        for (int l = wt; l < ntok * lines; l += kWorkers) {
-          const int r = l / lines;
-          const int64_t m = tok0 + r, n = ch0 + (l - r * lines) * 64;
-          if (m < a.M && n < a.N)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.residual + m * a.ldr + n));
-        }
-      }
-    }
     const int seg = wt & 3;
-    // per segment: offset of its 16 int8 bytes in a staging stage, and of its
-    // first 16-byte f16 chunk in an operand stage (the second is that ^ 16)
-    uint32_t lo8[kSegPerThread];
-    uint32_t so[kSegPerThread];
+    // per segment: offset of its 16 int8 bytes in a staging stage, and of
+    // its first 16-byte f16 chunk in an operand stage (the second is that ^
+    // 16), or ~0 when its B row lies beyond the current tile (set per item)
+    uint32_t lo8[kSegPerThread], so[kSegPerThread];
 #pragma unroll
     for (int i = 0; i < kSegPerThread; ++i) {
       const int r = (wt >> 2) + i * kBM;
       const bool is_a = r < kBM;
       const int rr = is_a ? r : r - kBM;
-      const bool in_tile = is_a || rr < bn;
       lo8[i] = (is_a ? 0u : static_cast<uint32_t>(kS8A)) + rr * kBK + seg * 16;
-      so[i] = in_tile ? (is_a ? 0u : static_cast<uint32_t>(kStageA)) + rr * 128 +
-                            static_cast<uint32_t>(((2 * seg) ^ (rr & 7)) * 16)
-                      : 0xFFFFFFFFu;
     }
     auto store_stage = [&](int s, const uint4 (&buf)[kSegPerThread]) {
       const uint32_t st_base = sStage + s * kStageBytes;
@@ -695,12 +771,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_shared_v4_if(addr ^ 16u, w[4], w[5], w[6], w[7], valid);
       }
     };
-    // Drain this warp's share of chunk c: I += int(D) (or, for the last
-    // chunk, stage the final values as T[token][channel]).
-    auto drain = [&](int c, bool last) -> bool {
-      const uint32_t dbar = dbuf ? static_cast<uint32_t>(c & 1) : 0u;
-      const uint32_t use = static_cast<uint32_t>(dbuf ? c >> 1 : c);
-      const uint32_t dcol = dbuf && (c & 1) ? static_cast<uint32_t>(p.bpiece) : kColD;
+    // Drain this warp's share of chunk gc (chunk lc of its item): I += int(D),
+    // or, for the item's last chunk, stage the final values as
+    // T[token][channel].  Either way the D buffer is then handed back.
+    auto drain = [&](int gc, int lc, bool last, int bn) -> bool {
+      const uint32_t dbar = dbuf ? static_cast<uint32_t>(gc & 1) : 0u;
+      const uint32_t use = static_cast<uint32_t>(dbuf ? gc >> 1 : gc);
+      const uint32_t dcol = dbuf && (gc & 1) ? static_cast<uint32_t>(p.bpiece) : kColD;
       const bool got = mbar_wait_warp(bar_acc_full + 8 * dbar, use & 1u, s_abort);
       if (!got) return false;
       tc_fence_after();
@@ -708,11 +785,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cb = slice; cb < rounds; cb += 4) {
         uint32_t d[16], iv[16];
         tmem_ld16(tmem + lane_base + dcol + cb * 16, d);
-        if (c > 0) tmem_ld16(tmem + lane_base + col_i + cb * 16, iv);
+        if (lc > 0) tmem_ld16(tmem + lane_base + col_i + cb * 16, iv);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          d[j] = static_cast<uint32_t>((c > 0 ? static_cast<int32_t>(iv[j]) : 0) +
+          d[j] = static_cast<uint32_t>((lc > 0 ? static_cast<int32_t>(iv[j]) : 0) +
                                        __float2int_rn(__uint_as_float(d[j])));
         if (!last) {
           tmem_st16(tmem + lane_base + col_i + cb * 16, d);
@@ -725,76 +802,187 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) T[(cb * 16 + j) * (kBM + 4) + trow] = d[j];
         }
       }
-      if (!last) {
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_acc_empty + 8 * dbar);
-      }
+      if (!last) tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_acc_empty + 8 * dbar);
       return true;
     };
 
     bool ok = true;
-    int next_drain = 0;  // next intermediate chunk to drain
-    int next_trigger = kChunkStages + nst - 1;
+    int gc = 0;                // chunk counter over all items
     int j = 0, s = 0;
     uint32_t ph8 = 0, ph = 0;  // staging / operand slots and phase parities
-    for (int it = 0; it < nk && ok; ++it) {
-      // chunk c's last MMA completes exactly when stage it - nst is
-      // released, so drain it here, after the next chunk's first stages have
-      // been prepared
-      if (next_drain < nchunks - 1 && it == next_trigger) {
-        ok = drain(next_drain, false);
-        ++next_drain;
-        next_trigger += kChunkStages;
-        if (!ok) break;
-      }
-      ok = mbar_wait_warp(bar_s8_full + 8 * j, ph8, s_abort);
-      if (!ok) break;
-      uint4 buf[kSegPerThread];
-      const uint32_t s8 = sS8 + j * kS8Bytes;
-#pragma unroll
-      for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
-        buf[i] = ld_shared_v4_if(s8 + lo8[i], so[i] != 0xFFFFFFFFu);
-      ok = mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, s_abort);
-      if (!ok) break;
-      store_stage(s, buf);
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_full + 8 * s);
-      // released only now: every value read from the staging slot has been
-      // consumed by the widening, so a TMA refill cannot overtake a load
-      if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);
-      if (++j == nst8) {
-        j = 0;
-        ph8 ^= 1u;
-      }
-      if (++s == nst) {
-        s = 0;
-        ph ^= 1u;
-      }
+    // this worker's epilogue scale for the coming item, loaded one item ahead
+    // so that its memory latency overlaps the previous item's output
+    float sc_next = 0.f;
+    {
+      Item first;
+      if (get_item(p, 0, first)) sc_next = item_scale(p, first, tile_width(first.ty), wt);
     }
-    while (ok && next_drain < nchunks - 1) ok = drain(next_drain++, false);
-    if (ok && nchunks > 0) ok = drain(nchunks - 1, true);
+    for (int n = 0;; ++n) {
+      int bn, nk;
+      {
+        // (only n stays live through the stage loop; the item is looked up
+        // again for its output)
+        Item itm;
+        if (!get_item(p, n, itm)) break;
+        // the previous item's output is finished: T and the scale copies are free
+        asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+        bn = tile_width(itm.ty);
+        nk = itm.k1 > itm.k0 ? itm.k1 - itm.k0 : 0;
+        const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
+        const int64_t tok0 = p.swap ? b0 : a0, ch0 = p.swap ? a0 : b0;
+        const int ntok = p.swap ? bn : kBM, nch = p.swap ? kBM : bn;
+        // the epilogue's scales (loaded ahead); the residual tile is
+        // prefetched into L2 so that the output does not wait on DRAM
+        s_as[wt] = sc_next;   // s_ws follows s_as: workers 256.. fill the channel scales
+        if (a.residual != nullptr && itm.kind != 1) {
+          const int lines = (nch * 2 + 127) / 128;  // 128-byte lines per token row
+          for (int l = wt; l < ntok * lines; l += kWorkers) {
+            const int r = l / lines;
+            const int64_t m = tok0 + r, nn = ch0 + (l - r * lines) * 64;
+            if (m < a.M && nn < a.N)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(a.residual + m * a.ldr + nn));
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kSegPerThread; ++i) {
+        const int r = (wt >> 2) + i * kBM;
+        const bool is_a = r < kBM;
+        const int rr = is_a ? r : r - kBM;
+        so[i] = is_a || rr < bn ? (is_a ? 0u : static_cast<uint32_t>(kStageA)) + rr * 128 +
+                                      static_cast<uint32_t>(((2 * seg) ^ (rr & 7)) * 16)
+                                : 0xFFFFFFFFu;
+      }
+      const int nchunks = (nk + kChunkStages - 1) / kChunkStages;
+      int next_drain = 0;  // next intermediate chunk to drain
+      int next_trigger = kChunkStages + nst - 1;
+      for (int it = 0; it < nk && ok; ++it) {
+        // chunk c's last MMA completes exactly when stage it - nst is
+        // released, so drain it here, after the next chunk's first stages
+        // have been prepared
+        if (next_drain < nchunks - 1 && it == next_trigger) {
+          ok = drain(gc + next_drain, next_drain, false, bn);
+          ++next_drain;
+          next_trigger += kChunkStages;
+          if (!ok) break;
+        }
+        ok = mbar_wait_warp(bar_s8_full + 8 * j, ph8, s_abort);
+        if (!ok) break;
+        uint4 buf[kSegPerThread];
+        const uint32_t s8 = sS8 + j * kS8Bytes;
+#pragma unroll
+        for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
+          buf[i] = ld_shared_v4_if(s8 + lo8[i], so[i] != 0xFFFFFFFFu);
+        ok = mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, s_abort);
+        if (!ok) break;
+        store_stage(s, buf);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_full + 8 * s);
+        // released only now: every value read from the staging slot has been
+        // consumed by the widening, so a TMA refill cannot overtake a load
+        if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);
+        if (++j == nst8) {
+          j = 0;
+          ph8 ^= 1u;
+        }
+        if (++s == nst) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      while (ok && next_drain < nchunks - 1) {
+        ok = drain(gc + next_drain, next_drain, false, bn);
+        ++next_drain;
+      }
+      if (ok && nchunks > 0) ok = drain(gc + nchunks - 1, nchunks - 1, true, bn);
+      gc += nchunks;
+      {
+        Item nx;
+        sc_next = get_item(p, n + 1, nx) ? item_scale(p, nx, tile_width(nx.ty), wt) : 0.f;
+      }
 
-    // ---- coalesced output of the staged tile by all 512 workers
-    const int rows_out = p.swap ? bn : kBM;
-    const int cols_out = p.swap ? kBM : bn;
-    const int64_t om = p.swap ? b0 : a0;   // first token of the tile
-    const int64_t on = p.swap ? a0 : b0;   // first channel of the tile
-    asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-    if (ok && nchunks > 0) tile_out(p, T, s_as, s_ws, rows_out, cols_out, om, on, a.split == 1 ? 0 : 1, wt, kWorkers);
-    if (a.split > 1) {
-      // integer split-K: the last CTA to finish this tile applies the epilogue
-      __threadfence();
+      // ---- output of the staged tile by all 512 workers
+      Item itm;
+      get_item(p, n, itm);
+      const int64_t tok0 = static_cast<int64_t>(p.swap ? itm.ty * p.bpiece : itm.tx * kBM);
+      const int64_t ch0 = static_cast<int64_t>(p.swap ? itm.tx * kBM : itm.ty * p.bpiece);
+      const int rows_out = p.swap ? bn : kBM;
+      const int cols_out = p.swap ? kBM : bn;
       asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-      const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
-      if (wt == 0) *s_last = (atomicAdd(a.ws_count + tile, 1u) == static_cast<unsigned>(a.split - 1));
-      asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-      if (*s_last) {
+      const bool have = ok && nchunks > 0;
+      if (itm.kind == 0) {
+        if (have) tile_out(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 0, wt, kWorkers);
+      } else if (itm.kind == 1) {
+        // integer split-K: the last CTA to finish this tile applies the epilogue
+        if (have) tile_out_split(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 1, wt);
         __threadfence();
-        tile_out(p, T, s_as, s_ws, rows_out, cols_out, om, on, 2, wt, kWorkers);
-        if (wt == 0) a.ws_count[tile] = 0u;
+        asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+        if (wt == 0) *s_last = (atomicAdd(a.ws_count + itm.tile, 1u) == static_cast<unsigned>(a.split - 1));
+        asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+        if (*s_last) {
+          __threadfence();
+          tile_out_split(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 2, wt);
+          if (wt == 0) a.ws_count[itm.tile] = 0u;
+        }
+      } else {
+        // shared tile of the balanced schedule: partial sums to this CTA's
+        // slot (plain stores); the last CTA to finish adds the other slots
+        const int groups = rows_out * (cols_out / 4);
+        const int stride = cols_out + 4;
+        int32_t* mine = p.slots + static_cast<int64_t>(itm.slot) * p.slot_elems;
+        if (have) {
+          for (int g = wt; g < groups; g += kWorkers) {
+            const int r = g / (cols_out / 4), c4 = (g - r * (cols_out / 4)) * 4;
+            __stcg(reinterpret_cast<int4*>(mine + r * cols_out + c4),
+                   *reinterpret_cast<const int4*>(T + r * stride + c4));
+          }
+        }
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+        int bf = 0, bl = 0;
+        shared_tile_ctas(p, itm.tile, bf, bl);
+        if (wt == 0) *s_last = (atomicAdd(p.cnt + itm.tile, 1u) == static_cast<unsigned>(bl - bf));
+        asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+        if (*s_last) {
+          __threadfence();
+          for (int c = bf; c <= bl; ++c) {
+            if (c == static_cast<int>(blockIdx.x)) continue;
+            const int32_t* other = p.slots + static_cast<int64_t>(shared_tile_slot(p, itm.tile, c)) * p.slot_elems;
+            // four independent L2 loads in flight before any of them is added
+            constexpr int kAhead = 4;
+            for (int g0 = wt; g0 < groups; g0 += kWorkers * kAhead) {
+              int4 v[kAhead];
+#pragma unroll
+              for (int u = 0; u < kAhead; ++u) {
+                const int g = g0 + u * kWorkers;
+                const int r = g / (cols_out / 4), c4 = (g - r * (cols_out / 4)) * 4;
+                v[u] = g < groups ? __ldcg(reinterpret_cast<const int4*>(other + r * cols_out + c4))
+                                  : make_int4(0, 0, 0, 0);
+              }
+#pragma unroll
+              for (int u = 0; u < kAhead; ++u) {
+                const int g = g0 + u * kWorkers;
+                if (g < groups) {
+                  const int r = g / (cols_out / 4), c4 = (g - r * (cols_out / 4)) * 4;
+                  int4* t4 = reinterpret_cast<int4*>(T + r * stride + c4);
+                  int4 tv = *t4;
+                  tv.x += v[u].x;
+                  tv.y += v[u].y;
+                  tv.z += v[u].z;
+                  tv.w += v[u].w;
+                  *t4 = tv;
+                }
+              }
+            }
+          }
+          asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
+          if (have) tile_out(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 0, wt, kWorkers);
+          if (wt == 0) p.cnt[itm.tile] = 0u;
+        }
       }
     }
   }
@@ -840,31 +1028,60 @@ static TcPlan tc_plan(int64_t M, int64_t N) {
   return pl;
 }
 
-// Split-K choice, only when the full-width tiles do not fill one wave of the
-// 152 SMs: minimise (waves of full-width CTAs) x (K per split + a fixed
-// per-CTA cost of about one 1024-K chunk).  Short token pieces of the swapped
-// orientation fill the gaps left by the full-width CTAs.
-static int tc_auto_split(int64_t M, int64_t N, int64_t K) {
-  constexpr int64_t kSMs = 152;
-  constexpr int64_t kCtaCost = 1024;
-  const TcPlan pl = tc_plan(M, N);
-  const int64_t b_rows = pl.swap ? M : N;
-  const int64_t full_pieces = b_rows / pl.bpiece > 0 ? b_rows / pl.bpiece : 1;
-  const int64_t long_tiles = pl.grid_x * full_pieces;
-  const int64_t kstages = cdiv(K, kBK);
-  if (long_tiles >= kSMs) return 1;  // a full wave already; integer atomics would cost more
-  int best = 1;
-  int64_t best_cost = INT64_MAX;
-  for (int sk = 1; sk <= 16; ++sk) {
-    if (sk > 1 && cdiv(kstages, sk) < 8) break;  // keep at least 512 K per split
-    const int64_t waves = cdiv(long_tiles * sk, kSMs);
-    const int64_t cost = waves * (cdiv(K, sk) + kCtaCost);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = sk;
-    }
+// The balanced schedule for T tiles of S K-stages on the 152 SMs (see
+// get_item): whole tiles in W rounds over G CTAs, then the K units of the
+// last R tiles shared out evenly.  Shares below one 1024-K chunk per CTA are
+// not worth their partial-sum traffic: then one round fewer of whole tiles
+// is taken, or, with few tiles, fewer CTAs share them, or (little K) only
+// whole tiles are used.
+struct TcSched {
+  int G, W, R;
+};
+
+static TcSched tc_balanced(int64_t T, int64_t S) {
+  constexpr int64_t kSMs = 152, kMinUnits = kChunkStages;
+  TcSched sc{static_cast<int>(kSMs), 0, 0};
+  if (T % kSMs == 0) {
+    sc.W = static_cast<int>(T / kSMs);
+    return sc;
   }
-  return best;
+  int64_t W = T / kSMs, R = T - W * kSMs;
+  if (R * S < kMinUnits * kSMs && W >= 1) {
+    W -= 1;
+    R += kSMs;
+  }
+  if (R * S >= kMinUnits * kSMs) {
+    sc.W = static_cast<int>(W);
+    sc.R = static_cast<int>(R);
+  } else if (W == 0) {
+    sc.G = static_cast<int>(std::max<int64_t>(R, std::min<int64_t>(kSMs, R * S / kMinUnits)));
+    sc.R = static_cast<int>(R);
+  } else {
+    sc.W = static_cast<int>(cdiv(T, kSMs));
+  }
+  return sc;
+}
+
+// Workspace of the balanced schedule: tile counters, then 2 partial tiles per
+// CTA; none when no tile is shared.
+static size_t tc_balanced_bytes(int64_t M, int64_t N, int64_t K, size_t* counter_bytes) {
+  const TcPlan pl = tc_plan(M, N);
+  const TcSched sc = tc_balanced(pl.grid_x * pl.grid_y, cdiv(K, kBK));
+  if (sc.R == 0 || sc.G == sc.R) {
+    if (counter_bytes != nullptr) *counter_bytes = 0;
+    return 0;
+  }
+  const size_t cb = (static_cast<size_t>(sc.R) * 4 + 255) & ~static_cast<size_t>(255);
+  if (counter_bytes != nullptr) *counter_bytes = cb;
+  return cb + static_cast<size_t>(2) * sc.G * kBM * pl.bpiece * 4;
+}
+
+// Workspace of explicit split-K (int32 atomics): the [M, N] accumulator, then
+// one counter per tile (counted at 128 x 128, which covers both kernels' tiles).
+static size_t atomic_bytes(int64_t M, int64_t N) {
+  const size_t tiles = static_cast<size_t>(cdiv(M, 128) * cdiv(N, 128));
+  return ((static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~static_cast<size_t>(255)) +
+         ((tiles * 4 + 255) & ~static_cast<size_t>(255));
 }
 
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
@@ -913,6 +1130,38 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
              (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
   p.nst = 3;
   p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * (kBM + pl.bpiece) * 128) / ((kBM + pl.bpiece) * kBK));
+  p.gx = static_cast<int>(pl.grid_x);
+  p.T = static_cast<int>(pl.grid_x * pl.grid_y);
+  p.S = static_cast<int>(cdiv(a.K, kBK));
+  dim3 grid;
+  if (a.split >= 1) {
+    // explicit split-K: one CTA per tile and K piece; int32 atomics when split
+    p.sched = 0;
+    if (a.split > 1) {
+      p.a.ws_acc = static_cast<int32_t*>(a.ws);
+      p.a.ws_count = reinterpret_cast<uint32_t*>(
+          static_cast<char*>(a.ws) +
+          ((static_cast<size_t>(a.M) * static_cast<size_t>(a.N) * 4 + 255) & ~static_cast<size_t>(255)));
+    }
+    grid = dim3(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y), static_cast<unsigned>(a.split));
+  } else {
+    // automatic: the balanced schedule, falling back to whole tiles in rounds
+    // when the caller's workspace cannot hold the shared tiles' partials
+    p.sched = 1;
+    TcSched sc = tc_balanced(p.T, p.S);
+    size_t cb = 0;
+    const size_t need = tc_balanced_bytes(a.M, a.N, a.K, &cb);
+    if (need > 0 && need > a.ws_bytes) sc = TcSched{152, static_cast<int>(cdiv(p.T, 152)), 0};
+    if (sc.R > 0 && need > 0) {
+      p.cnt = static_cast<uint32_t*>(a.ws);
+      p.slots = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + cb);
+    }
+    p.W = sc.W;
+    p.R = sc.R;
+    p.slot_elems = kBM * pl.bpiece;
+    const int64_t ctas = sc.R > 0 ? sc.G : std::min<int64_t>(sc.G, p.T);
+    grid = dim3(static_cast<unsigned>(ctas), 1, 1);
+  }
   CUtensorMap tmA, tmB;
   const int8_t* Am = pl.swap ? a.w : a.q;
   const int8_t* Bm = pl.swap ? a.q : a.w;
@@ -920,7 +1169,6 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(pl.grid_x), static_cast<unsigned>(pl.grid_y), static_cast<unsigned>(a.split));
   linear_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tmA, tmB);
   return cudaGetLastError();
 }
@@ -940,11 +1188,39 @@ int linear_kernel_kind(int64_t M, int64_t N, int64_t K) {
 }
 
 int linear_auto_split(int64_t M, int64_t N, int64_t K) {
-  return use_mma_path() ? mma_auto_split(M, N, K) : tc_auto_split(M, N, K);
+  return use_mma_path() ? mma_auto_split(M, N, K) : 0;
+}
+
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (use_mma_path() && split == 0) split = mma_auto_split(M, N, K);
+  if (split == 0) return tc_balanced_bytes(M, N, K, nullptr);
+  return split > 1 ? atomic_bytes(M, N) : 0;
+}
+
+size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, size_t cap) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (use_mma_path() && split == 0) split = mma_auto_split(M, N, K);
+  if (split == 0) {
+    size_t cb = 0;
+    const size_t need = tc_balanced_bytes(M, N, K, &cb);
+    return need > 0 && need <= cap ? cb : 0;  // beyond cap the call runs whole tiles only
+  }
+  const size_t need = split > 1 ? atomic_bytes(M, N) : 0;
+  return need <= cap ? need : SIZE_MAX;
 }
 
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream) {
-  return use_mma_path() ? launch_linear_mma(a, stream) : launch_linear_tc(a, stream);
+  if (!use_mma_path()) return launch_linear_tc(a, stream);
+  LinearArgs b = a;
+  if (b.split == 0) b.split = mma_auto_split(a.M, a.N, a.K);
+  if (b.split > 1) {
+    b.ws_acc = static_cast<int32_t*>(a.ws);
+    b.ws_count = reinterpret_cast<uint32_t*>(
+        static_cast<char*>(a.ws) +
+        ((static_cast<size_t>(a.M) * static_cast<size_t>(a.N) * 4 + 255) & ~static_cast<size_t>(255)));
+  }
+  return launch_linear_mma(b, stream);
 }
 
 cudaError_t read_and_clear_kernel_error(uint32_t* out) {

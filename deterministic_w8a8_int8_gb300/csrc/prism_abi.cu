@@ -100,8 +100,7 @@ int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K) { return prism::linea
 
 size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
   if (M <= 0 || N <= 0 || K <= 0 || split_k < 0 || split_k > PRISM_MAX_SPLIT_K) return 0;
-  const int s = split_k == 0 ? prism::linear_auto_split(M, N, K) : split_k;
-  return prism::linear_workspace_bytes(M, N, K, s);
+  return prism::linear_workspace_bytes(M, N, K, split_k);
 }
 
 int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
@@ -125,8 +124,7 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
   if (acc_out != nullptr && !aligned(acc_out, 4)) return PRISM_ERR_ALIGNMENT;
   if (M > 65535LL * 128 || N > (1LL << 31) * 64) return PRISM_ERR_UNSUPPORTED;
 
-  const int split = split_k == 0 ? prism::linear_auto_split(M, N, K) : split_k;
-  const size_t need = prism::linear_workspace_bytes(M, N, K, split);
+  const size_t need = prism::linear_workspace_bytes(M, N, K, split_k);
   prism::LinearArgs a{};
   a.q = q;
   a.ldq = ldq;
@@ -142,15 +140,14 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
   a.M = M;
   a.N = N;
   a.K = K;
-  a.split = split;
+  a.split = split_k;
   a.pair_io = aligned(out_bf16, 4) && ldo % 2 == 0 &&
               (residual_bf16 == nullptr || (aligned(residual_bf16, 4) && ldr % 2 == 0));
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need) return PRISM_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return PRISM_ERR_ALIGNMENT;
-    const size_t acc_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~static_cast<size_t>(255);
-    a.ws_acc = static_cast<int32_t*>(workspace);
-    a.ws_count = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + acc_bytes);
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
   }
   return prism::record_cuda(prism::launch_linear(a, static_cast<cudaStream_t>(cuda_stream)));
 }

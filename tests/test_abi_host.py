@@ -121,9 +121,13 @@ def test_workspace_and_dispatch_queries(L):
     assert L.prism_w8a8_workspace_bytes(64, 64, 64, 65) == 0
     for M, N, K in [(1, 5120, 17408), (304, 5120, 5120), (2048, 34816, 5120), (37, 384, 256)]:
         s = L.prism_w8a8_auto_split(M, N, K)
-        assert 1 <= s <= 64
-        assert L.prism_w8a8_workspace_bytes(M, N, K, 0) == L.prism_w8a8_workspace_bytes(M, N, K, s)
+        assert 0 <= s <= 64   # 0: the balanced schedule of the tensor-core kernel
+        if s > 0:
+            assert L.prism_w8a8_workspace_bytes(M, N, K, 0) == L.prism_w8a8_workspace_bytes(M, N, K, s)
         assert L.prism_w8a8_kernel_kind(M, N, K) in (1, 2, 3)
+    # the balanced schedule keeps partial tiles only when it shares tiles
+    assert L.prism_w8a8_workspace_bytes(37, 384, 256, 0) == 0
+    assert L.prism_w8a8_workspace_bytes(304, 15360, 5120, 0) > 0
     assert L.prism_w8a8_kernel_kind(0, 5, 16) == 0
 
 

@@ -272,3 +272,58 @@ def test_repeated_runs_bit_identical(cuda_device, M, N, K):
     for acc in accs:
         assert np.array_equal(host(acc), acco)
     assert prism.prism_device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K", [
+    (1024, 4864, 512),    # 152 tiles: whole tiles only, one round
+    (304, 1536, 5120),    # 24 tiles shared out over 120 CTAs (5 K ranges each)
+    (600, 2560, 2048),    # 50 tiles, K units shared over 152 CTAs
+    (304, 15360, 1024),   # 240 tiles: one round of whole tiles, the rest shared
+    (37, 384, 256),       # 3 tiles of 4 K stages: one CTA per tile
+    (640, 25600, 256),    # 500 tiles of 4 K stages: whole tiles in rounds
+    (96, 640, 17408),     # 5 tiles of 272 K stages over 152 CTAs
+])
+def test_balanced_schedule_matches_single_piece(cuda_device, M, N, K):
+    """The automatic (balanced) schedule -- whole tiles, then K ranges of the
+    remaining tiles shared between CTAs and summed from partial-tile slots --
+    gives the same bits as one K piece per tile, for shapes that reach each
+    branch of the schedule choice; the slots and counters are reused by a
+    second call."""
+    rng = np.random.default_rng(M * 7 + N + K)
+    q = dev(rng.integers(-127, 128, (M, K), dtype=np.int8))
+    w = dev(rng.integers(-127, 128, (N, K), dtype=np.int8))
+    a = dev((rng.random(M, dtype=np.float32) * 1e-3 + 1e-4).astype(np.float32))
+    s = dev((rng.random(N, dtype=np.float32) * 1e-2 + 1e-3).astype(np.float32))
+    rb = wl.bf16_bits(rng.normal(size=(M, N)).astype(np.float32))
+    ref, ref_acc = gpu_linear(q, a, w, s, dev_bf16(rb), split=1)
+    ref_bits, ref_acc = ref.view(torch.int16).cpu().numpy(), ref_acc.cpu().numpy()
+    ws_buf = prism.new_workspace(M, N, K, 0, torch.device("cuda", 0))
+    for _ in range(2):
+        acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        got = prism.prism_w8a8_linear(q, a, w, s, residual=dev_bf16(rb), split_k=0, workspace=ws_buf, acc_out=acc)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.view(torch.int16).cpu().numpy(), ref_bits)
+        assert np.array_equal(acc.cpu().numpy(), ref_acc)
+
+
+@pytest.mark.gpu
+def test_balanced_schedule_without_room_uses_whole_tiles(cuda_device):
+    """Given less workspace than the balanced schedule's partial tiles need,
+    an automatic call is refused; the no-workspace entry point runs the same
+    shape with whole tiles and gives the same bits."""
+    M, N, K = 304, 15360, 1024
+    rng = np.random.default_rng(5)
+    q = dev(rng.integers(-127, 128, (M, K), dtype=np.int8))
+    w = dev(rng.integers(-127, 128, (N, K), dtype=np.int8))
+    a = dev(np.full(M, 1e-3, np.float32))
+    s = dev(np.full(N, 1e-2, np.float32))
+    ref, _ = gpu_linear(q, a, w, s, None, split=1)
+    ref = ref.view(torch.int16).cpu().numpy()
+    need = prism.prism_w8a8_workspace_bytes(M, N, K, 0)
+    assert need > prism.PRISM_NOALLOC_SCRATCH_BYTES
+    with pytest.raises(prism.PrismError):
+        prism.prism_w8a8_linear(q, a, w, s, split_k=0,
+                                workspace=torch.zeros(need // 2, dtype=torch.uint8, device="cuda"))
+    out = prism.prism_w8a8_linear_noalloc(q, a, w, s, split_k=0)
+    assert np.array_equal(out.view(torch.int16).cpu().numpy(), ref)
