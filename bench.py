@@ -456,7 +456,8 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": "forest_bucket_m304_k5120: quant + qkv(n15360) + quant + o_proj(n5120,+res) "
                                "+ candidate readout(3 pos, v248000)",
-                   "global_batch_rows": M * world, "split_k": {"qkv": split_q, "o_proj": split_o},
+                   "global_batch_rows": M * world, "schedule": {"qkv": "balanced" if split_q == 0 else f"split_k={split_q}",
+                                "o_proj": "balanced" if split_o == 0 else f"split_k={split_o}"},
                    "l2": f"inputs larger than L2: {N_ROTATE} rotated weight sets "
                          f"({N_ROTATE * (work.qkv.N + work.o.N) * K / 1e6:.0f} MB) + 1.27 GB LM head",
                    "launch": "direct C-ABI calls, arguments marshalled once",

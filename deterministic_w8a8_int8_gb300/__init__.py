@@ -183,7 +183,8 @@ def prism_w8a8_linear(q, a_scale, w, w_scale, residual=None, out=None, acc_out=N
 
     ``residual`` may be ``out`` itself (in-place residual add).  ``workspace``
     must be a zeroed uint8 tensor of at least prism_w8a8_workspace_bytes bytes
-    when split-K is in use; one is allocated (and zeroed) per call when None."""
+    when the schedule needs one (split-K > 1, or an automatic call that shares
+    tiles between CTAs); one is allocated (and zeroed) per call when None."""
     import torch
     _require(q, torch.int8, "q", 2)
     _require(w, torch.int8, "w", 2)

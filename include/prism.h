@@ -99,8 +99,11 @@ int prism_quant_act(const void *x_bf16, int64_t ldx, const float *inv_smooth,
 
 /*
  * Bytes of workspace prism_w8a8_linear needs for this shape and split-K
- * setting (split_k = 0 means the automatic choice, as in the linear call).
- * Returns 0 when no workspace is needed (split-K of 1).
+ * setting (split_k = 0 means the automatic schedule, as in the linear call:
+ * arrival counters plus two partial int32 tiles per CTA when it shares tiles
+ * between CTAs; about 4*M*N bytes plus counters for split_k > 1).  Returns 0
+ * when no workspace is needed (split_k = 1, or an automatic schedule of whole
+ * tiles only).
  */
 size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
 
@@ -116,9 +119,13 @@ size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
  *   out, ldo       [M, N] bf16 output
  *   acc_out        [M, N] int32 dense (stride N) copy of the accumulator, or
  *                  NULL (a debugging aid; costs 4*M*N bytes of writes)
- *   split_k        0 = automatic, else 1..PRISM_MAX_SPLIT_K.  The K range is
- *                  cut into split_k pieces whose int32 partial sums are added
- *                  as integers; the result does not depend on split_k.
+ *   split_k        0 = automatic: a balanced schedule that gives every SM the
+ *                  same number of K stages -- whole tiles first, then the K
+ *                  ranges of the remaining tiles shared between CTAs, whose
+ *                  int32 partial sums are added as integers by the last CTA
+ *                  to finish each tile.  1..PRISM_MAX_SPLIT_K: every tile's
+ *                  K range cut into split_k equal pieces, partial sums added
+ *                  as integers.  The result does not depend on split_k.
  *   workspace      device memory of at least
  *                  prism_w8a8_workspace_bytes(M, N, K, split_k) bytes, 256-byte
  *                  aligned, ZEROED by the caller before its first use.  Every
@@ -155,9 +162,10 @@ int prism_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
  * prism_w8a8_linear (bit-identical outputs), minus workspace and
  * workspace_bytes.  Split-K scratch comes from a fixed array of
  * PRISM_NOALLOC_SCRATCH_BYTES inside the library; the call allocates nothing.
- *   - Shapes whose split-K scratch exceeds that size (about 4*M*N bytes when
- *     split_k > 1; split_k = 1 needs none) return PRISM_ERR_UNSUPPORTED and
- *     enqueue nothing.
+ *   - Explicit split_k > 1 on shapes whose scratch exceeds that size (about
+ *     4*M*N bytes) returns PRISM_ERR_UNSUPPORTED and enqueues nothing.
+ *   - split_k = 0 uses the balanced schedule when its partial tiles fit the
+ *     array, else whole tiles only (same bits either way).
  *   - All calls on one device share the array.  Each call zeroes the part it
  *     uses on its own stream before computing, but calls that overlap on the
  *     GPU (other streams, unordered host threads) race on it: order them on
@@ -222,7 +230,9 @@ int prism_last_cuda_error(char *buf, size_t buf_bytes);
  */
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K);
 
-/* The split-K factor an automatic (split_k = 0) call would use. */
+/* The split-K factor an automatic (split_k = 0) call would use: 0 for the
+ * tensor-core kernel's balanced schedule (K ranges of varying length, see
+ * prism_w8a8_linear), else the uniform factor of the mma.sync kernel. */
 int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K);
 
 /* Device error bits (PRISM_DEVSTATUS_*) raised by kernels since the last
