@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "prism.h"
 
@@ -95,6 +96,34 @@ int record_cuda(cudaError_t e);
 
 }  // namespace prism
 
+// Programmatic dependent launch: every library kernel is launched so that it
+// may start while the previous kernel of its stream is still finishing.  It
+// lets its own dependents launch at once (pdl_trigger: the runtime starts a
+// dependent grid only when every CTA of this one has started and signalled,
+// or exited, so a multi-wave grid cannot be starved), and waits for its
+// predecessor to complete, with its memory visible, before touching any data
+// (pdl_wait).  Without a predecessor kernel the wait returns at once.
+namespace prism {
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_kernel(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+}  // namespace prism
+
 // Internal launchers (one per kernel family), defined in their .cu files.
 namespace prism {
 cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K,
@@ -115,6 +144,7 @@ struct LinearArgs {
   int64_t M, N, K;
   int split;            // 0: automatic schedule; >= 1: explicit split-K
   int pair_io;          // 1: out/residual rows allow 4-byte bf16 pairs
+  int no_pdl;           // 1: launch without overlapping the stream's previous work
   void* ws;             // caller's workspace (256-byte aligned) or null
   size_t ws_bytes;      // its size
   int32_t* ws_acc;      // split-K > 1: [M, N] int32, zero between calls (set by the launcher)

@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(kThreads, 2) linear_mma_kernel(const LinearArg
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageA;
   __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -232,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 2) linear_mma_kernel(const LinearArg
 }
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
@@ -252,8 +253,7 @@ cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(cdiv(a.N, kBN)), static_cast<unsigned>(cdiv(a.M, kBM)),
             static_cast<unsigned>(a.split));
-  linear_mma_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(linear_mma_kernel, grid, dim3(kThreads), kSmemBytes, stream, a.no_pdl == 0, a);
 }
 
 }  // namespace prism

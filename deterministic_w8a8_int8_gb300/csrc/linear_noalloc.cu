@@ -104,6 +104,7 @@ extern "C" int prism_w8a8_linear_noalloc(const int8_t* q, int64_t ldq, const flo
   a.N = N;
   a.K = K;
   a.split = split_k;
+  a.no_pdl = 1;  // the scratch clear below must complete before the kernel starts
   a.pair_io = aligned_to(out_bf16, 4) && ldo % 2 == 0 &&
               (residual_bf16 == nullptr || (aligned_to(residual_bf16, 4) && ldr % 2 == 0));
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);

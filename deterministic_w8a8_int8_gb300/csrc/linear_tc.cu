@@ -78,7 +78,7 @@ constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
 // enough TMA loads are in flight to cover their latency).
 constexpr int kRingRegion = 216 * 1024;
 constexpr int kBarBytes = 512;
-constexpr int kScaleBytes = 2 * kBNMax * 4;   // the tile's a_scale and w_scale values
+constexpr int kScaleBytes = 2 * 2 * kBNMax * 4;   // two items' a_scale and w_scale values
 constexpr int kSmemBytes = 1024 + kRingRegion + kBarBytes + kScaleBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;             // fp32 chunk accumulator (single-buffered layout)
@@ -103,8 +103,8 @@ struct TcParams {
   int W;         // balanced schedule: rounds of whole tiles per CTA
   int R;         // balanced schedule: tiles whose K units are shared out
   uint32_t* cnt;   // balanced schedule: arrival counters of the shared tiles (zero between calls)
-  int32_t* slots;  // balanced schedule: 2 partial tiles per CTA
-  int slot_elems;  // int32 elements of one slot (128 * bpiece)
+  int32_t* acc;    // balanced schedule: one int32 accumulator per shared tile (zero between calls)
+  int slot_elems;  // int32 elements of one accumulator (128 * bpiece)
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -248,230 +248,100 @@ __device__ __forceinline__ void st_shared_v4_if(uint32_t addr, uint32_t a, uint3
 }
 
 // --------------------------------------------------------------- epilogue --
-__device__ __forceinline__ void emit(const LinearArgs& a, int64_t m, int64_t n, int32_t v) {
-  const float as = __ldg(a.a_scale + m);
-  const float ws = __ldg(a.w_scale + n);
-  const uint32_t o = a.residual != nullptr ? epilogue_bf16_res(v, as, ws, bf16_bits_to_float(a.residual[m * a.ldr + n]))
-                                           : epilogue_bf16(v, as, ws);
-  a.out[m * a.ldo + n] = static_cast<uint16_t>(o);
-  if (a.acc_out != nullptr) a.acc_out[m * a.N + n] = v;
-}
 
-// Coalesced tile output.  The final int32 tile sits in shared memory as
-// T[rows_out][cols_out] (row stride cols_out + 4 words, so the per-row writes
-// of the drain threads hit distinct banks).  Each participating thread
-// then owns groups of 4 consecutive columns, a warp covering contiguous
-// column ranges of one row, so global loads and stores are coalesced.  The
-// residual and scale loads of kRowBatch rows are issued before any of them is
-// used, so they overlap instead of paying one memory latency each.
-//   mode 0: epilogue to bf16 out (+ residual, + acc_out)
-//   mode 1: integer atomics of the tile into the split-K workspace
-//   mode 2: read the finished sum back from the workspace (and re-zero it),
-//           then the epilogue
-constexpr int kRowBatch = 4;
-constexpr int kMaxGroupsPerThread = kBNMax / 4 / 32;   // 2
-
-// Epilogue of a tile whose channel width is 128 (kWide false) or 256 (true)
-// and lies wholly inside N, with vector I/O and no int32 dump: warp w writes
-// token rows w, w + 16, ... (a warp-uniform row test, no per-element
-// branches), lane l channels 4l..4l+3 (and 128 + 4l.. when wide); the lane's
-// w_scale values stay in registers and the residuals of kB rows are loaded
-// before any of them is used.
-template <bool kRes, bool kWide>
-__device__ __forceinline__ void tile_out_fast(const TcParams& p, const uint32_t* T, const float* s_as,
-                                              const float* s_ws, int rows_valid, int cols_out, int64_t m0,
-                                              int64_t n0, int t) {
+// Output of one accumulator round.  Lane trow of a TMEM quadrant holds the
+// int32 results of A row a0 + trow for the 16 B rows b0 + 16 cb + j; in the
+// swapped orientation A rows are output channels and B rows tokens, else the
+// reverse.  s_as / s_ws hold the tile's a_scale (by token) and w_scale (by
+// channel).  The residual values of the round are all loaded before any
+// output is stored, so an in-place residual (residual == out) is safe.
+__device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, const float* s_ws, int64_t a0,
+                                          int64_t b0, int trow, int cb, const int32_t (&v)[16]) {
   const LinearArgs& a = p.a;
-  constexpr int kB = 4;
-  const int stride = cols_out + 4;
-  const int w = t >> 5, l = t & 31;
-  const float4 ws0 = reinterpret_cast<const float4*>(s_ws)[l];
-  const float4 ws1 = kWide ? reinterpret_cast<const float4*>(s_ws)[l + 32] : make_float4(0.f, 0.f, 0.f, 0.f);
-  uint16_t* out0 = a.out + m0 * a.ldo + n0 + 4 * l;
-  const uint16_t* res0 = kRes ? a.residual + m0 * a.ldr + n0 + 4 * l : nullptr;
-  for (int rb = w; rb < rows_valid; rb += 16 * kB) {
-    uint2 rv[kB][2];
+  const bool res = a.residual != nullptr;
+  if (p.swap) {
+    const int64_t n = a0 + trow, mb = b0 + cb * 16;
+    if (n >= a.N) return;
+    const int jn = a.M - mb < 16 ? static_cast<int>(a.M - mb) : 16;
+    const float ws = s_ws[trow];
+    float r[16];
 #pragma unroll
-    for (int b = 0; b < kB; ++b) {
-      const int r = rb + 16 * b;
-      rv[b][0] = rv[b][1] = make_uint2(0u, 0u);
-      if (kRes && r < rows_valid) {
-        rv[b][0] = *reinterpret_cast<const uint2*>(res0 + r * a.ldr);
-        if (kWide) rv[b][1] = *reinterpret_cast<const uint2*>(res0 + r * a.ldr + 128);
-      }
-    }
+    for (int j = 0; j < 16; ++j)
+      r[j] = res && j < jn ? bf16_bits_to_float(a.residual[(mb + j) * a.ldr + n]) : 0.f;
 #pragma unroll
-    for (int b = 0; b < kB; ++b) {
-      const int r = rb + 16 * b;
-      if (r < rows_valid) {
-        const float as = s_as[r];
-#pragma unroll
-        for (int h = 0; h < (kWide ? 2 : 1); ++h) {
-          const uint4 tv = *reinterpret_cast<const uint4*>(T + r * stride + 4 * l + 128 * h);
-          const float4 w4 = h == 0 ? ws0 : ws1;
-          uint32_t o0, o1;
-          if (kRes) {
-            o0 = epilogue_bf16_res(static_cast<int32_t>(tv.x), as, w4.x, bf16_lo(rv[b][h].x)) |
-                 (epilogue_bf16_res(static_cast<int32_t>(tv.y), as, w4.y, bf16_hi(rv[b][h].x)) << 16);
-            o1 = epilogue_bf16_res(static_cast<int32_t>(tv.z), as, w4.z, bf16_lo(rv[b][h].y)) |
-                 (epilogue_bf16_res(static_cast<int32_t>(tv.w), as, w4.w, bf16_hi(rv[b][h].y)) << 16);
-          } else {
-            o0 = epilogue_bf16(static_cast<int32_t>(tv.x), as, w4.x) |
-                 (epilogue_bf16(static_cast<int32_t>(tv.y), as, w4.y) << 16);
-            o1 = epilogue_bf16(static_cast<int32_t>(tv.z), as, w4.z) |
-                 (epilogue_bf16(static_cast<int32_t>(tv.w), as, w4.w) << 16);
-          }
-          *reinterpret_cast<uint2*>(out0 + r * a.ldo + 128 * h) = make_uint2(o0, o1);
-        }
+    for (int j = 0; j < 16; ++j) {
+      if (j < jn) {
+        const float as = s_as[cb * 16 + j];
+        const uint32_t o = res ? epilogue_bf16_res(v[j], as, ws, r[j]) : epilogue_bf16(v[j], as, ws);
+        a.out[(mb + j) * a.ldo + n] = static_cast<uint16_t>(o);
+        if (a.acc_out != nullptr) a.acc_out[(mb + j) * a.N + n] = v[j];
       }
-    }
-  }
-}
-
-// s_as[r] / s_ws[c]: a_scale of the tile's token r and w_scale of its channel
-// c, copied into shared memory when the CTA started.
-__device__ __forceinline__ void tile_out(const TcParams& p, const uint32_t* T, const float* s_as,
-                                         const float* s_ws, int rows_out, int cols_out, int64_t m0,
-                                         int64_t n0, int mode, int t, int nthreads) {
-  const LinearArgs& a = p.a;
-  const int stride = cols_out + 4;
-  const int groups = cols_out / 4;                 // 4-column groups per row
-  const int per_row = groups < 32 ? groups : 32;   // threads on one row
-  const int rows_per_pass = nthreads / per_row;
-  const int gpt = groups / per_row;                // groups per thread per row (1 or 2)
-  const int g0 = t % per_row;
-  const bool has_res = a.residual != nullptr;
-
-  if (mode == 2) {
-    // split-K read-back: copy the finished integer sums into this thread's
-    // own entries of the staged tile (re-zeroing the workspace), one row at a
-    // time (this path is rare; it keeps few registers live), then run the
-    // ordinary epilogue from the tile
-    uint32_t* Tw = const_cast<uint32_t*>(T);
-    const bool vec = (a.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.ws_acc) & 15) == 0);
-    for (int r = t / per_row; r < rows_out; r += rows_per_pass) {
-      const int64_t m = m0 + r;
-      if (m >= a.M) continue;
-      for (int q = 0; q < gpt; ++q) {
-        const int c = 4 * (g0 + q * per_row);
-        const int64_t n = n0 + c;
-        int32_t* wp = a.ws_acc + m * a.N + n;
-        int4 v = make_int4(0, 0, 0, 0);
-        if (vec && n + 4 <= a.N) {
-          v = __ldcg(reinterpret_cast<const int4*>(wp));
-          __stcg(reinterpret_cast<int4*>(wp), make_int4(0, 0, 0, 0));
-        } else {
-          if (n < a.N) { v.x = __ldcg(wp); __stcg(wp, 0); }
-          if (n + 1 < a.N) { v.y = __ldcg(wp + 1); __stcg(wp + 1, 0); }
-          if (n + 2 < a.N) { v.z = __ldcg(wp + 2); __stcg(wp + 2, 0); }
-          if (n + 3 < a.N) { v.w = __ldcg(wp + 3); __stcg(wp + 3, 0); }
-        }
-        *reinterpret_cast<int4*>(Tw + r * stride + c) = v;
-      }
-    }
-    mode = 0;
-  }
-
-  if (mode == 0 && p.vec_io && a.acc_out == nullptr && (cols_out == 128 || cols_out == 256) &&
-      n0 + cols_out <= a.N && nthreads == 512) {
-    const int rows_valid = static_cast<int>(a.M - m0 < rows_out ? a.M - m0 : rows_out);
-    const bool res = a.residual != nullptr;
-    if (cols_out == 256) {
-      if (res) tile_out_fast<true, true>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
-      else tile_out_fast<false, true>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
-    } else {
-      if (res) tile_out_fast<true, false>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
-      else tile_out_fast<false, false>(p, T, s_as, s_ws, rows_valid, cols_out, m0, n0, t);
     }
     return;
   }
-
-  float4 wsv[kMaxGroupsPerThread];
-#pragma unroll
-  for (int q = 0; q < kMaxGroupsPerThread; ++q) {
-    const int64_t n = n0 + 4 * (g0 + q * per_row);
-    wsv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (mode != 1 && q < gpt && p.vec_io && n + 4 <= a.N)
-      wsv[q] = *reinterpret_cast<const float4*>(s_ws + 4 * (g0 + q * per_row));
-  }
-
-  for (int rb = t / per_row; rb < rows_out; rb += rows_per_pass * kRowBatch) {
-    uint2 rv[kRowBatch][kMaxGroupsPerThread];
-    float as[kRowBatch];
-    // ---- issue every load of the batch
-#pragma unroll
-    for (int b = 0; b < kRowBatch; ++b) {
-      const int r = rb + b * rows_per_pass;
-      const int64_t m = m0 + r;
-      const bool row_ok = r < rows_out && m < a.M;
-      as[b] = (mode != 1 && row_ok) ? s_as[r] : 0.f;
-#pragma unroll
-      for (int q = 0; q < kMaxGroupsPerThread; ++q) {
-        const int c = 4 * (g0 + q * per_row);
-        const int64_t n = n0 + c;
-        const bool ok = row_ok && q < gpt;
-        rv[b][q] = make_uint2(0u, 0u);
-        if (ok && mode != 1 && has_res && p.vec_io && n + 4 <= a.N)
-          rv[b][q] = *reinterpret_cast<const uint2*>(a.residual + m * a.ldr + n);
-      }
+  const int64_t m = a0 + trow, nb = b0 + cb * 16;
+  if (m >= a.M) return;
+  const float as = s_as[trow];
+  const float* w = s_ws + cb * 16;
+  if (p.vec_io && nb + 16 <= a.N) {
+    uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
+    if (res) {
+      r0 = *reinterpret_cast<const uint4*>(a.residual + m * a.ldr + nb);
+      r1 = *reinterpret_cast<const uint4*>(a.residual + m * a.ldr + nb + 8);
     }
-    // ---- use them
+    const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    uint32_t o[8];
 #pragma unroll
-    for (int b = 0; b < kRowBatch; ++b) {
-      const int r = rb + b * rows_per_pass;
-      const int64_t m = m0 + r;
-      if (r >= rows_out || m >= a.M) continue;
+    for (int i = 0; i < 8; ++i) {
+      const int j = 2 * i;
+      o[i] = res ? (epilogue_bf16_res(v[j], as, w[j], bf16_lo(rw[i])) |
+                    (epilogue_bf16_res(v[j + 1], as, w[j + 1], bf16_hi(rw[i])) << 16))
+                 : (epilogue_bf16(v[j], as, w[j]) | (epilogue_bf16(v[j + 1], as, w[j + 1]) << 16));
+    }
+    *reinterpret_cast<uint4*>(a.out + m * a.ldo + nb) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(a.out + m * a.ldo + nb + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+    if (a.acc_out != nullptr) {
 #pragma unroll
-      for (int q = 0; q < kMaxGroupsPerThread; ++q) {
-        if (q >= gpt) continue;
-        const int c = 4 * (g0 + q * per_row);
-        const int64_t n = n0 + c;
-        int32_t vv[4];
-        const uint4 tv = *reinterpret_cast<const uint4*>(T + r * stride + c);  // read at use time
-        vv[0] = static_cast<int32_t>(tv.x);
-        vv[1] = static_cast<int32_t>(tv.y);
-        vv[2] = static_cast<int32_t>(tv.z);
-        vv[3] = static_cast<int32_t>(tv.w);
-        if (mode == 1) {
+      for (int j = 0; j < 16; ++j) a.acc_out[m * a.N + nb + j] = v[j];
+    }
+    return;
+  }
+  float r[16];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (n + j < a.N) atomicAdd(a.ws_acc + m * a.N + n + j, vv[j]);
-          continue;
-        }
-        if (p.vec_io && n + 4 <= a.N) {
-          const float4 w4 = wsv[q];
-          uint32_t o0, o1;
-          if (has_res) {
-            o0 = epilogue_bf16_res(vv[0], as[b], w4.x, bf16_lo(rv[b][q].x)) |
-                 (epilogue_bf16_res(vv[1], as[b], w4.y, bf16_hi(rv[b][q].x)) << 16);
-            o1 = epilogue_bf16_res(vv[2], as[b], w4.z, bf16_lo(rv[b][q].y)) |
-                 (epilogue_bf16_res(vv[3], as[b], w4.w, bf16_hi(rv[b][q].y)) << 16);
-          } else {
-            o0 = epilogue_bf16(vv[0], as[b], w4.x) | (epilogue_bf16(vv[1], as[b], w4.y) << 16);
-            o1 = epilogue_bf16(vv[2], as[b], w4.z) | (epilogue_bf16(vv[3], as[b], w4.w) << 16);
-          }
-          *reinterpret_cast<uint2*>(a.out + m * a.ldo + n) = make_uint2(o0, o1);
-          if (a.acc_out != nullptr) {
+  for (int j = 0; j < 16; ++j) r[j] = res && nb + j < a.N ? bf16_bits_to_float(a.residual[m * a.ldr + nb + j]) : 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) a.acc_out[m * a.N + n + j] = vv[j];
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (n + j < a.N) emit(a, m, n + j, vv[j]);
-        }
-      }
+  for (int j = 0; j < 16; ++j) {
+    if (nb + j < a.N) {
+      const uint32_t o = res ? epilogue_bf16_res(v[j], as, w[j], r[j]) : epilogue_bf16(v[j], as, w[j]);
+      a.out[m * a.ldo + nb + j] = static_cast<uint16_t>(o);
+      if (a.acc_out != nullptr) a.acc_out[m * a.N + nb + j] = v[j];
     }
   }
 }
 
-// The atomic split-K output modes (1: add the tile into the workspace, 2:
-// read the finished sum back, then the epilogue).
-__device__ __forceinline__ void tile_out_split(const TcParams& p, const uint32_t* T, const float* s_as,
-                                            const float* s_ws, int rows_out, int cols_out, int64_t m0,
-                                            int64_t n0, int mode, int t) {
-  tile_out(p, T, s_as, s_ws, rows_out, cols_out, m0, n0, mode, t, kWorkers);
+// (m, n) of element j of a round, and whether it lies inside the matrix.
+__device__ __forceinline__ bool round_elem(const TcParams& p, int64_t a0, int64_t b0, int trow, int cb, int j,
+                                           int64_t& m, int64_t& n) {
+  const int64_t ar = a0 + trow, br = b0 + cb * 16 + j;
+  m = p.swap ? br : ar;
+  n = p.swap ? ar : br;
+  return m < p.a.M && n < p.a.N;
 }
+
+// Explicit split-K: add a round into the [M, N] int32 workspace.
+__device__ __forceinline__ void round_atomic(const TcParams& p, int64_t a0, int64_t b0, int trow, int cb,
+                                             const int32_t (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    int64_t m, n;
+    if (round_elem(p, a0, b0, trow, cb, j, m, n)) atomicAdd(p.a.ws_acc + m * p.a.N + n, v[j]);
+  }
+}
+
+// A shared tile's accumulator is kept in TMEM order: element (trow, 16 cb +
+// j) at word (16 cb + j) * 128 + trow, so that a warp's 32 lanes touch 128
+// contiguous bytes.
+__device__ __forceinline__ int slot_index(int trow, int cb, int j) { return (cb * 16 + j) * kBM + trow; }
 
 // ------------------------------------------------------------------ kernel --
 // One unit of work of a CTA: output tile (tx, ty) -- A block tx of 128 rows,
@@ -480,10 +350,11 @@ __device__ __forceinline__ void tile_out_split(const TcParams& p, const uint32_t
 //   kind 1: one of a.split equal K pieces (explicit split-K): int32 atomics
 //           into the workspace tile; the last piece's CTA applies the epilogue.
 //   kind 2: a K range of a tile that the balanced schedule shares between
-//           CTAs: the partial int32 tile goes to this CTA's slot; the last CTA
-//           to finish the tile adds the other slots and applies the epilogue.
+//           CTAs: the partial int32 sums are added (integer reductions) into
+//           the tile's accumulator; the last CTA to finish the tile reads it
+//           back, re-zeroes it and applies the epilogue.
 struct Item {
-  int tx, ty, k0, k1, kind, tile, slot;
+  int tx, ty, k0, k1, kind, tile;
 };
 
 // Work item n of this CTA; every role of the CTA walks the same list.
@@ -504,7 +375,6 @@ __device__ __forceinline__ bool get_item(const TcParams& p, int n, Item& it) {
     it.k1 = it.k0 + per < p.S ? it.k0 + per : p.S;
     it.kind = p.a.split > 1 ? 1 : 0;
     it.tile = it.ty * p.gx + it.tx;
-    it.slot = 0;
     return true;
   }
   const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
@@ -517,7 +387,6 @@ __device__ __forceinline__ bool get_item(const TcParams& p, int n, Item& it) {
     it.k1 = p.S;
     it.kind = 0;
     it.tile = t;
-    it.slot = 0;
     return true;
   }
   if (p.R == 0) return false;
@@ -535,24 +404,18 @@ __device__ __forceinline__ bool get_item(const TcParams& p, int n, Item& it) {
   it.k1 = (u1 < ts + p.S ? u1 : ts + p.S) - ts;
   it.kind = (it.k0 == 0 && it.k1 == p.S) ? 0 : 2;
   it.tile = st;
-  it.slot = 2 * b + (j == 0 ? 0 : 1);  // a CTA's partial items are its first and its last
   return true;
 }
 
 // CTAs bf..bl of the balanced schedule whose K ranges meet shared tile st
-// (the CTA holding unit u is floor(((u + 1) G - 1) / U)), and the slot CTA
-// c used for it.
+// (the CTA holding unit u is floor(((u + 1) G - 1) / U)).
 __device__ __forceinline__ void shared_tile_ctas(const TcParams& p, int st, int& bf, int& bl) {
   const int G = static_cast<int>(gridDim.x);
   const int U = p.R * p.S;
   bf = ((st * p.S + 1) * G - 1) / U;
   bl = ((st * p.S + p.S) * G - 1) / U;
 }
-__device__ __forceinline__ int shared_tile_slot(const TcParams& p, int st, int c) {
-  const int U = p.R * p.S;
-  const int first = (c * U / static_cast<int>(gridDim.x)) / p.S;  // first shared tile of CTA c
-  return 2 * c + (st == first ? 0 : 1);
-}
+
 
 // Worker wt's share of an item's epilogue scales: a_scale of token wt of the
 // tile (wt < 256) or w_scale of channel wt - 256 (0 beyond the tile or matrix).
@@ -594,8 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(scalars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(scalars + 4);
   int* s_last = reinterpret_cast<int*>(scalars + 8);
-  float* s_as = reinterpret_cast<float*>(bar_ptr + kBarBytes);   // kBNMax token scales
-  float* s_ws = s_as + kBNMax;                                    // kBNMax channel scales
+  float* s_as = reinterpret_cast<float*>(bar_ptr + kBarBytes);   // 2 x (kBNMax token + kBNMax channel scales)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -637,6 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  // the prologue above touches no global data; inputs and workspace only now
+  pdl_trigger();
+  pdl_wait();
 
   if (warp == kMmaWarp) {
     // ======================= MMA issuer (one thread) =========================
@@ -734,7 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // wt / 4, wt / 4 + 128 and wt / 4 + 256 of the stacked [A | B] tile; the
     // shared-memory offsets are fixed, only K moves.
     // Drain: warp w reads TMEM lanes 32 (w % 4) .. +31; the four warps of a
-    // quadrant take 16-column rounds j, j + 4, j + 8, ... of the accumulator.
+    // quadrant take 16-column rounds j, j + 4, j + 8, ... of the accumulator,
+    // and at an item's last chunk each thread writes out exactly the elements
+    // it drained.
     // Every worker passes the same sequence of named barriers whatever
     // happens (a timed-out wait only skips work), so none can be left waiting.
     const int wi = warp < kMmaWarp ? warp : warp - 1;   // worker index 0..15
@@ -743,7 +610,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int slice = warp < kMmaWarp ? 0 : (warp - 1) / 4;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int trow = quad * 32 + lane;                    // this thread's TMEM lane
-    uint32_t* T = reinterpret_cast<uint32_t*>(smem);
     const int seg = wt & 3;
     // per segment: offset of its 16 int8 bytes in a staging stage, and of
     // its first 16-byte f16 chunk in an operand stage (the second is that ^
@@ -772,9 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     // Drain this warp's share of chunk gc (chunk lc of its item): I += int(D),
-    // or, for the item's last chunk, stage the final values as
-    // T[token][channel].  Either way the D buffer is then handed back.
-    auto drain = [&](int gc, int lc, bool last, int bn) -> bool {
+    // or, for the item's last chunk (out != nullptr), hand each round of final
+    // int32 sums to out(cb, v).  Either way the D buffer is then handed back.
+    auto drain = [&](int gc, int lc, int bn, auto&& out, bool last) -> bool {
       const uint32_t dbar = dbuf ? static_cast<uint32_t>(gc & 1) : 0u;
       const uint32_t use = static_cast<uint32_t>(dbuf ? gc >> 1 : gc);
       const uint32_t dcol = dbuf && (gc & 1) ? static_cast<uint32_t>(p.bpiece) : kColD;
@@ -787,19 +653,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem + lane_base + dcol + cb * 16, d);
         if (lc > 0) tmem_ld16(tmem + lane_base + col_i + cb * 16, iv);
         tmem_wait_ld();
+        int32_t v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          d[j] = static_cast<uint32_t>((lc > 0 ? static_cast<int32_t>(iv[j]) : 0) +
-                                       __float2int_rn(__uint_as_float(d[j])));
+          v[j] = (lc > 0 ? static_cast<int32_t>(iv[j]) : 0) + __float2int_rn(__uint_as_float(d[j]));
         if (!last) {
-          tmem_st16(tmem + lane_base + col_i + cb * 16, d);
-        } else if (!p.swap) {
-          uint4* dst = reinterpret_cast<uint4*>(T + trow * (bn + 4) + cb * 16);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+          tmem_st16(tmem + lane_base + col_i + cb * 16, reinterpret_cast<const uint32_t(&)[16]>(v));
         } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) T[(cb * 16 + j) * (kBM + 4) + trow] = d[j];
+          out(cb, v);
         }
       }
       if (!last) tmem_wait_st();
@@ -808,17 +669,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_acc_empty + 8 * dbar);
       return true;
     };
+    auto no_out = [](int, const int32_t (&)[16]) {};
 
     bool ok = true;
     int gc = 0;                // chunk counter over all items
     int j = 0, s = 0;
     uint32_t ph8 = 0, ph = 0;  // staging / operand slots and phase parities
-    // this worker's epilogue scale for the coming item, loaded one item ahead
-    // so that its memory latency overlaps the previous item's output
-    float sc_next = 0.f;
+    // The epilogue scales of item n sit in buffer n % 2 of s_scale (token
+    // scales then channel scales, 2 x kBNMax each); worker wt fills entry wt.
+    // Item n + 1's are stored while item n finishes, and the next item-start
+    // barrier orders them before any read.
+    float* s_scale = s_as;
     {
       Item first;
-      if (get_item(p, 0, first)) sc_next = item_scale(p, first, tile_width(first.ty), wt);
+      s_scale[wt] = get_item(p, 0, first) ? item_scale(p, first, tile_width(first.ty), wt) : 0.f;
     }
     for (int n = 0;; ++n) {
       int bn, nk;
@@ -827,17 +691,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // again for its output)
         Item itm;
         if (!get_item(p, n, itm)) break;
-        // the previous item's output is finished: T and the scale copies are free
+        // the previous item's output is finished and this item's scales are
+        // in place
         asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
         bn = tile_width(itm.ty);
         nk = itm.k1 > itm.k0 ? itm.k1 - itm.k0 : 0;
-        const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
-        const int64_t tok0 = p.swap ? b0 : a0, ch0 = p.swap ? a0 : b0;
-        const int ntok = p.swap ? bn : kBM, nch = p.swap ? kBM : bn;
-        // the epilogue's scales (loaded ahead); the residual tile is
-        // prefetched into L2 so that the output does not wait on DRAM
-        s_as[wt] = sc_next;   // s_ws follows s_as: workers 256.. fill the channel scales
         if (a.residual != nullptr && itm.kind != 1) {
+          // prefetch the item's residual tile into L2 for its epilogue
+          const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
+          const int64_t tok0 = p.swap ? b0 : a0, ch0 = p.swap ? a0 : b0;
+          const int ntok = p.swap ? bn : kBM, nch = p.swap ? kBM : bn;
           const int lines = (nch * 2 + 127) / 128;  // 128-byte lines per token row
           for (int l = wt; l < ntok * lines; l += kWorkers) {
             const int r = l / lines;
@@ -864,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // released, so drain it here, after the next chunk's first stages
         // have been prepared
         if (next_drain < nchunks - 1 && it == next_trigger) {
-          ok = drain(gc + next_drain, next_drain, false, bn);
+          ok = drain(gc + next_drain, next_drain, bn, no_out, false);
           ++next_drain;
           next_trigger += kChunkStages;
           if (!ok) break;
@@ -895,95 +758,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       while (ok && next_drain < nchunks - 1) {
-        ok = drain(gc + next_drain, next_drain, false, bn);
+        ok = drain(gc + next_drain, next_drain, bn, no_out, false);
         ++next_drain;
       }
-      if (ok && nchunks > 0) ok = drain(gc + nchunks - 1, nchunks - 1, true, bn);
-      gc += nchunks;
+
+      // ---- the item's last chunk: drain straight into its output
+      Item itm;
+      get_item(p, n, itm);
+      const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
+      const float* sa = s_scale + (n & 1) * (2 * kBNMax);
+      const float* sw = sa + kBNMax;
+      float sc_next;  // loaded now, stored after the output (its latency overlaps)
       {
         Item nx;
         sc_next = get_item(p, n + 1, nx) ? item_scale(p, nx, tile_width(nx.ty), wt) : 0.f;
       }
-
-      // ---- output of the staged tile by all 512 workers
-      Item itm;
-      get_item(p, n, itm);
-      const int64_t tok0 = static_cast<int64_t>(p.swap ? itm.ty * p.bpiece : itm.tx * kBM);
-      const int64_t ch0 = static_cast<int64_t>(p.swap ? itm.tx * kBM : itm.ty * p.bpiece);
-      const int rows_out = p.swap ? bn : kBM;
-      const int cols_out = p.swap ? kBM : bn;
-      asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
       const bool have = ok && nchunks > 0;
+      const int glast = gc + nchunks - 1;
       if (itm.kind == 0) {
-        if (have) tile_out(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 0, wt, kWorkers);
-      } else if (itm.kind == 1) {
-        // integer split-K: the last CTA to finish this tile applies the epilogue
-        if (have) tile_out_split(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 1, wt);
-        __threadfence();
-        asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-        if (wt == 0) *s_last = (atomicAdd(a.ws_count + itm.tile, 1u) == static_cast<unsigned>(a.split - 1));
-        asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-        if (*s_last) {
-          __threadfence();
-          tile_out_split(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 2, wt);
-          if (wt == 0) a.ws_count[itm.tile] = 0u;
+        if (have) {
+          auto out = [&](int cb, const int32_t (&v)[16]) { round_out(p, sa, sw, a0, b0, trow, cb, v); };
+          ok = drain(glast, nchunks - 1, bn, out, true);
         }
       } else {
-        // shared tile of the balanced schedule: partial sums to this CTA's
-        // slot (plain stores); the last CTA to finish adds the other slots
-        const int groups = rows_out * (cols_out / 4);
-        const int stride = cols_out + 4;
-        int32_t* mine = p.slots + static_cast<int64_t>(itm.slot) * p.slot_elems;
+        // a K piece: this CTA's partial sums go to the workspace; the last CTA
+        // to finish the tile sums all pieces and applies the epilogue
+        int32_t* tacc = itm.kind == 2 ? p.acc + static_cast<int64_t>(itm.tile) * p.slot_elems : nullptr;
         if (have) {
-          for (int g = wt; g < groups; g += kWorkers) {
-            const int r = g / (cols_out / 4), c4 = (g - r * (cols_out / 4)) * 4;
-            __stcg(reinterpret_cast<int4*>(mine + r * cols_out + c4),
-                   *reinterpret_cast<const int4*>(T + r * stride + c4));
+          if (itm.kind == 1) {
+            auto out = [&](int cb, const int32_t (&v)[16]) { round_atomic(p, a0, b0, trow, cb, v); };
+            ok = drain(glast, nchunks - 1, bn, out, true);
+          } else {
+            auto out = [&](int cb, const int32_t (&v)[16]) {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) atomicAdd(tacc + slot_index(trow, cb, jj), v[jj]);
+            };
+            ok = drain(glast, nchunks - 1, bn, out, true);
           }
         }
         __threadfence();
         asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
         int bf = 0, bl = 0;
-        shared_tile_ctas(p, itm.tile, bf, bl);
-        if (wt == 0) *s_last = (atomicAdd(p.cnt + itm.tile, 1u) == static_cast<unsigned>(bl - bf));
+        if (itm.kind == 2) shared_tile_ctas(p, itm.tile, bf, bl);
+        const unsigned target = itm.kind == 1 ? static_cast<unsigned>(a.split - 1) : static_cast<unsigned>(bl - bf);
+        uint32_t* counter = itm.kind == 1 ? a.ws_count + itm.tile : p.cnt + itm.tile;
+        if (wt == 0) *s_last = (atomicAdd(counter, 1u) == target);
         asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
         if (*s_last) {
           __threadfence();
-          for (int c = bf; c <= bl; ++c) {
-            if (c == static_cast<int>(blockIdx.x)) continue;
-            const int32_t* other = p.slots + static_cast<int64_t>(shared_tile_slot(p, itm.tile, c)) * p.slot_elems;
-            // four independent L2 loads in flight before any of them is added
-            constexpr int kAhead = 4;
-            for (int g0 = wt; g0 < groups; g0 += kWorkers * kAhead) {
-              int4 v[kAhead];
+          for (int cb = slice; cb < bn / 16; cb += 4) {
+            int32_t v[16];
+            if (itm.kind == 1) {
 #pragma unroll
-              for (int u = 0; u < kAhead; ++u) {
-                const int g = g0 + u * kWorkers;
-                const int r = g / (cols_out / 4), c4 = (g - r * (cols_out / 4)) * 4;
-                v[u] = g < groups ? __ldcg(reinterpret_cast<const int4*>(other + r * cols_out + c4))
-                                  : make_int4(0, 0, 0, 0);
-              }
-#pragma unroll
-              for (int u = 0; u < kAhead; ++u) {
-                const int g = g0 + u * kWorkers;
-                if (g < groups) {
-                  const int r = g / (cols_out / 4), c4 = (g - r * (cols_out / 4)) * 4;
-                  int4* t4 = reinterpret_cast<int4*>(T + r * stride + c4);
-                  int4 tv = *t4;
-                  tv.x += v[u].x;
-                  tv.y += v[u].y;
-                  tv.z += v[u].z;
-                  tv.w += v[u].w;
-                  *t4 = tv;
+              for (int jj = 0; jj < 16; ++jj) {
+                int64_t m, nn;
+                v[jj] = 0;
+                if (round_elem(p, a0, b0, trow, cb, jj, m, nn)) {
+                  int32_t* wp = a.ws_acc + m * a.N + nn;
+                  v[jj] = __ldcg(wp);
+                  __stcg(wp, 0);
                 }
               }
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) v[jj] = __ldcg(tacc + slot_index(trow, cb, jj));
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) __stcg(tacc + slot_index(trow, cb, jj), 0);
             }
+            round_out(p, sa, sw, a0, b0, trow, cb, v);
           }
-          asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-          if (have) tile_out(p, T, s_as, s_ws, rows_out, cols_out, tok0, ch0, 0, wt, kWorkers);
-          if (wt == 0) p.cnt[itm.tile] = 0u;
+          if (wt == 0) *counter = 0u;
         }
       }
+      gc += nchunks;
+      s_scale[((n + 1) & 1) * (2 * kBNMax) + wt] = sc_next;
     }
   }
 
@@ -1062,8 +910,9 @@ static TcSched tc_balanced(int64_t T, int64_t S) {
   return sc;
 }
 
-// Workspace of the balanced schedule: tile counters, then 2 partial tiles per
-// CTA; none when no tile is shared.
+// Workspace of the balanced schedule: tile counters, then one int32
+// accumulator per shared tile (all zero between calls); none when no tile is
+// shared.
 static size_t tc_balanced_bytes(int64_t M, int64_t N, int64_t K, size_t* counter_bytes) {
   const TcPlan pl = tc_plan(M, N);
   const TcSched sc = tc_balanced(pl.grid_x * pl.grid_y, cdiv(K, kBK));
@@ -1073,7 +922,7 @@ static size_t tc_balanced_bytes(int64_t M, int64_t N, int64_t K, size_t* counter
   }
   const size_t cb = (static_cast<size_t>(sc.R) * 4 + 255) & ~static_cast<size_t>(255);
   if (counter_bytes != nullptr) *counter_bytes = cb;
-  return cb + static_cast<size_t>(2) * sc.G * kBM * pl.bpiece * 4;
+  return cb + static_cast<size_t>(sc.R) * kBM * pl.bpiece * 4;
 }
 
 // Workspace of explicit split-K (int32 atomics): the [M, N] accumulator, then
@@ -1154,7 +1003,7 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
     if (need > 0 && need > a.ws_bytes) sc = TcSched{152, static_cast<int>(cdiv(p.T, 152)), 0};
     if (sc.R > 0 && need > 0) {
       p.cnt = static_cast<uint32_t*>(a.ws);
-      p.slots = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + cb);
+      p.acc = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + cb);
     }
     p.W = sc.W;
     p.R = sc.R;
@@ -1169,8 +1018,7 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece);
   if (e != cudaSuccess) return e;
-  linear_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tmA, tmB);
-  return cudaGetLastError();
+  return launch_kernel(linear_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream, a.no_pdl == 0, p, tmA, tmB);
 }
 
 // PRISM_LINEAR_PATH=mma routes the linear to the mma.sync s8 kernel (a
@@ -1202,9 +1050,8 @@ size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, s
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (use_mma_path() && split == 0) split = mma_auto_split(M, N, K);
   if (split == 0) {
-    size_t cb = 0;
-    const size_t need = tc_balanced_bytes(M, N, K, &cb);
-    return need > 0 && need <= cap ? cb : 0;  // beyond cap the call runs whole tiles only
+    const size_t need = tc_balanced_bytes(M, N, K, nullptr);
+    return need <= cap ? need : 0;  // beyond cap the call runs whole tiles only
   }
   const size_t need = split > 1 ? atomic_bytes(M, N) : 0;
   return need <= cap ? need : SIZE_MAX;

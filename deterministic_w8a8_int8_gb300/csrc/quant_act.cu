@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(kBlock)
   constexpr int kRows = kBlock / TEAM;
   constexpr int kWarpsPerTeam = TEAM / 32;
   __shared__ float red[kBlock / 32];
+  pdl_trigger();
+  pdl_wait();
   const int team = threadIdx.x / TEAM;
   const int lt = threadIdx.x % TEAM;
   const int64_t m = static_cast<int64_t>(blockIdx.x) * kRows + team;
@@ -135,9 +137,8 @@ cudaError_t launch_team(const void* x, int64_t ldx, const float* inv_s, int64_t 
                         int8_t* q, int64_t ldq, float* a_scale, cudaStream_t stream) {
   constexpr int kRows = kBlock / TEAM;
   const int64_t blocks = (M + kRows - 1) / kRows;
-  quant_act_kernel<TEAM, CACHE><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
-      static_cast<const uint16_t*>(x), ldx, inv_s, M, K, q, ldq, a_scale);
-  return cudaGetLastError();
+  return launch_kernel(quant_act_kernel<TEAM, CACHE>, dim3(static_cast<unsigned>(blocks)), dim3(kBlock), 0,
+                       stream, true, static_cast<const uint16_t*>(x), ldx, inv_s, M, K, q, ldq, a_scale);
 }
 
 }  // namespace

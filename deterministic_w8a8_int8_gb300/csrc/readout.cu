@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kThreads)
                    const int32_t* __restrict__ ids, int64_t T, float* __restrict__ logits,
                    float* __restrict__ probs, uint32_t* __restrict__ err) {
   extern __shared__ __align__(16) int8_t sq[];
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s_logit[PRISM_MAX_CANDIDATES];
   __shared__ float s_prob[PRISM_MAX_CANDIDATES];
   __shared__ float s_red[kWarps];
@@ -207,10 +209,9 @@ cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const
   const int smem = static_cast<int>((K + 15) & ~static_cast<int64_t>(15));
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel), PRISM_MAX_READOUT_K);
   if (e != cudaSuccess) return e;
-  readout_kernel<<<static_cast<unsigned>(P), kThreads, smem, stream>>>(
-      static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, K, off, ids, T, logits, probs,
-      err);
-  return cudaGetLastError();
+  return launch_kernel(readout_kernel, dim3(static_cast<unsigned>(P)), dim3(kThreads), static_cast<size_t>(smem),
+                       stream, true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, K, off,
+                       ids, T, logits, probs, err);
 }
 
 }  // namespace prism

@@ -100,8 +100,8 @@ int prism_quant_act(const void *x_bf16, int64_t ldx, const float *inv_smooth,
 /*
  * Bytes of workspace prism_w8a8_linear needs for this shape and split-K
  * setting (split_k = 0 means the automatic schedule, as in the linear call:
- * arrival counters plus two partial int32 tiles per CTA when it shares tiles
- * between CTAs; about 4*M*N bytes plus counters for split_k > 1).  Returns 0
+ * arrival counters plus one int32 accumulator tile per tile it shares between
+ * CTAs; about 4*M*N bytes plus counters for split_k > 1).  Returns 0
  * when no workspace is needed (split_k = 1, or an automatic schedule of whole
  * tiles only).
  */
@@ -122,8 +122,9 @@ size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
  *   split_k        0 = automatic: a balanced schedule that gives every SM the
  *                  same number of K stages -- whole tiles first, then the K
  *                  ranges of the remaining tiles shared between CTAs, whose
- *                  int32 partial sums are added as integers by the last CTA
- *                  to finish each tile.  1..PRISM_MAX_SPLIT_K: every tile's
+ *                  int32 partial sums are added (integer reductions) into the
+ *                  tile's accumulator, read back by the last CTA to finish
+ *                  the tile.  1..PRISM_MAX_SPLIT_K: every tile's
  *                  K range cut into split_k equal pieces, partial sums added
  *                  as integers.  The result does not depend on split_k.
  *   workspace      device memory of at least
