@@ -15,7 +15,10 @@
 //      s = e_1 + ... + e_n, prob_c = e_c / s, every step binary32 RN.
 // Bytes: 2K (hidden row) + count * (K + 4) (candidate rows and scales) per
 // position, plus 12 bytes per candidate (id, logit, prob) -- HBM- and
-// latency-bound; nothing is written to global memory but the outputs.
+// latency-bound; nothing is written to global memory but the outputs.  For K
+// up to 8192 each warp starts streaming its first candidate row right after
+// the offsets are checked (the id is range-checked first), and the hidden
+// row is read once into registers.
 #include "common.cuh"
 
 namespace prism {
@@ -68,7 +71,16 @@ __device__ __forceinline__ float smooth(float v, const float* inv_s, int64_t k) 
   return inv_s != nullptr ? __fmul_rn(v, __ldg(inv_s + k)) : v;
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Hidden rows of up to kRegK elements are read once into registers; the
+// first candidate row of each warp (up to kRegK bytes) is fetched into
+// registers as soon as its id is known to be in range, so that its memory
+// latency overlaps the quantisation of the hidden row.
+constexpr int kRegK = 8192;
+constexpr int kHidVec = kRegK / 8 / kThreads;   // uint4 (8 bf16) per thread: 4
+constexpr int kRowVec = kRegK / 16 / 32;        // uint4 (16 int8) per lane: 16
+
+template <bool kReg>
+__global__ void __launch_bounds__(kThreads, 1)
     readout_kernel(const uint16_t* __restrict__ h, int64_t ldh, const float* __restrict__ inv_s,
                    const int8_t* __restrict__ W, int64_t ldw, const float* __restrict__ lm_scale,
                    int64_t V, int64_t K, const int32_t* __restrict__ off,
@@ -83,6 +95,7 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ unsigned s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t p = blockIdx.x;
+  const int64_t nchunk = K >> 4;   // 16-byte chunks of a row
 
   // ---- 1. validate this position's candidate list
   if (tid == 0) s_bad = 0u;
@@ -90,10 +103,26 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t b = off[p], e = off[p + 1];
   const bool off_ok = b >= 0 && e <= T && b <= e;
   const int64_t cnt = off_ok ? e - b : 0;
+  const bool cnt_ok = off_ok && cnt >= 1 && cnt <= PRISM_MAX_CANDIDATES;
+  // this warp's first candidate row, fetched early when its id is in range
+  uint4 row[kReg ? kRowVec : 1];
+  int32_t id0 = -1;
+  if (kReg && cnt_ok && warp < cnt) {
+    const int32_t id = ids[b + warp];
+    if (id >= 0 && id < V) {
+      id0 = id;
+      const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
+#pragma unroll
+      for (int i = 0; i < kRowVec; ++i) {
+        const int64_t c = lane + 32 * i;
+        row[i] = c < nchunk ? ld_stream_16(wr + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
   unsigned bad = 0u;
   if (!off_ok) {
     bad = PRISM_DEV_ERR_OFFSETS;
-  } else if (cnt < 1 || cnt > PRISM_MAX_CANDIDATES) {
+  } else if (!cnt_ok) {
     bad = PRISM_DEV_ERR_COUNT;
   } else if (tid < cnt) {
     const int32_t id = ids[b + tid];
@@ -117,14 +146,35 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---- 2. quantise the hidden row into shared memory
   const uint16_t* hr = h + p * ldh;
+  uint4 hv[kReg ? kHidVec : 1];
   float amax = 0.0f;
-  for (int64_t k = static_cast<int64_t>(tid) * 8; k < K; k += kThreads * 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(hr + k));
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  if (kReg) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      amax = fmaxf(amax, fabsf(smooth(bf16_lo(w4[i]), inv_s, k + 2 * i)));
-      amax = fmaxf(amax, fabsf(smooth(bf16_hi(w4[i]), inv_s, k + 2 * i + 1)));
+    for (int i = 0; i < kHidVec; ++i) {
+      const int64_t k = (static_cast<int64_t>(tid) + static_cast<int64_t>(i) * kThreads) * 8;
+      hv[i] = k < K ? __ldg(reinterpret_cast<const uint4*>(hr + k)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kHidVec; ++i) {
+      const int64_t k = (static_cast<int64_t>(tid) + static_cast<int64_t>(i) * kThreads) * 8;
+      if (k < K) {
+        const uint32_t w4[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          amax = fmaxf(amax, fabsf(smooth(bf16_lo(w4[j]), inv_s, k + 2 * j)));
+          amax = fmaxf(amax, fabsf(smooth(bf16_hi(w4[j]), inv_s, k + 2 * j + 1)));
+        }
+      }
+    }
+  } else {
+    for (int64_t k = static_cast<int64_t>(tid) * 8; k < K; k += kThreads * 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(hr + k));
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(smooth(bf16_lo(w4[i]), inv_s, k + 2 * i)));
+        amax = fmaxf(amax, fabsf(smooth(bf16_hi(w4[i]), inv_s, k + 2 * i + 1)));
+      }
     }
   }
 #pragma unroll
@@ -137,8 +187,7 @@ __global__ void __launch_bounds__(kThreads)
   const bool zero_row = !(amax >= 0x1p-120f);
   const float inv_a = zero_row ? 0.0f : __fdiv_rn(127.0f, amax);
   const float a_scale = zero_row ? 0.0f : __fdiv_rn(amax, 127.0f);
-  for (int64_t k = static_cast<int64_t>(tid) * 8; k < K; k += kThreads * 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(hr + k));
+  auto quant8 = [&](const uint4 v, int64_t k) {
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
     uint32_t packed[2] = {0u, 0u};
 #pragma unroll
@@ -149,27 +198,45 @@ __global__ void __launch_bounds__(kThreads)
       packed[i >> 1] |= two << (16 * (i & 1));
     }
     *reinterpret_cast<uint2*>(sq + k) = make_uint2(packed[0], packed[1]);
+  };
+  if (kReg) {
+#pragma unroll
+    for (int i = 0; i < kHidVec; ++i) {
+      const int64_t k = (static_cast<int64_t>(tid) + static_cast<int64_t>(i) * kThreads) * 8;
+      if (k < K) quant8(hv[i], k);
+    }
+  } else {
+    for (int64_t k = static_cast<int64_t>(tid) * 8; k < K; k += kThreads * 8)
+      quant8(__ldg(reinterpret_cast<const uint4*>(hr + k)), k);
   }
   __syncthreads();
 
   // ---- 3. one warp per candidate: exact int32 dot against the gathered row
-  const int64_t nchunk = K >> 4;
   for (int64_t i = warp; i < cnt; i += kWarps) {
     const int32_t id = ids[b + i];
     const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
     int acc = 0;
-    int64_t c = lane;
-    for (; c + 32 * 3 < nchunk; c += 32 * 4) {
-      const uint4 w0 = ld_stream_16(wr + (c)*16);
-      const uint4 w1 = ld_stream_16(wr + (c + 32) * 16);
-      const uint4 w2 = ld_stream_16(wr + (c + 64) * 16);
-      const uint4 w3 = ld_stream_16(wr + (c + 96) * 16);
-      acc = dot16(w0, *reinterpret_cast<const uint4*>(sq + c * 16), acc);
-      acc = dot16(w1, *reinterpret_cast<const uint4*>(sq + (c + 32) * 16), acc);
-      acc = dot16(w2, *reinterpret_cast<const uint4*>(sq + (c + 64) * 16), acc);
-      acc = dot16(w3, *reinterpret_cast<const uint4*>(sq + (c + 96) * 16), acc);
+    if (kReg && i == warp && id == id0) {
+#pragma unroll
+      for (int j = 0; j < kRowVec; ++j) {
+        const int64_t c = lane + 32 * j;
+        if (c < nchunk) acc = dot16(row[j], *reinterpret_cast<const uint4*>(sq + c * 16), acc);
+      }
+    } else {
+      int64_t c = lane;
+      for (; c + 32 * 3 < nchunk; c += 32 * 4) {
+        const uint4 w0 = ld_stream_16(wr + (c)*16);
+        const uint4 w1 = ld_stream_16(wr + (c + 32) * 16);
+        const uint4 w2 = ld_stream_16(wr + (c + 64) * 16);
+        const uint4 w3 = ld_stream_16(wr + (c + 96) * 16);
+        acc = dot16(w0, *reinterpret_cast<const uint4*>(sq + c * 16), acc);
+        acc = dot16(w1, *reinterpret_cast<const uint4*>(sq + (c + 32) * 16), acc);
+        acc = dot16(w2, *reinterpret_cast<const uint4*>(sq + (c + 64) * 16), acc);
+        acc = dot16(w3, *reinterpret_cast<const uint4*>(sq + (c + 96) * 16), acc);
+      }
+      for (; c < nchunk; c += 32)
+        acc = dot16(ld_stream_16(wr + c * 16), *reinterpret_cast<const uint4*>(sq + c * 16), acc);
     }
-    for (; c < nchunk; c += 32) acc = dot16(ld_stream_16(wr + c * 16), *reinterpret_cast<const uint4*>(sq + c * 16), acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
@@ -207,11 +274,18 @@ cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const
                            const int32_t* off, const int32_t* ids, int64_t P, int64_t T,
                            float* logits, float* probs, uint32_t* err, cudaStream_t stream) {
   const int smem = static_cast<int>((K + 15) & ~static_cast<int64_t>(15));
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel), PRISM_MAX_READOUT_K);
+  if (K <= kRegK) {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<true>), kRegK);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(readout_kernel<true>, dim3(static_cast<unsigned>(P)), dim3(kThreads),
+                         static_cast<size_t>(smem), stream, true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw,
+                         lm_scale, V, K, off, ids, T, logits, probs, err);
+  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<false>), PRISM_MAX_READOUT_K);
   if (e != cudaSuccess) return e;
-  return launch_kernel(readout_kernel, dim3(static_cast<unsigned>(P)), dim3(kThreads), static_cast<size_t>(smem),
-                       stream, true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, K, off,
-                       ids, T, logits, probs, err);
+  return launch_kernel(readout_kernel<false>, dim3(static_cast<unsigned>(P)), dim3(kThreads),
+                       static_cast<size_t>(smem), stream, true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw,
+                       lm_scale, V, K, off, ids, T, logits, probs, err);
 }
 
 }  // namespace prism
