@@ -70,6 +70,8 @@ def _load():
             "oracle_exp_batch": (None, [P, I64, P]),
             "oracle_candidate_readout": (I32, [P, I64, P, P, I64, P, I64, I64, P, P, I64, I64, P, P]),
             "oracle_bf16_to_float": (None, [P, I64, P]),
+            "oracle_f16_to_float": (None, [P, I64, P]),
+            "oracle_smooth_requant": (None, [P, I64, P, I64, P, I64, I64, P, I64, P]),
             "oracle_float_to_bf16": (None, [P, I64, P]),
             "oracle_set_threads": (None, [I32]),
             "oracle_get_threads": (I32, []),
@@ -122,6 +124,30 @@ def quant_act(x_bf16_bits: np.ndarray, inv_s: np.ndarray | None):
     a = np.empty((M,), np.float32)
     _load().oracle_quant_act(_p(x), K, _p(s), M, K, _p(q), K, _p(a))
     return q, a
+
+
+def smooth_requant(q: np.ndarray, d_f16_bits: np.ndarray, s: np.ndarray | None):
+    """SmoothQuant startup requantisation of Q8_0 weights.  ``q`` int8 [N, K]
+    (K a multiple of 32), ``d_f16_bits`` uint16 [N, K/32] (binary16 block
+    scales), ``s`` float32 [K] or None.  Returns (w int8 [N, K], w_scale
+    float32 [N])."""
+    q = _c(q, np.int8)
+    N, K = q.shape
+    assert K % 32 == 0
+    d = _c(d_f16_bits, np.uint16)
+    assert d.shape == (N, K // 32)
+    sv = None if s is None else _c(s, np.float32)
+    w = np.empty((N, K), np.int8)
+    ws = np.empty((N,), np.float32)
+    _load().oracle_smooth_requant(_p(q), K, _p(d), K // 32, _p(sv), N, K, _p(w), K, _p(ws))
+    return w, ws
+
+
+def f16_to_float(h) -> np.ndarray:
+    h = _c(h, np.uint16)
+    f = np.empty(h.shape, np.float32)
+    _load().oracle_f16_to_float(_p(h), h.size, _p(f))
+    return f
 
 
 def gemm_s32(q: np.ndarray, w: np.ndarray) -> np.ndarray:

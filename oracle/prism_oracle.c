@@ -17,7 +17,8 @@
  *
  * Sources (page, section):
  *  [P1-evidence]  StartLux-Prism (English), "Compute shared evidence once":
- *                 Q8_0 weights requantised with SmoothQuant at startup,
+ *                 Q8_0 weights requantised with SmoothQuant at startup
+ *                 (oracle_smooth_requant),
  *                 activations quantised per token for W8A8 execution; the
  *                 last layer restricted to the positions needed for answers.
  *  [P1-bitwise]   same page, "Bitwise consistency is not lossless
@@ -144,6 +145,97 @@ void oracle_quant_act(const uint16_t *x, int64_t ldx, const float *inv_s,
             qr[k] = (int8_t)t;
         }
         a_scale[m] = amax / 127.0f;
+    }
+}
+
+/* ------------------------------------ SmoothQuant startup requantisation --- */
+/*
+ * [P1-evidence]: the stored Q8_0 weights are requantised with SmoothQuant at
+ * startup.  Q8_0 keeps each weight row in blocks of 32 int8 values that share
+ * one binary16 scale d.  SmoothQuant moves activation outliers into the
+ * weights: input channel k of every weight row is multiplied by s_k while the
+ * activations are divided by it (oracle_quant_act receives 1/s_k).  The
+ * result is requantised per output channel into the int8 weights and binary32
+ * per-channel scales that the W8A8 linear consumes.
+ *
+ * Reading (the pages name the steps only):
+ *     v_nk       = (d_n(k/32) * q_nk) * s_k         d*q is exact in binary32 (an
+ *                                                   11-bit significand times a 7-bit
+ *                                                   integer); one RN for the product with s_k
+ *     amax_n     = max_k |v_nk|
+ *     inv_n      = 127 / amax_n                     (binary32 RN)
+ *     w_nk       = clamp(rint(v_nk * inv_n), -127, 127)
+ *     w_scale_n  = amax_n / 127                     (binary32 RN)
+ * the rounding and scale form of the activation quantiser; a row whose amax is
+ * below 2^-120 requantises to zeros with scale 0.  s == NULL means s_k = 1.
+ * d is given as binary16 bit patterns, [N, K/32] with row stride ldd; K is a
+ * multiple of 32.  Inputs must keep every v finite.
+ */
+
+/* binary16 -> binary32, exact (normals, subnormals, zeros, infinities; a NaN
+ * stays a NaN). */
+static float f16_to_float(uint16_t h)
+{
+    const uint32_t sign = (uint32_t)(h >> 15) << 31;
+    const uint32_t e = (h >> 10) & 0x1fu;
+    const uint32_t m = h & 0x3ffu;
+    float f;
+    if (e == 0) {
+        f = ldexpf((float)m, -24);                 /* subnormal or zero: m * 2^-24, exact */
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        u |= sign;
+        memcpy(&f, &u, sizeof f);
+        return f;
+    }
+    uint32_t u;
+    if (e == 31)
+        u = sign | 0x7f800000u | (m << 13);        /* infinity or NaN */
+    else
+        u = sign | ((e - 15u + 127u) << 23) | (m << 13);
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+void oracle_f16_to_float(const uint16_t *h, int64_t n, float *f)
+{
+    for (int64_t i = 0; i < n; ++i)
+        f[i] = f16_to_float(h[i]);
+}
+
+void oracle_smooth_requant(const int8_t *q, int64_t ldq, const uint16_t *d, int64_t ldd,
+                           const float *s, int64_t N, int64_t K, int8_t *w, int64_t ldw,
+                           float *w_scale)
+{
+    const float tiny = ldexpf(1.0f, -120);
+    int64_t n;
+#pragma omp parallel for schedule(static)
+    for (n = 0; n < N; ++n) {
+        const int8_t *qr = q + n * ldq;
+        const uint16_t *dr = d + n * ldd;
+        int8_t *wr = w + n * ldw;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = f16_to_float(dr[k / 32]) * (float)qr[k];
+            if (s) v = v * s[k];
+            float a = fabsf(v);
+            if (a > amax) amax = a;
+        }
+        if (!(amax >= tiny)) {
+            for (int64_t k = 0; k < K; ++k) wr[k] = 0;
+            w_scale[n] = 0.0f;
+            continue;
+        }
+        float inv = 127.0f / amax;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = f16_to_float(dr[k / 32]) * (float)qr[k];
+            if (s) v = v * s[k];
+            float t = rintf(v * inv);            /* default mode: ties to even */
+            if (t > 127.0f) t = 127.0f;
+            if (t < -127.0f) t = -127.0f;
+            wr[k] = (int8_t)t;
+        }
+        w_scale[n] = amax / 127.0f;
     }
 }
 

@@ -74,6 +74,155 @@ def bits(x_f32: np.ndarray) -> np.ndarray:
     return wl.bf16_bits(np.asarray(x_f32, np.float32))
 
 
+# ------------------------------------------- SmoothQuant requantisation ----
+# StartLux-Prism, "Compute shared evidence once": Q8_0 weights (blocks of 32
+# int8 with one binary16 scale) requantised with SmoothQuant at startup.
+F16_ONE = 0x3C00
+
+
+def _f16_bits(x) -> np.ndarray:
+    return np.asarray(x, np.float16).view(np.uint16)
+
+
+def test_f16_decoder_matches_library_on_every_pattern():
+    h = np.arange(65536, dtype=np.uint16)
+    got = oracle.f16_to_float(h)
+    ref = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_requant_unit_blocks_reduce_to_activation_quantiser():
+    # with every block scale 1, requantising q * s is the activation
+    # quantiser applied to x = q (integers <= 127 are exact in bf16) with
+    # inv_s = s -- a special case of an independently pinned function
+    rng = np.random.default_rng(31)
+    for N, K in [(7, 64), (33, 256), (3, 1024)]:
+        q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+        s = rng.uniform(0.25, 4.0, K).astype(np.float32)
+        d = np.full((N, K // 32), F16_ONE, np.uint16)
+        for sv in (s, None):
+            w, ws = oracle.smooth_requant(q, d, sv)
+            qa, aa = oracle.quant_act(wl.bf16_bits(q.astype(np.float32)), sv)
+            assert np.array_equal(w, qa)
+            assert np.array_equal(ws.view(np.uint32), aa.view(np.uint32))
+
+
+def test_requant_block_scales_index_by_k_over_32():
+    # a power-of-two block scale d moves into the smoothing factor exactly:
+    # (d * q) * s == q * (d * s), one rounding either way; so each row must
+    # equal the activation quantiser with inv_s_k = d[k // 32] * s_k
+    rng = np.random.default_rng(32)
+    N, K = 9, 256
+    q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    e = rng.integers(-6, 7, (N, K // 32))
+    d = _f16_bits(np.exp2(e.astype(np.float64)))
+    s = rng.uniform(0.5, 2.0, K).astype(np.float32)
+    w, ws = oracle.smooth_requant(q, d, s)
+    for n in range(N):
+        fold = (np.exp2(e[n]).repeat(32) * s.astype(np.float64)).astype(np.float32)
+        assert np.array_equal(fold.astype(np.float64), np.exp2(e[n]).repeat(32) * s.astype(np.float64))
+        qa, aa = oracle.quant_act(wl.bf16_bits(q[n:n + 1].astype(np.float32)), fold)
+        assert np.array_equal(w[n], qa[0]), n
+        assert ws[n] == aa[0], n
+
+
+def test_requant_closed_form_exact_rationals():
+    # v = RN(d * q * s) (d * q exact), w_scale = RN(amax / 127),
+    # w = clamp(rint(RN(v * RN(127 / amax)))), on exact rationals
+    rng = np.random.default_rng(33)
+    N, K = 6, 96
+    q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    d = _f16_bits(rng.uniform(1e-3, 3.0, (N, K // 32)))
+    s = (rng.uniform(0.2, 5.0, K)).astype(np.float32)
+    w, ws = oracle.smooth_requant(q, d, s)
+    df = d.view(np.float16).astype(np.float64)
+    for n in range(N):
+        v = [rn32(Fr(float(df[n, k // 32])) * int(q[n, k]) * Fr(float(s[k]))) for k in range(K)]
+        amax = max(abs(x) for x in v)
+        assert ws[n] == np.float32(rn32(Fr(amax) / 127))
+        inv = rn32(Fr(127) / Fr(amax))
+        for k in range(K):
+            t = rn32(Fr(v[k]) * Fr(inv))
+            assert w[n, k] == max(-127, min(127, round(t)))
+
+
+def test_requant_matches_library_binary32_arithmetic():
+    # the same steps in numpy binary32 (each op one RN), on enough rows that
+    # multiplying by RN(127/amax) and dividing by RN(amax/127) give different
+    # codes somewhere: the test is sensitive to that reading
+    rng = np.random.default_rng(36)
+    N, K = 600, 256
+    q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    d = _f16_bits(rng.uniform(1e-3, 2.0, (N, K // 32)))
+    s = rng.uniform(0.3, 3.0, K).astype(np.float32)
+    w, ws = oracle.smooth_requant(q, d, s)
+    df = d.view(np.float16).astype(np.float32).repeat(32, axis=1)
+    v = (df * q.astype(np.float32)) * s[None, :]          # d*q exact, then one RN
+    amax = np.abs(v).max(axis=1).astype(np.float32)
+    inv = np.float32(127.0) / amax
+    codes = np.clip(np.rint(v * inv[:, None]), -127, 127).astype(np.int8)
+    assert np.array_equal(w, codes)
+    assert np.array_equal(ws, amax / np.float32(127.0))
+    # a row built so that the reading matters: amax = a (from q = 127 with
+    # s_0 = RN(a / 127), RN(127 * s_0) == a) and one value v (q = 1, s_1 = v)
+    # where rint(RN(v * RN(127 / a))) = 16 but rint(RN(v / RN(a / 127))) = 15
+    a, vv = np.float32(3.7288472652435303), np.float32(0.455095499753952)
+    s0 = a / np.float32(127.0)
+    assert np.float32(127.0) * s0 == a
+    K1 = 32
+    q1 = np.zeros((1, K1), np.int8)
+    q1[0, 0], q1[0, 1] = 127, 1
+    s1 = np.zeros(K1, np.float32)
+    s1[0], s1[1] = s0, vv
+    w1, ws1 = oracle.smooth_requant(q1, np.full((1, 1), F16_ONE, np.uint16), s1)
+    inv_r = rn32(Fr(127) / Fr(float(a)))
+    mul = round(rn32(Fr(float(vv)) * Fr(inv_r)))
+    div = round(rn32(Fr(float(vv)) / Fr(rn32(Fr(float(a)) / 127))))
+    assert (mul, div) == (16, 15)
+    assert w1[0, 0] == 127 and w1[0, 1] == mul
+
+
+def test_requant_identity_equivariance_and_tiny_rows():
+    rng = np.random.default_rng(34)
+    N, K = 5, 128
+    q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    q[:, 0] = 127                                      # every row reaches 127
+    one = np.full((N, K // 32), F16_ONE, np.uint16)
+    w, ws = oracle.smooth_requant(q, one, None)
+    assert np.array_equal(w, q) and np.all(ws == np.float32(1.0))
+    # scaling every block scale by 2^e leaves the codes and scales w_scale by 2^e
+    for e in (-8, 5):
+        d2 = _f16_bits(np.full((N, K // 32), 2.0 ** e))
+        w2, ws2 = oracle.smooth_requant(q, d2, None)
+        assert np.array_equal(w2, q) and np.all(ws2 == np.float32(2.0 ** e))
+    # all-zero rows and rows below 2^-120 give zero codes and scale 0
+    qz = q.copy()
+    qz[1] = 0
+    tiny = one.copy()
+    tiny[2] = 0x0001                                   # f16 2^-24: |v| <= 127 * 2^-134 < 2^-120
+    s = np.full(K, 2.0 ** -110, np.float32)
+    wz, wsz = oracle.smooth_requant(qz, tiny, s)
+    assert not wz[1].any() and wsz[1] == 0.0
+    assert not wz[2].any() and wsz[2] == 0.0
+    assert wsz[0] > 0.0
+
+
+def test_requant_error_bound():
+    rng = np.random.default_rng(35)
+    N, K = 16, 512
+    q = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    d = _f16_bits(rng.uniform(1e-3, 0.1, (N, K // 32)))
+    s = rng.uniform(0.5, 8.0, K).astype(np.float32)
+    w, ws = oracle.smooth_requant(q, d, s)
+    v = d.view(np.float16).astype(np.float64).repeat(32, axis=1) * q * s.astype(np.float64)
+    err = np.abs(w.astype(np.float64) * ws[:, None].astype(np.float64) - v)
+    # half a code step, plus the binary32 roundings of v, the scale and the reciprocal
+    assert np.all(err <= ws[:, None] * (0.5 + 2.0 ** -20) + np.abs(v) * 2.0 ** -21)
+    assert np.all(np.abs(w).max(axis=1) == 127)
+
+
 # ------------------------------------------------------------ quantiser ----
 def test_quant_hand_worked_examples():
     cases = json.load(open(os.path.join(GOLDEN, "quant_examples.json")))["cases"]
