@@ -623,6 +623,34 @@ def run_kernel_quant(args):
     return 0
 
 
+def run_kernel_requant(args):
+    """Time prism_smooth_requant alone on one projection's Q8_0 weight
+    (load-time step, HBM-bound); --case names a REQUANT_CONFIGS entry."""
+    import torch
+
+    import deterministic_w8a8_int8_gb300 as prism
+
+    dev = torch.device("cuda", 0)
+    c = wl.make_q8_0(args.case)
+    N, K = c.q.shape
+    # enough input copies that one pass over them exceeds L2 twice over
+    n_rot = max(1, int(np.ceil(2 * 129e6 / (N * K))))
+    qs = [torch.from_numpy(c.q).to(dev) for _ in range(n_rot)]
+    d = torch.from_numpy(c.d.view(np.int16)).to(dev)
+    s = torch.from_numpy(c.s).to(dev)
+    w = torch.empty((N, K), dtype=torch.int8, device=dev)
+    ws = torch.empty((N,), dtype=torch.float32, device=dev)
+    calls = [lambda i=i: prism.prism_smooth_requant(qs[i % n_rot], d, s, w=w, w_scale=ws)
+             for i in range(max(args.steps, n_rot))]
+    avg = graph_time_us(calls)
+    byts = 2 * N * K + 2 * N * (K // 32) + 4 * K + 4 * N
+    hbm, _, _ = load_peaks()
+    print(json.dumps({"kernel": "prism_smooth_requant", "case": args.case, "N": N, "K": K, "avg_us": avg,
+                      "gbs": byts / avg / 1e3, "frac_hbm": byts / avg / 1e3 / hbm,
+                      "timing": "CUDA graph of back-to-back calls, %d weight copies" % n_rot}), flush=True)
+    return 0
+
+
 def run_kernel_readout(args):
     """Time prism_candidate_readout alone: P answer positions of a 248,000 x
     5120 LM head (several head copies rotated so gathers come from HBM)."""
@@ -679,8 +707,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["linear", "quant", "readout"], help="time one call type alone")
-    ap.add_argument("--case", default="forest_qkv_m304_k5120_n15360", choices=sorted(wl.LINEAR_CONFIGS))
+    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant"],
+                    help="time one call type alone")
+    ap.add_argument("--case", default=None, choices=sorted(wl.LINEAR_CONFIGS) + sorted(wl.REQUANT_CONFIGS),
+                    help="workload of --kernel (a linear case; for requant a weight as loaded)")
     ap.add_argument("--rows", type=int, default=None, help="use the first ROWS token rows of --case")
     ap.add_argument("--split", type=int, default=None, help="split-K for --kernel (default automatic)")
     args = ap.parse_args()
@@ -688,6 +718,14 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel == "requant":
+        args.case = args.case or "qkv_n15360_k5120"
+        if args.case not in wl.REQUANT_CONFIGS:
+            ap.error("--kernel requant takes --case from " + ", ".join(sorted(wl.REQUANT_CONFIGS)))
+        return run_kernel_requant(args)
+    args.case = args.case or "forest_qkv_m304_k5120_n15360"
+    if args.case not in wl.LINEAR_CONFIGS:
+        ap.error("--case must be a linear case for this mode")
     if args.kernel == "quant":
         return run_kernel_quant(args)
     if args.kernel == "readout":

@@ -11,6 +11,7 @@ PyTorch is used for device memory and the current CUDA stream only.
 Entry points (same names as the C ABI):
   prism_quant_act(x, inv_s)                      -> (q, a_scale)
   prism_w8a8_linear(q, a_scale, w, w_scale, ...) -> out
+  prism_smooth_requant(q, d, smooth)             -> (w, w_scale)
   prism_candidate_readout(hidden, ...)           -> (logits, probs)
 """
 from __future__ import annotations
@@ -49,6 +50,7 @@ SIGNATURES = {
                                          _I64, _I64, _I64, _I32, _P]),
     "prism_candidate_readout": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _P, _P,
                                        _I64, _I64, _P, _P, _P, _P]),
+    "prism_smooth_requant": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _P, _I64, _P, _P]),
     "prism_status_string": (ctypes.c_char_p, [_I32]),
     "prism_version": (_I32, []),
     "prism_w8a8_kernel_kind": (_I32, [_I64, _I64, _I64]),
@@ -166,6 +168,33 @@ def prism_quant_act(x, inv_s=None, q=None, a_scale=None, stream=None):
                                _ptr(a_scale), _stream(stream))
     _check("prism_quant_act", st)
     return q, a_scale
+
+
+def prism_smooth_requant(q, d, smooth=None, w=None, w_scale=None, stream=None):
+    """Requantise Q8_0 weights with SmoothQuant factors folded in.
+
+    ``q`` int8 [N, K] codes, ``d`` [N, K/32] block scales (float16, or int16
+    holding binary16 bits), ``smooth`` float32 [K] or None.  Returns
+    (int8 w [N, K], float32 w_scale [N]); ``w`` may be ``q`` (in place)."""
+    import torch
+    _require(q, torch.int8, "q", 2)
+    N, K = q.shape
+    if d.dtype not in (torch.float16, torch.int16):
+        raise TypeError(f"d must be float16 or int16 (binary16 bits), got {d.dtype}")
+    if not d.is_cuda or d.dim() != 2 or (d.shape[1] > 1 and d.stride(1) != 1):
+        raise ValueError("d must be a 2-D CUDA tensor with contiguous rows")
+    if smooth is not None:
+        _require(smooth, torch.float32, "smooth", 1)
+    if w is None:
+        w = torch.empty((N, K), dtype=torch.int8, device=q.device)
+    if w_scale is None:
+        w_scale = torch.empty((N,), dtype=torch.float32, device=q.device)
+    _require(w, torch.int8, "w", 2)
+    _require(w_scale, torch.float32, "w_scale", 1)
+    st = lib().prism_smooth_requant(_ptr(q), q.stride(0), _ptr(d), d.stride(0), _ptr(smooth), N, K,
+                                    _ptr(w), w.stride(0), _ptr(w_scale), _stream(stream))
+    _check("prism_smooth_requant", st)
+    return w, w_scale
 
 
 def new_workspace(M: int, N: int, K: int, split_k: int = 0, device=None):

@@ -165,6 +165,11 @@ cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream);
 // Sticky device error bits raised by kernels (bounded waits that expired).
 cudaError_t read_and_clear_kernel_error(uint32_t* out);
 
+// SmoothQuant requantisation of Q8_0 weights (requant.cu).
+cudaError_t launch_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d, int64_t ldd, const float* s,
+                                  int64_t N, int64_t K, int8_t* w, int64_t ldw, float* w_scale,
+                                  cudaStream_t stream);
+
 cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const int8_t* W,
                            int64_t ldw, const float* lm_scale, int64_t V, int64_t K,
                            const int32_t* off, const int32_t* ids, int64_t P, int64_t T,

@@ -89,6 +89,24 @@ int prism_quant_act(const void* x_bf16, int64_t ldx, const float* inv_smooth, in
                                                      static_cast<cudaStream_t>(cuda_stream)));
 }
 
+int prism_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d_f16, int64_t ldd, const float* smooth,
+                         int64_t N, int64_t K, int8_t* w, int64_t ldw, float* w_scale, void* cuda_stream) {
+  if (N < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (N == 0) return PRISM_OK;
+  if (q == nullptr || d_f16 == nullptr || w == nullptr || w_scale == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (K % 32 != 0) return PRISM_ERR_ALIGNMENT;
+  if (ldq < K || ldw < K || ldd < K / 32) return PRISM_ERR_INVALID_ARG;
+  if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+  if (ldq % 16 != 0 || ldw % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(d_f16, 2) || !aligned(w_scale, 4)) return PRISM_ERR_ALIGNMENT;
+  if (smooth != nullptr && !aligned(smooth, 16)) return PRISM_ERR_ALIGNMENT;
+  if (N > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  // w == q (in place) is allowed only with one stride for both.
+  if (static_cast<const void*>(w) == static_cast<const void*>(q) && ldw != ldq) return PRISM_ERR_INVALID_ARG;
+  return prism::record_cuda(prism::launch_smooth_requant(q, ldq, d_f16, ldd, smooth, N, K, w, ldw, w_scale,
+                                                          static_cast<cudaStream_t>(cuda_stream)));
+}
+
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K) { return prism::linear_kernel_kind(M, N, K); }
 
 int prism_device_status(uint32_t* flags) {

@@ -1,0 +1,305 @@
+// requant.cu -- SmoothQuant requantisation of Q8_0 weights at load time
+// (StartLux-Prism, "Compute shared evidence once": the stored 8-bit weights
+// are requantised with the smoothing factors folded in before serving).
+//
+//   v_nk      = RN(RN(d_n,k/32 * q_nk) * s_k)      d * q is exact in binary32
+//   amax_n    = max_k |v_nk|
+//   w_nk      = rint_even(RN(v_nk * RN(127 / amax_n)))
+//   w_scale_n = RN(amax_n / 127);   amax_n < 2^-120  =>  w_n = 0, w_scale_n = 0
+//
+// No clamp is needed: |v| <= amax, so |v * RN(127/amax)| <= 127 (1 + 2^-24)
+// before rounding, which rounds to at most the next binary32 above 127 and
+// then to the integer 127.
+//
+// HBM-bound, run once per weight: per element 1 byte of codes in, 1/16 byte
+// of block scales in, 1 byte out.  One CTA is one team that owns a row at a
+// time (persistent over rows).  Each thread holds C 16-element vectors of the
+// row: it issues the loads of the next row's codes first, then smooths the
+// current row into registers (pass 1, with the max), and quantises from those
+// registers (pass 2), so that each element is decoded and smoothed once and
+// the DRAM latency of row r+1 hides behind the arithmetic of row r.  s is staged once per CTA in shared memory,
+// laid out [4][K/16] float4 so that consecutive threads read consecutive
+// 16-byte words.  int8 -> binary32 and binary32 -> rounded integer go through
+// exact integer tricks on the 2^23 binade instead of conversion instructions.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace prism {
+namespace {
+
+constexpr int kMaxTeam = 512;
+constexpr int kCachedMaxK = 24576;   // 512 threads x 3 vectors of 16; s in 96 KB of shared memory
+constexpr float kTiny = 0x1p-120f;
+
+// Codes i and i+1 of a word as floats: (2^23 + (c + 128)) - (2^23 + 128),
+// both steps exact.  xw is the code word with every byte's top bit flipped;
+// the pair goes through one packed subtraction.
+__device__ __forceinline__ float2 code_pair(uint32_t xw, int i) {
+  const float lo = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7540u | static_cast<uint32_t>(i)));
+  const float hi = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7540u | static_cast<uint32_t>(i + 1)));
+  return __fadd2_rn(make_float2(lo, hi), make_float2(-8388736.0f, -8388736.0f));
+}
+
+// rint_even(t) for |t| < 2^22 as the low byte of RN(t + 1.5 * 2^23): the sum
+// lies in [2^23, 2^24), where the unit in the last place is 1, so the single
+// rounding of the addition is the rounding of t to an integer, ties to even
+// (1.5 * 2^23 is even), and the integer sits in the low mantissa bits.
+// t = RN(v * inv) must be rounded on its own first: a fused multiply-add
+// would round v * inv + M once and send the products that RN rounds up onto
+// a tie x.5 to x instead of the even neighbour.  So both steps are scalar
+// __fmul_rn / __fadd_rn, which are never contracted.  (The assembler does
+// fuse the packed f32x2 multiply and add, even written as PTX with explicit
+// .rn: packed arithmetic is used below only where no product feeds an add.)
+__device__ __forceinline__ uint32_t round_low_byte(float v, float inv) {
+  return __float_as_uint(__fadd_rn(__fmul_rn(v, inv), 12582912.0f));
+}
+__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
+__device__ __forceinline__ float f16_bits_to_float(uint32_t h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// 16 smoothed values of one vector: codes (4 words), block scale df, s from
+// shared memory (sv[j] holds s_k for k = 4j .. 4j+3 of the vector).  Packed
+// binary32 arithmetic, each component rounded like the scalar operation:
+// v = RN(RN(c * d) * s), the first product exact.  An add feeds a multiply
+// here, never the reverse, so there is nothing to fuse.
+struct Vec16 {
+  float2 v[8];
+};
+__device__ __forceinline__ Vec16 smooth16(uint4 codes, float df, const float4 (&sv)[4]) {
+  Vec16 r;
+  const uint32_t w[4] = {codes.x ^ 0x80808080u, codes.y ^ 0x80808080u, codes.z ^ 0x80808080u,
+                         codes.w ^ 0x80808080u};
+  const float2 d2 = make_float2(df, df);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    r.v[2 * j] = __fmul2_rn(__fmul2_rn(code_pair(w[j], 0), d2), make_float2(sv[j].x, sv[j].y));
+    r.v[2 * j + 1] = __fmul2_rn(__fmul2_rn(code_pair(w[j], 2), d2), make_float2(sv[j].z, sv[j].w));
+  }
+  return r;
+}
+__device__ __forceinline__ float absmax16(const Vec16& r, float m) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(fmaxf(m, fabsf(r.v[e].x)), fabsf(r.v[e].y));
+  return m;
+}
+__device__ __forceinline__ uint4 requant16(const Vec16& r, float inv) {
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    o[j] = pack4(round_low_byte(r.v[2 * j].x, inv), round_low_byte(r.v[2 * j].y, inv),
+                 round_low_byte(r.v[2 * j + 1].x, inv), round_low_byte(r.v[2 * j + 1].y, inv));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Coherent 16-byte load that does not allocate in L1 (w may be q: a row is
+// read completely before it is written, by the same CTA).
+__device__ __forceinline__ uint4 ld_codes(const int8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// The max of m (>= 0) over the CTA, on its bit pattern (ordered like the
+// value for non-negative floats) with warp reductions.  red is a [2][warps]
+// double buffer indexed by row parity, so that one barrier per row suffices:
+// a warp writes slot par of row r + 2 only after every thread has passed row
+// r + 1's barrier, which is after every read of row r's slots.
+__device__ __forceinline__ float team_max(float m, uint32_t (*red)[kMaxTeam / 32], int par) {
+  const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) red[par][threadIdx.x >> 5] = wm;
+  __syncthreads();
+  const uint32_t x = lane < static_cast<int>(blockDim.x >> 5) ? red[par][lane] : 0u;
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, x));
+}
+
+template <int C>
+__global__ void __launch_bounds__(kMaxTeam)
+    smooth_requant_kernel(const int8_t* q, int64_t ldq, const uint16_t* __restrict__ d, int64_t ldd,
+                          const float* __restrict__ s, int64_t N, int K, int8_t* w, int64_t ldw,
+                          float* __restrict__ w_scale) {
+  extern __shared__ float4 s_sm[];   // [4][nvec]
+  __shared__ uint32_t red[2][kMaxTeam / 32];
+  pdl_trigger();
+  pdl_wait();
+  const int team = blockDim.x;
+  const int lt = threadIdx.x;
+  const int nvec = K >> 4;
+  for (int f = lt; f < (K >> 2); f += team) {
+    const float4 sv = s != nullptr ? __ldg(reinterpret_cast<const float4*>(s) + f) : make_float4(1.f, 1.f, 1.f, 1.f);
+    s_sm[(f & 3) * nvec + (f >> 2)] = sv;
+  }
+  __syncthreads();
+
+  uint4 cur[C];
+  uint32_t dcur[C];
+  int64_t r = blockIdx.x;
+  auto load_row = [&](int64_t row, uint4(&c)[C], uint32_t(&dd)[C]) {
+    const int8_t* qr = q + row * ldq;
+    const uint16_t* dr = d + row * ldd;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int v = lt + i * team;
+      if (v < nvec) {
+        c[i] = ld_codes(qr + 16 * static_cast<int64_t>(v));
+        dd[i] = __ldg(dr + (v >> 1));
+      }
+    }
+  };
+  if (r < N) load_row(r, cur, dcur);
+  int par = 0;
+  for (; r < N; r += gridDim.x) {
+    uint4 nxt[C];
+    uint32_t dnxt[C];
+    const int64_t rn = r + gridDim.x;
+    if (rn < N) load_row(rn, nxt, dnxt);
+
+    // pass 1: the smoothed row, kept in registers for pass 2
+    Vec16 x[C];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int v = lt + i * team;
+      if (v < nvec) {
+        const float4 sv[4] = {s_sm[v], s_sm[nvec + v], s_sm[2 * nvec + v], s_sm[3 * nvec + v]};
+        x[i] = smooth16(cur[i], f16_bits_to_float(dcur[i]), sv);
+        amax = absmax16(x[i], amax);
+      }
+    }
+    amax = team_max(amax, red, par);
+    par ^= 1;
+    const bool zero_row = !(amax >= kTiny);
+    const float inv = zero_row ? 0.0f : __fdiv_rn(127.0f, amax);
+    if (lt == 0) w_scale[r] = zero_row ? 0.0f : __fdiv_rn(amax, 127.0f);
+
+    // pass 2
+    int8_t* wr = w + r * ldw;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int v = lt + i * team;
+      if (v < nvec) *reinterpret_cast<uint4*>(wr + 16 * static_cast<int64_t>(v)) = requant16(x[i], inv);
+    }
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      cur[i] = nxt[i];
+      dcur[i] = dnxt[i];
+    }
+  }
+}
+
+// Rows longer than the register cache: the same arithmetic with every vector
+// read from global memory in both passes (the second read hits L2).  One
+// thread reads and later writes only its own vectors, so w may be q.
+__global__ void __launch_bounds__(kMaxTeam)
+    smooth_requant_long_kernel(const int8_t* q, int64_t ldq, const uint16_t* __restrict__ d, int64_t ldd,
+                               const float* __restrict__ s, int64_t N, int K, int8_t* w, int64_t ldw,
+                               float* __restrict__ w_scale) {
+  __shared__ uint32_t red[2][kMaxTeam / 32];
+  pdl_trigger();
+  pdl_wait();
+  const int nvec = K >> 4;
+  const float4 one4 = make_float4(1.f, 1.f, 1.f, 1.f);
+  const float4* s4g = reinterpret_cast<const float4*>(s);
+  int par = 0;
+  for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
+    const int8_t* qr = q + r * ldq;
+    const uint16_t* dr = d + r * ldd;
+    float amax = 0.0f;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const float4 sv[4] = {s4g ? __ldg(s4g + 4 * v) : one4, s4g ? __ldg(s4g + 4 * v + 1) : one4,
+                            s4g ? __ldg(s4g + 4 * v + 2) : one4, s4g ? __ldg(s4g + 4 * v + 3) : one4};
+      const Vec16 x = smooth16(ld_codes(qr + 16 * static_cast<int64_t>(v)), f16_bits_to_float(__ldg(dr + (v >> 1))), sv);
+      amax = absmax16(x, amax);
+    }
+    amax = team_max(amax, red, par);
+    par ^= 1;
+    const bool zero_row = !(amax >= kTiny);
+    const float inv = zero_row ? 0.0f : __fdiv_rn(127.0f, amax);
+    if (threadIdx.x == 0) w_scale[r] = zero_row ? 0.0f : __fdiv_rn(amax, 127.0f);
+    int8_t* wr = w + r * ldw;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const float4 sv[4] = {s4g ? __ldg(s4g + 4 * v) : one4, s4g ? __ldg(s4g + 4 * v + 1) : one4,
+                            s4g ? __ldg(s4g + 4 * v + 2) : one4, s4g ? __ldg(s4g + 4 * v + 3) : one4};
+      const Vec16 x = smooth16(ld_codes(qr + 16 * static_cast<int64_t>(v)), f16_bits_to_float(__ldg(dr + (v >> 1))), sv);
+      *reinterpret_cast<uint4*>(wr + 16 * static_cast<int64_t>(v)) = requant16(x, inv);
+    }
+  }
+}
+
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Persistent grid: as many CTAs as fit at once, then trimmed to
+// ceil(N / rows_each) CTAs, rows_each = ceil(N / that), so that every CTA
+// takes rows_each or rows_each - 1 rows and no partial last wave is left.
+template <typename Kernel>
+cudaError_t persistent_grid(Kernel kernel, int team, size_t smem, int64_t N, int* grid) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, team, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t gmax = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+  const int64_t rows_each = cdiv64(N, gmax);
+  *grid = static_cast<int>(cdiv64(N, rows_each));
+  return cudaSuccess;
+}
+
+template <int C>
+cudaError_t launch_cached(int team, const int8_t* q, int64_t ldq, const uint16_t* d, int64_t ldd, const float* s,
+                          int64_t N, int K, int8_t* w, int64_t ldw, float* w_scale, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(K) * sizeof(float);
+  const void* fn = reinterpret_cast<const void*>(smooth_requant_kernel<C>);
+  cudaError_t e = ensure_smem_attr(fn, static_cast<int>(smem));
+  int grid = 0;
+  if (e == cudaSuccess) e = persistent_grid(smooth_requant_kernel<C>, team, smem, N, &grid);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(smooth_requant_kernel<C>, dim3(grid), dim3(team), smem, stream, true, q, ldq, d, ldd, s, N,
+                       K, w, ldw, w_scale);
+}
+
+}  // namespace
+
+// Team shape for a row of K: the fewest 16-element vectors per thread (C of
+// 1 to 3) that keep the team within kMaxTeam threads; returns C, or 0 for
+// rows that take the uncached kernel.  *team gets the CTA size.
+int requant_shape(int K, int* team) {
+  const int nvec = K / 16;
+  if (K <= kCachedMaxK) {
+    for (int c = 1; c <= 3; ++c) {
+      const int warps = (nvec + 32 * c - 1) / (32 * c);
+      if (warps * 32 <= kMaxTeam) {
+        *team = warps * 32;
+        return c;
+      }
+    }
+  }
+  *team = kMaxTeam;
+  return 0;
+}
+
+cudaError_t launch_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d, int64_t ldd, const float* s,
+                                  int64_t N, int64_t K, int8_t* w, int64_t ldw, float* w_scale,
+                                  cudaStream_t stream) {
+  int team = 0;
+  const int k = static_cast<int>(K);
+  switch (requant_shape(k, &team)) {
+    case 1: return launch_cached<1>(team, q, ldq, d, ldd, s, N, k, w, ldw, w_scale, stream);
+    case 2: return launch_cached<2>(team, q, ldq, d, ldd, s, N, k, w, ldw, w_scale, stream);
+    case 3: return launch_cached<3>(team, q, ldq, d, ldd, s, N, k, w, ldw, w_scale, stream);
+    default: break;
+  }
+  int grid = 0;
+  cudaError_t e = persistent_grid(smooth_requant_long_kernel, team, 0, N, &grid);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(smooth_requant_long_kernel, dim3(grid), dim3(team), 0, stream, true, q, ldq, d, ldd, s, N, k,
+                       w, ldw, w_scale);
+}
+
+}  // namespace prism

@@ -182,6 +182,34 @@ int prism_w8a8_linear_noalloc(const int8_t *q, int64_t ldq, const float *a_scale
                               void *cuda_stream);
 
 /*
+ * prism_smooth_requant -- load-time SmoothQuant requantisation of Q8_0
+ * weights (StartLux-Prism, "Compute shared evidence once": the stored 8-bit
+ * weights are requantised with the smoothing factors folded in).  Per output
+ * row n and input channel k, in binary32 with one rounding per step:
+ *     v        = (d[n, k/32] * q[n, k]) * s[k]      (the first product is exact)
+ *     amax     = max_k |v|
+ *     w[n, k]  = round-half-even(v * (127 / amax))  (always within +-127)
+ *     w_scale[n] = amax / 127
+ * and a row whose amax is below 2^-120 becomes zeros with scale 0.
+ *
+ *   q, ldq        [N, K] int8 Q8_0 codes (ldq % 16 == 0, 16-byte aligned)
+ *   d_f16, ldd    [N, K/32] binary16 block scales as raw bits (2-byte
+ *                 aligned, ldd >= K/32)
+ *   smooth        [K] float32 s_k (multiplies channel k; 16-byte aligned), or
+ *                 NULL for s_k = 1
+ *   w, ldw        [N, K] int8 out (ldw % 16 == 0, 16-byte aligned).  w may be
+ *                 q itself (in place, ldw == ldq); any other overlap with an
+ *                 input is not allowed.
+ *   w_scale       [N] float32 out (4-byte aligned)
+ *   N >= 0 (N == 0 enqueues nothing), 32 <= K <= PRISM_MAX_K, K % 32 == 0.
+ * Every v must be finite.  The outputs feed prism_w8a8_linear as w, w_scale.
+ */
+int prism_smooth_requant(const int8_t *q, int64_t ldq, const uint16_t *d_f16,
+                         int64_t ldd, const float *smooth, int64_t N, int64_t K,
+                         int8_t *w, int64_t ldw, float *w_scale,
+                         void *cuda_stream);
+
+/*
  * prism_candidate_readout -- logits and probabilities for the candidate
  * tokens of each answer position only; the softmax runs over the candidates
  * (post "把决策模型推理从 vLLM 换到 Prism", sections 方案 and 实现要点: equal to

@@ -188,3 +188,41 @@ def make_readout(name: str, **overrides) -> ReadoutCase:
     kw.update(overrides)
     return readout_case(name, kw["P"], kw["K"], kw["V"], kw["seed"],
                         kw.get("cmin", 2), kw.get("cmax", 10))
+
+
+# ------------------------------------------------- Q8_0 weights as stored ---
+# Load-time requantisation inputs: the stored 8-bit codes of a weight [N, K]
+# in 32-wide blocks, one binary16 scale per block, and the smoothing vector s
+# [K] that the requantisation folds in.  Recipe, in draw order: codes
+# clip(rint(40 N(0,1))); block scales U(2e-4, 2e-3) rounded to binary16;
+# s = exp(N(0, 0.5)) in float32 with 1% of channels (at least one) multiplied
+# by 30, the outlier channels that SmoothQuant moves into the weights.
+REQUANT_CONFIGS = {
+    # name: (N, K, seed) -- the projections of the 27B model as loaded
+    "qkv_n15360_k5120": (15360, HIDDEN, 11),
+    "gateup_n34816_k5120": (2 * FFN, HIDDEN, 12),
+    "down_n5120_k17408": (HIDDEN, FFN, 13),
+}
+
+
+@dataclasses.dataclass
+class Q8Case:
+    name: str
+    q: np.ndarray        # int8 [N, K]
+    d: np.ndarray        # uint16 binary16 bits [N, K/32]
+    s: np.ndarray        # float32 [K]
+
+
+def q8_0_case(name: str, N: int, K: int, seed: int) -> Q8Case:
+    rng = np.random.default_rng(seed)
+    q = draw_weights(rng, (N, K), "normal")
+    d = rng.uniform(2e-4, 2e-3, size=(N, K // 32)).astype(np.float16).view(np.uint16)
+    s = np.exp(rng.standard_normal(K) * 0.5).astype(np.float32)
+    out = rng.choice(K, size=max(1, K // 100), replace=False)
+    s[out] *= np.float32(30.0)
+    return Q8Case(name, q, d, s)
+
+
+def make_q8_0(name: str) -> Q8Case:
+    N, K, seed = REQUANT_CONFIGS[name]
+    return q8_0_case(name, N, K, seed)
