@@ -17,10 +17,13 @@
 // row: it issues the loads of the next row's codes first, then smooths the
 // current row into registers (pass 1, with the max), and quantises from those
 // registers (pass 2), so that each element is decoded and smoothed once and
-// the DRAM latency of row r+1 hides behind the arithmetic of row r.  s is staged once per CTA in shared memory,
-// laid out [4][K/16] float4 so that consecutive threads read consecutive
-// 16-byte words.  int8 -> binary32 and binary32 -> rounded integer go through
-// exact integer tricks on the 2^23 binade instead of conversion instructions.
+// the DRAM latency of row r+1 hides behind the arithmetic of row r.  s is
+// staged once per CTA in shared memory, laid out [4][K/16] float4 so that
+// consecutive threads read consecutive 16-byte words.  The arithmetic runs on
+// packed pairs (Blackwell's f32x2 operations), which round each component
+// like the scalar operation; the codes are decoded and multiplied by their
+// block scale in one exact fused operation on the 2^23 binade, and rounded
+// to integers with the same binade's unit in the last place.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -32,30 +35,35 @@ constexpr int kMaxTeam = 512;
 constexpr int kCachedMaxK = 24576;   // 512 threads x 3 vectors of 16; s in 96 KB of shared memory
 constexpr float kTiny = 0x1p-120f;
 
-// Codes i and i+1 of a word as floats: (2^23 + (c + 128)) - (2^23 + 128),
-// both steps exact.  xw is the code word with every byte's top bit flipped;
-// the pair goes through one packed subtraction.
-__device__ __forceinline__ float2 code_pair(uint32_t xw, int i) {
-  const float lo = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7540u | static_cast<uint32_t>(i)));
-  const float hi = __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7540u | static_cast<uint32_t>(i + 1)));
-  return __fadd2_rn(make_float2(lo, hi), make_float2(-8388736.0f, -8388736.0f));
+// Exact c * d for codes i and i+1 of a word in one packed fused multiply-add.
+// xw is the code word with every byte's top bit flipped (u = c + 128); the
+// byte goes to bits 8..15 of 2^23, F = 2^23 + 256 u, and
+//     F * (d / 256) - (2^15 + 2^7) d = (u - 128) d = c d.
+// d / 256 is exact (d is a binary16 value, at least 2^-24 when nonzero),
+// (2^15 + 2^7) d has at most 20 significant bits so it is exact too, and the
+// fused operation rounds the exact result c d, which has at most 19
+// significant bits, only once: it comes out exact.
+__device__ __forceinline__ float2 code_pair_times_d(uint32_t xw, int i, float2 d_256, float2 neg_bias) {
+  const uint32_t sel = 0x7504u | (static_cast<uint32_t>(i) << 4);
+  const float lo = __uint_as_float(__byte_perm(xw, 0x4B000000u, sel));
+  const float hi = __uint_as_float(__byte_perm(xw, 0x4B000000u, sel + 0x10u));
+  return __ffma2_rn(make_float2(lo, hi), d_256, neg_bias);
 }
 
-// rint_even(t) for |t| < 2^22 as the low byte of RN(t + 1.5 * 2^23): the sum
-// lies in [2^23, 2^24), where the unit in the last place is 1, so the single
-// rounding of the addition is the rounding of t to an integer, ties to even
-// (1.5 * 2^23 is even), and the integer sits in the low mantissa bits.
-// t = RN(v * inv) must be rounded on its own first: a fused multiply-add
-// would round v * inv + M once and send the products that RN rounds up onto
-// a tie x.5 to x instead of the even neighbour.  So both steps are scalar
-// __fmul_rn / __fadd_rn, which are never contracted.  (The assembler does
-// fuse the packed f32x2 multiply and add, even written as PTX with explicit
-// .rn: packed arithmetic is used below only where no product feeds an add.)
-__device__ __forceinline__ uint32_t round_low_byte(float v, float inv) {
-  return __float_as_uint(__fadd_rn(__fmul_rn(v, inv), 12582912.0f));
-}
-__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+// w = rint_even(RN(v * inv)) for two values, as the low 16 bits.  t =
+// RN(v * inv) is one packed multiply; rint_even(t) for |t| < 2^22 is then the
+// low byte of RN(t + 1.5 * 2^23): that sum lies in [2^23, 2^24), where the
+// unit in the last place is 1, so the addition's single rounding rounds t to
+// an integer, ties to even (1.5 * 2^23 is even), and the integer lands in the
+// low mantissa bits.  t must be rounded on its own first -- a fused
+// multiply-add would send the products that RN rounds up onto a tie x.5 to
+// the odd neighbour -- so the additions are scalar __fadd_rn, which is never
+// merged into a multiply-add.  (The packed add is: the assembler fuses a
+// packed multiply and a packed add, even written as PTX with explicit .rn.)
+__device__ __forceinline__ uint32_t round_pair_lo16(float2 v, float2 inv2) {
+  const float2 t = __fmul2_rn(v, inv2);
+  return __byte_perm(__float_as_uint(__fadd_rn(t.x, 12582912.0f)), __float_as_uint(__fadd_rn(t.y, 12582912.0f)),
+                     0x0040u);
 }
 
 __device__ __forceinline__ float f16_bits_to_float(uint32_t h) {
@@ -63,10 +71,8 @@ __device__ __forceinline__ float f16_bits_to_float(uint32_t h) {
 }
 
 // 16 smoothed values of one vector: codes (4 words), block scale df, s from
-// shared memory (sv[j] holds s_k for k = 4j .. 4j+3 of the vector).  Packed
-// binary32 arithmetic, each component rounded like the scalar operation:
-// v = RN(RN(c * d) * s), the first product exact.  An add feeds a multiply
-// here, never the reverse, so there is nothing to fuse.
+// shared memory (sv[j] holds s_k for k = 4j .. 4j+3 of the vector):
+// v = RN(c * d * s), c * d exact.
 struct Vec16 {
   float2 v[8];
 };
@@ -74,11 +80,13 @@ __device__ __forceinline__ Vec16 smooth16(uint4 codes, float df, const float4 (&
   Vec16 r;
   const uint32_t w[4] = {codes.x ^ 0x80808080u, codes.y ^ 0x80808080u, codes.z ^ 0x80808080u,
                          codes.w ^ 0x80808080u};
-  const float2 d2 = make_float2(df, df);
+  const float d256 = __fmul_rn(df, 0x1p-8f);
+  const float nb = __fmul_rn(df, -32896.0f);
+  const float2 d2 = make_float2(d256, d256), b2 = make_float2(nb, nb);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    r.v[2 * j] = __fmul2_rn(__fmul2_rn(code_pair(w[j], 0), d2), make_float2(sv[j].x, sv[j].y));
-    r.v[2 * j + 1] = __fmul2_rn(__fmul2_rn(code_pair(w[j], 2), d2), make_float2(sv[j].z, sv[j].w));
+    r.v[2 * j] = __fmul2_rn(code_pair_times_d(w[j], 0, d2, b2), make_float2(sv[j].x, sv[j].y));
+    r.v[2 * j + 1] = __fmul2_rn(code_pair_times_d(w[j], 2, d2, b2), make_float2(sv[j].z, sv[j].w));
   }
   return r;
 }
@@ -87,12 +95,14 @@ __device__ __forceinline__ float absmax16(const Vec16& r, float m) {
   for (int e = 0; e < 8; ++e) m = fmaxf(fmaxf(m, fabsf(r.v[e].x)), fabsf(r.v[e].y));
   return m;
 }
+// |RN(v * inv)| <= 127.00001 (see the top of the file): every integer is
+// within +-127.
 __device__ __forceinline__ uint4 requant16(const Vec16& r, float inv) {
+  const float2 inv2 = make_float2(inv, inv);
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    o[j] = pack4(round_low_byte(r.v[2 * j].x, inv), round_low_byte(r.v[2 * j].y, inv),
-                 round_low_byte(r.v[2 * j + 1].x, inv), round_low_byte(r.v[2 * j + 1].y, inv));
+    o[j] = __byte_perm(round_pair_lo16(r.v[2 * j], inv2), round_pair_lo16(r.v[2 * j + 1], inv2), 0x5410u);
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
