@@ -66,6 +66,9 @@ def _load():
             "oracle_gemm_s32_splitk": (I32, [P, I64, P, I64, I64, I64, I64, I32, P, I64]),
             "oracle_epilogue": (None, [P, I64, P, P, P, I64, I64, I64, P, I64]),
             "oracle_w8a8_linear": (I32, [P, I64, P, P, I64, P, P, I64, I64, I64, I64, P, I64, P]),
+            "oracle_quant_act_rows": (ctypes.c_uint32, [P, I64, I64, P, I64, P, I64, P, I64, P]),
+            "oracle_w8a8_linear_rows": (I32, [P, I64, P, P, I64, P, P, I64, I64, P, I64, I64, I64, P, I64,
+                                              P, P]),
             "oracle_exp": (F, [F]),
             "oracle_exp_batch": (None, [P, I64, P]),
             "oracle_candidate_readout": (I32, [P, I64, P, P, I64, P, I64, I64, P, P, I64, I64, P, P]),
@@ -206,6 +209,47 @@ def w8a8_linear(q, a_scale, w, w_scale, residual_bits=None):
     if rc:
         raise OverflowError("int32 accumulator overflow")
     return out, acc
+
+
+ERR_ROW_RANGE = 16   # a row index outside the indexed matrix
+
+
+def quant_act_rows(x_bf16_bits: np.ndarray, rows, inv_s: np.ndarray | None):
+    """Quantisation of the rows ``rows`` of ``x_bf16_bits`` [M_x, K] (the last
+    layer restricted to answer positions).  Returns (q int8 [n, K], a_scale
+    float32 [n], error bits)."""
+    x = _c(x_bf16_bits, np.uint16)
+    M_x, K = x.shape
+    r = _c(np.asarray(rows, dtype=np.int32), np.int32)
+    n = r.size
+    s = None if inv_s is None else _c(inv_s, np.float32)
+    q = np.empty((n, K), np.int8)
+    a = np.empty((n,), np.float32)
+    err = _load().oracle_quant_act_rows(_p(x), K, M_x, _p(r), n, _p(s), K, _p(q), K, _p(a))
+    return q, a, int(err)
+
+
+def w8a8_linear_rows(q, a_scale, w, w_scale, residual_bits, res_rows):
+    """The linear whose residual row m is ``residual_bits[res_rows[m]]``.
+    Returns (out bf16 bits uint16 [M, N], acc int32, error bits)."""
+    q = _c(q, np.int8)
+    w = _c(w, np.int8)
+    M, K = q.shape
+    N = w.shape[0]
+    a = _c(a_scale, np.float32)
+    ws = _c(w_scale, np.float32)
+    r = _c(residual_bits, np.uint16)
+    M_res = r.shape[0]
+    rr = _c(np.asarray(res_rows, dtype=np.int32), np.int32)
+    assert rr.size == M
+    out = np.empty((M, N), np.uint16)
+    acc = np.empty((M, N), np.int32)
+    err = ctypes.c_uint32(0)
+    rc = _load().oracle_w8a8_linear_rows(_p(q), K, _p(a), _p(w), K, _p(ws), _p(r), N, M_res, _p(rr),
+                                         M, N, K, _p(out), N, _p(acc), ctypes.byref(err))
+    if rc:
+        raise OverflowError("int32 accumulator overflow")
+    return out, acc, int(err.value)
 
 
 def exp(x) -> np.ndarray:

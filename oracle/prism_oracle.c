@@ -50,6 +50,8 @@
 #define ORACLE_MAX_K 133144        /* largest K with K * 127 * 127 <= 2^31 - 1 */
 #define ORACLE_MAX_CANDIDATES 64   /* hard cap per answer position [P4-review] */
 
+#define ORACLE_ERR_ROW_RANGE 16u   /* a row index outside the indexed matrix */
+
 /* ---------------------------------------------------------------- bf16 --- */
 
 /* bfloat16 is the top half of a binary32: widening is exact. */
@@ -342,6 +344,64 @@ int oracle_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
     int rc = oracle_gemm_s32(q, ldq, w, ldw, M, N, K, acc, N);
     if (rc) return rc;
     oracle_epilogue(acc, N, a_scale, w_scale, residual, ldr, M, N, out, ldo);
+    return 0;
+}
+
+/* ------------------------------------- restriction to answer positions --- */
+/*
+ * [P1-shared]: in the last layer only the positions needed for answers are
+ * computed.  Every step of the layer is per token, so the restricted layer is
+ * the full layer's rows at those positions; these two functions state it by
+ * running the full definitions above on the selected rows.
+ *
+ * oracle_quant_act_rows: q row i, a_scale[i] = the quantisation of x row
+ * rows[i] (x has M_x rows).  An index outside [0, M_x) gives a zero q row,
+ * a NaN scale, and ORACLE_ERR_ROW_RANGE in the returned error bits.
+ */
+uint32_t oracle_quant_act_rows(const uint16_t *x, int64_t ldx, int64_t M_x,
+                               const int32_t *rows, int64_t n_rows,
+                               const float *inv_s, int64_t K, int8_t *q,
+                               int64_t ldq, float *a_scale)
+{
+    uint32_t err = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t r = rows[i];
+        if (r < 0 || r >= M_x) {
+            memset(q + i * ldq, 0, (size_t)K);
+            a_scale[i] = NAN;
+            err |= ORACLE_ERR_ROW_RANGE;
+            continue;
+        }
+        oracle_quant_act(x + r * ldx, ldx, inv_s, 1, K, q + i * ldq, ldq, a_scale + i);
+    }
+    return err;
+}
+
+/*
+ * oracle_w8a8_linear_rows: oracle_w8a8_linear whose residual row for output
+ * row m is residual row res_rows[m] (the residual has M_res rows).  An index
+ * outside [0, M_res) makes output row m NaN (bf16 0x7fc0) and sets
+ * ORACLE_ERR_ROW_RANGE in *err.  Returns what oracle_w8a8_linear returns.
+ */
+int oracle_w8a8_linear_rows(const int8_t *q, int64_t ldq, const float *a_scale,
+                            const int8_t *w, int64_t ldw, const float *w_scale,
+                            const uint16_t *residual, int64_t ldr, int64_t M_res,
+                            const int32_t *res_rows, int64_t M, int64_t N,
+                            int64_t K, uint16_t *out, int64_t ldo,
+                            int32_t *acc_out, uint32_t *err)
+{
+    int rc = oracle_gemm_s32(q, ldq, w, ldw, M, N, K, acc_out, N);
+    if (rc) return rc;
+    for (int64_t m = 0; m < M; ++m) {
+        const int64_t r = res_rows[m];
+        if (r < 0 || r >= M_res) {
+            for (int64_t n = 0; n < N; ++n) out[m * ldo + n] = 0x7fc0u;
+            *err |= ORACLE_ERR_ROW_RANGE;
+            continue;
+        }
+        oracle_epilogue(acc_out + m * N, N, a_scale + m, w_scale, residual + r * ldr, ldr, 1, N,
+                        out + m * ldo, ldo);
+    }
     return 0;
 }
 

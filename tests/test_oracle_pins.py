@@ -581,3 +581,64 @@ def test_readout_softmax_arithmetic_exact_rationals():
         for i, v in enumerate(ev):
             want = rn32(Fr(v) / s) if v else 0.0
             assert probs[b + i] == np.float32(want), (p, i)
+
+
+# ---------------------------------------------- restriction to answer rows ---
+# StartLux-Prism, "Compute shared evidence once": the last layer computes only
+# the positions needed for answers.  Every step is per token, so the
+# restricted layer must reproduce the full layer's rows at those positions:
+# the pins compare the row-indexed oracle functions with the full ones.
+
+def _layer_inputs(seed, M_x=40, K=256, N=96):
+    rng = np.random.default_rng(seed)
+    x = wl.bf16_bits(rng.standard_normal((M_x, K), dtype=np.float32) * 3)
+    inv_s = rng.uniform(0.5, 2.0, K).astype(np.float32)
+    w = wl.draw_weights(rng, (N, K), "normal")
+    ws = rng.uniform(0.001, 0.02, N).astype(np.float32)
+    res = wl.bf16_bits(rng.standard_normal((M_x, N), dtype=np.float32))
+    return x, inv_s, w, ws, res
+
+
+def test_rows_quantiser_is_the_full_quantiser_on_those_rows():
+    x, inv_s, *_ = _layer_inputs(1)
+    rows = np.array([7, 0, 39, 7, 13], np.int32)           # any order, repeats allowed
+    q_full, a_full = oracle.quant_act(x, inv_s)
+    q, a, err = oracle.quant_act_rows(x, rows, inv_s)
+    assert err == 0
+    assert np.array_equal(q, q_full[rows])
+    assert np.array_equal(a.view(np.uint32), a_full[rows].view(np.uint32))
+
+
+def test_restricted_layer_equals_full_layer_rows():
+    x, inv_s, w, ws, res = _layer_inputs(2)
+    rows = np.array([39, 2, 20], np.int32)
+    q_full, a_full = oracle.quant_act(x, inv_s)
+    out_full, acc_full = oracle.w8a8_linear(q_full, a_full, w, ws, res)
+    q, a, err = oracle.quant_act_rows(x, rows, inv_s)
+    out, acc, err2 = oracle.w8a8_linear_rows(q, a, w, ws, res, rows)
+    assert err == 0 and err2 == 0
+    assert np.array_equal(acc, acc_full[rows])
+    assert np.array_equal(out, out_full[rows])
+    # the residual row is the one the index names, not the output row's own
+    out_wrong, _, _ = oracle.w8a8_linear_rows(q, a, w, ws, res, np.arange(3, dtype=np.int32))
+    assert not np.array_equal(out_wrong, out)
+
+
+def test_rows_out_of_range_flag_and_poison_only_their_row():
+    x, inv_s, w, ws, res = _layer_inputs(3)
+    q, a, err = oracle.quant_act_rows(x, np.array([5, -1, 40], np.int32), inv_s)
+    assert err == oracle.ERR_ROW_RANGE
+    assert np.isnan(a[1]) and np.isnan(a[2]) and not np.isnan(a[0])
+    assert not q[1:].any()
+    q_ok, a_ok, _ = oracle.quant_act_rows(x, np.array([5, 6, 7], np.int32), inv_s)
+    out, _, err = oracle.w8a8_linear_rows(q_ok, a_ok, w, ws, res, np.array([5, 40, 7], np.int32))
+    assert err == oracle.ERR_ROW_RANGE
+    assert (out[1] == 0x7FC0).all()
+    good, _, _ = oracle.w8a8_linear_rows(q_ok, a_ok, w, ws, res, np.array([5, 6, 7], np.int32))
+    assert np.array_equal(out[[0, 2]], good[[0, 2]])
+
+
+def test_rows_empty_selection():
+    x, inv_s, *_ = _layer_inputs(4)
+    q, a, err = oracle.quant_act_rows(x, np.zeros(0, np.int32), inv_s)
+    assert q.shape == (0, x.shape[1]) and a.shape == (0,) and err == 0
