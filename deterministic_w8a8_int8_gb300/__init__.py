@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
   prism_quant_act(x, inv_s)                      -> (q, a_scale)
   prism_w8a8_linear(q, a_scale, w, w_scale, ...) -> out
   prism_smooth_requant(q, d, smooth)             -> (w, w_scale)
+  prism_quant_act_rows(x, rows, inv_s)           -> (q, a_scale)   answer rows only
+  prism_w8a8_linear_rows(q, a_scale, w, w_scale, residual, residual_rows) -> out
   prism_candidate_readout(hidden, ...)           -> (logits, probs)
 """
 from __future__ import annotations
@@ -38,6 +40,7 @@ PRISM_DEV_ERR_OFFSETS = 1
 PRISM_DEV_ERR_COUNT = 2
 PRISM_DEV_ERR_ID_RANGE = 4
 PRISM_DEV_ERR_DUPLICATE = 8
+PRISM_DEV_ERR_ROW_RANGE = 16
 
 # (restype, argtypes) of every symbol the header declares
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
@@ -51,6 +54,9 @@ SIGNATURES = {
     "prism_candidate_readout": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _P, _P,
                                        _I64, _I64, _P, _P, _P, _P]),
     "prism_smooth_requant": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "prism_quant_act_rows": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
+    "prism_w8a8_linear_rows": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P,
+                                      _I64, _I64, _I64, _I32, _P, _SZ, _P, _P]),
     "prism_status_string": (ctypes.c_char_p, [_I32]),
     "prism_version": (_I32, []),
     "prism_w8a8_kernel_kind": (_I32, [_I64, _I64, _I64]),
@@ -242,6 +248,70 @@ def prism_w8a8_linear(q, a_scale, w, w_scale, residual=None, out=None, acc_out=N
         _ptr(residual), 0 if residual is None else residual.stride(0), _ptr(out), out.stride(0),
         _ptr(acc_out), M, N, K, int(split_k), _ptr(workspace), ws_bytes, _stream(stream))
     _check("prism_w8a8_linear", st)
+    return out
+
+
+def prism_quant_act_rows(x, rows, inv_s=None, q=None, a_scale=None, err=None, stream=None):
+    """Quantisation of the rows ``rows`` (int32 [n]) of bf16 ``x`` [M_x, K]
+    -> (int8 q [n, K], float32 a_scale [n]).  ``err``: optional int32 [1]
+    device word that collects PRISM_DEV_ERR_ROW_RANGE."""
+    import torch
+    _require(x, torch.bfloat16, "x", 2)
+    _require(rows, torch.int32, "rows", 1)
+    M_x, K = x.shape
+    n = rows.numel()
+    if inv_s is not None:
+        _require(inv_s, torch.float32, "inv_s", 1)
+    if q is None:
+        q = torch.empty((n, K), dtype=torch.int8, device=x.device)
+    if a_scale is None:
+        a_scale = torch.empty((n,), dtype=torch.float32, device=x.device)
+    _require(q, torch.int8, "q", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    if err is not None:
+        _require(err, torch.int32, "err", 1)
+    st = lib().prism_quant_act_rows(_ptr(x), x.stride(0), M_x, _ptr(rows), n, _ptr(inv_s), K, _ptr(q),
+                                    q.stride(0), _ptr(a_scale), _ptr(err), _stream(stream))
+    _check("prism_quant_act_rows", st)
+    return q, a_scale
+
+
+def prism_w8a8_linear_rows(q, a_scale, w, w_scale, residual, residual_rows, out=None, acc_out=None,
+                           split_k: int = 0, workspace=None, err=None, stream=None):
+    """prism_w8a8_linear whose residual row for output row m is
+    ``residual[residual_rows[m]]`` (``residual`` [M_res, N] bf16, the full
+    hidden state; ``residual_rows`` int32 [M]).  ``out`` must not overlap
+    ``residual``.  ``err``: optional int32 [1] device error word."""
+    import torch
+    _require(q, torch.int8, "q", 2)
+    _require(w, torch.int8, "w", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    _require(w_scale, torch.float32, "w_scale", 1)
+    _require(residual, torch.bfloat16, "residual", 2)
+    _require(residual_rows, torch.int32, "residual_rows", 1)
+    M, K = q.shape
+    N = w.shape[0]
+    if w.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N or residual_rows.numel() != M:
+        raise ValueError("shape mismatch")
+    if residual.shape[1] != N:
+        raise ValueError("residual shape")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
+    _require(out, torch.bfloat16, "out", 2)
+    if acc_out is not None:
+        _require(acc_out, torch.int32, "acc_out", 2)
+        if not acc_out.is_contiguous() or tuple(acc_out.shape) != (M, N):
+            raise ValueError("acc_out must be a contiguous [M, N] int32 tensor")
+    if err is not None:
+        _require(err, torch.int32, "err", 1)
+    if workspace is None:
+        workspace = new_workspace(M, N, K, split_k, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().prism_w8a8_linear_rows(
+        _ptr(q), q.stride(0), _ptr(a_scale), _ptr(w), w.stride(0), _ptr(w_scale),
+        _ptr(residual), residual.stride(0), residual.shape[0], _ptr(residual_rows), _ptr(out), out.stride(0),
+        _ptr(acc_out), M, N, K, int(split_k), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
+    _check("prism_w8a8_linear_rows", st)
     return out
 
 

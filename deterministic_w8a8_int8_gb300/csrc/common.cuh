@@ -126,8 +126,11 @@ cudaError_t launch_kernel(Kernel kernel, dim3 grid, dim3 block, size_t smem, cud
 
 // Internal launchers (one per kernel family), defined in their .cu files.
 namespace prism {
-cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K,
-                             int8_t* q, int64_t ldq, float* a_scale, cudaStream_t stream);
+// rows: null, or output row m quantises x row rows[m] of M_x (err gets
+// PRISM_DEV_ERR_ROW_RANGE for an index outside [0, M_x); may be null).
+cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K, int8_t* q,
+                             int64_t ldq, float* a_scale, const int32_t* rows, int64_t M_x, uint32_t* err,
+                             cudaStream_t stream);
 
 struct LinearArgs {
   const int8_t* q;
@@ -149,7 +152,25 @@ struct LinearArgs {
   size_t ws_bytes;      // its size
   int32_t* ws_acc;      // split-K > 1: [M, N] int32, zero between calls (set by the launcher)
   uint32_t* ws_count;   // split-K > 1: [tiles] arrival counters, zero between calls
+  const int32_t* res_rows;  // null, or the residual row of output row m is res_rows[m] ...
+  int64_t M_res;            // ... of the residual's M_res rows
+  uint32_t* err;            // PRISM_DEV_ERR_* bits (row index out of range), or null
 };
+
+// The residual row of output row m: row m itself, or row res_rows[m] (the
+// last layer restricted to answer positions).  Null for an index outside
+// [0, M_res), after setting PRISM_DEV_ERR_ROW_RANGE: that row's outputs
+// become NaN and nothing outside the residual is read.
+__device__ __forceinline__ const uint16_t* residual_row(const LinearArgs& a, int64_t m) {
+  if (a.res_rows == nullptr) return a.residual + m * a.ldr;
+  const int64_t r = __ldg(a.res_rows + m);
+  if (r < 0 || r >= a.M_res) {
+    if (a.err != nullptr) atomicOr(a.err, PRISM_DEV_ERR_ROW_RANGE);
+    return nullptr;
+  }
+  return a.residual + r * a.ldr;
+}
+constexpr uint32_t kBf16NaN = 0x7fc0u;
 // Workspace bytes a call needs (split 0 = the automatic schedule).
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
 // Leading bytes of the workspace that must be zero when a call starts, for a

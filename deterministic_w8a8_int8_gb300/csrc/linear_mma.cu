@@ -47,9 +47,13 @@ __device__ __forceinline__ void store_pair(const LinearArgs& a, int64_t row, int
       if (e == 1 && !two) break;
       const int32_t v = e ? v1 : v0;
       const float ws1 = __ldg(a.w_scale + col + e);
-      const uint32_t o = a.residual != nullptr
-                             ? epilogue_bf16_res(v, as1, ws1, bf16_bits_to_float(a.residual[row * a.ldr + col + e]))
-                             : epilogue_bf16(v, as1, ws1);
+      uint32_t o;
+      if (a.residual != nullptr) {
+        const uint16_t* rp = residual_row(a, row);
+        o = epilogue_bf16_res(v, as1, ws1, bf16_bits_to_float(rp != nullptr ? rp[col + e] : kBf16NaN));
+      } else {
+        o = epilogue_bf16(v, as1, ws1);
+      }
       a.out[row * a.ldo + col + e] = static_cast<uint16_t>(o);
       if (a.acc_out != nullptr) a.acc_out[row * a.N + col + e] = v;
     }
@@ -58,8 +62,12 @@ __device__ __forceinline__ void store_pair(const LinearArgs& a, int64_t row, int
   const float w0 = __ldg(a.w_scale + col);
   const float w1 = two ? __ldg(a.w_scale + col + 1) : 0.0f;
   uint32_t o0, o1 = 0;
-  if (a.residual != nullptr) {
-    const uint16_t* rp = a.residual + row * a.ldr + col;
+  const uint16_t* rrow = a.residual != nullptr ? residual_row(a, row) : nullptr;
+  if (a.residual != nullptr && rrow == nullptr) {
+    o0 = epilogue_bf16_res(v0, as, w0, bf16_bits_to_float(kBf16NaN));
+    if (two) o1 = epilogue_bf16_res(v1, as, w1, bf16_bits_to_float(kBf16NaN));
+  } else if (a.residual != nullptr) {
+    const uint16_t* rp = rrow + col;
     if (two) {
       const uint32_t rr = *reinterpret_cast<const uint32_t*>(rp);
       o0 = epilogue_bf16_res(v0, as, w0, bf16_lo(rr));

@@ -255,6 +255,10 @@ __device__ __forceinline__ void st_shared_v4_if(uint32_t addr, uint32_t a, uint3
 // reverse.  s_as / s_ws hold the tile's a_scale (by token) and w_scale (by
 // channel).  The residual values of the round are all loaded before any
 // output is stored, so an in-place residual (residual == out) is safe.
+// kRows: the residual row of output row m is a.res_rows[m] (compiled only
+// into the kernel instance for row-indexed calls, so the ordinary path keeps
+// its code).
+template <bool kRows>
 __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, const float* s_ws, int64_t a0,
                                           int64_t b0, int trow, int cb, const int32_t (&v)[16]) {
   const LinearArgs& a = p.a;
@@ -265,9 +269,20 @@ __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, 
     const int jn = a.M - mb < 16 ? static_cast<int>(a.M - mb) : 16;
     const float ws = s_ws[trow];
     float r[16];
+    if constexpr (kRows) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      r[j] = res && j < jn ? bf16_bits_to_float(a.residual[(mb + j) * a.ldr + n]) : 0.f;
+      for (int j = 0; j < 16; ++j) {
+        r[j] = 0.f;
+        if (res && j < jn) {
+          const uint16_t* rp = residual_row(a, mb + j);
+          r[j] = bf16_bits_to_float(rp != nullptr ? rp[n] : kBf16NaN);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        r[j] = res && j < jn ? bf16_bits_to_float(a.residual[(mb + j) * a.ldr + n]) : 0.f;
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       if (j < jn) {
@@ -286,8 +301,18 @@ __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, 
   if (p.vec_io && nb + 16 <= a.N) {
     uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
     if (res) {
-      r0 = *reinterpret_cast<const uint4*>(a.residual + m * a.ldr + nb);
-      r1 = *reinterpret_cast<const uint4*>(a.residual + m * a.ldr + nb + 8);
+      if constexpr (kRows) {
+        const uint16_t* rp = residual_row(a, m);
+        if (rp != nullptr) {
+          r0 = *reinterpret_cast<const uint4*>(rp + nb);
+          r1 = *reinterpret_cast<const uint4*>(rp + nb + 8);
+        } else {
+          r0 = r1 = make_uint4(kBf16NaN * 0x10001u, kBf16NaN * 0x10001u, kBf16NaN * 0x10001u, kBf16NaN * 0x10001u);
+        }
+      } else {
+        r0 = *reinterpret_cast<const uint4*>(a.residual + m * a.ldr + nb);
+        r1 = *reinterpret_cast<const uint4*>(a.residual + m * a.ldr + nb + 8);
+      }
     }
     const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
     uint32_t o[8];
@@ -307,8 +332,15 @@ __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, 
     return;
   }
   float r[16];
+  if constexpr (kRows) {
+    const uint16_t* rp = res ? residual_row(a, m) : nullptr;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) r[j] = res && nb + j < a.N ? bf16_bits_to_float(a.residual[m * a.ldr + nb + j]) : 0.f;
+    for (int j = 0; j < 16; ++j)
+      r[j] = res && nb + j < a.N ? bf16_bits_to_float(rp != nullptr ? rp[nb + j] : kBf16NaN) : 0.f;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) r[j] = res && nb + j < a.N ? bf16_bits_to_float(a.residual[m * a.ldr + nb + j]) : 0.f;
+  }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (nb + j < a.N) {
@@ -431,6 +463,7 @@ __device__ __forceinline__ float item_scale(const TcParams& p, const Item& itm, 
   return i < (p.swap ? kBM : bn) && n < a.N ? __ldg(a.w_scale + n) : 0.f;
 }
 
+template <bool kRows>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
@@ -705,8 +738,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int l = wt; l < ntok * lines; l += kWorkers) {
             const int r = l / lines;
             const int64_t m = tok0 + r, nn = ch0 + (l - r * lines) * 64;
-            if (m < a.M && nn < a.N)
+            if constexpr (kRows) {
+              const int64_t src = m < a.M ? __ldg(a.res_rows + m) : -1;
+              if (nn < a.N && src >= 0 && src < a.M_res)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.residual + src * a.ldr + nn));
+            } else if (m < a.M && nn < a.N) {
               asm volatile("prefetch.global.L2 [%0];" ::"l"(a.residual + m * a.ldr + nn));
+            }
           }
         }
       }
@@ -777,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int glast = gc + nchunks - 1;
       if (itm.kind == 0) {
         if (have) {
-          auto out = [&](int cb, const int32_t (&v)[16]) { round_out(p, sa, sw, a0, b0, trow, cb, v); };
+          auto out = [&](int cb, const int32_t (&v)[16]) { round_out<kRows>(p, sa, sw, a0, b0, trow, cb, v); };
           ok = drain(glast, nchunks - 1, bn, out, true);
         }
       } else {
@@ -825,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj) __stcg(tacc + slot_index(trow, cb, jj), 0);
             }
-            round_out(p, sa, sw, a0, b0, trow, cb, v);
+            round_out<kRows>(p, sa, sw, a0, b0, trow, cb, v);
           }
           if (wt == 0) *counter = 0u;
         }
@@ -966,7 +1004,8 @@ static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int
 }
 
 static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(linear_tc_kernel), kSmemBytes);
+  auto kernel = a.res_rows != nullptr ? linear_tc_kernel<true> : linear_tc_kernel<false>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   const TcPlan pl = tc_plan(a.M, a.N);
   TcParams p{};
@@ -1018,7 +1057,7 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece);
   if (e != cudaSuccess) return e;
-  return launch_kernel(linear_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream, a.no_pdl == 0, p, tmA, tmB);
+  return launch_kernel(kernel, grid, dim3(kThreads), kSmemBytes, stream, a.no_pdl == 0, p, tmA, tmB);
 }
 
 // PRISM_LINEAR_PATH=mma routes the linear to the mma.sync s8 kernel (a

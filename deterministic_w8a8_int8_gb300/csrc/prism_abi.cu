@@ -85,8 +85,8 @@ int prism_quant_act(const void* x_bf16, int64_t ldx, const float* inv_smooth, in
   if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(a_scale, 4)) return PRISM_ERR_ALIGNMENT;
   if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
   if (M > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
-  return prism::record_cuda(prism::launch_quant_act(x_bf16, ldx, inv_smooth, M, K, q, ldq, a_scale,
-                                                     static_cast<cudaStream_t>(cuda_stream)));
+  return prism::record_cuda(prism::launch_quant_act(x_bf16, ldx, inv_smooth, M, K, q, ldq, a_scale, nullptr, M,
+                                                     nullptr, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int prism_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d_f16, int64_t ldd, const float* smooth,
@@ -107,6 +107,25 @@ int prism_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d_f16, in
                                                           static_cast<cudaStream_t>(cuda_stream)));
 }
 
+int prism_quant_act_rows(const void* x_bf16, int64_t ldx, int64_t M_x, const int32_t* rows, int64_t n_rows,
+                         const float* inv_smooth, int64_t K, int8_t* q, int64_t ldq, float* a_scale,
+                         uint32_t* dev_error_word, void* cuda_stream) {
+  if (n_rows < 0 || M_x < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (n_rows == 0) return PRISM_OK;
+  if (x_bf16 == nullptr || rows == nullptr || q == nullptr || a_scale == nullptr || M_x == 0)
+    return PRISM_ERR_INVALID_ARG;
+  if (ldx < K || ldq < K) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+  if (ldx % 8 != 0 || ldq % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(a_scale, 4) || !aligned(rows, 4)) return PRISM_ERR_ALIGNMENT;
+  if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
+  if (dev_error_word != nullptr && !aligned(dev_error_word, 4)) return PRISM_ERR_ALIGNMENT;
+  if (n_rows > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  return prism::record_cuda(prism::launch_quant_act(x_bf16, ldx, inv_smooth, n_rows, K, q, ldq, a_scale, rows, M_x,
+                                                     dev_error_word, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K) { return prism::linear_kernel_kind(M, N, K); }
 
 int prism_device_status(uint32_t* flags) {
@@ -121,10 +140,11 @@ size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) 
   return prism::linear_workspace_bytes(M, N, K, split_k);
 }
 
-int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
-                      const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16,
-                      int64_t ldo, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k,
-                      void* workspace, size_t workspace_bytes, void* cuda_stream) {
+static int linear_impl(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
+                       const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16,
+                       int64_t ldo, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k,
+                       void* workspace, size_t workspace_bytes, const int32_t* res_rows, int64_t M_res,
+                       uint32_t* err, void* cuda_stream) {
   if (M < 0 || N < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
   if (split_k < 0) return PRISM_ERR_INVALID_ARG;
   if (split_k > PRISM_MAX_SPLIT_K) return PRISM_ERR_UNSUPPORTED;
@@ -159,6 +179,9 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
   a.N = N;
   a.K = K;
   a.split = split_k;
+  a.res_rows = res_rows;
+  a.M_res = M_res;
+  a.err = err;
   a.pair_io = aligned(out_bf16, 4) && ldo % 2 == 0 &&
               (residual_bf16 == nullptr || (aligned(residual_bf16, 4) && ldr % 2 == 0));
   if (need > 0) {
@@ -168,6 +191,34 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
     a.ws_bytes = workspace_bytes;
   }
   return prism::record_cuda(prism::launch_linear(a, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
+                      const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16,
+                      int64_t ldo, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return linear_impl(q, ldq, a_scale, w, ldw, w_scale, residual_bf16, ldr, out_bf16, ldo, acc_out, M, N, K, split_k,
+                     workspace, workspace_bytes, nullptr, 0, nullptr, cuda_stream);
+}
+
+int prism_w8a8_linear_rows(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
+                           const float* w_scale, const void* residual_bf16, int64_t ldr, int64_t M_res,
+                           const int32_t* residual_rows, void* out_bf16, int64_t ldo, int32_t* acc_out,
+                           int64_t M, int64_t N, int64_t K, int split_k, void* workspace,
+                           size_t workspace_bytes, uint32_t* dev_error_word, void* cuda_stream) {
+  if (M < 0 || M_res < 0) return PRISM_ERR_INVALID_ARG;
+  if (M > 0 && N > 0) {
+    if (residual_bf16 == nullptr || residual_rows == nullptr || M_res == 0) return PRISM_ERR_INVALID_ARG;
+    if (!aligned(residual_rows, 4) || (dev_error_word != nullptr && !aligned(dev_error_word, 4)))
+      return PRISM_ERR_ALIGNMENT;
+    // Output rows may be residual rows of other CTAs' tiles: no overlap.
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(out_bf16), r0 = reinterpret_cast<uintptr_t>(residual_bf16);
+    const uintptr_t o1 = o0 + static_cast<uintptr_t>((M - 1) * ldo + N) * 2;
+    const uintptr_t r1 = r0 + static_cast<uintptr_t>((M_res - 1) * ldr + N) * 2;
+    if (o0 < r1 && r0 < o1) return PRISM_ERR_INVALID_ARG;
+  }
+  return linear_impl(q, ldq, a_scale, w, ldw, w_scale, residual_bf16, ldr, out_bf16, ldo, acc_out, M, N, K, split_k,
+                     workspace, workspace_bytes, residual_rows, M_res, dev_error_word, cuda_stream);
 }
 
 int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* inv_smooth,

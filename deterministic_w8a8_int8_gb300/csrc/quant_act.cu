@@ -65,21 +65,29 @@ __device__ __forceinline__ float vmaxabs(const Vec8& r, float m) {
   return m;
 }
 
-template <int TEAM, int CACHE>
+// rows != nullptr: output row m quantises x row rows[m] of the M_x rows of x
+// (the last layer restricted to answer positions); an index outside [0, M_x)
+// gives a zero q row, a NaN scale and PRISM_DEV_ERR_ROW_RANGE in *err.
+template <int TEAM, int CACHE, bool kRows>
 __global__ void __launch_bounds__(kBlock)
     quant_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, const float* __restrict__ inv_s,
                      int64_t M, int64_t K, int8_t* __restrict__ q, int64_t ldq,
-                     float* __restrict__ a_scale) {
-  constexpr int kRows = kBlock / TEAM;
+                     float* __restrict__ a_scale, const int32_t* __restrict__ rows, int64_t M_x,
+                     uint32_t* err) {
+  constexpr int kTeams = kBlock / TEAM;
   constexpr int kWarpsPerTeam = TEAM / 32;
   __shared__ float red[kBlock / 32];
   pdl_trigger();
   pdl_wait();
   const int team = threadIdx.x / TEAM;
   const int lt = threadIdx.x % TEAM;
-  const int64_t m = static_cast<int64_t>(blockIdx.x) * kRows + team;
-  const bool active = m < M;
-  const uint16_t* xr = x + (active ? m : 0) * ldx;
+  const int64_t m = static_cast<int64_t>(blockIdx.x) * kTeams + team;
+  const bool in_grid = m < M;
+  int64_t src = m;
+  if constexpr (kRows) src = in_grid ? __ldg(rows + m) : -1;
+  const bool row_ok = kRows ? (src >= 0 && src < M_x) : in_grid;
+  const bool active = in_grid && row_ok;
+  const uint16_t* xr = x + (active ? src : 0) * ldx;
   const int64_t nvec = K >> 3;
 
   Vec8 cache[CACHE];
@@ -105,7 +113,16 @@ __global__ void __launch_bounds__(kBlock)
 #pragma unroll
     for (int i = 0; i < kWarpsPerTeam; ++i) amax = fmaxf(amax, red[w0 + i]);
   }
-  if (!active) return;
+  if (!in_grid) return;
+  if (kRows && !row_ok) {
+    int8_t* qr = q + m * ldq;
+    for (int64_t v = lt; v < (K >> 3); v += TEAM) *reinterpret_cast<uint2*>(qr + v * 8) = make_uint2(0u, 0u);
+    if (lt == 0) {
+      a_scale[m] = __uint_as_float(0x7fc00000u);
+      if (err != nullptr) atomicOr(err, PRISM_DEV_ERR_ROW_RANGE);
+    }
+    return;
+  }
 
   int8_t* qr = q + m * ldq;
   const bool zero_row = !(amax >= 0x1p-120f);
@@ -133,24 +150,29 @@ __global__ void __launch_bounds__(kBlock)
 }
 
 template <int TEAM, int CACHE>
-cudaError_t launch_team(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K,
-                        int8_t* q, int64_t ldq, float* a_scale, cudaStream_t stream) {
-  constexpr int kRows = kBlock / TEAM;
-  const int64_t blocks = (M + kRows - 1) / kRows;
-  return launch_kernel(quant_act_kernel<TEAM, CACHE>, dim3(static_cast<unsigned>(blocks)), dim3(kBlock), 0,
-                       stream, true, static_cast<const uint16_t*>(x), ldx, inv_s, M, K, q, ldq, a_scale);
+cudaError_t launch_team(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K, int8_t* q,
+                        int64_t ldq, float* a_scale, const int32_t* rows, int64_t M_x, uint32_t* err,
+                        cudaStream_t stream) {
+  constexpr int kTeams = kBlock / TEAM;
+  const int64_t blocks = (M + kTeams - 1) / kTeams;
+  auto kernel = rows != nullptr ? quant_act_kernel<TEAM, CACHE, true> : quant_act_kernel<TEAM, CACHE, false>;
+  return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kBlock), 0, stream, true,
+                       static_cast<const uint16_t*>(x), ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err);
 }
 
 }  // namespace
 
-cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K,
-                             int8_t* q, int64_t ldq, float* a_scale, cudaStream_t stream) {
+cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K, int8_t* q,
+                             int64_t ldq, float* a_scale, const int32_t* rows, int64_t M_x, uint32_t* err,
+                             cudaStream_t stream) {
+  if (rows == nullptr) M_x = M;
   // Team size grows with K so that a row fits the team's register cache
   // (TEAM * CACHE * 8 elements); longer rows re-read their tail from L2.
-  if (K <= 32 * 8 * 4) return launch_team<32, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
-  if (K <= 64 * 8 * 4) return launch_team<64, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
-  if (K <= 128 * 8 * 4) return launch_team<128, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
-  return launch_team<256, 9>(x, ldx, inv_s, M, K, q, ldq, a_scale, stream);
+  if (K <= 32 * 8 * 4) return launch_team<32, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
+  if (K <= 64 * 8 * 4) return launch_team<64, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
+  if (K <= 128 * 8 * 4)
+    return launch_team<128, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
+  return launch_team<256, 9>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
 }
 
 }  // namespace prism

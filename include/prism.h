@@ -81,6 +81,7 @@ typedef enum {
 #define PRISM_DEV_ERR_COUNT     2u /* count outside [1, PRISM_MAX_CANDIDATES] */
 #define PRISM_DEV_ERR_ID_RANGE  4u /* candidate id outside [0, V)             */
 #define PRISM_DEV_ERR_DUPLICATE 8u /* the same id twice in one position       */
+#define PRISM_DEV_ERR_ROW_RANGE 16u /* a row index outside the indexed matrix */
 
 /*
  * prism_quant_act -- per-token activation quantisation with SmoothQuant
@@ -96,6 +97,28 @@ typedef enum {
 int prism_quant_act(const void *x_bf16, int64_t ldx, const float *inv_smooth,
                     int64_t M, int64_t K, int8_t *q, int64_t ldq,
                     float *a_scale, void *cuda_stream);
+
+/*
+ * prism_quant_act_rows -- prism_quant_act on selected rows of x: output row i
+ * (q row i, a_scale[i]) is the quantisation of x row rows[i].  For the last
+ * layer restricted to the positions needed for answers (StartLux-Prism,
+ * "Compute shared evidence once"): every step is per token, so the results
+ * are the full layer's rows at those positions, bit for bit.
+ *
+ *   x_bf16, ldx, M_x  [M_x, K] bf16, all positions (alignment as prism_quant_act)
+ *   rows, n_rows      [n_rows] int32 device indices into x, any order,
+ *                     repeats allowed (4-byte aligned)
+ *   inv_smooth, K, q, ldq, a_scale   as prism_quant_act, with n_rows rows out
+ *   dev_error_word    device uint32 or NULL: an index outside [0, M_x) ORs
+ *                     in PRISM_DEV_ERR_ROW_RANGE and that row comes out as
+ *                     q = 0, a_scale = NaN (so a linear on it gives NaN).
+ *   n_rows == 0 enqueues nothing.
+ */
+int prism_quant_act_rows(const void *x_bf16, int64_t ldx, int64_t M_x,
+                         const int32_t *rows, int64_t n_rows,
+                         const float *inv_smooth, int64_t K, int8_t *q,
+                         int64_t ldq, float *a_scale, uint32_t *dev_error_word,
+                         void *cuda_stream);
 
 /*
  * Bytes of workspace prism_w8a8_linear needs for this shape and split-K
@@ -145,6 +168,32 @@ int prism_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
                       int64_t ldo, int32_t *acc_out, int64_t M, int64_t N,
                       int64_t K, int split_k, void *workspace,
                       size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * prism_w8a8_linear_rows -- prism_w8a8_linear whose residual row for output
+ * row m is residual row residual_rows[m]: the residual add of a layer
+ * restricted to answer positions, reading the full hidden state's rows
+ * (StartLux-Prism, "Compute shared evidence once").  Output row m equals row
+ * residual_rows[m] of the full layer's output when q row m is that
+ * position's quantised input.
+ *
+ *   residual_bf16, ldr, M_res  [M_res, N] bf16, required (not NULL)
+ *   residual_rows              [M] int32 device indices (4-byte aligned)
+ *   dev_error_word             device uint32 or NULL: an index outside
+ *                              [0, M_res) ORs in PRISM_DEV_ERR_ROW_RANGE and
+ *                              that output row becomes NaN (bf16 0x7fc0)
+ *   out must not overlap the residual (output rows may be other tiles'
+ *   residual rows).  Every other argument, the workspace rules and the
+ *   alignment rules are those of prism_w8a8_linear.
+ */
+int prism_w8a8_linear_rows(const int8_t *q, int64_t ldq, const float *a_scale,
+                           const int8_t *w, int64_t ldw, const float *w_scale,
+                           const void *residual_bf16, int64_t ldr, int64_t M_res,
+                           const int32_t *residual_rows, void *out_bf16,
+                           int64_t ldo, int32_t *acc_out, int64_t M, int64_t N,
+                           int64_t K, int split_k, void *workspace,
+                           size_t workspace_bytes, uint32_t *dev_error_word,
+                           void *cuda_stream);
 
 /* Size of the fixed scratch array compiled into libprism.so for
  * prism_w8a8_linear_noalloc.  Every GPU that loads the library reserves it
