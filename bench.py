@@ -651,6 +651,73 @@ def run_kernel_requant(args):
     return 0
 
 
+def answer_rows(M: int, P: int) -> np.ndarray:
+    """P answer positions among M tokens: the last token of each of P
+    16-token questions at the end of the sequence when they fit (256
+    evidence tokens + 3 x 16 question tokens for M = 304), else the last
+    token of P equal segments."""
+    if M >= 16 * P + 1:
+        return np.array([M - 1 - 16 * (P - 1 - i) for i in range(P)], np.int32)
+    return np.array([(i + 1) * M // P - 1 for i in range(P)], np.int32)
+
+
+def run_kernel_restricted(args):
+    """The last layer's projection restricted to the answer positions
+    (gathered quantisation + linear with the residual rows of the full hidden
+    state) against the same projection on every position; --case is the
+    linear case (default the o_proj shape), --rows the number of answer
+    positions (default 3)."""
+    import torch
+
+    import deterministic_w8a8_int8_gb300 as prism
+
+    dev = torch.device("cuda", 0)
+    c = wl.make_linear(args.case)
+    M, K, N = c.M, c.K, c.N
+    P = 3 if args.rows is None else args.rows
+    rows = torch.from_numpy(answer_rows(M, P)).to(dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x = torch.from_numpy(c.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    inv = t(c.inv_s)
+    n_rot = max(1, int(np.ceil(3 * 129e6 / (N * K))))
+    Ws = [t(c.w) for _ in range(n_rot)]
+    S = t(c.w_scale)
+    res = c.residual_bits if c.residual_bits is not None else wl.bf16_bits(
+        np.random.default_rng(1).standard_normal((M, N), dtype=np.float32))
+    R = torch.from_numpy(res.view(np.int16)).view(torch.bfloat16).to(dev)
+    qr = torch.empty((P, K), dtype=torch.int8, device=dev)
+    ar = torch.empty((P,), dtype=torch.float32, device=dev)
+    outr = torch.empty((P, N), dtype=torch.bfloat16, device=dev)
+    wsr = prism.new_workspace(P, N, K, 0, dev)
+    qf = torch.empty((M, K), dtype=torch.int8, device=dev)
+    af = torch.empty((M,), dtype=torch.float32, device=dev)
+    outf = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    wsf = prism.new_workspace(M, N, K, 0, dev)
+
+    def restricted(i):
+        prism.prism_quant_act_rows(x, rows, inv, q=qr, a_scale=ar)
+        prism.prism_w8a8_linear_rows(qr, ar, Ws[i % n_rot], S, R, rows, out=outr, workspace=wsr)
+
+    def full(i):
+        prism.prism_quant_act(x, inv, q=qf, a_scale=af)
+        prism.prism_w8a8_linear(qf, af, Ws[i % n_rot], S, residual=R, out=outf, workspace=wsf)
+
+    n = max(args.steps, n_rot)
+    t_r = graph_time_us([lambda i=i: restricted(i) for i in range(n)])   # per quantise + linear pair
+    t_f = graph_time_us([lambda i=i: full(i) for i in range(n)])
+    torch.cuda.synchronize()
+    assert torch.equal(outr.view(torch.int16), outf[rows.long()].view(torch.int16)), "restricted != full rows"
+    byts = 3 * P * K + 4 * P + P * K + N * K + 4 * N + 4 * P + 4 * P * N
+    hbm, _, _ = load_peaks()
+    print(json.dumps({"kernel": "restricted_last_layer", "case": args.case, "M_full": M, "M_answer": P,
+                      "N": N, "K": K, "restricted_us": t_r, "full_us": t_f, "speedup": t_f / t_r,
+                      "restricted_gbs": byts / t_r / 1e3, "frac_hbm": byts / t_r / 1e3 / hbm,
+                      "check": "restricted output == full output rows (bitwise)",
+                      "timing": "CUDA graph of back-to-back quantise + linear pairs, %d weight copies" % n_rot}),
+          flush=True)
+    return 0
+
+
 def run_kernel_readout(args):
     """Time prism_candidate_readout alone: P answer positions of a 248,000 x
     5120 LM head (several head copies rotated so gathers come from HBM)."""
@@ -707,7 +774,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant"],
+    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted"],
                     help="time one call type alone")
     ap.add_argument("--case", default=None, choices=sorted(wl.LINEAR_CONFIGS) + sorted(wl.REQUANT_CONFIGS),
                     help="workload of --kernel (a linear case; for requant a weight as loaded)")
@@ -723,11 +790,15 @@ def main():
         if args.case not in wl.REQUANT_CONFIGS:
             ap.error("--kernel requant takes --case from " + ", ".join(sorted(wl.REQUANT_CONFIGS)))
         return run_kernel_requant(args)
+    if args.kernel == "restricted":
+        args.case = args.case or "forest_oproj_m304_k5120_n5120"
     args.case = args.case or "forest_qkv_m304_k5120_n15360"
     if args.case not in wl.LINEAR_CONFIGS:
         ap.error("--case must be a linear case for this mode")
     if args.kernel == "quant":
         return run_kernel_quant(args)
+    if args.kernel == "restricted":
+        return run_kernel_restricted(args)
     if args.kernel == "readout":
         return run_kernel_readout(args)
     if args.kernel:
