@@ -182,6 +182,7 @@ int linear_kernel_kind(int64_t M, int64_t N, int64_t K);
 int linear_auto_split(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream);
 int mma_auto_split(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_linear_gemv(const LinearArgs& a, cudaStream_t stream);
 cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream);
 // Sticky device error bits raised by kernels (bounded waits that expired).
 cudaError_t read_and_clear_kernel_error(uint32_t* out);

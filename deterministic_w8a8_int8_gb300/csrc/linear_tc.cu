@@ -1060,17 +1060,24 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   return launch_kernel(kernel, grid, dim3(kThreads), kSmemBytes, stream, a.no_pdl == 0, p, tmA, tmB);
 }
 
-// PRISM_LINEAR_PATH=mma routes the linear to the mma.sync s8 kernel (a
-// diagnostic for cross-checking the two contraction kernels); read per call.
-static bool use_mma_path() {
+// PRISM_LINEAR_PATH=mma routes the linear to the mma.sync s8 kernel and
+// PRISM_LINEAR_PATH=tc keeps calls of few rows on the tcgen05 kernel (both
+// diagnostics for cross-checking the contraction kernels); read per call.
+static bool path_is(const char* name) {
   const char* s = std::getenv("PRISM_LINEAR_PATH");
-  return s != nullptr && std::strcmp(s, "mma") == 0;
+  return s != nullptr && std::strcmp(s, name) == 0;
 }
+static bool use_mma_path() { return path_is("mma"); }
+// Calls of at most this many token rows stream the weights through the
+// dp4a kernel (linear_gemv.cu) unless the tcgen05 kernel is forced.
+constexpr int64_t kGemvMaxM = 8;
+static bool use_gemv_path(int64_t M) { return M <= kGemvMaxM && !path_is("tc") && !path_is("mma"); }
 
 int linear_kernel_kind(int64_t M, int64_t N, int64_t K) {
   (void)K;
   if (M <= 0 || N <= 0) return 0;
   if (use_mma_path()) return 1;
+  if (use_gemv_path(M)) return 4;
   return tc_plan(M, N).swap ? 3 : 2;
 }
 
@@ -1080,6 +1087,7 @@ int linear_auto_split(int64_t M, int64_t N, int64_t K) {
 
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (use_gemv_path(M)) return 0;
   if (use_mma_path() && split == 0) split = mma_auto_split(M, N, K);
   if (split == 0) return tc_balanced_bytes(M, N, K, nullptr);
   return split > 1 ? atomic_bytes(M, N) : 0;
@@ -1087,6 +1095,7 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
 
 size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, size_t cap) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (use_gemv_path(M)) return 0;
   if (use_mma_path() && split == 0) split = mma_auto_split(M, N, K);
   if (split == 0) {
     const size_t need = tc_balanced_bytes(M, N, K, nullptr);
@@ -1097,6 +1106,7 @@ size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, s
 }
 
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream) {
+  if (use_gemv_path(a.M)) return launch_linear_gemv(a, stream);
   if (!use_mma_path()) return launch_linear_tc(a, stream);
   LinearArgs b = a;
   if (b.split == 0) b.split = mma_auto_split(a.M, a.N, a.K);

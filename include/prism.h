@@ -125,8 +125,8 @@ int prism_quant_act_rows(const void *x_bf16, int64_t ldx, int64_t M_x,
  * setting (split_k = 0 means the automatic schedule, as in the linear call:
  * arrival counters plus one int32 accumulator tile per tile it shares between
  * CTAs; about 4*M*N bytes plus counters for split_k > 1).  Returns 0
- * when no workspace is needed (split_k = 1, or an automatic schedule of whole
- * tiles only).
+ * when no workspace is needed (split_k = 1, an automatic schedule of whole
+ * tiles only, or a call of at most 8 rows, which needs no split).
  */
 size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
 
@@ -302,9 +302,11 @@ int prism_last_cuda_error(char *buf, size_t buf_bytes);
  * Which contraction kernel prism_w8a8_linear would launch for this shape:
  * 0 = none (empty); 1 = warp-level mma.sync s8 kernel; 2 = tcgen05 kernel,
  * tokens on the 128-row MMA side; 3 = tcgen05 kernel, output channels on the
- * 128-row side and tokens on the N side (few rows).  The tcgen05 kernel is the
- * default; setting the environment variable PRISM_LINEAR_PATH=mma selects
- * the mma.sync kernel (a diagnostic; results are bit-identical).
+ * 128-row side and tokens on the N side; 4 = weight-streaming dp4a kernel
+ * (calls of at most 8 token rows: decode steps, answer rows).  Kinds 2-4 are
+ * the default; the environment variable PRISM_LINEAR_PATH=mma selects the
+ * mma.sync kernel and PRISM_LINEAR_PATH=tc keeps few-row calls on tcgen05
+ * (diagnostics; results are bit-identical on every kernel).
  */
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K);
 

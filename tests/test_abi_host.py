@@ -124,7 +124,13 @@ def test_workspace_and_dispatch_queries(L):
         assert 0 <= s <= 64   # 0: the balanced schedule of the tensor-core kernel
         if s > 0:
             assert L.prism_w8a8_workspace_bytes(M, N, K, 0) == L.prism_w8a8_workspace_bytes(M, N, K, s)
-        assert L.prism_w8a8_kernel_kind(M, N, K) in (1, 2, 3)
+        assert L.prism_w8a8_kernel_kind(M, N, K) in (1, 2, 3, 4)
+    # calls of at most 8 token rows stream the weights (kind 4), need no workspace
+    for M in (1, 3, 8):
+        assert L.prism_w8a8_kernel_kind(M, 5120, 17408) == 4
+        assert L.prism_w8a8_workspace_bytes(M, 5120, 17408, 0) == 0
+        assert L.prism_w8a8_workspace_bytes(M, 5120, 17408, 16) == 0
+    assert L.prism_w8a8_kernel_kind(9, 5120, 17408) in (2, 3)
     # the balanced schedule keeps partial tiles only when it shares tiles
     assert L.prism_w8a8_workspace_bytes(37, 384, 256, 0) == 0
     assert L.prism_w8a8_workspace_bytes(304, 15360, 5120, 0) > 0

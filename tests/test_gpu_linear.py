@@ -197,9 +197,9 @@ def test_full_size_sampled_parity(cuda_device, name):
 def _with_path(path, fn):
     import os
     old = os.environ.get("PRISM_LINEAR_PATH")
-    if path == "mma":
-        os.environ["PRISM_LINEAR_PATH"] = "mma"
-    else:
+    if path in ("mma", "tc"):
+        os.environ["PRISM_LINEAR_PATH"] = path
+    else:                      # the library's own choice
         os.environ.pop("PRISM_LINEAR_PATH", None)
     try:
         return fn()

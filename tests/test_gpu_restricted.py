@@ -7,7 +7,8 @@ rows at the answer positions (the restriction must not change an answer).
 
 Shapes cover both orientations of the tensor-core kernel (few rows: weights
 on the MMA's M side; many rows: tokens on it), explicit split-K, the
-mma.sync kernel, every quantiser team size, repeated and unordered indices,
+mma.sync kernel, the dp4a weight-streaming kernel that few-row calls take by
+default, every quantiser team size, repeated and unordered indices,
 out-of-range indices (error bit, NaN rows, the rest untouched) and the
 overlap refusal."""
 import ctypes
@@ -40,9 +41,9 @@ def _inputs(M_x, K, N, seed):
 
 def _with_path(path, fn):
     old = os.environ.get("PRISM_LINEAR_PATH")
-    if path == "mma":
-        os.environ["PRISM_LINEAR_PATH"] = "mma"
-    else:
+    if path in ("mma", "tc"):
+        os.environ["PRISM_LINEAR_PATH"] = path
+    else:                      # the library's own choice
         os.environ.pop("PRISM_LINEAR_PATH", None)
     try:
         return fn()
@@ -81,6 +82,8 @@ def test_quant_rows_match_oracle(cuda_device, M_x, K, n):
     (600, 1024, 640, 300, 0, "tc"),       # enough rows for the token-side orientation
     (304, 2048, 1536, 3, 4, "tc"),        # explicit split-K
     (300, 1024, 640, 40, 0, "mma"),       # the mma.sync kernel
+    (304, 5120, 5120, 3, 0, "gemv"),      # the library's choice for 3 rows: the dp4a weight stream
+    (2048, 17408, 5120, 8, 0, "gemv"),
 ])
 def test_restricted_layer_matches_oracle_and_full_rows(cuda_device, M_x, K, N, n, split, path):
     rng, x, inv_s, w, ws, res = _inputs(M_x, K, N, 3 * M_x + N)
