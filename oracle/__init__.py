@@ -62,6 +62,8 @@ def _load():
         P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
         sig = {
             "oracle_quant_act": (None, [P, I64, P, I64, I64, P, I64, P]),
+            "oracle_act_amax": (None, [P, I64, P, I64, I64, P]),
+            "oracle_quant_act_amax": (None, [P, I64, P, P, I64, I64, P, I64, P]),
             "oracle_gemm_s32": (I32, [P, I64, P, I64, I64, I64, I64, P, I64]),
             "oracle_gemm_s32_splitk": (I32, [P, I64, P, I64, I64, I64, I64, I32, P, I64]),
             "oracle_epilogue": (None, [P, I64, P, P, P, I64, I64, I64, P, I64]),
@@ -127,6 +129,46 @@ def quant_act(x_bf16_bits: np.ndarray, inv_s: np.ndarray | None):
     a = np.empty((M,), np.float32)
     _load().oracle_quant_act(_p(x), K, _p(s), M, K, _p(q), K, _p(a))
     return q, a
+
+
+def act_amax(x_bf16_bits: np.ndarray, inv_s: np.ndarray | None) -> np.ndarray:
+    """Per-row max |x * inv_s| (the quantiser's first half), float32 [M]."""
+    x = _c(x_bf16_bits, np.uint16)
+    M, K = x.shape
+    s = None if inv_s is None else _c(inv_s, np.float32)
+    amax = np.empty((M,), np.float32)
+    _load().oracle_act_amax(_p(x), K, _p(s), M, K, _p(amax))
+    return amax
+
+
+def quant_act_amax(x_bf16_bits: np.ndarray, inv_s: np.ndarray | None, amax: np.ndarray):
+    """The quantiser's second half with given row maxima.  Returns (q, a_scale)."""
+    x = _c(x_bf16_bits, np.uint16)
+    M, K = x.shape
+    s = None if inv_s is None else _c(inv_s, np.float32)
+    am = _c(amax, np.float32)
+    q = np.empty((M, K), np.int8)
+    a = np.empty((M,), np.float32)
+    _load().oracle_quant_act_amax(_p(x), K, _p(s), _p(am), M, K, _p(q), K, _p(a))
+    return q, a
+
+
+def tp_row_parallel_linear(x_bf16_bits, inv_s, w, w_scale, residual_bits, bounds):
+    """A row-parallel tensor-parallel linear over the K shards [bounds[r],
+    bounds[r+1]): each rank's shard row maxima, their maximum (the MAX
+    all-reduce), each rank's codes with that maximum, its exact int32 partial
+    contraction, the partials' sum (the SUM all-reduce), then the epilogue.
+    Returns (out bf16 bits, acc int32, per-rank partials)."""
+    amax = np.max(np.stack([act_amax(x_bf16_bits[:, b0:b1], None if inv_s is None else inv_s[b0:b1])
+                            for b0, b1 in zip(bounds[:-1], bounds[1:])]), axis=0)
+    parts, a_scale = [], None
+    for b0, b1 in zip(bounds[:-1], bounds[1:]):
+        q, a_scale = quant_act_amax(x_bf16_bits[:, b0:b1], None if inv_s is None else inv_s[b0:b1], amax)
+        parts.append(gemm_s32(q, w[:, b0:b1]))
+    total = np.sum(np.stack(parts).astype(np.int64), axis=0)
+    assert np.abs(total).max(initial=0) <= 2**31 - 1
+    acc = total.astype(np.int32)
+    return epilogue(acc, a_scale, w_scale, residual_bits), acc, parts
 
 
 def smooth_requant(q: np.ndarray, d_f16_bits: np.ndarray, s: np.ndarray | None):

@@ -115,9 +115,33 @@ int oracle_get_threads(void)
  * A row whose amax is below 2^-120 (all zeros, or so tiny that 127/amax
  * would overflow) quantises to q = 0 with a_scale = 0.
  */
-void oracle_quant_act(const uint16_t *x, int64_t ldx, const float *inv_s,
-                      int64_t M, int64_t K, int8_t *q, int64_t ldq,
-                      float *a_scale)
+/* The two halves of the quantiser.  oracle_act_amax: amax_m = max_k
+ * |x_mk * inv_s_k| (binary32, exact max).  oracle_quant_act_amax: the codes and
+ * scale of each row from a given amax_m, which for one device is the row's
+ * own; a tensor-parallel layer whose ranks hold K-shards of the row passes
+ * the maximum over the ranks' amax, so every rank uses the scale of the
+ * whole row ([P1-bitwise]: the same bits on any number of GPUs). */
+void oracle_act_amax(const uint16_t *x, int64_t ldx, const float *inv_s,
+                     int64_t M, int64_t K, float *amax)
+{
+    int64_t m;
+#pragma omp parallel for schedule(static)
+    for (m = 0; m < M; ++m) {
+        const uint16_t *xr = x + m * ldx;
+        float am = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float xs = bf16_to_float(xr[k]);
+            if (inv_s) xs = xs * inv_s[k];
+            float a = fabsf(xs);
+            if (a > am) am = a;
+        }
+        amax[m] = am;
+    }
+}
+
+void oracle_quant_act_amax(const uint16_t *x, int64_t ldx, const float *inv_s,
+                           const float *amax, int64_t M, int64_t K, int8_t *q,
+                           int64_t ldq, float *a_scale)
 {
     const float tiny = ldexpf(1.0f, -120);
     int64_t m;
@@ -125,19 +149,13 @@ void oracle_quant_act(const uint16_t *x, int64_t ldx, const float *inv_s,
     for (m = 0; m < M; ++m) {
         const uint16_t *xr = x + m * ldx;
         int8_t *qr = q + m * ldq;
-        float amax = 0.0f;
-        for (int64_t k = 0; k < K; ++k) {
-            float xs = bf16_to_float(xr[k]);
-            if (inv_s) xs = xs * inv_s[k];
-            float a = fabsf(xs);
-            if (a > amax) amax = a;
-        }
-        if (!(amax >= tiny)) {
+        const float am = amax[m];
+        if (!(am >= tiny)) {
             for (int64_t k = 0; k < K; ++k) qr[k] = 0;
             a_scale[m] = 0.0f;
             continue;
         }
-        float inv_a = 127.0f / amax;
+        float inv_a = 127.0f / am;
         for (int64_t k = 0; k < K; ++k) {
             float xs = bf16_to_float(xr[k]);
             if (inv_s) xs = xs * inv_s[k];
@@ -146,8 +164,18 @@ void oracle_quant_act(const uint16_t *x, int64_t ldx, const float *inv_s,
             if (t < -127.0f) t = -127.0f;
             qr[k] = (int8_t)t;
         }
-        a_scale[m] = amax / 127.0f;
+        a_scale[m] = am / 127.0f;
     }
+}
+
+void oracle_quant_act(const uint16_t *x, int64_t ldx, const float *inv_s,
+                      int64_t M, int64_t K, int8_t *q, int64_t ldq,
+                      float *a_scale)
+{
+    /* a_scale first holds the row maxima, then the scales (row by row, each
+     * amax is read before its scale overwrites it) */
+    oracle_act_amax(x, ldx, inv_s, M, K, a_scale);
+    oracle_quant_act_amax(x, ldx, inv_s, a_scale, M, K, q, ldq, a_scale);
 }
 
 /* ------------------------------------ SmoothQuant startup requantisation --- */

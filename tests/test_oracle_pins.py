@@ -642,3 +642,55 @@ def test_rows_empty_selection():
     x, inv_s, *_ = _layer_inputs(4)
     q, a, err = oracle.quant_act_rows(x, np.zeros(0, np.int32), inv_s)
     assert q.shape == (0, x.shape[1]) and a.shape == (0,) and err == 0
+
+
+# ------------------------------------------ tensor-parallel integer combine ---
+# StartLux-Prism, "Bitwise consistency is not lossless quantization": with
+# tensor parallelism the int32 partial sums are combined before any scaling,
+# so the layer gives the same bits on any number of GPUs.  A row-parallel
+# rank holds a K-shard of every token row: the ranks agree on the row's
+# scale through a MAX all-reduce of their shard maxima, then SUM their exact
+# partials.
+
+def _tp_inputs(seed, M=24, K=320, N=72):
+    rng = np.random.default_rng(seed)
+    x = wl.bf16_bits(rng.standard_normal((M, K), dtype=np.float32) * 2)
+    x[:, 7] = wl.bf16_bits(rng.standard_normal(M, dtype=np.float32) * 40)   # an outlier channel
+    inv_s = rng.uniform(0.5, 2.0, K).astype(np.float32)
+    w = wl.draw_weights(rng, (N, K), "uniform")
+    ws = rng.uniform(0.001, 0.02, N).astype(np.float32)
+    res = wl.bf16_bits(rng.standard_normal((M, N), dtype=np.float32))
+    return x, inv_s, w, ws, res
+
+
+def test_act_amax_restated_in_numpy():
+    x, inv_s, *_ = _tp_inputs(11)
+    xs = wl.bits_to_f32(x) * inv_s                      # binary32 products, RN
+    assert np.array_equal(oracle.act_amax(x, inv_s).view(np.uint32),
+                          np.abs(xs).max(axis=1).astype(np.float32).view(np.uint32))
+
+
+def test_quant_with_a_larger_shared_amax_restated_in_numpy():
+    """A rank quantises its shard with the whole row's (larger) maximum:
+    q = clip(rint(xs * RN(127 / amax))), scale RN(amax / 127)."""
+    x, inv_s, *_ = _tp_inputs(12)
+    amax = oracle.act_amax(x, inv_s) * np.float32(3.0)
+    q, a = oracle.quant_act_amax(x[:, :100], inv_s[:100], amax)
+    xs = wl.bits_to_f32(x[:, :100]) * inv_s[:100]
+    inv = (np.float32(127.0) / amax).astype(np.float32)
+    ref = np.clip(np.rint((xs * inv[:, None]).astype(np.float32)), -127, 127).astype(np.int8)
+    assert np.array_equal(q, ref)
+    assert np.array_equal(a.view(np.uint32), (amax / np.float32(127.0)).astype(np.float32).view(np.uint32))
+    assert np.abs(q).max() < 127                        # this shard does not hold the row maximum
+
+
+@pytest.mark.parametrize("bounds", [[0, 160, 320], [0, 16, 48, 320], [0, 304, 320], [0, 64, 128, 192, 256, 320]])
+def test_tp_row_parallel_equals_one_device(bounds):
+    x, inv_s, w, ws, res = _tp_inputs(13)
+    q, a = oracle.quant_act(x, inv_s)
+    out1, acc1 = oracle.w8a8_linear(q, a, w, ws, res)
+    out, acc, parts = oracle.tp_row_parallel_linear(x, inv_s, w, ws, res, bounds)
+    assert np.array_equal(acc, acc1)
+    assert np.array_equal(out, out1)
+    # each rank's partial is its shard's own contraction with the shared scale
+    assert len(parts) == len(bounds) - 1 and not np.array_equal(parts[0], acc1)
