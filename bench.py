@@ -718,6 +718,69 @@ def run_kernel_restricted(args):
     return 0
 
 
+def run_kernel_tp(args):
+    """One rank of a row-parallel tensor-parallel layer over --rows ranks
+    (default 2) on --case: its shard maxima, its codes with the shared
+    maximum, its exact int32 partial and the epilogue after the combine,
+    timed on one GPU (the two all-reduces between them are the caller's
+    collectives and are not timed here), next to the one-device layer."""
+    import torch
+
+    import deterministic_w8a8_int8_gb300 as prism
+
+    dev = torch.device("cuda", 0)
+    c = wl.make_linear(args.case)
+    M, K, N = c.M, c.K, c.N
+    world = 2 if args.rows is None else args.rows
+    Kr = K // world
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x = torch.from_numpy(c.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    xr = x[:, :Kr].contiguous()
+    inv = t(c.inv_s)
+    invr = inv[:Kr].contiguous()
+    n_rot = max(1, int(np.ceil(3 * 129e6 / (N * Kr))))
+    Wr = [t(c.w[:, :Kr]) for _ in range(n_rot)]
+    Wf = [t(c.w) for _ in range(max(1, int(np.ceil(3 * 129e6 / (N * K)))))]
+    S = t(c.w_scale)
+    R = None if c.residual_bits is None else torch.from_numpy(c.residual_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    amax = torch.empty((M,), dtype=torch.float32, device=dev)
+    q = torch.empty((M, Kr), dtype=torch.int8, device=dev)
+    a = torch.empty((M,), dtype=torch.float32, device=dev)
+    acc = torch.empty((M, N), dtype=torch.int32, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    # the epilogue reads accumulator copies that together exceed L2 twice over
+    n_acc = max(2, int(np.ceil(2 * 129e6 / (M * N * 4))))
+    accs = [torch.randint(-2**20, 2**20, (M, N), dtype=torch.int32, device=dev) for _ in range(n_acc)]
+    wsr = prism.new_workspace(M, N, Kr, 0, dev)
+    qf = torch.empty((M, K), dtype=torch.int8, device=dev)
+    af = torch.empty((M,), dtype=torch.float32, device=dev)
+    wsf = prism.new_workspace(M, N, K, 0, dev)
+    n = max(args.steps, n_rot)
+    steps = {
+        "act_amax": [lambda: prism.prism_act_amax(xr, invr, amax=amax)] * n,
+        "quant_act_amax": [lambda: prism.prism_quant_act_amax(xr, invr, amax, q=q, a_scale=a)] * n,
+        "gemm_s32": [lambda i=i: prism.prism_w8a8_gemm_s32(q, Wr[i % n_rot], acc=acc, workspace=wsr)
+                     for i in range(n)],
+        "epilogue": [lambda i=i: prism.prism_w8a8_epilogue(accs[i % n_acc], a, S, residual=R, out=out)
+                     for i in range(max(n, n_acc))],
+    }
+    prism.prism_act_amax(xr, invr, amax=amax)
+    us = {k: graph_time_us(v) for k, v in steps.items()}
+    full = graph_time_us([lambda i=i: (prism.prism_quant_act(x, inv, q=qf, a_scale=af),
+                                       prism.prism_w8a8_linear(qf, af, Wf[i % len(Wf)], S, residual=R, out=outf,
+                                                               workspace=wsf))
+                          for i, outf in zip(range(n), [torch.empty_like(out)] * n)])
+    epi_bytes = M * N * (4 + 2 + (2 if R is not None else 0)) + 4 * (M + N)
+    hbm, _, _ = load_peaks()
+    print(json.dumps({"kernel": "tp_row_parallel_rank", "case": args.case, "ranks": world, "M": M, "N": N,
+                      "K_rank": Kr, "rank_us": us, "rank_total_us": sum(us.values()), "one_device_us": full,
+                      "epilogue_gbs": epi_bytes / us["epilogue"] / 1e3,
+                      "epilogue_frac_hbm": epi_bytes / us["epilogue"] / 1e3 / hbm,
+                      "timing": "CUDA graphs of back-to-back calls; collectives not included; the epilogue "
+                                "rotates %d accumulator copies" % n_acc}), flush=True)
+    return 0
+
+
 def run_kernel_readout(args):
     """Time prism_candidate_readout alone: P answer positions of a 248,000 x
     5120 LM head (several head copies rotated so gathers come from HBM)."""
@@ -774,7 +837,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted"],
+    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted", "tp"],
                     help="time one call type alone")
     ap.add_argument("--case", default=None, choices=sorted(wl.LINEAR_CONFIGS) + sorted(wl.REQUANT_CONFIGS),
                     help="workload of --kernel (a linear case; for requant a weight as loaded)")
@@ -799,6 +862,8 @@ def main():
         return run_kernel_quant(args)
     if args.kernel == "restricted":
         return run_kernel_restricted(args)
+    if args.kernel == "tp":
+        return run_kernel_tp(args)
     if args.kernel == "readout":
         return run_kernel_readout(args)
     if args.kernel:

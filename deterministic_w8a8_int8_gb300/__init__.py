@@ -14,6 +14,9 @@ Entry points (same names as the C ABI):
   prism_smooth_requant(q, d, smooth)             -> (w, w_scale)
   prism_quant_act_rows(x, rows, inv_s)           -> (q, a_scale)   answer rows only
   prism_w8a8_linear_rows(q, a_scale, w, w_scale, residual, residual_rows) -> out
+  prism_act_amax, prism_quant_act_amax, prism_w8a8_gemm_s32, prism_w8a8_epilogue
+                                                 the tensor-parallel building blocks
+  tp_row_parallel_linear(x_shard, ...)           those blocks around torch.distributed
   prism_candidate_readout(hidden, ...)           -> (logits, probs)
 """
 from __future__ import annotations
@@ -57,6 +60,10 @@ SIGNATURES = {
     "prism_quant_act_rows": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
     "prism_w8a8_linear_rows": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P,
                                       _I64, _I64, _I64, _I32, _P, _SZ, _P, _P]),
+    "prism_act_amax": (_I32, [_P, _I64, _P, _I64, _I64, _P, _P]),
+    "prism_quant_act_amax": (_I32, [_P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "prism_w8a8_gemm_s32": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "prism_w8a8_epilogue": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I64, _I64, _I64, _P]),
     "prism_status_string": (ctypes.c_char_p, [_I32]),
     "prism_version": (_I32, []),
     "prism_w8a8_kernel_kind": (_I32, [_I64, _I64, _I64]),
@@ -313,6 +320,111 @@ def prism_w8a8_linear_rows(q, a_scale, w, w_scale, residual, residual_rows, out=
         _ptr(acc_out), M, N, K, int(split_k), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
     _check("prism_w8a8_linear_rows", st)
     return out
+
+
+def prism_act_amax(x, inv_s=None, amax=None, stream=None):
+    """Row maxima max_k |x * inv_s| of bf16 ``x`` [M, K] -> float32 [M]."""
+    import torch
+    _require(x, torch.bfloat16, "x", 2)
+    M, K = x.shape
+    if inv_s is not None:
+        _require(inv_s, torch.float32, "inv_s", 1)
+    if amax is None:
+        amax = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _require(amax, torch.float32, "amax", 1)
+    _check("prism_act_amax", lib().prism_act_amax(_ptr(x), x.stride(0), _ptr(inv_s), M, K, _ptr(amax),
+                                                  _stream(stream)))
+    return amax
+
+
+def prism_quant_act_amax(x, inv_s, amax, q=None, a_scale=None, stream=None):
+    """prism_quant_act with given row maxima ``amax`` [M] -> (q, a_scale)."""
+    import torch
+    _require(x, torch.bfloat16, "x", 2)
+    _require(amax, torch.float32, "amax", 1)
+    M, K = x.shape
+    if inv_s is not None:
+        _require(inv_s, torch.float32, "inv_s", 1)
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if a_scale is None:
+        a_scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _require(q, torch.int8, "q", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    _check("prism_quant_act_amax", lib().prism_quant_act_amax(
+        _ptr(x), x.stride(0), _ptr(inv_s), _ptr(amax), M, K, _ptr(q), q.stride(0), _ptr(a_scale), _stream(stream)))
+    return q, a_scale
+
+
+def prism_w8a8_gemm_s32(q, w, acc=None, split_k: int = 0, workspace=None, stream=None):
+    """Exact int32 ``q @ w^T`` -> dense int32 [M, N] (no scaling)."""
+    import torch
+    _require(q, torch.int8, "q", 2)
+    _require(w, torch.int8, "w", 2)
+    M, K = q.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("shape mismatch")
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=q.device)
+    if acc.dtype != torch.int32 or not acc.is_contiguous() or tuple(acc.shape) != (M, N):
+        raise ValueError("acc must be a contiguous [M, N] int32 tensor")
+    if workspace is None:
+        workspace = new_workspace(M, N, K, split_k, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("prism_w8a8_gemm_s32", lib().prism_w8a8_gemm_s32(
+        _ptr(q), q.stride(0), _ptr(w), w.stride(0), _ptr(acc), M, N, K, int(split_k), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+    return acc
+
+
+def prism_w8a8_epilogue(acc, a_scale, w_scale, residual=None, out=None, stream=None):
+    """bf16 out[M, N] from int32 ``acc`` [M, N] with the linear's epilogue."""
+    import torch
+    _require(acc, torch.int32, "acc", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    _require(w_scale, torch.float32, "w_scale", 1)
+    M, N = acc.shape
+    if a_scale.numel() != M or w_scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if residual is not None:
+        _require(residual, torch.bfloat16, "residual", 2)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=acc.device)
+    _require(out, torch.bfloat16, "out", 2)
+    _check("prism_w8a8_epilogue", lib().prism_w8a8_epilogue(
+        _ptr(acc), acc.stride(0), _ptr(a_scale), _ptr(w_scale), _ptr(residual),
+        0 if residual is None else residual.stride(0), _ptr(out), out.stride(0), M, N, _stream(stream)))
+    return out
+
+
+class KernelOps:
+    """The per-rank steps of tp_row_parallel_linear on this library's kernels."""
+    act_amax = staticmethod(lambda x, inv_s: prism_act_amax(x, inv_s))
+    quant_act_amax = staticmethod(lambda x, inv_s, amax: prism_quant_act_amax(x, inv_s, amax))
+    gemm_s32 = staticmethod(lambda q, w: prism_w8a8_gemm_s32(q, w))
+    epilogue = staticmethod(lambda acc, a_scale, w_scale, residual: prism_w8a8_epilogue(acc, a_scale, w_scale,
+                                                                                       residual))
+
+
+def tp_row_parallel_linear(x, inv_s, w, w_scale, residual=None, group=None, ops=KernelOps):
+    """One rank of a row-parallel tensor-parallel W8A8 linear.
+
+    ``x`` [M, K_r] bf16 and ``inv_s`` [K_r] are this rank's columns of the
+    activations, ``w`` [N, K_r] int8 its columns of the weight; ``w_scale``
+    [N] and ``residual`` [M, N] are replicated.  The ranks agree on each
+    token's scale (MAX all-reduce of the shard maxima), contract their shards
+    exactly in int32, add the partial sums (SUM all-reduce) and scale once, so
+    every rank returns the one-device output bit for bit.  ``group`` is a
+    torch.distributed process group (None: the default group); ``ops`` holds
+    the per-rank steps (act_amax, quant_act_amax, gemm_s32, epilogue)."""
+    import torch.distributed as dist
+    amax = ops.act_amax(x, inv_s)
+    dist.all_reduce(amax, op=dist.ReduceOp.MAX, group=group)
+    q, a_scale = ops.quant_act_amax(x, inv_s, amax)
+    acc = ops.gemm_s32(q, w)
+    dist.all_reduce(acc, op=dist.ReduceOp.SUM, group=group)
+    return ops.epilogue(acc, a_scale, w_scale, residual)
 
 
 def prism_w8a8_linear_noalloc(q, a_scale, w, w_scale, residual=None, out=None, acc_out=None,

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <utility>
 
 #include "prism.h"
@@ -126,8 +127,25 @@ cudaError_t launch_kernel(Kernel kernel, dim3 grid, dim3 block, size_t smem, cud
 
 // Internal launchers (one per kernel family), defined in their .cu files.
 namespace prism {
-// rows: null, or output row m quantises x row rows[m] of M_x (err gets
-// PRISM_DEV_ERR_ROW_RANGE for an index outside [0, M_x); may be null).
+// One quantiser call.  rows: null, or output row m quantises x row rows[m]
+// of M_x (err gets PRISM_DEV_ERR_ROW_RANGE for an index outside [0, M_x);
+// may be null).  amax_out: write only the row maxima.  amax_in: quantise
+// with these row maxima.  At most one of rows, amax_out, amax_in.
+struct QuantCall {
+  const void* x;
+  int64_t ldx;
+  const float* inv_s;
+  int64_t M, K;
+  int8_t* q;
+  int64_t ldq;
+  float* a_scale;
+  const int32_t* rows;
+  int64_t M_x;
+  uint32_t* err;
+  float* amax_out;
+  const float* amax_in;
+};
+cudaError_t launch_quant(const QuantCall& c, cudaStream_t stream);
 cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K, int8_t* q,
                              int64_t ldq, float* a_scale, const int32_t* rows, int64_t M_x, uint32_t* err,
                              cudaStream_t stream);
@@ -155,6 +173,7 @@ struct LinearArgs {
   const int32_t* res_rows;  // null, or the residual row of output row m is res_rows[m] ...
   int64_t M_res;            // ... of the residual's M_res rows
   uint32_t* err;            // PRISM_DEV_ERR_* bits (row index out of range), or null
+  int acc_only;             // 1: write only acc_out (dense [M, N] int32); no scales, out, residual
 };
 
 // The residual row of output row m: row m itself, or row res_rows[m] (the
@@ -191,6 +210,11 @@ cudaError_t read_and_clear_kernel_error(uint32_t* out);
 cudaError_t launch_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d, int64_t ldd, const float* s,
                                   int64_t N, int64_t K, int8_t* w, int64_t ldw, float* w_scale,
                                   cudaStream_t stream);
+
+// The epilogue alone on given int32 accumulators (epilogue.cu).
+cudaError_t launch_epilogue(const int32_t* acc, int64_t ldc, const float* a_scale, const float* w_scale,
+                            const uint16_t* residual, int64_t ldr, uint16_t* out, int64_t ldo, int64_t M, int64_t N,
+                            cudaStream_t stream);
 
 cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const int8_t* W,
                            int64_t ldw, const float* lm_scale, int64_t V, int64_t K,

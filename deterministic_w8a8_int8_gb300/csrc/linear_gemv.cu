@@ -31,11 +31,12 @@ __device__ __forceinline__ int dp4a_16(const uint4& a, const uint4& b, int c) {
 }
 
 // MB: token rows rounded up (rows m >= M stay zero and are not written).
-// kRows: residual rows through a.res_rows (see residual_row).
+// kMode: 0 plain; 1 residual rows through a.res_rows (see residual_row); 2
+// only the exact int32 accumulators, into acc_out.
 // R: output channels per group; U: 16-byte chunks per channel in flight per
 // lane; S: warps sharing one group, each over a contiguous 1/S of K (their
 // exact partial sums are added through shared memory).
-template <int MB, bool kRows, int R, int U, int S>
+template <int MB, int kMode, int R, int U, int S>
 __global__ void __launch_bounds__(kThreads)
     linear_gemv_kernel(const __grid_constant__ LinearArgs a) {
   static_assert(MB * R <= 32 && kWarps % S == 0, "shape");
@@ -106,11 +107,15 @@ __global__ void __launch_bounds__(kThreads)
   const int m = lane / R, r = lane % R;
   const int64_t n = n0 + r;
   if (!live || m >= MB || m >= M || n >= a.N) return;
+  if constexpr (kMode == 2) {
+    a.acc_out[m * a.N + n] = mine;
+    return;
+  }
   const float as = __ldg(a.a_scale + m), ws = __ldg(a.w_scale + n);
   uint32_t o;
   if (a.residual != nullptr) {
     uint16_t rv;
-    if constexpr (kRows) {
+    if constexpr (kMode == 1) {
       const uint16_t* rp = residual_row(a, m);
       rv = rp != nullptr ? rp[n] : static_cast<uint16_t>(kBf16NaN);
     } else {
@@ -129,9 +134,9 @@ cudaError_t launch_mb(const LinearArgs& a, cudaStream_t stream) {
   const int64_t groups = (a.N + R - 1) / R;
   constexpr int kGroupsPerCta = kWarps / S;
   const dim3 grid(static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta));
-  if (a.res_rows != nullptr)
-    return launch_kernel(linear_gemv_kernel<MB, true, R, U, S>, grid, dim3(kThreads), 0, stream, a.no_pdl == 0, a);
-  return launch_kernel(linear_gemv_kernel<MB, false, R, U, S>, grid, dim3(kThreads), 0, stream, a.no_pdl == 0, a);
+  auto kernel = a.acc_only ? linear_gemv_kernel<MB, 2, R, U, S>
+                : a.res_rows != nullptr ? linear_gemv_kernel<MB, 1, R, U, S> : linear_gemv_kernel<MB, 0, R, U, S>;
+  return launch_kernel(kernel, grid, dim3(kThreads), 0, stream, a.no_pdl == 0, a);
 }
 
 }  // namespace

@@ -38,8 +38,14 @@ __device__ __forceinline__ int swz(int r, int c) { return r * kBK + ((c ^ ((r >>
 
 __device__ __forceinline__ void store_pair(const LinearArgs& a, int64_t row, int64_t col, int32_t v0,
                                            int32_t v1) {
-  const float as = __ldg(a.a_scale + row);
   const bool two = col + 1 < a.N;
+  if (a.acc_only) {   // a tensor-parallel partial: the exact accumulators only
+    int32_t* cp = a.acc_out + row * a.N + col;
+    cp[0] = v0;
+    if (two) cp[1] = v1;
+    return;
+  }
+  const float as = __ldg(a.a_scale + row);
   if (!a.pair_io) {  // odd row strides or 2-byte-aligned bases: element stores
     const float as1 = __ldg(a.a_scale + row);
 #pragma unroll

@@ -255,13 +255,40 @@ __device__ __forceinline__ void st_shared_v4_if(uint32_t addr, uint32_t a, uint3
 // reverse.  s_as / s_ws hold the tile's a_scale (by token) and w_scale (by
 // channel).  The residual values of the round are all loaded before any
 // output is stored, so an in-place residual (residual == out) is safe.
-// kRows: the residual row of output row m is a.res_rows[m] (compiled only
-// into the kernel instance for row-indexed calls, so the ordinary path keeps
-// its code).
-template <bool kRows>
+// Kernel modes, each compiled into its own instance so that the ordinary
+// path keeps its code: kTcPlain; kTcRows, the residual row of output row m
+// is a.res_rows[m]; kTcAccOnly, only the exact int32 accumulators are
+// written (a tensor-parallel rank's partial sums, scaled after their sum).
+enum TcMode { kTcPlain = 0, kTcRows = 1, kTcAccOnly = 2 };
+
+template <int kMode>
 __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, const float* s_ws, int64_t a0,
                                           int64_t b0, int trow, int cb, const int32_t (&v)[16]) {
   const LinearArgs& a = p.a;
+  if constexpr (kMode == kTcAccOnly) {
+    if (p.swap) {
+      const int64_t n = a0 + trow, mb = b0 + cb * 16;
+      if (n >= a.N) return;
+      const int jn = a.M - mb < 16 ? static_cast<int>(a.M - mb) : 16;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < jn) a.acc_out[(mb + j) * a.N + n] = v[j];
+      return;
+    }
+    const int64_t m = a0 + trow, nb = b0 + cb * 16;
+    if (m >= a.M) return;
+    int32_t* dst = a.acc_out + m * a.N + nb;
+    if (nb + 16 <= a.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        reinterpret_cast<int4*>(dst)[i] = make_int4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (nb + j < a.N) dst[j] = v[j];
+    }
+    return;
+  }
   const bool res = a.residual != nullptr;
   if (p.swap) {
     const int64_t n = a0 + trow, mb = b0 + cb * 16;
@@ -269,7 +296,7 @@ __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, 
     const int jn = a.M - mb < 16 ? static_cast<int>(a.M - mb) : 16;
     const float ws = s_ws[trow];
     float r[16];
-    if constexpr (kRows) {
+    if constexpr (kMode == kTcRows) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         r[j] = 0.f;
@@ -301,7 +328,7 @@ __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, 
   if (p.vec_io && nb + 16 <= a.N) {
     uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
     if (res) {
-      if constexpr (kRows) {
+      if constexpr (kMode == kTcRows) {
         const uint16_t* rp = residual_row(a, m);
         if (rp != nullptr) {
           r0 = *reinterpret_cast<const uint4*>(rp + nb);
@@ -332,7 +359,7 @@ __device__ __forceinline__ void round_out(const TcParams& p, const float* s_as, 
     return;
   }
   float r[16];
-  if constexpr (kRows) {
+  if constexpr (kMode == kTcRows) {
     const uint16_t* rp = res ? residual_row(a, m) : nullptr;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
@@ -452,6 +479,7 @@ __device__ __forceinline__ void shared_tile_ctas(const TcParams& p, int st, int&
 // Worker wt's share of an item's epilogue scales: a_scale of token wt of the
 // tile (wt < 256) or w_scale of channel wt - 256 (0 beyond the tile or matrix).
 __device__ __forceinline__ float item_scale(const TcParams& p, const Item& itm, int bn, int wt) {
+  if (p.a.a_scale == nullptr) return 0.f;   // accumulators only: no scales
   const LinearArgs& a = p.a;
   const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
   if (wt < kBNMax) {
@@ -463,7 +491,7 @@ __device__ __forceinline__ float item_scale(const TcParams& p, const Item& itm, 
   return i < (p.swap ? kBM : bn) && n < a.N ? __ldg(a.w_scale + n) : 0.f;
 }
 
-template <bool kRows>
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
@@ -738,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int l = wt; l < ntok * lines; l += kWorkers) {
             const int r = l / lines;
             const int64_t m = tok0 + r, nn = ch0 + (l - r * lines) * 64;
-            if constexpr (kRows) {
+            if constexpr (kMode == kTcRows) {
               const int64_t src = m < a.M ? __ldg(a.res_rows + m) : -1;
               if (nn < a.N && src >= 0 && src < a.M_res)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(a.residual + src * a.ldr + nn));
@@ -815,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int glast = gc + nchunks - 1;
       if (itm.kind == 0) {
         if (have) {
-          auto out = [&](int cb, const int32_t (&v)[16]) { round_out<kRows>(p, sa, sw, a0, b0, trow, cb, v); };
+          auto out = [&](int cb, const int32_t (&v)[16]) { round_out<kMode>(p, sa, sw, a0, b0, trow, cb, v); };
           ok = drain(glast, nchunks - 1, bn, out, true);
         }
       } else {
@@ -863,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj) __stcg(tacc + slot_index(trow, cb, jj), 0);
             }
-            round_out<kRows>(p, sa, sw, a0, b0, trow, cb, v);
+            round_out<kMode>(p, sa, sw, a0, b0, trow, cb, v);
           }
           if (wt == 0) *counter = 0u;
         }
@@ -1004,7 +1032,8 @@ static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int
 }
 
 static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
-  auto kernel = a.res_rows != nullptr ? linear_tc_kernel<true> : linear_tc_kernel<false>;
+  auto kernel = a.acc_only ? linear_tc_kernel<kTcAccOnly>
+                : a.res_rows != nullptr ? linear_tc_kernel<kTcRows> : linear_tc_kernel<kTcPlain>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   const TcPlan pl = tc_plan(a.M, a.N);

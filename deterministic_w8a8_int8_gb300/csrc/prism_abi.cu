@@ -107,6 +107,83 @@ int prism_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d_f16, in
                                                           static_cast<cudaStream_t>(cuda_stream)));
 }
 
+static int linear_impl(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
+                       const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16,
+                       int64_t ldo, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k,
+                       void* workspace, size_t workspace_bytes, const int32_t* res_rows, int64_t M_res,
+                       uint32_t* err, int acc_only, void* cuda_stream);
+
+int prism_w8a8_gemm_s32(const int8_t* q, int64_t ldq, const int8_t* w, int64_t ldw, int32_t* acc, int64_t M,
+                        int64_t N, int64_t K, int split_k, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream) {
+  return linear_impl(q, ldq, nullptr, w, ldw, nullptr, nullptr, 0, nullptr, 0, acc, M, N, K, split_k, workspace,
+                     workspace_bytes, nullptr, 0, nullptr, 1, cuda_stream);
+}
+
+int prism_w8a8_epilogue(const int32_t* acc, int64_t ldc, const float* a_scale, const float* w_scale,
+                        const void* residual_bf16, int64_t ldr, void* out_bf16, int64_t ldo, int64_t M, int64_t N,
+                        void* cuda_stream) {
+  if (M < 0 || N < 0) return PRISM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return PRISM_OK;
+  if (acc == nullptr || a_scale == nullptr || w_scale == nullptr || out_bf16 == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldc < N || ldo < N || (residual_bf16 != nullptr && ldr < N)) return PRISM_ERR_INVALID_ARG;
+  if (!aligned(acc, 4) || !aligned(a_scale, 4) || !aligned(w_scale, 4) || !aligned(out_bf16, 2) ||
+      (residual_bf16 != nullptr && !aligned(residual_bf16, 2)))
+    return PRISM_ERR_ALIGNMENT;
+  return prism::record_cuda(prism::launch_epilogue(acc, ldc, a_scale, w_scale,
+                                                   static_cast<const uint16_t*>(residual_bf16), ldr,
+                                                   static_cast<uint16_t*>(out_bf16), ldo, M, N,
+                                                   static_cast<cudaStream_t>(cuda_stream)));
+}
+
+static int check_quant_args(const void* x_bf16, int64_t ldx, const float* inv_smooth, int64_t M, int64_t K) {
+  if (M < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (M > 0 && x_bf16 == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldx < K) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+  if (ldx % 8 != 0 || !aligned(x_bf16, 16)) return PRISM_ERR_ALIGNMENT;
+  if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
+  if (M > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  return PRISM_OK;
+}
+
+int prism_act_amax(const void* x_bf16, int64_t ldx, const float* inv_smooth, int64_t M, int64_t K, float* amax,
+                   void* cuda_stream) {
+  const int st = check_quant_args(x_bf16, ldx, inv_smooth, M, K);
+  if (st != PRISM_OK || M == 0) return st;
+  if (amax == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (!aligned(amax, 4)) return PRISM_ERR_ALIGNMENT;
+  prism::QuantCall c{};
+  c.x = x_bf16;
+  c.ldx = ldx;
+  c.inv_s = inv_smooth;
+  c.M = M;
+  c.K = K;
+  c.amax_out = amax;
+  return prism::record_cuda(prism::launch_quant(c, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int prism_quant_act_amax(const void* x_bf16, int64_t ldx, const float* inv_smooth, const float* amax, int64_t M,
+                         int64_t K, int8_t* q, int64_t ldq, float* a_scale, void* cuda_stream) {
+  const int st = check_quant_args(x_bf16, ldx, inv_smooth, M, K);
+  if (st != PRISM_OK || M == 0) return st;
+  if (amax == nullptr || q == nullptr || a_scale == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldq < K) return PRISM_ERR_INVALID_ARG;
+  if (ldq % 16 != 0 || !aligned(q, 16) || !aligned(a_scale, 4) || !aligned(amax, 4)) return PRISM_ERR_ALIGNMENT;
+  prism::QuantCall c{};
+  c.x = x_bf16;
+  c.ldx = ldx;
+  c.inv_s = inv_smooth;
+  c.M = M;
+  c.K = K;
+  c.q = q;
+  c.ldq = ldq;
+  c.a_scale = a_scale;
+  c.amax_in = amax;
+  return prism::record_cuda(prism::launch_quant(c, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 int prism_quant_act_rows(const void* x_bf16, int64_t ldx, int64_t M_x, const int32_t* rows, int64_t n_rows,
                          const float* inv_smooth, int64_t K, int8_t* q, int64_t ldq, float* a_scale,
                          uint32_t* dev_error_word, void* cuda_stream) {
@@ -140,24 +217,30 @@ size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) 
   return prism::linear_workspace_bytes(M, N, K, split_k);
 }
 
+// acc_only: only the dense int32 accumulators (acc_out) are produced; the
+// scales, residual and output are then NULL and unused.
 static int linear_impl(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
                        const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16,
                        int64_t ldo, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k,
                        void* workspace, size_t workspace_bytes, const int32_t* res_rows, int64_t M_res,
-                       uint32_t* err, void* cuda_stream) {
+                       uint32_t* err, int acc_only, void* cuda_stream) {
   if (M < 0 || N < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
   if (split_k < 0) return PRISM_ERR_INVALID_ARG;
   if (split_k > PRISM_MAX_SPLIT_K) return PRISM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return PRISM_OK;
-  if (q == nullptr || a_scale == nullptr || w == nullptr || w_scale == nullptr || out_bf16 == nullptr)
-    return PRISM_ERR_INVALID_ARG;
-  if (ldq < K || ldw < K || ldo < N || (residual_bf16 != nullptr && ldr < N)) return PRISM_ERR_INVALID_ARG;
+  if (q == nullptr || w == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (acc_only) {
+    if (acc_out == nullptr) return PRISM_ERR_INVALID_ARG;
+  } else {
+    if (a_scale == nullptr || w_scale == nullptr || out_bf16 == nullptr) return PRISM_ERR_INVALID_ARG;
+    if (ldo < N || (residual_bf16 != nullptr && ldr < N)) return PRISM_ERR_INVALID_ARG;
+    if (!aligned(out_bf16, 2) || !aligned(a_scale, 4) || !aligned(w_scale, 4)) return PRISM_ERR_ALIGNMENT;
+  }
+  if (ldq < K || ldw < K) return PRISM_ERR_INVALID_ARG;
   if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
   if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
   if (ldq % 16 != 0 || ldw % 16 != 0) return PRISM_ERR_ALIGNMENT;
-  if (!aligned(q, 16) || !aligned(w, 16) || !aligned(out_bf16, 2) || !aligned(a_scale, 4) ||
-      !aligned(w_scale, 4))
-    return PRISM_ERR_ALIGNMENT;
+  if (!aligned(q, 16) || !aligned(w, 16)) return PRISM_ERR_ALIGNMENT;
   if (residual_bf16 != nullptr && !aligned(residual_bf16, 2)) return PRISM_ERR_ALIGNMENT;
   if (acc_out != nullptr && !aligned(acc_out, 4)) return PRISM_ERR_ALIGNMENT;
   if (M > 65535LL * 128 || N > (1LL << 31) * 64) return PRISM_ERR_UNSUPPORTED;
@@ -182,7 +265,8 @@ static int linear_impl(const int8_t* q, int64_t ldq, const float* a_scale, const
   a.res_rows = res_rows;
   a.M_res = M_res;
   a.err = err;
-  a.pair_io = aligned(out_bf16, 4) && ldo % 2 == 0 &&
+  a.acc_only = acc_only;
+  a.pair_io = !acc_only && aligned(out_bf16, 4) && ldo % 2 == 0 &&
               (residual_bf16 == nullptr || (aligned(residual_bf16, 4) && ldr % 2 == 0));
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need) return PRISM_ERR_WORKSPACE;
@@ -198,7 +282,7 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
                       int64_t ldo, int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k,
                       void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return linear_impl(q, ldq, a_scale, w, ldw, w_scale, residual_bf16, ldr, out_bf16, ldo, acc_out, M, N, K, split_k,
-                     workspace, workspace_bytes, nullptr, 0, nullptr, cuda_stream);
+                     workspace, workspace_bytes, nullptr, 0, nullptr, 0, cuda_stream);
 }
 
 int prism_w8a8_linear_rows(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,
@@ -218,7 +302,7 @@ int prism_w8a8_linear_rows(const int8_t* q, int64_t ldq, const float* a_scale, c
     if (o0 < r1 && r0 < o1) return PRISM_ERR_INVALID_ARG;
   }
   return linear_impl(q, ldq, a_scale, w, ldw, w_scale, residual_bf16, ldr, out_bf16, ldo, acc_out, M, N, K, split_k,
-                     workspace, workspace_bytes, residual_rows, M_res, dev_error_word, cuda_stream);
+                     workspace, workspace_bytes, residual_rows, M_res, dev_error_word, 0, cuda_stream);
 }
 
 int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* inv_smooth,

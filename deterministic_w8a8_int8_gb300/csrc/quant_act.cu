@@ -65,15 +65,20 @@ __device__ __forceinline__ float vmaxabs(const Vec8& r, float m) {
   return m;
 }
 
-// rows != nullptr: output row m quantises x row rows[m] of the M_x rows of x
-// (the last layer restricted to answer positions); an index outside [0, M_x)
-// gives a zero q row, a NaN scale and PRISM_DEV_ERR_ROW_RANGE in *err.
-template <int TEAM, int CACHE, bool kRows>
+// Modes.  kPlain: the quantiser.  kRows: output row m quantises x row
+// rows[m] of the M_x rows of x (the last layer restricted to answer
+// positions); an index outside [0, M_x) gives a zero q row, a NaN scale and
+// PRISM_DEV_ERR_ROW_RANGE in *err.  kAmaxOut: only the row maxima, into
+// amax_io (a tensor-parallel rank's shard maxima).  kAmaxIn: the codes and
+// scale from the given maxima amax_io (the maximum over the ranks).
+enum QuantMode { kPlain = 0, kRows = 1, kAmaxOut = 2, kAmaxIn = 3 };
+
+template <int TEAM, int CACHE, int kMode>
 __global__ void __launch_bounds__(kBlock)
     quant_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, const float* __restrict__ inv_s,
                      int64_t M, int64_t K, int8_t* __restrict__ q, int64_t ldq,
                      float* __restrict__ a_scale, const int32_t* __restrict__ rows, int64_t M_x,
-                     uint32_t* err) {
+                     uint32_t* err, float* __restrict__ amax_io) {
   constexpr int kTeams = kBlock / TEAM;
   constexpr int kWarpsPerTeam = TEAM / 32;
   __shared__ float red[kBlock / 32];
@@ -84,8 +89,8 @@ __global__ void __launch_bounds__(kBlock)
   const int64_t m = static_cast<int64_t>(blockIdx.x) * kTeams + team;
   const bool in_grid = m < M;
   int64_t src = m;
-  if constexpr (kRows) src = in_grid ? __ldg(rows + m) : -1;
-  const bool row_ok = kRows ? (src >= 0 && src < M_x) : in_grid;
+  if constexpr (kMode == kRows) src = in_grid ? __ldg(rows + m) : -1;
+  const bool row_ok = kMode == kRows ? (src >= 0 && src < M_x) : in_grid;
   const bool active = in_grid && row_ok;
   const uint16_t* xr = x + (active ? src : 0) * ldx;
   const int64_t nvec = K >> 3;
@@ -101,8 +106,9 @@ __global__ void __launch_bounds__(kBlock)
         amax = vmaxabs(cache[c], amax);
       }
     }
-    for (int64_t v = lt + static_cast<int64_t>(CACHE) * TEAM; v < nvec; v += TEAM)
-      amax = vmaxabs(load_smoothed(xr, inv_s, v * 8), amax);
+    if constexpr (kMode != kAmaxIn)
+      for (int64_t v = lt + static_cast<int64_t>(CACHE) * TEAM; v < nvec; v += TEAM)
+        amax = vmaxabs(load_smoothed(xr, inv_s, v * 8), amax);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -114,7 +120,12 @@ __global__ void __launch_bounds__(kBlock)
     for (int i = 0; i < kWarpsPerTeam; ++i) amax = fmaxf(amax, red[w0 + i]);
   }
   if (!in_grid) return;
-  if (kRows && !row_ok) {
+  if constexpr (kMode == kAmaxOut) {
+    if (lt == 0) amax_io[m] = amax;
+    return;
+  }
+  if constexpr (kMode == kAmaxIn) amax = __ldg(amax_io + m);
+  if (kMode == kRows && !row_ok) {
     int8_t* qr = q + m * ldq;
     for (int64_t v = lt; v < (K >> 3); v += TEAM) *reinterpret_cast<uint2*>(qr + v * 8) = make_uint2(0u, 0u);
     if (lt == 0) {
@@ -150,29 +161,46 @@ __global__ void __launch_bounds__(kBlock)
 }
 
 template <int TEAM, int CACHE>
-cudaError_t launch_team(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K, int8_t* q,
-                        int64_t ldq, float* a_scale, const int32_t* rows, int64_t M_x, uint32_t* err,
-                        cudaStream_t stream) {
+cudaError_t launch_team(const QuantCall& c, cudaStream_t stream) {
   constexpr int kTeams = kBlock / TEAM;
-  const int64_t blocks = (M + kTeams - 1) / kTeams;
-  auto kernel = rows != nullptr ? quant_act_kernel<TEAM, CACHE, true> : quant_act_kernel<TEAM, CACHE, false>;
+  const int64_t blocks = (c.M + kTeams - 1) / kTeams;
+  auto kernel = c.rows != nullptr      ? quant_act_kernel<TEAM, CACHE, kRows>
+                : c.amax_out != nullptr ? quant_act_kernel<TEAM, CACHE, kAmaxOut>
+                : c.amax_in != nullptr  ? quant_act_kernel<TEAM, CACHE, kAmaxIn>
+                                        : quant_act_kernel<TEAM, CACHE, kPlain>;
+  float* amax_io = c.amax_out != nullptr ? c.amax_out : const_cast<float*>(c.amax_in);
   return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kBlock), 0, stream, true,
-                       static_cast<const uint16_t*>(x), ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err);
+                       static_cast<const uint16_t*>(c.x), c.ldx, c.inv_s, c.M, c.K, c.q, c.ldq, c.a_scale, c.rows,
+                       c.rows != nullptr ? c.M_x : c.M, c.err, amax_io);
 }
 
 }  // namespace
 
+cudaError_t launch_quant(const QuantCall& c, cudaStream_t stream) {
+  // Team size grows with K so that a row fits the team's register cache
+  // (TEAM * CACHE * 8 elements); longer rows re-read their tail from L2.
+  if (c.K <= 32 * 8 * 4) return launch_team<32, 4>(c, stream);
+  if (c.K <= 64 * 8 * 4) return launch_team<64, 4>(c, stream);
+  if (c.K <= 128 * 8 * 4) return launch_team<128, 4>(c, stream);
+  return launch_team<256, 9>(c, stream);
+}
+
 cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K, int8_t* q,
                              int64_t ldq, float* a_scale, const int32_t* rows, int64_t M_x, uint32_t* err,
                              cudaStream_t stream) {
-  if (rows == nullptr) M_x = M;
-  // Team size grows with K so that a row fits the team's register cache
-  // (TEAM * CACHE * 8 elements); longer rows re-read their tail from L2.
-  if (K <= 32 * 8 * 4) return launch_team<32, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
-  if (K <= 64 * 8 * 4) return launch_team<64, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
-  if (K <= 128 * 8 * 4)
-    return launch_team<128, 4>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
-  return launch_team<256, 9>(x, ldx, inv_s, M, K, q, ldq, a_scale, rows, M_x, err, stream);
+  QuantCall c{};
+  c.x = x;
+  c.ldx = ldx;
+  c.inv_s = inv_s;
+  c.M = M;
+  c.K = K;
+  c.q = q;
+  c.ldq = ldq;
+  c.a_scale = a_scale;
+  c.rows = rows;
+  c.M_x = M_x;
+  c.err = err;
+  return launch_quant(c, stream);
 }
 
 }  // namespace prism

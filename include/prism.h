@@ -195,6 +195,56 @@ int prism_w8a8_linear_rows(const int8_t *q, int64_t ldq, const float *a_scale,
                            size_t workspace_bytes, uint32_t *dev_error_word,
                            void *cuda_stream);
 
+/*
+ * Tensor-parallel building blocks (StartLux-Prism, "Bitwise consistency is
+ * not lossless quantization": with tensor parallelism the int32 partial sums
+ * are combined before scaling, so a layer gives the same bits on any number
+ * of GPUs).  A row-parallel layer whose rank r holds columns [k_r, k_r+1) of
+ * the activations and of the weight runs
+ *     prism_act_amax       on its activation shard        -> amax[M]
+ *     MAX all-reduce of amax across the ranks (exact)
+ *     prism_quant_act_amax on its shard with that amax    -> q, a_scale
+ *     prism_w8a8_gemm_s32  on its shard                   -> acc[M, N] int32
+ *     SUM all-reduce of acc across the ranks (exact: integers)
+ *     prism_w8a8_epilogue  on the sum                     -> out[M, N]
+ * and every rank ends with the one-device layer's output, bit for bit.  The
+ * collectives are the caller's (NCCL or any other integer/float reduction).
+ */
+
+/* amax[m] = max_k |x[m, k] * inv_smooth[k]| (binary32, exact max): the first
+ * half of prism_quant_act.  Arguments and alignment as prism_quant_act;
+ * amax [M] float32 out, 4-byte aligned.  M == 0 enqueues nothing. */
+int prism_act_amax(const void *x_bf16, int64_t ldx, const float *inv_smooth,
+                   int64_t M, int64_t K, float *amax, void *cuda_stream);
+
+/* The second half of prism_quant_act: q and a_scale of each row from the
+ * given amax[m] (rows below 2^-120 give q = 0, a_scale = 0), the codes
+ * rint_even(x * inv_s * RN(127 / amax)) clamped to +-127.  With amax the
+ * maximum over a row's shards, each rank's codes are the full row's codes
+ * for its columns.  Arguments and alignment as prism_quant_act. */
+int prism_quant_act_amax(const void *x_bf16, int64_t ldx, const float *inv_smooth,
+                         const float *amax, int64_t M, int64_t K, int8_t *q,
+                         int64_t ldq, float *a_scale, void *cuda_stream);
+
+/* acc[M, N] = q @ w^T exactly in int32 (dense, row stride N, 4-byte aligned;
+ * 16-byte aligned and N % 4 == 0 takes vector stores), no scaling: a rank's
+ * partial sums.  q, w, split_k, workspace and alignment as prism_w8a8_linear. */
+int prism_w8a8_gemm_s32(const int8_t *q, int64_t ldq, const int8_t *w,
+                        int64_t ldw, int32_t *acc, int64_t M, int64_t N,
+                        int64_t K, int split_k, void *workspace,
+                        size_t workspace_bytes, void *cuda_stream);
+
+/* out[m, n] = bf16_rne(((float(acc[m, n]) * a_scale[m]) * w_scale[n])
+ *                      [+ residual[m, n]]) -- the linear's epilogue, one
+ * binary32 RN operation per step, on given int32 accumulators [M, N] (row
+ * stride ldc >= N).  residual may be NULL or the same buffer as out.
+ * Alignment: acc, a_scale, w_scale 4 bytes, out and residual 2 bytes (16
+ * bytes with ldc % 4 == 0 and ldo, ldr % 8 == 0 take vector accesses). */
+int prism_w8a8_epilogue(const int32_t *acc, int64_t ldc, const float *a_scale,
+                        const float *w_scale, const void *residual_bf16,
+                        int64_t ldr, void *out_bf16, int64_t ldo, int64_t M,
+                        int64_t N, void *cuda_stream);
+
 /* Size of the fixed scratch array compiled into libprism.so for
  * prism_w8a8_linear_noalloc.  Every GPU that loads the library reserves it
  * until the process exits. */
