@@ -748,9 +748,12 @@ def run_kernel_tp(args):
     a = torch.empty((M,), dtype=torch.float32, device=dev)
     acc = torch.empty((M, N), dtype=torch.int32, device=dev)
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    # the epilogue reads accumulator copies that together exceed L2 twice over
-    n_acc = max(2, int(np.ceil(2 * 129e6 / (M * N * 4))))
+    # the epilogue rotates accumulator, residual and output copies that
+    # together exceed L2 twice over
+    n_acc = max(2, int(np.ceil(2 * 129e6 / (M * N * 8))))
     accs = [torch.randint(-2**20, 2**20, (M, N), dtype=torch.int32, device=dev) for _ in range(n_acc)]
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(n_acc)]
+    Rs = [None if R is None else R.clone() for _ in range(n_acc)]
     wsr = prism.new_workspace(M, N, Kr, 0, dev)
     qf = torch.empty((M, K), dtype=torch.int8, device=dev)
     af = torch.empty((M,), dtype=torch.float32, device=dev)
@@ -761,7 +764,8 @@ def run_kernel_tp(args):
         "quant_act_amax": [lambda: prism.prism_quant_act_amax(xr, invr, amax, q=q, a_scale=a)] * n,
         "gemm_s32": [lambda i=i: prism.prism_w8a8_gemm_s32(q, Wr[i % n_rot], acc=acc, workspace=wsr)
                      for i in range(n)],
-        "epilogue": [lambda i=i: prism.prism_w8a8_epilogue(accs[i % n_acc], a, S, residual=R, out=out)
+        "epilogue": [lambda i=i: prism.prism_w8a8_epilogue(accs[i % n_acc], a, S, residual=Rs[i % n_acc],
+                                                           out=outs[i % n_acc])
                      for i in range(max(n, n_acc))],
     }
     prism.prism_act_amax(xr, invr, amax=amax)
@@ -777,7 +781,7 @@ def run_kernel_tp(args):
                       "epilogue_gbs": epi_bytes / us["epilogue"] / 1e3,
                       "epilogue_frac_hbm": epi_bytes / us["epilogue"] / 1e3 / hbm,
                       "timing": "CUDA graphs of back-to-back calls; collectives not included; the epilogue "
-                                "rotates %d accumulator copies" % n_acc}), flush=True)
+                                "rotates %d accumulator / residual / output copies" % n_acc}), flush=True)
     return 0
 
 
