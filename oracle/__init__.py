@@ -71,6 +71,8 @@ def _load():
             "oracle_quant_act_rows": (ctypes.c_uint32, [P, I64, I64, P, I64, P, I64, P, I64, P]),
             "oracle_w8a8_linear_rows": (I32, [P, I64, P, P, I64, P, P, I64, I64, P, I64, I64, I64, P, I64,
                                               P, P]),
+            "oracle_unpack_w4": (None, [P, I64, I64, I64, P, I64]),
+            "oracle_w4a8_linear": (I32, [P, I64, P, P, I64, P, P, I64, I64, I64, I64, P, I64, P, P]),
             "oracle_exp": (F, [F]),
             "oracle_exp_batch": (None, [P, I64, P]),
             "oracle_candidate_readout": (I32, [P, I64, P, P, I64, P, I64, I64, P, P, I64, I64, P, P]),
@@ -248,6 +250,36 @@ def w8a8_linear(q, a_scale, w, w_scale, residual_bits=None):
     acc = np.empty((M, N), np.int32)
     rc = _load().oracle_w8a8_linear(_p(q), K, _p(a), _p(w), K, _p(ws), _p(r), N,
                                     M, N, K, _p(out), N, _p(acc))
+    if rc:
+        raise OverflowError("int32 accumulator overflow")
+    return out, acc
+
+
+def unpack_w4(w4: np.ndarray, K: int) -> np.ndarray:
+    """Packed 4-bit codes uint8 [N, K/2] (low nibble = even k) -> int8 [N, K]."""
+    w4 = _c(w4, np.uint8)
+    N = w4.shape[0]
+    assert K % 2 == 0 and w4.shape[1] == K // 2
+    w = np.empty((N, K), np.int8)
+    _load().oracle_unpack_w4(_p(w4), K // 2, N, K, _p(w), K)
+    return w
+
+
+def w4a8_linear(q, a_scale, w4, w_scale, residual_bits=None):
+    """The W8A8 linear on packed 4-bit weights.  Returns (out bf16 bits, acc)."""
+    q = _c(q, np.int8)
+    w4 = _c(w4, np.uint8)
+    M, K = q.shape
+    N = w4.shape[0]
+    assert w4.shape[1] == K // 2
+    a = _c(a_scale, np.float32)
+    ws = _c(w_scale, np.float32)
+    r = None if residual_bits is None else _c(residual_bits, np.uint16)
+    out = np.empty((M, N), np.uint16)
+    acc = np.empty((M, N), np.int32)
+    scratch = np.empty((N, K), np.int8)
+    rc = _load().oracle_w4a8_linear(_p(q), K, _p(a), _p(w4), K // 2, _p(ws), _p(r), N, M, N, K,
+                                    _p(out), N, _p(acc), _p(scratch))
     if rc:
         raise OverflowError("int32 accumulator overflow")
     return out, acc

@@ -375,6 +375,39 @@ int oracle_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
     return 0;
 }
 
+/* ------------------------------------------------------------ W4A8 --- */
+/*
+ * [P1-shared] names Q4_K_M weights loaded directly and a W4A8 run; the pages
+ * give no arithmetic.  Reading: 4-bit weights are symmetric per output
+ * channel, codes in [-7, 7] with one binary32 scale per channel (the form a
+ * load-time requantisation leaves, as for Q8_0), packed two per byte: byte j
+ * of a row holds code 2j in its low nibble and code 2j+1 in its high nibble,
+ * each a 4-bit two's complement number.  W4A8 is then the W8A8 linear on the
+ * unpacked codes: the same exact int32 contraction and epilogue.
+ */
+void oracle_unpack_w4(const uint8_t *w4, int64_t ldw4, int64_t N, int64_t K,
+                      int8_t *w, int64_t ldw)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            const unsigned b = w4[n * ldw4 + k / 2];
+            const unsigned nib = (k % 2 == 0) ? (b & 0xfu) : (b >> 4);
+            w[n * ldw + k] = (int8_t)(nib < 8 ? (int)nib : (int)nib - 16);
+        }
+}
+
+int oracle_w4a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
+                       const uint8_t *w4, int64_t ldw4, const float *w_scale,
+                       const uint16_t *residual, int64_t ldr, int64_t M,
+                       int64_t N, int64_t K, uint16_t *out, int64_t ldo,
+                       int32_t *acc_out, int8_t *w_scratch)
+{
+    /* w_scratch: N * K bytes for the unpacked codes */
+    oracle_unpack_w4(w4, ldw4, N, K, w_scratch, K);
+    return oracle_w8a8_linear(q, ldq, a_scale, w_scratch, K, w_scale, residual, ldr,
+                              M, N, K, out, ldo, acc_out);
+}
+
 /* ------------------------------------- restriction to answer positions --- */
 /*
  * [P1-shared]: in the last layer only the positions needed for answers are

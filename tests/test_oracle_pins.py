@@ -694,3 +694,53 @@ def test_tp_row_parallel_equals_one_device(bounds):
     assert np.array_equal(out, out1)
     # each rank's partial is its shard's own contraction with the shared scale
     assert len(parts) == len(bounds) - 1 and not np.array_equal(parts[0], acc1)
+
+
+# ------------------------------------------------------------------- W4A8 ---
+# StartLux-Prism, "Compute shared evidence once" (Q4_K_M files, a W4A8 run):
+# 4-bit codes packed two per byte, then the W8A8 definition on the codes.
+
+def test_unpack_w4_every_byte_restated_with_shifts():
+    b = np.arange(256, dtype=np.uint8)[None, :]
+    got = oracle.unpack_w4(b, 512)
+    lo = (b.astype(np.int8) << 4).astype(np.int8) >> 4        # arithmetic shifts on int8
+    hi = b.astype(np.int8) >> 4
+    want = np.empty((1, 512), np.int8)
+    want[:, 0::2], want[:, 1::2] = lo, hi
+    assert np.array_equal(got, want)
+    assert got.min() == -8 and got.max() == 7
+
+
+def test_pack_then_unpack_is_identity():
+    rng = np.random.default_rng(5)
+    codes = rng.integers(-8, 8, size=(7, 96)).astype(np.int8)
+    assert np.array_equal(oracle.unpack_w4(wl.pack_w4(codes), 96), codes)
+
+
+def test_w4a8_brute_force_from_nibbles():
+    rng = np.random.default_rng(6)
+    M, K, N = 3, 32, 5
+    q = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    w4 = rng.integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    a = rng.uniform(1e-3, 1e-2, M).astype(np.float32)
+    s = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    res = wl.bf16_bits(rng.standard_normal((M, N), dtype=np.float32))
+
+    def nib(byte, high):
+        v = (int(byte) >> 4) if high else (int(byte) & 15)
+        return v - 16 if v >= 8 else v
+    acc = np.array([[sum(int(q[m, k]) * nib(w4[n, k // 2], k % 2) for k in range(K)) for n in range(N)]
+                    for m in range(M)], np.int64)
+    out, acc_o = oracle.w4a8_linear(q, a, w4, s, res)
+    assert np.array_equal(acc_o, acc)
+    assert np.array_equal(out, oracle.epilogue(acc.astype(np.int32), a, s, res))
+
+
+def test_w4a8_extremes_at_max_k():
+    K = 133136
+    q = np.full((2, K), 127, np.int8)
+    q[1] = -127
+    w4 = np.full((2, K // 2), 0x88, np.uint8)                 # every code -8
+    w4[1] = 0x77                                              # every code 7
+    _, acc = oracle.w4a8_linear(q, np.ones(2, np.float32), w4, np.ones(2, np.float32))
+    assert acc.tolist() == [[-K * 127 * 8, K * 127 * 7], [K * 127 * 8, -K * 127 * 7]]

@@ -226,3 +226,18 @@ def q8_0_case(name: str, N: int, K: int, seed: int) -> Q8Case:
 def make_q8_0(name: str) -> Q8Case:
     N, K, seed = REQUANT_CONFIGS[name]
     return q8_0_case(name, N, K, seed)
+
+
+# ------------------------------------------------------------ W4 weights ---
+# 4-bit weights for W4A8: codes clip(rint(2.5 N(0,1)), -7, 7) (symmetric per
+# output channel, the form a load-time requantisation leaves), packed two
+# per byte, code 2j in the low nibble of byte j, code 2j+1 in the high one.
+def draw_w4_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    g = rng.standard_normal(shape, dtype=np.float32) * np.float32(2.5)
+    return np.clip(np.rint(g), -7, 7).astype(np.int8)
+
+
+def pack_w4(codes: np.ndarray) -> np.ndarray:
+    """int8 codes in [-8, 7], [N, K] with K even -> uint8 [N, K/2]."""
+    c = codes.astype(np.int16) & 0xF
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
