@@ -785,6 +785,48 @@ def run_kernel_tp(args):
     return 0
 
 
+def run_kernel_w4a8(args):
+    """W4A8 on packed 4-bit weights of --case's shape (codes drawn like the
+    pages' 4-bit weights; --rows token rows, default 1) next to W8A8 on the
+    same shape, graph-timed on rotated weight copies."""
+    import torch
+
+    import deterministic_w8a8_int8_gb300 as prism
+
+    dev = torch.device("cuda", 0)
+    c = wl.make_linear(args.case)
+    M = 1 if args.rows is None else args.rows
+    K, N = c.K, c.N
+    rng = np.random.default_rng(17)
+    codes = wl.draw_w4_codes(rng, (N, K))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x = torch.from_numpy(c.x_bits[:M].view(np.int16)).view(torch.bfloat16).to(dev)
+    q, a = prism.prism_quant_act(x, t(c.inv_s))
+    S = t(c.w_scale)
+    R = None if c.residual_bits is None else torch.from_numpy(c.residual_bits[:M].view(np.int16)).view(torch.bfloat16).to(dev)
+    n4 = max(1, int(np.ceil(3 * 129e6 / (N * K // 2))))
+    n8 = max(1, int(np.ceil(3 * 129e6 / (N * K))))
+    W4 = [t(wl.pack_w4(codes)) for _ in range(n4)]
+    W8 = [t(codes) for _ in range(n8)]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    need = prism.prism_w4a8_workspace_bytes(M, N, K, 0)
+    ws4 = torch.zeros(need, dtype=torch.uint8, device=dev) if need else None
+    ws8 = prism.new_workspace(M, N, K, 0, dev)
+    n = max(args.steps, n4, n8)
+    t4 = graph_time_us([lambda i=i: prism.prism_w4a8_linear(q, a, W4[i % n4], S, residual=R, out=out,
+                                                            workspace=ws4) for i in range(n)])
+    t8 = graph_time_us([lambda i=i: prism.prism_w8a8_linear(q, a, W8[i % n8], S, residual=R, out=out,
+                                                            workspace=ws8) for i in range(n)])
+    byts = N * K // 2 + M * K + 4 * (M + N) + 2 * M * N * (2 if R is not None else 1)
+    hbm, _, _ = load_peaks()
+    print(json.dumps({"kernel": "prism_w4a8_linear", "case": args.case, "M": M, "N": N, "K": K,
+                      "kind": prism.prism_w8a8_kernel_kind(M, N, K), "w4a8_us": t4, "w8a8_us": t8,
+                      "speedup_vs_w8a8": t8 / t4, "w4a8_gbs": byts / t4 / 1e3,
+                      "frac_hbm": byts / t4 / 1e3 / hbm,
+                      "timing": "CUDA graphs of back-to-back calls, %d / %d weight copies" % (n4, n8)}), flush=True)
+    return 0
+
+
 def run_kernel_readout(args):
     """Time prism_candidate_readout alone: P answer positions of a 248,000 x
     5120 LM head (several head copies rotated so gathers come from HBM)."""
@@ -841,7 +883,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted", "tp"],
+    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted", "tp", "w4a8"],
                     help="time one call type alone")
     ap.add_argument("--case", default=None, choices=sorted(wl.LINEAR_CONFIGS) + sorted(wl.REQUANT_CONFIGS),
                     help="workload of --kernel (a linear case; for requant a weight as loaded)")
@@ -868,6 +910,8 @@ def main():
         return run_kernel_restricted(args)
     if args.kernel == "tp":
         return run_kernel_tp(args)
+    if args.kernel == "w4a8":
+        return run_kernel_w4a8(args)
     if args.kernel == "readout":
         return run_kernel_readout(args)
     if args.kernel:

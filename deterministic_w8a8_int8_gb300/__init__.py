@@ -17,6 +17,8 @@ Entry points (same names as the C ABI):
   prism_act_amax, prism_quant_act_amax, prism_w8a8_gemm_s32, prism_w8a8_epilogue
                                                  the tensor-parallel building blocks
   tp_row_parallel_linear(x_shard, ...)           those blocks around torch.distributed
+  prism_w4a8_linear(q, a_scale, w4, w_scale, ...) -> out   packed 4-bit weights
+  prism_unpack_w4(w4, K)                         -> int8 codes
   prism_candidate_readout(hidden, ...)           -> (logits, probs)
 """
 from __future__ import annotations
@@ -64,6 +66,10 @@ SIGNATURES = {
     "prism_quant_act_amax": (_I32, [_P, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
     "prism_w8a8_gemm_s32": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "prism_w8a8_epilogue": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I64, _I64, _I64, _P]),
+    "prism_w4a8_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "prism_w4a8_linear": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I32,
+                                 _P, _SZ, _P]),
+    "prism_unpack_w4": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P]),
     "prism_status_string": (ctypes.c_char_p, [_I32]),
     "prism_version": (_I32, []),
     "prism_w8a8_kernel_kind": (_I32, [_I64, _I64, _I64]),
@@ -320,6 +326,56 @@ def prism_w8a8_linear_rows(q, a_scale, w, w_scale, residual, residual_rows, out=
         _ptr(acc_out), M, N, K, int(split_k), _ptr(workspace), ws_bytes, _ptr(err), _stream(stream))
     _check("prism_w8a8_linear_rows", st)
     return out
+
+
+def prism_w4a8_workspace_bytes(M: int, N: int, K: int, split_k: int = 0) -> int:
+    return int(lib().prism_w4a8_workspace_bytes(M, N, K, split_k))
+
+
+def prism_w4a8_linear(q, a_scale, w4, w_scale, residual=None, out=None, acc_out=None, split_k: int = 0,
+                      workspace=None, stream=None):
+    """The W8A8 linear on packed 4-bit weights ``w4`` uint8 [N, K/2] (code
+    2j in the low nibble of byte j).  ``workspace``: a zeroed uint8 tensor of
+    prism_w4a8_workspace_bytes bytes (allocated and zeroed when None)."""
+    import torch
+    _require(q, torch.int8, "q", 2)
+    _require(w4, torch.uint8, "w4", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    _require(w_scale, torch.float32, "w_scale", 1)
+    M, K = q.shape
+    N = w4.shape[0]
+    if 2 * w4.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if residual is not None:
+        _require(residual, torch.bfloat16, "residual", 2)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
+    _require(out, torch.bfloat16, "out", 2)
+    if acc_out is not None and (acc_out.dtype != torch.int32 or not acc_out.is_contiguous()
+                                or tuple(acc_out.shape) != (M, N)):
+        raise ValueError("acc_out must be a contiguous [M, N] int32 tensor")
+    if workspace is None:
+        need = prism_w4a8_workspace_bytes(M, N, K, split_k)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device) if need else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("prism_w4a8_linear", lib().prism_w4a8_linear(
+        _ptr(q), q.stride(0), _ptr(a_scale), _ptr(w4), w4.stride(0), _ptr(w_scale), _ptr(residual),
+        0 if residual is None else residual.stride(0), _ptr(out), out.stride(0), _ptr(acc_out), M, N, K,
+        int(split_k), _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
+
+
+def prism_unpack_w4(w4, K: int, w=None, stream=None):
+    """Packed 4-bit codes uint8 [N, K/2] -> int8 [N, K]."""
+    import torch
+    _require(w4, torch.uint8, "w4", 2)
+    N = w4.shape[0]
+    if w is None:
+        w = torch.empty((N, K), dtype=torch.int8, device=w4.device)
+    _require(w, torch.int8, "w", 2)
+    _check("prism_unpack_w4", lib().prism_unpack_w4(_ptr(w4), w4.stride(0), N, K, _ptr(w), w.stride(0),
+                                                    _stream(stream)))
+    return w
 
 
 def prism_act_amax(x, inv_s=None, amax=None, stream=None):

@@ -202,6 +202,12 @@ int linear_auto_split(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream);
 int mma_auto_split(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_linear_gemv(const LinearArgs& a, cudaStream_t stream);
+// W4A8 on few rows: a.w points at packed 4-bit codes [N, K/2] (row stride
+// a.ldw bytes), K % 32 == 0.
+cudaError_t launch_linear_gemv_w4(const LinearArgs& a, cudaStream_t stream);
+// Packed 4-bit codes [N, K/2] -> int8 [N, K] (K % 32 == 0, 16-byte rows).
+cudaError_t launch_unpack_w4(const uint8_t* w4, int64_t ldw4, int64_t N, int64_t K, int8_t* w8, int64_t ldw8,
+                             cudaStream_t stream);
 cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream);
 // Sticky device error bits raised by kernels (bounded waits that expired).
 cudaError_t read_and_clear_kernel_error(uint32_t* out);

@@ -113,6 +113,77 @@ static int linear_impl(const int8_t* q, int64_t ldq, const float* a_scale, const
                        void* workspace, size_t workspace_bytes, const int32_t* res_rows, int64_t M_res,
                        uint32_t* err, int acc_only, void* cuda_stream);
 
+static size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+size_t prism_w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+  if (M <= 0 || N <= 0 || K <= 0 || split_k < 0 || split_k > PRISM_MAX_SPLIT_K) return 0;
+  if (prism::linear_kernel_kind(M, N, K) == 4) return 0;   // few rows: packed weights streamed directly
+  return align256(static_cast<size_t>(N) * static_cast<size_t>(K)) + prism::linear_workspace_bytes(M, N, K, split_k);
+}
+
+int prism_unpack_w4(const uint8_t* w4, int64_t ldw4, int64_t N, int64_t K, int8_t* w, int64_t ldw, void* cuda_stream) {
+  if (N < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (N == 0) return PRISM_OK;
+  if (w4 == nullptr || w == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (K % 32 != 0) return PRISM_ERR_ALIGNMENT;
+  if (ldw4 < K / 2 || ldw < K) return PRISM_ERR_INVALID_ARG;
+  if (ldw4 % 16 != 0 || ldw % 16 != 0 || !aligned(w4, 16) || !aligned(w, 16)) return PRISM_ERR_ALIGNMENT;
+  return prism::record_cuda(prism::launch_unpack_w4(w4, ldw4, N, K, w, ldw, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int prism_w4a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const uint8_t* w4, int64_t ldw4,
+                      const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16, int64_t ldo,
+                      int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k, void* workspace,
+                      size_t workspace_bytes, void* cuda_stream) {
+  if (M < 0 || N < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (split_k < 0) return PRISM_ERR_INVALID_ARG;
+  if (split_k > PRISM_MAX_SPLIT_K) return PRISM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return PRISM_OK;
+  if (w4 == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (K % 32 != 0) return PRISM_ERR_ALIGNMENT;
+  if (ldw4 < K / 2) return PRISM_ERR_INVALID_ARG;
+  if (ldw4 % 16 != 0 || !aligned(w4, 16)) return PRISM_ERR_ALIGNMENT;
+  const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if (prism::linear_kernel_kind(M, N, K) == 4) {
+    // few rows: the dp4a kernel streams the packed codes (the W8A8 call's
+    // argument rules, with the packed row as the weight)
+    if (q == nullptr || a_scale == nullptr || w_scale == nullptr || out_bf16 == nullptr) return PRISM_ERR_INVALID_ARG;
+    if (ldq < K || ldo < N || (residual_bf16 != nullptr && ldr < N)) return PRISM_ERR_INVALID_ARG;
+    if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+    if (ldq % 16 != 0 || !aligned(q, 16) || !aligned(out_bf16, 2) || !aligned(a_scale, 4) || !aligned(w_scale, 4))
+      return PRISM_ERR_ALIGNMENT;
+    if ((residual_bf16 != nullptr && !aligned(residual_bf16, 2)) || (acc_out != nullptr && !aligned(acc_out, 4)))
+      return PRISM_ERR_ALIGNMENT;
+    prism::LinearArgs a{};
+    a.q = q;
+    a.ldq = ldq;
+    a.a_scale = a_scale;
+    a.w = reinterpret_cast<const int8_t*>(w4);
+    a.ldw = ldw4;
+    a.w_scale = w_scale;
+    a.residual = static_cast<const uint16_t*>(residual_bf16);
+    a.ldr = ldr;
+    a.out = static_cast<uint16_t*>(out_bf16);
+    a.ldo = ldo;
+    a.acc_out = acc_out;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    return prism::record_cuda(prism::launch_linear_gemv_w4(a, stream));
+  }
+  // more rows: unpack into the head of the workspace, then the W8A8 kernel
+  // with the rest of it
+  const size_t head = align256(static_cast<size_t>(N) * static_cast<size_t>(K));
+  if (workspace == nullptr || workspace_bytes < head) return PRISM_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PRISM_ERR_ALIGNMENT;
+  int8_t* w8 = static_cast<int8_t*>(workspace);
+  const int st = prism::record_cuda(prism::launch_unpack_w4(w4, ldw4, N, K, w8, K, stream));
+  if (st != PRISM_OK) return st;
+  void* rest = workspace_bytes > head ? static_cast<char*>(workspace) + head : nullptr;
+  return linear_impl(q, ldq, a_scale, w8, K, w_scale, residual_bf16, ldr, out_bf16, ldo, acc_out, M, N, K, split_k,
+                     rest, workspace_bytes - head, nullptr, 0, nullptr, 0, cuda_stream);
+}
+
 int prism_w8a8_gemm_s32(const int8_t* q, int64_t ldq, const int8_t* w, int64_t ldw, int32_t* acc, int64_t M,
                         int64_t N, int64_t K, int split_k, void* workspace, size_t workspace_bytes,
                         void* cuda_stream) {

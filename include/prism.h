@@ -245,6 +245,40 @@ int prism_w8a8_epilogue(const int32_t *acc, int64_t ldc, const float *a_scale,
                         int64_t ldr, void *out_bf16, int64_t ldo, int64_t M,
                         int64_t N, void *cuda_stream);
 
+/*
+ * W4A8 on 4-bit weights (StartLux-Prism, "Compute shared evidence once":
+ * Q4_K_M files and a W4A8 run).  The weight is symmetric per output channel:
+ * codes in [-8, 7] (a load-time requantisation gives [-7, 7]) with one
+ * float32 scale per channel, packed two per byte -- byte j of a row holds
+ * code 2j in its low nibble and code 2j+1 in its high nibble (4-bit two's
+ * complement).  The result is the W8A8 linear's on the unpacked codes, bit
+ * for bit: the same exact int32 contraction and epilogue.
+ *
+ *   w4, ldw4   [N, K/2] packed bytes, row stride ldw4 >= K/2 bytes
+ *              (ldw4 % 16 == 0, 16-byte aligned); K % 32 == 0
+ *   every other argument as prism_w8a8_linear, except the workspace:
+ *   workspace  at least prism_w4a8_workspace_bytes(M, N, K, split_k) bytes,
+ *              256-byte aligned.  Calls of at most 8 rows stream the packed
+ *              codes directly and need none; larger calls unpack the codes
+ *              into its first 256-aligned N*K bytes (rewritten every call)
+ *              and give the rest to the W8A8 kernel, whose part must be
+ *              zero at the first call (zero the whole buffer once).
+ */
+size_t prism_w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+int prism_w4a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
+                      const uint8_t *w4, int64_t ldw4, const float *w_scale,
+                      const void *residual_bf16, int64_t ldr, void *out_bf16,
+                      int64_t ldo, int32_t *acc_out, int64_t M, int64_t N,
+                      int64_t K, int split_k, void *workspace,
+                      size_t workspace_bytes, void *cuda_stream);
+
+/* Packed 4-bit codes [N, K/2] -> int8 codes [N, K] (for callers that keep
+ * an unpacked copy for prism_w8a8_linear).  K % 32 == 0; ldw4, ldw % 16 == 0;
+ * both 16-byte aligned. */
+int prism_unpack_w4(const uint8_t *w4, int64_t ldw4, int64_t N, int64_t K,
+                    int8_t *w, int64_t ldw, void *cuda_stream);
+
 /* Size of the fixed scratch array compiled into libprism.so for
  * prism_w8a8_linear_noalloc.  Every GPU that loads the library reserves it
  * until the process exits. */
