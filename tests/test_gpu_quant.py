@@ -1,6 +1,7 @@
 """GPU parity of prism_quant_act against the CPU oracle: int8 codes and
 per-token scales bit-exact, including ragged, strided, extreme and degenerate
-rows, for every team size and the register-cache / re-read boundary."""
+rows, for every register-cache width of the persistent kernel, the long-row
+kernel beyond it, and many rows per CTA."""
 import numpy as np
 import pytest
 import torch
@@ -35,9 +36,14 @@ def check(x_bits, inv_s, **kw):
     assert np.array_equal(ag.view(np.uint32), ao.view(np.uint32))
 
 
+# The persistent kernel takes rows up to 24576 with C = 1..6 vectors of 8 per
+# thread in teams of up to 512; every width appears, with the 24576 boundary
+# and the long-row kernel past it, and shapes with many rows per CTA (the
+# prefetching row loop: 3000 x 5120, 2048 x 17408).
 @pytest.mark.parametrize("M,K", [(1, 16), (5, 48), (37, 256), (3, 272), (7, 1040), (9, 2064),
-                                 (4, 4112), (3, 8192), (2, 18432), (2, 20016), (64, 17408),
-                                 (304, 5120)])
+                                 (4, 4112), (3, 8192), (40, 12288), (40, 12304), (20, 16384),
+                                 (2, 18432), (2, 20016), (64, 17408), (20, 24576), (8, 24592),
+                                 (304, 5120), (3000, 5120), (2048, 17408)])
 @pytest.mark.parametrize("smooth", [True, False])
 def test_quant_parity_shapes(cuda_device, M, K, smooth):
     rng = np.random.default_rng(M * 7919 + K)

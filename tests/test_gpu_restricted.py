@@ -59,7 +59,8 @@ def _with_path(path, fn):
     (304, 2048, 3),        # 64-thread teams: one request's three answer positions
     (300, 4096, 40),       # 128-thread teams
     (2048, 5120, 192),     # 256-thread teams: 64 clients x 3 answers
-    (64, 17408, 17),       # rows longer than the register cache
+    (64, 17408, 17),       # five vectors per thread
+    (2048, 5120, 2000),    # many gathered rows per CTA (the prefetching row loop)
 ])
 def test_quant_rows_match_oracle(cuda_device, M_x, K, n):
     rng, x, inv_s, *_ = _inputs(M_x, K, 8, M_x + K)
