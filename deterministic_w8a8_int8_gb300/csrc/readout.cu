@@ -72,15 +72,17 @@ __device__ __forceinline__ float smooth(float v, const float* inv_s, int64_t k) 
 }
 
 // Hidden rows of up to kRegK elements are read once into registers; the
-// first candidate row of each warp (up to kRegK bytes) is fetched into
-// registers as soon as its id is known to be in range, so that its memory
-// latency overlaps the quantisation of the hidden row.
+// first 5 KB of each warp's first candidate row (all of a 5120-wide row) are
+// fetched into registers as soon as its id is known to be in range, so that
+// their memory latency overlaps the quantisation of the hidden row (any rest
+// of a longer row is read when the dot product reaches it).  Two CTAs fit on an SM (at most 128
+// registers), so 192 answer positions run in one wave on 152 SMs.
 constexpr int kRegK = 8192;
 constexpr int kHidVec = kRegK / 8 / kThreads;   // uint4 (8 bf16) per thread: 4
-constexpr int kRowVec = kRegK / 16 / 32;        // uint4 (16 int8) per lane: 16
+constexpr int kRowVec = 10;                     // uint4 (16 int8) per lane: 5 KB of the row per warp
 
 template <bool kReg>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     readout_kernel(const uint16_t* __restrict__ h, int64_t ldh, const float* __restrict__ inv_s,
                    const int8_t* __restrict__ W, int64_t ldw, const float* __restrict__ lm_scale,
                    int64_t V, int64_t K, const int32_t* __restrict__ off,
@@ -222,6 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t c = lane + 32 * j;
         if (c < nchunk) acc = dot16(row[j], *reinterpret_cast<const uint4*>(sq + c * 16), acc);
       }
+      for (int64_t c = lane + 32 * kRowVec; c < nchunk; c += 32)
+        acc = dot16(ld_stream_16(wr + c * 16), *reinterpret_cast<const uint4*>(sq + c * 16), acc);
     } else {
       int64_t c = lane;
       for (; c + 32 * 3 < nchunk; c += 32 * 4) {
