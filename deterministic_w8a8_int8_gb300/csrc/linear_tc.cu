@@ -26,12 +26,15 @@
 //   warp 4        TMEM allocator; lane 0 issues every tcgen05.mma;
 //   16 workers    (the other warps, four per TMEM lane quadrant) do all the
 //                 rest: exact int8->f16 widening from the staging ring into
-//                 128-byte-swizzled K-major f16 tiles (3 stages); at each
-//                 1024-K chunk boundary each warp drains its quarter of its
-//                 quadrant's accumulator columns; at the end all 512 threads
-//                 write the tile out.
-// mbarriers: s8_full (TMA transaction count), s8_empty, full and acc_empty
-// (one arrival per worker warp), empty and acc_full (tcgen05.commit).  Worker
+//                 128-byte-swizzled K-major f16 tiles (3 stages), in two
+//                 groups of 8 warps that take alternate stages, so that one
+//                 group's widening overlaps the other's wait for its data;
+//                 at each 1024-K chunk boundary each warp drains its quarter
+//                 of its quadrant's accumulator columns; at the end all 512
+//                 threads write the tile out.
+// mbarriers: s8_full (TMA transaction count), s8_empty and full (one arrival
+// per warp of the stage's group), acc_empty (one per worker warp), empty and
+// acc_full (tcgen05.commit).  Worker
 // warps wait with all 32 lanes polling and agreeing on the outcome, so a warp
 // never splits around a single polling lane.  Every
 // wait is bounded by a 2-second global-timer limit; on expiry the CTA records
@@ -83,8 +86,12 @@ constexpr int kSmemBytes = 1024 + kRingRegion + kBarBytes + kScaleBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;             // fp32 chunk accumulator (single-buffered layout)
 constexpr uint32_t kColI = 256;           // int32 running sum (single-buffered layout)
-constexpr int kSegPerThread = (kBM * 4 + kBNMax * 4) / kWorkers;  // 3 x 16 B per stage
-static_assert((kBM * 4 + kBNMax * 4) % kWorkers == 0 && kWorkers / 4 == kBM, "segment layout");
+// The worker warps form two groups of 8 (two warps per TMEM lane quadrant)
+// that widen alternate stages; a group thread converts 2 passes x 3
+// segments of 16 int8 bytes per stage it owns.
+constexpr int kGroupWarps = kWorkerWarps / 2;
+constexpr int kSegPerThread = 3;
+static_assert(2 * kSegPerThread * kGroupWarps * 32 == (kBM + kBNMax) * 4, "segment layout");
 static_assert((kChunkStages & (kChunkStages - 1)) == 0, "chunk stages must be a power of two");
 constexpr uint32_t kDevErrTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -535,12 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
-      mbar_init(bar_full + 8 * s, kWorkerWarps);
+      mbar_init(bar_full + 8 * s, kGroupWarps);
       mbar_init(bar_empty + 8 * s, 1);
     }
     for (int j = 0; j < nst8; ++j) {
       mbar_init(bar_s8_full + 8 * j, 1);
-      mbar_init(bar_s8_empty + 8 * j, kWorkerWarps);
+      mbar_init(bar_s8_empty + 8 * j, kGroupWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_acc_full + 8 * b, 1);
@@ -671,19 +678,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int slice = warp < kMmaWarp ? 0 : (warp - 1) / 4;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int trow = quad * 32 + lane;                    // this thread's TMEM lane
-    const int seg = wt & 3;
-    // per segment: offset of its 16 int8 bytes in a staging stage, and of
-    // its first 16-byte f16 chunk in an operand stage (the second is that ^
-    // 16), or ~0 when its B row lies beyond the current tile (set per item)
-    uint32_t lo8[kSegPerThread], so[kSegPerThread];
+    // widening: group grp (slices 0, 2 or 1, 3) owns the stages of its
+    // parity in the CTA's stage sequence; group thread gt converts segment
+    // gt % 4 of rows gt / 4 + 64 pass + 128 i of the stacked [A | B] tile
+    const int grp = slice & 1;
+    const int gt = (slice >> 1) * 128 + quad * 32 + lane;
+    const int seg = gt & 3;
+    // per segment of pass 0: offset of its 16 int8 bytes in a staging stage
+    // (pass 1: + 64 rows), and per segment of both passes the offset of its
+    // first 16-byte f16 chunk in an operand stage (the second is that ^ 16),
+    // or ~0 when its B row lies beyond the current tile (set per item)
+    uint32_t lo8[kSegPerThread], so[2 * kSegPerThread];
 #pragma unroll
     for (int i = 0; i < kSegPerThread; ++i) {
-      const int r = (wt >> 2) + i * kBM;
+      const int r = (gt >> 2) + i * kBM;
       const bool is_a = r < kBM;
       const int rr = is_a ? r : r - kBM;
       lo8[i] = (is_a ? 0u : static_cast<uint32_t>(kS8A)) + rr * kBK + seg * 16;
     }
-    auto store_stage = [&](int s, const uint4 (&buf)[kSegPerThread]) {
+    auto store_stage = [&](int s, int pass, const uint4 (&buf)[kSegPerThread]) {
       const uint32_t st_base = sStage + s * kStageBytes;
 #pragma unroll
       for (int i = 0; i < kSegPerThread; ++i) {
@@ -692,8 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         widen4(buf[i].y, w[2], w[3]);
         widen4(buf[i].z, w[4], w[5]);
         widen4(buf[i].w, w[6], w[7]);
-        const bool valid = so[i] != 0xFFFFFFFFu;   // rows beyond the tile lie outside the stage
-        const uint32_t addr = st_base + (valid ? so[i] : 0u);
+        const uint32_t o = so[pass * kSegPerThread + i];
+        const bool valid = o != 0xFFFFFFFFu;   // rows beyond the tile lie outside the stage
+        const uint32_t addr = st_base + (valid ? o : 0u);
         st_shared_v4_if(addr, w[0], w[1], w[2], w[3], valid);
         st_shared_v4_if(addr ^ 16u, w[4], w[5], w[6], w[7], valid);
       }
@@ -734,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool ok = true;
     int gc = 0;                // chunk counter over all items
+    int gst = 0;               // stage counter over all items
     int j = 0, s = 0;
     uint32_t ph8 = 0, ph = 0;  // staging / operand slots and phase parities
     // The epilogue scales of item n sit in buffer n % 2 of s_scale (token
@@ -777,8 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll
-      for (int i = 0; i < kSegPerThread; ++i) {
-        const int r = (wt >> 2) + i * kBM;
+      for (int i = 0; i < 2 * kSegPerThread; ++i) {
+        const int r = (gt >> 2) + (i % kSegPerThread) * kBM + (i / kSegPerThread) * 64;
         const bool is_a = r < kBM;
         const int rr = is_a ? r : r - kBM;
         so[i] = is_a || rr < bn ? (is_a ? 0u : static_cast<uint32_t>(kStageA)) + rr * 128 +
@@ -798,22 +813,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           next_trigger += kChunkStages;
           if (!ok) break;
         }
-        ok = mbar_wait_warp(bar_s8_full + 8 * j, ph8, s_abort);
-        if (!ok) break;
-        uint4 buf[kSegPerThread];
-        const uint32_t s8 = sS8 + j * kS8Bytes;
+        if (((gst + it) & 1) == grp) {
+          // this group's stage: widen it while the other group waits for
+          // the next one
+          ok = mbar_wait_warp(bar_s8_full + 8 * j, ph8, s_abort);
+          if (!ok) break;
+          uint4 buf[kSegPerThread];
+          const uint32_t s8 = sS8 + j * kS8Bytes;
 #pragma unroll
-        for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
-          buf[i] = ld_shared_v4_if(s8 + lo8[i], so[i] != 0xFFFFFFFFu);
-        ok = mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, s_abort);
-        if (!ok) break;
-        store_stage(s, buf);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_full + 8 * s);
-        // released only now: every value read from the staging slot has been
-        // consumed by the widening, so a TMA refill cannot overtake a load
-        if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);
+          for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
+            buf[i] = ld_shared_v4_if(s8 + lo8[i], so[i] != 0xFFFFFFFFu);
+          ok = mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, s_abort);
+          if (!ok) break;
+          store_stage(s, 0, buf);
+#pragma unroll
+          for (int i = 0; i < kSegPerThread; ++i)
+            buf[i] = ld_shared_v4_if(s8 + lo8[i] + 64 * kBK, so[kSegPerThread + i] != 0xFFFFFFFFu);
+          store_stage(s, 1, buf);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_full + 8 * s);
+          // released only now: every value read from the staging slot has
+          // been consumed by the widening, so a TMA refill cannot overtake a
+          // load
+          if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j);
+        }
         if (++j == nst8) {
           j = 0;
           ph8 ^= 1u;
@@ -897,6 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       gc += nchunks;
+      gst += nk;
       s_scale[((n + 1) & 1) * (2 * kBNMax) + wt] = sc_next;
     }
   }
