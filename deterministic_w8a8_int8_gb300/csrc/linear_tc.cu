@@ -67,14 +67,13 @@ namespace {
 constexpr int kMaxStages = 8;            // f16 operand / int8 staging stages (runtime count)
 constexpr int kBM = 128;                  // A rows per tile = TMEM lanes
 constexpr int kBNMax = 256;               // max B rows per tile = MMA N
-constexpr int kBK = 64;                   // K elements per stage (128 B of f16 per row)
+constexpr int kBK = 64;                   // K elements per f16 operand slot (128 B of f16 per row)
 constexpr int kChunkStages = 16;          // 16 * 64 = 1024 K per exact fp32 chunk
 constexpr int kWorkerWarps = 16;          // convert, drain and write out; 4 per TMEM lane quadrant
 constexpr int kWorkers = kWorkerWarps * 32;
 constexpr int kMmaWarp = 4;               // TMEM allocator + MMA issuer
 constexpr int kTmaWarp = 17;              // lane 0 issues the TMA loads
 constexpr int kThreads = kWorkers + 64;   // 576: 18 warps, at most 96 registers each
-constexpr int kS8A = kBM * kBK;           // bytes of one int8 A box (128 rows x 64)
 constexpr int kStageA = kBM * 128;        // bytes of one f16 A stage
 // One 216 KB region holds both rings: f16 operand stages first, then int8
 // staging stages (the int8 ring gets whatever the f16 ring leaves, so that
@@ -101,12 +100,12 @@ struct TcParams {
   int swap;      // 0 normal, 1 swapped
   int bpiece;    // B rows per tile (multiple of 32, <= 256)
   int vec_io;    // vector epilogue loads/stores allowed (16-byte aligned out/residual, ldo/ldr % 8 == 0)
-  int nst;       // f16 operand stages, each (128 + bpiece) x 128 bytes
-  int nst8;      // int8 staging stages, each (128 + bpiece) x 64 bytes
+  int nst;       // f16 operand stages, each kSub slots of (128 + bpiece) x 128 bytes
+  int nst8;      // int8 staging stages, each (128 + bpiece) x 64 kSub bytes
   int sched;     // 0: one tile (K piece) per CTA; 1: balanced schedule (see get_item)
   int gx;        // A blocks of 128 rows (tile index = ty * gx + tx)
   int T;         // tiles
-  int S;         // K stages of 64
+  int S;         // K stages of 64 kSub
   int W;         // balanced schedule: rounds of whole tiles per CTA
   int R;         // balanced schedule: tiles whose K units are shared out
   uint32_t* cnt;   // balanced schedule: arrival counters of the shared tiles (zero between calls)
@@ -498,10 +497,16 @@ __device__ __forceinline__ float item_scale(const TcParams& p, const Item& itm, 
   return i < (p.swap ? kBM : bn) && n < a.N ? __ldg(a.w_scale + n) : 0.f;
 }
 
-template <int kMode>
+// kSub: f16 operand slots (64 K each) per stage.  Stages of 128 K (kSub = 2,
+// narrow tiles) halve the barrier round trips, MMA-issue loop turns and TMA
+// boxes per K (the boxes then carry 128-byte rows).
+template <int kMode, int kSub>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
+  constexpr int kBK8 = kBK * kSub;               // K bytes per staging row
+  constexpr int kS8A = kBM * kBK8;               // bytes of one int8 A box
+  constexpr int kChunkL = kChunkStages / kSub;   // stages per 1024-K chunk
   extern __shared__ uint8_t smem_raw[];
   const LinearArgs& a = p.a;
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -509,9 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (base - raw_addr);
   const int nst = p.nst, nst8 = p.nst8;
   const uint32_t kStageBytes = static_cast<uint32_t>((kBM + p.bpiece) * 128);
-  const uint32_t kS8Bytes = static_cast<uint32_t>((kBM + p.bpiece) * kBK);
-  const uint32_t sStage = base;                               // nst x (A tile | B tile), f16
-  const uint32_t sS8 = sStage + nst * kStageBytes;            // nst8 x (A box | B box), int8
+  const uint32_t kS8Bytes = static_cast<uint32_t>((kBM + p.bpiece) * kBK8);
+  const uint32_t sStage = base;                               // nst x kSub x (A tile | B tile), f16
+  const uint32_t sS8 = sStage + nst * kSub * kStageBytes;     // nst8 x (A box | B box), int8
   const uint32_t bars = base + kRingRegion;
   uint8_t* bar_ptr = smem + (bars - base);
   const uint32_t bar_full = bars;                             // kMaxStages x 8 B each
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nk = itm.k1 - itm.k0;
         const uint32_t idesc = idesc_f16_f32(tile_width(itm.ty));
         for (int it = 0; it < nk; ++it) {
-          const int cpos = it & (kChunkStages - 1);
+          const int cpos = it & (kChunkL - 1);
           if (cpos == 0) {
             // chunk c reuses the D buffer of chunk c - 2 (double-buffered) or
             // c - 1: wait until the workers have drained it
@@ -606,14 +611,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sStage + s * kStageBytes);
-          const uint64_t bd = smem_desc_sw128(sStage + s * kStageBytes + kStageA);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            tc_mma(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc, (cpos | k) != 0 ? 1u : 0u);
+          for (int h = 0; h < kSub; ++h) {
+            const uint64_t ad = smem_desc_sw128(sStage + (s * kSub + h) * kStageBytes);
+            const uint64_t bd = smem_desc_sw128(sStage + (s * kSub + h) * kStageBytes + kStageA);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              tc_mma(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc, (cpos | h | k) != 0 ? 1u : 0u);
+          }
           issued = true;
           tc_commit(bar_empty + 8 * s);
-          if (cpos == kChunkStages - 1 || it == nk - 1) tc_commit(bar_acc_full + 8 * dbar);
+          if (cpos == kChunkL - 1 || it == nk - 1) tc_commit(bar_acc_full + 8 * dbar);
           if (++s == nst) {
             s = 0;
             ph ^= 1u;
@@ -636,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kTmaWarp) {
     // ======================= TMA producer (one thread) ========================
     if (lane == 0) {
-      const uint32_t tx = static_cast<uint32_t>(kS8A + kBK * p.bpiece);
+      const uint32_t tx = static_cast<uint32_t>(kS8A + kBK8 * p.bpiece);
       int j = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -649,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t dst = sS8 + j * kS8Bytes;
-          const int32_t x = it * kBK;
+          const int32_t x = it * kBK8;
           mbar_expect_tx(bar_s8_full + 8 * j, tx);
           tma_load_2d(dst, &tmA, x, ya, bar_s8_full + 8 * j);
           tma_load_2d(dst + kS8A, &tmB, x, yb, bar_s8_full + 8 * j);
@@ -694,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = (gt >> 2) + i * kBM;
       const bool is_a = r < kBM;
       const int rr = is_a ? r : r - kBM;
-      lo8[i] = (is_a ? 0u : static_cast<uint32_t>(kS8A)) + rr * kBK + seg * 16;
+      lo8[i] = (is_a ? 0u : static_cast<uint32_t>(kS8A)) + rr * kBK8 + seg * 16;
     }
     auto store_stage = [&](int s, int pass, const uint4 (&buf)[kSegPerThread]) {
       const uint32_t st_base = sStage + s * kStageBytes;
@@ -800,9 +808,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       static_cast<uint32_t>(((2 * seg) ^ (rr & 7)) * 16)
                                 : 0xFFFFFFFFu;
       }
-      const int nchunks = (nk + kChunkStages - 1) / kChunkStages;
+      const int nchunks = (nk + kChunkL - 1) / kChunkL;
       int next_drain = 0;  // next intermediate chunk to drain
-      int next_trigger = kChunkStages + nst - 1;
+      int next_trigger = kChunkL + nst - 1;
       for (int it = 0; it < nk && ok; ++it) {
         // chunk c's last MMA completes exactly when stage it - nst is
         // released, so drain it here, after the next chunk's first stages
@@ -810,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (next_drain < nchunks - 1 && it == next_trigger) {
           ok = drain(gc + next_drain, next_drain, bn, no_out, false);
           ++next_drain;
-          next_trigger += kChunkStages;
+          next_trigger += kChunkL;
           if (!ok) break;
         }
         if (((gst + it) & 1) == grp) {
@@ -821,15 +829,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 buf[kSegPerThread];
           const uint32_t s8 = sS8 + j * kS8Bytes;
 #pragma unroll
-          for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
-            buf[i] = ld_shared_v4_if(s8 + lo8[i], so[i] != 0xFFFFFFFFu);
-          ok = mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, s_abort);
-          if (!ok) break;
-          store_stage(s, 0, buf);
+          for (int h = 0; h < kSub; ++h) {
 #pragma unroll
-          for (int i = 0; i < kSegPerThread; ++i)
-            buf[i] = ld_shared_v4_if(s8 + lo8[i] + 64 * kBK, so[kSegPerThread + i] != 0xFFFFFFFFu);
-          store_stage(s, 1, buf);
+            for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+              for (int i = 0; i < kSegPerThread; ++i)  // rows beyond the tile lie outside the stage: skip
+                buf[i] = ld_shared_v4_if(s8 + lo8[i] + pass * 64 * kBK8 + h * kBK,
+                                         so[pass * kSegPerThread + i] != 0xFFFFFFFFu);
+              if (h == 0 && pass == 0) {
+                ok = mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, s_abort);
+                if (!ok) break;
+              }
+              store_stage(s * kSub + h, pass, buf);
+            }
+            if (!ok) break;
+          }
+          if (!ok) break;
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_full + 8 * s);
@@ -946,10 +961,11 @@ inline int64_t cdiv(int64_t x, int64_t y) { return (x + y - 1) / y; }
 struct TcPlan {
   int swap;
   int bpiece;
+  int sub;       // f16 operand slots of 64 K per stage (see linear_tc_kernel)
   int64_t grid_x, grid_y;
 };
 
-static TcPlan tc_plan(int64_t M, int64_t N) {
+static TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
   TcPlan pl{};
   pl.swap = M < 512 ? 1 : 0;
   if (pl.swap) {
@@ -964,6 +980,11 @@ static TcPlan tc_plan(int64_t M, int64_t N) {
     pl.grid_x = cdiv(M, kBM);
     pl.grid_y = cdiv(N, 256);
   }
+  // two slots per stage for tiles up to 96 wide: 2 f16 stages and at least 3
+  // int8 stages of 128 K fit the 216 KB ring (measured: 16-96 rows 7-13 %
+  // faster; at 128 and 160 wide only 2 int8 stages fit, and the smaller
+  // staging depth made them 7 % slower)
+  pl.sub = pl.bpiece <= 96 && K >= 128 ? 2 : 1;
   return pl;
 }
 
@@ -977,8 +998,9 @@ struct TcSched {
   int G, W, R;
 };
 
-static TcSched tc_balanced(int64_t T, int64_t S) {
-  constexpr int64_t kSMs = 152, kMinUnits = kChunkStages;
+static TcSched tc_balanced(int64_t T, int64_t S, int sub) {
+  constexpr int64_t kSMs = 152;
+  const int64_t kMinUnits = kChunkStages / sub;
   TcSched sc{static_cast<int>(kSMs), 0, 0};
   if (T % kSMs == 0) {
     sc.W = static_cast<int>(T / kSMs);
@@ -1005,8 +1027,8 @@ static TcSched tc_balanced(int64_t T, int64_t S) {
 // accumulator per shared tile (all zero between calls); none when no tile is
 // shared.
 static size_t tc_balanced_bytes(int64_t M, int64_t N, int64_t K, size_t* counter_bytes) {
-  const TcPlan pl = tc_plan(M, N);
-  const TcSched sc = tc_balanced(pl.grid_x * pl.grid_y, cdiv(K, kBK));
+  const TcPlan pl = tc_plan(M, N, K);
+  const TcSched sc = tc_balanced(pl.grid_x * pl.grid_y, cdiv(K, kBK * pl.sub), pl.sub);
   if (sc.R == 0 || sc.G == sc.R) {
     if (counter_bytes != nullptr) *counter_bytes = 0;
     return 0;
@@ -1042,13 +1064,14 @@ static EncodeTiledFn encode_fn() {
 }
 
 // Row-major int8 [rows, K] matrix with row stride ld bytes, read in boxes of
-// 64 K-bytes x box_rows rows; out-of-range rows and K read as zero.
-static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int64_t K, int64_t ld, int box_rows) {
+// box_k K-bytes x box_rows rows; out-of-range rows and K read as zero.
+static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int64_t K, int64_t ld, int box_rows,
+                            int box_k) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1057,11 +1080,15 @@ static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int
 }
 
 static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
-  auto kernel = a.acc_only ? linear_tc_kernel<kTcAccOnly>
-                : a.res_rows != nullptr ? linear_tc_kernel<kTcRows> : linear_tc_kernel<kTcPlain>;
+  const TcPlan pl = tc_plan(a.M, a.N, a.K);
+  auto kernel = pl.sub == 2 ? (a.acc_only                ? linear_tc_kernel<kTcAccOnly, 2>
+                               : a.res_rows != nullptr ? linear_tc_kernel<kTcRows, 2>
+                                                       : linear_tc_kernel<kTcPlain, 2>)
+                            : (a.acc_only                ? linear_tc_kernel<kTcAccOnly, 1>
+                               : a.res_rows != nullptr ? linear_tc_kernel<kTcRows, 1>
+                                                       : linear_tc_kernel<kTcPlain, 1>);
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
-  const TcPlan pl = tc_plan(a.M, a.N);
   TcParams p{};
   p.a = a;
   p.swap = pl.swap;
@@ -1070,11 +1097,12 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const uintptr_t wb = reinterpret_cast<uintptr_t>(a.w_scale);
   p.vec_io = (ob % 16 == 0) && (a.ldo % 8 == 0) && (wb % 16 == 0) &&
              (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
-  p.nst = 3;
-  p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * (kBM + pl.bpiece) * 128) / ((kBM + pl.bpiece) * kBK));
+  p.nst = pl.sub == 2 ? 2 : 3;
+  p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * pl.sub * (kBM + pl.bpiece) * 128) /
+                                    ((kBM + pl.bpiece) * kBK * pl.sub));
   p.gx = static_cast<int>(pl.grid_x);
   p.T = static_cast<int>(pl.grid_x * pl.grid_y);
-  p.S = static_cast<int>(cdiv(a.K, kBK));
+  p.S = static_cast<int>(cdiv(a.K, kBK * pl.sub));
   dim3 grid;
   if (a.split >= 1) {
     // explicit split-K: one CTA per tile and K piece; int32 atomics when split
@@ -1090,7 +1118,7 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
     // automatic: the balanced schedule, falling back to whole tiles in rounds
     // when the caller's workspace cannot hold the shared tiles' partials
     p.sched = 1;
-    TcSched sc = tc_balanced(p.T, p.S);
+    TcSched sc = tc_balanced(p.T, p.S, pl.sub);
     size_t cb = 0;
     const size_t need = tc_balanced_bytes(a.M, a.N, a.K, &cb);
     if (need > 0 && need > a.ws_bytes) sc = TcSched{152, static_cast<int>(cdiv(p.T, 152)), 0};
@@ -1107,9 +1135,9 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   CUtensorMap tmA, tmB;
   const int8_t* Am = pl.swap ? a.w : a.q;
   const int8_t* Bm = pl.swap ? a.q : a.w;
-  e = make_map(&tmA, Am, pl.swap ? a.N : a.M, a.K, pl.swap ? a.ldw : a.ldq, kBM);
+  e = make_map(&tmA, Am, pl.swap ? a.N : a.M, a.K, pl.swap ? a.ldw : a.ldq, kBM, kBK * pl.sub);
   if (e != cudaSuccess) return e;
-  e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece);
+  e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece, kBK * pl.sub);
   if (e != cudaSuccess) return e;
   return launch_kernel(kernel, grid, dim3(kThreads), kSmemBytes, stream, a.no_pdl == 0, p, tmA, tmB);
 }
@@ -1132,7 +1160,7 @@ int linear_kernel_kind(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0) return 0;
   if (use_mma_path()) return 1;
   if (use_gemv_path(M)) return 4;
-  return tc_plan(M, N).swap ? 3 : 2;
+  return tc_plan(M, N, K).swap ? 3 : 2;
 }
 
 int linear_auto_split(int64_t M, int64_t N, int64_t K) {
