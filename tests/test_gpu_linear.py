@@ -210,7 +210,7 @@ def _with_path(path, fn):
             os.environ["PRISM_LINEAR_PATH"] = old
 
 
-@pytest.mark.parametrize("M", [5, 130, 600])
+@pytest.mark.parametrize("M", [5, 40, 130, 600])
 def test_tensor_core_chunks_exact_at_2_pow_24(cuda_device, M):
     """Every fp32 chunk of <= 1024 products stays an exact integer: all
     +-127 operands (chunk partials up to 1024 * 16129 = 16,516,096) and single
@@ -234,6 +234,26 @@ def test_tensor_core_chunks_exact_at_2_pow_24(cuda_device, M):
         out, acc = gpu_linear(dev(q), dev(a), dev(w), dev(ws), None, split=split)
         assert np.array_equal(host(acc), acco)
         assert np.array_equal(host_bits(out), outo)
+    assert prism.prism_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [9, 96, 97, 128])
+@pytest.mark.parametrize("K", [64, 128, 192, 2064])
+def test_stage_width_boundaries(cuda_device, M, K):
+    """Tensor-core tiles up to 96 wide stream stages of 128 K (two 64-K f16
+    slots per stage, 128-byte TMA rows), wider tiles stages of 64 K: both
+    sides of that width boundary, one whole stage, a half-filled last stage
+    and K below one stage give the oracle's bits, under the automatic
+    schedule and explicit split-K alike."""
+    N = 264
+    xb, w, w_scale, rb = random_problem(M, N, K, 7 * M + K)
+    _, _, outo, acco = oracle_full(xb, None, w, w_scale, rb)
+    q, a = prism.prism_quant_act(dev_bf16(xb))
+    W, S, R = dev(w), dev(w_scale), dev_bf16(rb)
+    for split in (0, 3):
+        out, acc = _with_path("tc", lambda: gpu_linear(q, a, W, S, R, split=split))
+        assert np.array_equal(host(acc), acco), split
+        assert np.array_equal(host_bits(out), outo), split
     assert prism.prism_device_status() == 0
 
 
