@@ -58,6 +58,8 @@ def _with_path(path, fn):
     (304, 2048, 1536, [0, 1024, 2048], 4, "auto"),    # explicit split-K
     (1, 17408, 5120, [0, 4352, 8704, 13056, 17408], 0, "auto"),   # a decode row over four ranks: dp4a kernel
     (8, 5120, 640, [0, 2048, 5120], 0, "auto"),
+    (40, 5120, 1536, [0, 2048, 5120], 0, "auto"),     # tcgen05 accumulator-only mode on 128-K stages
+    (8, 2048, 640, [0, 1024, 2048], 3, "tc"),         # the same, explicit split-K
     (300, 1024, 640, [0, 512, 1024], 0, "mma"),
 ])
 def test_ranks_reproduce_one_device_layer(cuda_device, M, K, N, bounds, split, path):
