@@ -408,6 +408,93 @@ __device__ __forceinline__ void round_atomic(const TcParams& p, int64_t a0, int6
 // contiguous bytes.
 __device__ __forceinline__ int slot_index(int trow, int cb, int j) { return (cb * 16 + j) * kBM + trow; }
 
+// The last arriver's read-back of a shared tile in the swapped orientation
+// (output channels on the TMEM lanes, tokens on the columns): unit u is
+// column c = u / 32 and lanes 4 (u % 32) .. + 3 of the accumulator slot, one
+// 16-byte load; its outputs are 4 consecutive channels n0 .. n0 + 3 of token
+// row m = b0 + c.  A thread loads a batch of units (slots, then residuals)
+// before it writes any, so their L2 round trips overlap; each output element
+// is the same fixed-order epilogue as round_out, and an element's residual
+// is read before its output is written (in-place residual).
+template <int kMode>
+__device__ __forceinline__ void readback_swap(const TcParams& p, const float* s_as, const float* s_ws, int64_t a0,
+                                           int64_t b0, int bn, int32_t* tacc, int wt) {
+  const LinearArgs& a = p.a;
+  const bool res = kMode != kTcAccOnly && a.residual != nullptr;
+  const int units = bn * (kBM / 4);
+  constexpr int kB = 4;
+  for (int u0 = wt; u0 < units; u0 += kB * kWorkers) {
+    int4 v[kB];
+    uint32_t r[kB][2];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int u = u0 + b * kWorkers;
+      v[b] = make_int4(0, 0, 0, 0);
+      r[b][0] = r[b][1] = 0u;
+      if (u >= units) continue;
+      const int c = u / (kBM / 4), r4 = (u % (kBM / 4)) * 4;
+      v[b] = __ldcg(reinterpret_cast<const int4*>(tacc + c * kBM + r4));
+      const int64_t m = b0 + c, n0 = a0 + r4;
+      if (!res || m >= a.M) continue;
+      const uint16_t* rp;
+      if constexpr (kMode == kTcRows) {
+        rp = residual_row(a, m);
+      } else {
+        rp = a.residual + m * a.ldr;
+      }
+      if (rp == nullptr) {
+        r[b][0] = r[b][1] = kBf16NaN * 0x10001u;
+      } else if (p.vec_io && n0 + 4 <= a.N) {
+        const uint2 q = *reinterpret_cast<const uint2*>(rp + n0);
+        r[b][0] = q.x;
+        r[b][1] = q.y;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (n0 + i < a.N) r[b][i >> 1] |= static_cast<uint32_t>(rp[n0 + i]) << (16 * (i & 1));
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int u = u0 + b * kWorkers;
+      if (u >= units) continue;
+      const int c = u / (kBM / 4), r4 = (u % (kBM / 4)) * 4;
+      __stcg(reinterpret_cast<int4*>(tacc + c * kBM + r4), make_int4(0, 0, 0, 0));
+      const int64_t m = b0 + c, n0 = a0 + r4;
+      if (m >= a.M || n0 >= a.N) continue;
+      const int32_t vv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+      const bool quad = n0 + 4 <= a.N;
+      if (a.acc_out != nullptr) {
+        int32_t* dst = a.acc_out + m * a.N + n0;
+        if (quad && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+          *reinterpret_cast<int4*>(dst) = v[b];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (n0 + i < a.N) dst[i] = vv[i];
+        }
+      }
+      if constexpr (kMode == kTcAccOnly) continue;
+      const float as = s_as[c];
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float ws = s_ws[r4 + i];
+        const uint16_t rb = static_cast<uint16_t>(r[b][i >> 1] >> (16 * (i & 1)));
+        o[i] = res ? epilogue_bf16_res(vv[i], as, ws, bf16_bits_to_float(rb)) : epilogue_bf16(vv[i], as, ws);
+      }
+      uint16_t* op = a.out + m * a.ldo + n0;
+      if (p.vec_io && quad) {
+        *reinterpret_cast<uint2*>(op) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (n0 + i < a.N) op[i] = static_cast<uint16_t>(o[i]);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel --
 // One unit of work of a CTA: output tile (tx, ty) -- A block tx of 128 rows,
 // B piece ty of bpiece rows -- over the K stages [k0, k1) of 64.
@@ -909,7 +996,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t* counter = itm.kind == 1 ? a.ws_count + itm.tile : p.cnt + itm.tile;
         if (wt == 0) *s_last = (atomicAdd(counter, 1u) == target);
         asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
-        if (*s_last) {
+        if (*s_last && itm.kind == 2 && p.swap) {
+          __threadfence();
+          readback_swap<kMode>(p, sa, sw, a0, b0, bn, tacc, wt);
+          if (wt == 0) *counter = 0u;
+        } else if (*s_last) {
           __threadfence();
           for (int cb = slice; cb < bn / 16; cb += 4) {
             int32_t v[16];
