@@ -994,7 +994,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (itm.kind == 2) shared_tile_ctas(p, itm.tile, bf, bl);
         const unsigned target = itm.kind == 1 ? static_cast<unsigned>(a.split - 1) : static_cast<unsigned>(bl - bf);
         uint32_t* counter = itm.kind == 1 ? a.ws_count + itm.tile : p.cnt + itm.tile;
-        if (wt == 0) *s_last = (atomicAdd(counter, 1u) == target);
+        // release: every worker's reductions reached thread 0 through the
+        // barrier above; its fence makes them visible at GPU scope before its
+        // arrival.  acquire: the last arriver's fence after the arrival
+        // orders the read-back after every other CTA's reductions.
+        if (wt == 0) {
+          __threadfence();
+          const bool last = atomicAdd(counter, 1u) == target;
+          __threadfence();
+          *s_last = last;
+        }
         asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
         if (*s_last && itm.kind == 2 && p.swap) {
           __threadfence();
