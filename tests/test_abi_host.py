@@ -137,6 +137,49 @@ def test_workspace_and_dispatch_queries(L):
     assert L.prism_w8a8_kernel_kind(0, 5, 16) == 0
 
 
+def _cdiv(x, y):
+    return (x + y - 1) // y
+
+
+def _balanced_workspace_bytes(M, N, K):
+    """The tensor-core kernel's automatic schedule restated: orientation and
+    token-piece width, 64- or 128-K stages, W rounds of whole tiles on the
+    152 SMs and R tiles whose K stages are shared (shares of at least one
+    1024-K chunk), then the bytes of R arrival counters and R int32 tiles."""
+    if M <= 8:                                  # the dp4a weight stream
+        return 0
+    if M < 512:                                 # tokens on the MMA's N side
+        bpiece = _cdiv(_cdiv(M, _cdiv(M, 256)), 32) * 32
+        T = _cdiv(N, 128) * _cdiv(M, bpiece)
+    else:
+        bpiece = 256
+        T = _cdiv(M, 128) * _cdiv(N, 256)
+    sub = 2 if bpiece <= 96 and K >= 128 else 1
+    S, min_units, sms = _cdiv(K, 64 * sub), 16 // sub, 152
+    if T % sms == 0:
+        return 0
+    W, R = T // sms, T % sms
+    if R * S < min_units * sms and W >= 1:
+        W, R = W - 1, R + sms
+    if R * S >= min_units * sms:
+        G = sms
+    elif W == 0:
+        G = max(R, min(sms, R * S // min_units))
+    else:
+        return 0
+    if R == 0 or G == R:
+        return 0
+    return ((R * 4 + 255) & ~255) + R * 128 * bpiece * 4
+
+
+def test_balanced_schedule_workspace_matches_its_statement(L, monkeypatch):
+    monkeypatch.delenv("PRISM_LINEAR_PATH", raising=False)
+    for M in (1, 8, 9, 37, 64, 96, 97, 128, 160, 192, 304, 511, 512, 600, 2048, 8192):
+        for N in (384, 640, 5120, 15360, 34816):
+            for K in (64, 128, 2064, 5120, 17408):
+                assert L.prism_w8a8_workspace_bytes(M, N, K, 0) == _balanced_workspace_bytes(M, N, K), (M, N, K)
+
+
 def ro(L, P=4, T=8, V=100, K=64, h=A, ldh=64, s=None, W=A, ldw=64, sc=A, off=A, ids=A,
        lg=A, pr=A, err=None):
     return L.prism_candidate_readout(h, ldh, s, W, ldw, sc, V, K, off, ids, P, T, lg, pr, err, None)
