@@ -350,7 +350,7 @@ def run_gpu(args):
                                    None, M, No, K, 0, vp(ws_o), wso_b, st)),
             (L.prism_candidate_readout, (vp(hid), hid.stride(0), None, vp(lm_head), K, vp(lm_scale),
                                          wl.VOCAB, K, vp(off), vp(ids), len(ANSWER_ROWS), T_, vp(logits),
-                                         vp(probs), vp(err), st)),
+                                         vp(probs), vp(err), None, 0, st)),
         ]
 
     rot_calls = [calls_for(s) for s in sets]
@@ -876,6 +876,55 @@ def run_kernel_readout(args):
     return 0
 
 
+def run_kernel_int8_peak(args):
+    """The dense int8 rate a library reaches on this GPU, beside bf16: torch's
+    int8 matmul (torch._int_mm, int8 x int8 -> int32) and bf16 torch.matmul,
+    8192^3 each, best of 10 timed calls (burst) and back to back for 4 s
+    (sustained), with SM clocks sampled during the sustained loops.  This is
+    what decides which tensor pipe the exact contraction runs on."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    n = 8192
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    a8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev, generator=g)
+    b8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev, generator=g).t().contiguous().t()
+    a16 = a8.to(torch.bfloat16)
+    b16 = b8.to(torch.bfloat16)
+    ops = 2.0 * n ** 3
+    res = {}
+    for name, fn in (("int8_int_mm", lambda: torch._int_mm(a8, b8)), ("bf16_matmul", lambda: a16 @ b16)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) * 1e-3)
+        with ClockSampler(0) as cs:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(10, int(4.0 / best))
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+        sus = e0.elapsed_time(e1) * 1e-3 / reps
+        res[name] = {"burst_tops": ops / best / 1e12, "sustained_tops": ops / sus / 1e12, "reps": reps,
+                     "clocks": cs.summary()}
+    # the int8 product is exact: a block of it against int64 arithmetic on the host
+    blk = a8[:64].cpu().to(torch.int64) @ b8[:, :64].cpu().to(torch.int64)
+    assert torch.equal(torch._int_mm(a8, b8)[:64, :64].cpu().to(torch.int64), blk)
+    print(json.dumps({"kernel": "library dense peaks", "n": n, **res,
+                      "gpu": torch.cuda.get_device_name(dev)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -883,7 +932,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted", "tp", "w4a8"],
+    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted", "tp", "w4a8",
+                                         "int8_peak"],
                     help="time one call type alone")
     ap.add_argument("--case", default=None, choices=sorted(wl.LINEAR_CONFIGS) + sorted(wl.REQUANT_CONFIGS),
                     help="workload of --kernel (a linear case; for requant a weight as loaded)")
@@ -894,6 +944,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel == "int8_peak":
+        return run_kernel_int8_peak(args)
     if args.kernel == "requant":
         args.case = args.case or "qkv_n15360_k5120"
         if args.case not in wl.REQUANT_CONFIGS:

@@ -57,7 +57,8 @@ SIGNATURES = {
     "prism_w8a8_linear_noalloc": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _P, _I64, _P,
                                          _I64, _I64, _I64, _I32, _P]),
     "prism_candidate_readout": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _P, _P,
-                                       _I64, _I64, _P, _P, _P, _P]),
+                                       _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "prism_readout_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "prism_smooth_requant": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _P, _I64, _P, _P]),
     "prism_quant_act_rows": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
     "prism_w8a8_linear_rows": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P,
@@ -131,13 +132,13 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _require(t, dtype, name, ndim):
+def _require(t, dtype, name, ndim, on_device=True):
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
+    if on_device and not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims")
@@ -145,6 +146,34 @@ def _require(t, dtype, name, ndim):
         raise ValueError(f"{name} rows must be contiguous")
     if ndim == 1 and t.numel() > 1 and t.stride(0) != 1:
         raise ValueError(f"{name} must be contiguous")
+
+
+def _linear_operands(q, a_scale, w, w_scale, residual, out, acc_out, on_device=True):
+    """Checks the tensors of a linear call before anything is launched: dtypes,
+    contiguous rows, and every shape against [M, K] x [N, K] (residual, out
+    and acc_out [M, N]; acc_out dense).  Returns (M, N, K)."""
+    import torch
+    _require(q, torch.int8, "q", 2, on_device)
+    _require(w, torch.int8, "w", 2, on_device)
+    _require(a_scale, torch.float32, "a_scale", 1, on_device)
+    _require(w_scale, torch.float32, "w_scale", 1, on_device)
+    M, K = q.shape
+    N = w.shape[0]
+    if w.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if residual is not None:
+        _require(residual, torch.bfloat16, "residual", 2, on_device)
+        if tuple(residual.shape) != (M, N):
+            raise ValueError("residual must be [M, N]")
+    if out is not None:
+        _require(out, torch.bfloat16, "out", 2, on_device)
+        if tuple(out.shape) != (M, N):
+            raise ValueError("out must be [M, N]")
+    if acc_out is not None:
+        _require(acc_out, torch.int32, "acc_out", 2, on_device)
+        if not acc_out.is_contiguous() or tuple(acc_out.shape) != (M, N):
+            raise ValueError("acc_out must be a contiguous [M, N] int32 tensor")
+    return M, N, K
 
 
 def prism_w8a8_workspace_bytes(M: int, N: int, K: int, split_k: int = 0) -> int:
@@ -234,25 +263,9 @@ def prism_w8a8_linear(q, a_scale, w, w_scale, residual=None, out=None, acc_out=N
     when the schedule needs one (split-K > 1, or an automatic call that shares
     tiles between CTAs); one is allocated (and zeroed) per call when None."""
     import torch
-    _require(q, torch.int8, "q", 2)
-    _require(w, torch.int8, "w", 2)
-    _require(a_scale, torch.float32, "a_scale", 1)
-    _require(w_scale, torch.float32, "w_scale", 1)
-    M, K = q.shape
-    N = w.shape[0]
-    if w.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N:
-        raise ValueError("shape mismatch")
-    if residual is not None:
-        _require(residual, torch.bfloat16, "residual", 2)
-        if tuple(residual.shape) != (M, N):
-            raise ValueError("residual shape")
+    M, N, K = _linear_operands(q, a_scale, w, w_scale, residual, out, acc_out)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
-    _require(out, torch.bfloat16, "out", 2)
-    if acc_out is not None:
-        _require(acc_out, torch.int32, "acc_out", 2)
-        if not acc_out.is_contiguous() or tuple(acc_out.shape) != (M, N):
-            raise ValueError("acc_out must be a contiguous [M, N] int32 tensor")
     if workspace is None:
         workspace = new_workspace(M, N, K, split_k, q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -489,19 +502,9 @@ def prism_w8a8_linear_noalloc(q, a_scale, w, w_scale, residual=None, out=None, a
     scratch comes from a fixed array inside the library (see include/prism.h
     for its size limit and the rule that overlapping calls must not share it)."""
     import torch
-    _require(q, torch.int8, "q", 2)
-    _require(w, torch.int8, "w", 2)
-    _require(a_scale, torch.float32, "a_scale", 1)
-    _require(w_scale, torch.float32, "w_scale", 1)
-    M, K = q.shape
-    N = w.shape[0]
-    if w.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N:
-        raise ValueError("shape mismatch")
-    if residual is not None:
-        _require(residual, torch.bfloat16, "residual", 2)
+    M, N, K = _linear_operands(q, a_scale, w, w_scale, residual, out, acc_out)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
-    _require(out, torch.bfloat16, "out", 2)
     st = lib().prism_w8a8_linear_noalloc(
         _ptr(q), q.stride(0), _ptr(a_scale), _ptr(w), w.stride(0), _ptr(w_scale),
         _ptr(residual), 0 if residual is None else residual.stride(0), _ptr(out), out.stride(0),
@@ -510,9 +513,16 @@ def prism_w8a8_linear_noalloc(q, a_scale, w, w_scale, residual=None, out=None, a
     return out
 
 
+def prism_readout_workspace_bytes(P: int, T: int, K: int) -> int:
+    return int(lib().prism_readout_workspace_bytes(P, T, K))
+
+
 def prism_candidate_readout(hidden, inv_s, lm_head, lm_scale, cand_offsets, cand_ids,
-                            logits=None, probs=None, err=None, stream=None):
-    """Candidate-restricted read-out -> (logits float32 [T], probs float32 [T])."""
+                            logits=None, probs=None, err=None, workspace=None, stream=None):
+    """Candidate-restricted read-out -> (logits float32 [T], probs float32 [T]).
+    ``err``: optional int32 [1] device error word; ``workspace``: optional
+    uint8 device tensor of prism_readout_workspace_bytes bytes (allocated
+    when None and that size is nonzero)."""
     import torch
     _require(hidden, torch.bfloat16, "hidden", 2)
     _require(lm_head, torch.int8, "lm_head", 2)
@@ -530,9 +540,19 @@ def prism_candidate_readout(hidden, inv_s, lm_head, lm_scale, cand_offsets, cand
         logits = torch.empty((T,), dtype=torch.float32, device=hidden.device)
     if probs is None:
         probs = torch.empty((T,), dtype=torch.float32, device=hidden.device)
+    _require(logits, torch.float32, "logits", 1)
+    _require(probs, torch.float32, "probs", 1)
+    if logits.numel() != T or probs.numel() != T:
+        raise ValueError("logits and probs must hold T values")
+    if err is not None:
+        _require(err, torch.int32, "err", 1)
+    if workspace is None:
+        need = prism_readout_workspace_bytes(P, T, K)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=hidden.device) if need else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().prism_candidate_readout(
         _ptr(hidden), hidden.stride(0), _ptr(inv_s), _ptr(lm_head), lm_head.stride(0),
         _ptr(lm_scale), V, K, _ptr(cand_offsets), _ptr(cand_ids), P, T, _ptr(logits),
-        _ptr(probs), _ptr(err), _stream(stream))
+        _ptr(probs), _ptr(err), _ptr(workspace), ws_bytes, _stream(stream))
     _check("prism_candidate_readout", st)
     return logits, probs

@@ -209,6 +209,8 @@ cudaError_t launch_linear_gemv_w4(const LinearArgs& a, cudaStream_t stream);
 cudaError_t launch_unpack_w4(const uint8_t* w4, int64_t ldw4, int64_t N, int64_t K, int8_t* w8, int64_t ldw8,
                              cudaStream_t stream);
 cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream);
+// Streaming multiprocessors of the current device (one persistent CTA each).
+int sm_count();
 // Sticky device error bits raised by kernels (bounded waits that expired).
 cudaError_t read_and_clear_kernel_error(uint32_t* out);
 

@@ -20,11 +20,19 @@
 //     two calls whose work overlaps on the GPU (different streams, or
 //     different host threads without ordering) race on the array and may
 //     produce wrong results.  Order such calls on one stream.
-//   - The device address of the array is looked up once per device, by the
-//     first call made while that device is current (cudaGetSymbolAddress).
-//     Make that first call before any stream capture begins.
+//   - The device address of the array is looked up by the first call made
+//     in each CUDA context (cudaGetSymbolAddress, with that context's device
+//     current) and cached under the context's unique id.  Make that first
+//     call before any stream capture begins.  A context torn down and made
+//     again (cudaDeviceReset, primary-context release) has a new id, so the
+//     next call looks the address up again instead of using a stale one.
+//   - The stream must belong to the current device; a stream of another
+//     device is refused (the array is per device).
 #include <cstdint>
 #include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 
@@ -37,23 +45,74 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PRISM_NOALLOC_S
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
+// per device ordinal: the context the cached address belongs to, and the address
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (looked up once).
+// Unique id of the calling thread's current context (driver entry points
+// fetched once through the runtime, as for the tensor-map encoder).
+cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) {
+    // no context yet on this thread: the runtime makes the current device's
+    // primary context current (a caller's own current context is never replaced)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of g_noalloc_scratch in the current context (looked up once
+// per context, with the context's device current).
 cudaError_t scratch_for_current_device(void** out) {
+  unsigned long long ctx = 0;
+  cudaError_t e = current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     if (p == nullptr) return cudaErrorInvalidSymbol;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+// The stream belongs to the current device (NULL: the legacy default stream
+// of the current device).
+cudaError_t stream_on_current_device(cudaStream_t stream, bool* ok) {
+  int dev = 0, sdev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamGetDevice(stream, &sdev);
+  if (e != cudaSuccess) return e;
+  *ok = sdev == dev;
   return cudaSuccess;
 }
 
@@ -108,6 +167,10 @@ extern "C" int prism_w8a8_linear_noalloc(const int8_t* q, int64_t ldq, const flo
   a.pair_io = aligned_to(out_bf16, 4) && ldo % 2 == 0 &&
               (residual_bf16 == nullptr || (aligned_to(residual_bf16, 4) && ldr % 2 == 0));
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  bool same_device = false;
+  const int st0 = prism::record_cuda(prism::stream_on_current_device(stream, &same_device));
+  if (st0 != PRISM_OK) return st0;
+  if (!same_device) return PRISM_ERR_INVALID_ARG;
   if (zero > 0) {
     void* scratch = nullptr;
     const int st = prism::record_cuda(prism::scratch_for_current_device(&scratch));

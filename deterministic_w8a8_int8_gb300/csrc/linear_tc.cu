@@ -542,7 +542,7 @@ __device__ __forceinline__ bool get_item(const TcParams& p, int n, Item& it) {
     return true;
   }
   if (p.R == 0) return false;
-  // U * G < 2^31: R < 304, S <= 2081 (K <= 133144) and G <= 152
+  // U * G < 2^31: R < 2 G, S <= 2081 (K <= 133144) and G <= 512 (sm_count's cap)
   const int j = n - p.W;
   const int U = p.R * p.S;
   const int u0 = b * U / G, u1 = (b + 1) * U / G;
@@ -1088,7 +1088,7 @@ static TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
   return pl;
 }
 
-// The balanced schedule for T tiles of S K-stages on the 152 SMs (see
+// The balanced schedule for T tiles of S K-stages on the device's SMs (see
 // get_item): whole tiles in W rounds over G CTAs, then the K units of the
 // last R tiles shared out evenly.  Shares below one 1024-K chunk per CTA are
 // not worth their partial-sum traffic: then one round fewer of whole tiles
@@ -1098,8 +1098,36 @@ struct TcSched {
   int G, W, R;
 };
 
+}  // namespace prism
+#include <atomic>
+namespace prism {
+
+// Streaming multiprocessors of the current device (152 on a GB300), queried
+// once per device; the balanced schedule runs one CTA per SM.  Without a
+// usable device (a host that only sizes workspaces) the GB300's count is
+// taken, so that sizes agree with the launches on that part.
+int sm_count() {
+  constexpr int kMaxDev = 64, kDefault = 152;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return kDefault;
+  }
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return kDefault;
+    }
+    n = std::min(n, 512);   // keeps the schedule's unit arithmetic within int32
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 static TcSched tc_balanced(int64_t T, int64_t S, int sub) {
-  constexpr int64_t kSMs = 152;
+  const int64_t kSMs = sm_count();
   const int64_t kMinUnits = kChunkStages / sub;
   TcSched sc{static_cast<int>(kSMs), 0, 0};
   if (T % kSMs == 0) {
@@ -1221,7 +1249,10 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
     TcSched sc = tc_balanced(p.T, p.S, pl.sub);
     size_t cb = 0;
     const size_t need = tc_balanced_bytes(a.M, a.N, a.K, &cb);
-    if (need > 0 && need > a.ws_bytes) sc = TcSched{152, static_cast<int>(cdiv(p.T, 152)), 0};
+    if (need > 0 && need > a.ws_bytes) {
+      const int g = sm_count();
+      sc = TcSched{g, static_cast<int>(cdiv(p.T, g)), 0};
+    }
     if (sc.R > 0 && need > 0) {
       p.cnt = static_cast<uint32_t*>(a.ws);
       p.acc = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + cb);

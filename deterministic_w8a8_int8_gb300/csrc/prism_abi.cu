@@ -257,7 +257,7 @@ int prism_quant_act_amax(const void* x_bf16, int64_t ldx, const float* inv_smoot
 
 int prism_quant_act_rows(const void* x_bf16, int64_t ldx, int64_t M_x, const int32_t* rows, int64_t n_rows,
                          const float* inv_smooth, int64_t K, int8_t* q, int64_t ldq, float* a_scale,
-                         uint32_t* dev_error_word, void* cuda_stream) {
+                         int32_t* dev_error_word, void* cuda_stream) {
   if (n_rows < 0 || M_x < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
   if (n_rows == 0) return PRISM_OK;
   if (x_bf16 == nullptr || rows == nullptr || q == nullptr || a_scale == nullptr || M_x == 0)
@@ -271,7 +271,8 @@ int prism_quant_act_rows(const void* x_bf16, int64_t ldx, int64_t M_x, const int
   if (dev_error_word != nullptr && !aligned(dev_error_word, 4)) return PRISM_ERR_ALIGNMENT;
   if (n_rows > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
   return prism::record_cuda(prism::launch_quant_act(x_bf16, ldx, inv_smooth, n_rows, K, q, ldq, a_scale, rows, M_x,
-                                                     dev_error_word, static_cast<cudaStream_t>(cuda_stream)));
+                                                     reinterpret_cast<uint32_t*>(dev_error_word),
+                                                     static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K) { return prism::linear_kernel_kind(M, N, K); }
@@ -360,7 +361,7 @@ int prism_w8a8_linear_rows(const int8_t* q, int64_t ldq, const float* a_scale, c
                            const float* w_scale, const void* residual_bf16, int64_t ldr, int64_t M_res,
                            const int32_t* residual_rows, void* out_bf16, int64_t ldo, int32_t* acc_out,
                            int64_t M, int64_t N, int64_t K, int split_k, void* workspace,
-                           size_t workspace_bytes, uint32_t* dev_error_word, void* cuda_stream) {
+                           size_t workspace_bytes, int32_t* dev_error_word, void* cuda_stream) {
   if (M < 0 || M_res < 0) return PRISM_ERR_INVALID_ARG;
   if (M > 0 && N > 0) {
     if (residual_bf16 == nullptr || residual_rows == nullptr || M_res == 0) return PRISM_ERR_INVALID_ARG;
@@ -373,14 +374,17 @@ int prism_w8a8_linear_rows(const int8_t* q, int64_t ldq, const float* a_scale, c
     if (o0 < r1 && r0 < o1) return PRISM_ERR_INVALID_ARG;
   }
   return linear_impl(q, ldq, a_scale, w, ldw, w_scale, residual_bf16, ldr, out_bf16, ldo, acc_out, M, N, K, split_k,
-                     workspace, workspace_bytes, residual_rows, M_res, dev_error_word, 0, cuda_stream);
+                     workspace, workspace_bytes, residual_rows, M_res,
+                     reinterpret_cast<uint32_t*>(dev_error_word), 0, cuda_stream);
 }
 
 int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* inv_smooth,
                             const int8_t* lm_head, int64_t ldw, const float* lm_scale, int64_t V,
                             int64_t K, const int32_t* cand_offsets, const int32_t* cand_ids, int64_t P,
-                            int64_t T, float* logits, float* probs, uint32_t* dev_error_word,
-                            void* cuda_stream) {
+                            int64_t T, float* logits, float* probs, int32_t* dev_error_word,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  (void)workspace;   // no scratch: prism_readout_workspace_bytes is 0 for every shape
+  (void)workspace_bytes;
   if (P < 0 || T < 0 || V <= 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
   if (P == 0) return T == 0 ? PRISM_OK : PRISM_ERR_INVALID_ARG;
   if (hidden_bf16 == nullptr || lm_head == nullptr || lm_scale == nullptr || cand_offsets == nullptr ||
@@ -400,7 +404,15 @@ int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* i
   if (P > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
   return prism::record_cuda(prism::launch_readout(hidden_bf16, ldh, inv_smooth, lm_head, ldw, lm_scale, V,
                                                    K, cand_offsets, cand_ids, P, T, logits, probs,
-                                                   dev_error_word, static_cast<cudaStream_t>(cuda_stream)));
+                                                   reinterpret_cast<uint32_t*>(dev_error_word),
+                                                   static_cast<cudaStream_t>(cuda_stream)));
+}
+
+size_t prism_readout_workspace_bytes(int64_t P, int64_t T, int64_t K) {
+  (void)P;
+  (void)T;
+  (void)K;
+  return 0;
 }
 
 }  // extern "C"

@@ -66,7 +66,8 @@ typedef enum {
 } prism_status;
 
 /* Largest K for which every int32 accumulator is exact: K * 127 * 127 must
- * not exceed 2^31 - 1.  With K a multiple of 16 the usable maximum is 133136. */
+ * not exceed 2^31 - 1 (codes within +-127 on both sides).  With K a multiple
+ * of 16 the usable maximum is 133136. */
 #define PRISM_MAX_K 133144
 /* Largest split-K factor accepted by prism_w8a8_linear. */
 #define PRISM_MAX_SPLIT_K 64
@@ -109,7 +110,7 @@ int prism_quant_act(const void *x_bf16, int64_t ldx, const float *inv_smooth,
  *   rows, n_rows      [n_rows] int32 device indices into x, any order,
  *                     repeats allowed (4-byte aligned)
  *   inv_smooth, K, q, ldq, a_scale   as prism_quant_act, with n_rows rows out
- *   dev_error_word    device uint32 or NULL: an index outside [0, M_x) ORs
+ *   dev_error_word    device int32 or NULL: an index outside [0, M_x) ORs
  *                     in PRISM_DEV_ERR_ROW_RANGE and that row comes out as
  *                     q = 0, a_scale = NaN (so a linear on it gives NaN).
  *   n_rows == 0 enqueues nothing.
@@ -117,7 +118,7 @@ int prism_quant_act(const void *x_bf16, int64_t ldx, const float *inv_smooth,
 int prism_quant_act_rows(const void *x_bf16, int64_t ldx, int64_t M_x,
                          const int32_t *rows, int64_t n_rows,
                          const float *inv_smooth, int64_t K, int8_t *q,
-                         int64_t ldq, float *a_scale, uint32_t *dev_error_word,
+                         int64_t ldq, float *a_scale, int32_t *dev_error_word,
                          void *cuda_stream);
 
 /*
@@ -136,7 +137,11 @@ size_t prism_w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
  *
  *   q, ldq         [M, K] int8 activations (prism_quant_act's output)
  *   a_scale        [M] float32 per-token scales
- *   w, ldw         [N, K] int8 weights, K contiguous (nn.Linear layout)
+ *   w, ldw         [N, K] int8 weights, K contiguous (nn.Linear layout),
+ *                  codes in [-127, 127] like the activations' (the range
+ *                  prism_smooth_requant produces).  PRISM_MAX_K is the bound
+ *                  for that range; a code of -128 keeps the sums exact only
+ *                  while K * 127 * 128 < 2^31 (K <= 132096 in steps of 16).
  *   w_scale        [N] float32 per-output-channel scales
  *   residual, ldr  [M, N] bf16 or NULL; may be the same buffer as out
  *   out, ldo       [M, N] bf16 output
@@ -179,7 +184,7 @@ int prism_w8a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
  *
  *   residual_bf16, ldr, M_res  [M_res, N] bf16, required (not NULL)
  *   residual_rows              [M] int32 device indices (4-byte aligned)
- *   dev_error_word             device uint32 or NULL: an index outside
+ *   dev_error_word             device int32 or NULL: an index outside
  *                              [0, M_res) ORs in PRISM_DEV_ERR_ROW_RANGE and
  *                              that output row becomes NaN (bf16 0x7fc0)
  *   out must not overlap the residual (output rows may be other tiles'
@@ -192,7 +197,7 @@ int prism_w8a8_linear_rows(const int8_t *q, int64_t ldq, const float *a_scale,
                            const int32_t *residual_rows, void *out_bf16,
                            int64_t ldo, int32_t *acc_out, int64_t M, int64_t N,
                            int64_t K, int split_k, void *workspace,
-                           size_t workspace_bytes, uint32_t *dev_error_word,
+                           size_t workspace_bytes, int32_t *dev_error_word,
                            void *cuda_stream);
 
 /*
@@ -356,10 +361,18 @@ int prism_smooth_requant(const int8_t *q, int64_t ldq, const uint16_t *d_f16,
  *   cand_ids          [T] int32 token ids, distinct within a position,
  *                     1..PRISM_MAX_CANDIDATES per position
  *   logits, probs     [T] float32 out, in CSR order
- *   dev_error_word    device uint32: PRISM_DEV_ERR_* bits are OR-ed into it
+ *   dev_error_word    device int32: PRISM_DEV_ERR_* bits are OR-ed into it
  *                     for invalid positions, whose outputs are set to NaN.
  *                     The caller clears it.  May be NULL (errors then only
  *                     show as NaN outputs).
+ *   workspace, workspace_bytes
+ *                     device scratch of at least
+ *                     prism_readout_workspace_bytes(P, T, K) bytes.  This
+ *                     implementation needs none (each position is one CTA
+ *                     whose cross-thread state stays in shared memory), so
+ *                     the size query returns 0 and NULL / 0 are accepted;
+ *                     a caller that always sizes and passes the workspace
+ *                     stays correct if a later kernel needs scratch.
  *   P >= 0 (P == 0 enqueues nothing), T <= P * PRISM_MAX_CANDIDATES,
  *   16 <= K <= PRISM_MAX_READOUT_K, K % 16 == 0.
  */
@@ -369,7 +382,12 @@ int prism_candidate_readout(const void *hidden_bf16, int64_t ldh,
                             int64_t K, const int32_t *cand_offsets,
                             const int32_t *cand_ids, int64_t P, int64_t T,
                             float *logits, float *probs,
-                            uint32_t *dev_error_word, void *cuda_stream);
+                            int32_t *dev_error_word, void *workspace,
+                            size_t workspace_bytes, void *cuda_stream);
+
+/* Bytes of workspace prism_candidate_readout needs for P positions, T
+ * candidates and hidden size K: 0 for every shape in this implementation. */
+size_t prism_readout_workspace_bytes(int64_t P, int64_t T, int64_t K);
 
 /* Human-readable text for a prism_status value (static storage). */
 const char *prism_status_string(int status);

@@ -182,7 +182,7 @@ def test_balanced_schedule_workspace_matches_its_statement(L, monkeypatch):
 
 def ro(L, P=4, T=8, V=100, K=64, h=A, ldh=64, s=None, W=A, ldw=64, sc=A, off=A, ids=A,
        lg=A, pr=A, err=None):
-    return L.prism_candidate_readout(h, ldh, s, W, ldw, sc, V, K, off, ids, P, T, lg, pr, err, None)
+    return L.prism_candidate_readout(h, ldh, s, W, ldw, sc, V, K, off, ids, P, T, lg, pr, err, None, 0, None)
 
 
 def test_readout_validation(L):
@@ -199,3 +199,38 @@ def test_readout_validation(L):
     assert ro(L, ldh=68) == -2 and ro(L, ldw=72) == -2
     assert ro(L, h=A + 8) == -2 and ro(L, W=A + 8) == -2 and ro(L, off=A + 2) == -2
     assert ro(L, s=A + 4) == -2 and ro(L, err=A + 2) == -2
+    # the read-out needs no scratch for any shape
+    assert L.prism_readout_workspace_bytes(192, 1152, 5120) == 0 and L.prism_readout_workspace_bytes(0, 0, 16) == 0
+
+
+def test_linear_operand_checks_before_any_launch():
+    """The binding refuses mis-shaped or mis-typed outputs and residuals of a
+    linear call (the W8A8 linear and its no-workspace variant share these
+    checks) before the library is called: a short, strided or int64
+    acc_out, or a residual / out with the wrong row count, would otherwise
+    become out-of-bounds device accesses."""
+    import torch
+    import deterministic_w8a8_int8_gb300 as prism
+    M, N, K = 4, 8, 32
+    q = torch.zeros((M, K), dtype=torch.int8)
+    w = torch.zeros((N, K), dtype=torch.int8)
+    a, s = torch.ones(M), torch.ones(N)
+
+    def chk(residual=None, out=None, acc_out=None):
+        return prism._linear_operands(q, a, w, s, residual, out, acc_out, on_device=False)
+
+    assert chk() == (M, N, K)
+    assert chk(residual=torch.zeros((M, N), dtype=torch.bfloat16), out=torch.zeros((M, N), dtype=torch.bfloat16),
+               acc_out=torch.zeros((M, N), dtype=torch.int32)) == (M, N, K)
+    with pytest.raises(TypeError):
+        chk(acc_out=torch.zeros((M, N), dtype=torch.int64))
+    with pytest.raises(ValueError):
+        chk(acc_out=torch.zeros((M, 2 * N), dtype=torch.int32)[:, :N])      # strided rows
+    with pytest.raises(ValueError):
+        chk(acc_out=torch.zeros((M - 1, N), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        chk(residual=torch.zeros((M - 1, N), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        chk(out=torch.zeros((M + 1, N), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        prism.prism_w8a8_linear_noalloc(q, a, w, s, acc_out=torch.zeros((M, N), dtype=torch.int32))   # host tensors
