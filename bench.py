@@ -526,35 +526,49 @@ def run_kernel(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     L = prism.lib()
+    f16 = args.kernel == "linear_f16"
     c = wl.make_linear(args.case)
     M, K, N = c.M, c.K, c.N
     rows = M if args.rows is None else args.rows
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     x = torch.from_numpy(c.x_bits[:rows].view(np.int16)).view(torch.bfloat16).to(dev)
     inv = t(c.inv_s)
-    q = torch.empty((rows, K), dtype=torch.int8, device=dev)
     a = torch.empty((rows,), dtype=torch.float32, device=dev)
-    prism.prism_quant_act(x, inv, q=q, a_scale=a)
-    wbytes = N * K
+    if f16:
+        q = torch.empty((rows, K), dtype=torch.float16, device=dev)
+        prism.prism_quant_act_f16(x, inv, qh=q, a_scale=a)
+    else:
+        q = torch.empty((rows, K), dtype=torch.int8, device=dev)
+        prism.prism_quant_act(x, inv, q=q, a_scale=a)
+    wbytes = N * K * (2 if f16 else 1)
     n_rot = max(1, int(np.ceil(3 * 129e6 / wbytes)))
-    Ws = [t(c.w) for _ in range(n_rot)]
+    w8 = t(c.w)
+    Ws = [prism.prism_codes_to_f16(w8) if f16 else w8.clone() for _ in range(n_rot)]
+    del w8
     S = t(c.w_scale)
     R = None if c.residual_bits is None else torch.from_numpy(c.residual_bits[:rows].view(np.int16)).view(torch.bfloat16).to(dev)
     out = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
-    split = args.split if args.split is not None else prism.prism_w8a8_auto_split(rows, N, K)
-    ws = prism.new_workspace(rows, N, K, split, dev)
+    if f16:
+        split = args.split if args.split is not None else 0
+        ws = prism.new_workspace_f16(rows, N, K, split, dev)
+        fn = L.prism_w8a8_linear_f16
+    else:
+        split = args.split if args.split is not None else prism.prism_w8a8_auto_split(rows, N, K)
+        ws = prism.new_workspace(rows, N, K, split, dev)
+        fn = L.prism_w8a8_linear
     stream = torch.cuda.Stream(device=dev)
     st = ctypes.c_void_p(stream.cuda_stream)
     vp = lambda z: None if z is None else ctypes.c_void_p(z.data_ptr())
     calls = [(vp(q), K, vp(a), vp(W), K, vp(S), vp(R), N, vp(out), N, None, rows, N, K, split, vp(ws),
               0 if ws is None else ws.numel(), st) for W in Ws]
+    torch.cuda.synchronize()
     for i in range(args.warmup):
-        assert L.prism_w8a8_linear(*calls[i % n_rot]) == 0
+        assert fn(*calls[i % n_rot]) == 0
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         evs[i][0].record(stream)
-        assert L.prism_w8a8_linear(*calls[i % n_rot]) == 0
+        assert fn(*calls[i % n_rot]) == 0
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
@@ -562,8 +576,9 @@ def run_kernel(args):
     ops = 2 * rows * N * K
     byts = rows * K + N * K + 4 * N + 4 * rows + 2 * rows * N * (2 if R is not None else 1)
     hbm, bf16, src = load_peaks()
-    print(json.dumps({"kernel": "prism_w8a8_linear", "case": args.case, "M": rows, "N": N, "K": K,
-                      "split": split, "kind": prism.prism_w8a8_kernel_kind(rows, N, K),
+    print(json.dumps({"kernel": "prism_w8a8_linear_f16" if f16 else "prism_w8a8_linear", "case": args.case,
+                      "M": rows, "N": N, "K": K,
+                      "split": split, "kind": "f16 codes" if f16 else prism.prism_w8a8_kernel_kind(rows, N, K),
                       "avg_us": avg, "min_us": min(us), "tflops": ops / avg / 1e6,
                       "frac_bf16_peak": ops / avg / 1e6 / bf16, "gbs": byts / avg / 1e3,
                       "frac_hbm": byts / avg / 1e3 / hbm, "weight_copies": n_rot,
@@ -932,8 +947,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["linear", "quant", "readout", "requant", "restricted", "tp", "w4a8",
-                                         "int8_peak"],
+    ap.add_argument("--kernel", choices=["linear", "linear_f16", "quant", "readout", "requant", "restricted", "tp",
+                                         "w4a8", "int8_peak"],
                     help="time one call type alone")
     ap.add_argument("--case", default=None, choices=sorted(wl.LINEAR_CONFIGS) + sorted(wl.REQUANT_CONFIGS),
                     help="workload of --kernel (a linear case; for requant a weight as loaded)")

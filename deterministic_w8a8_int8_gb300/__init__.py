@@ -20,6 +20,9 @@ Entry points (same names as the C ABI):
   prism_w4a8_linear(q, a_scale, w4, w_scale, ...) -> out   packed 4-bit weights
   prism_unpack_w4(w4, K)                         -> int8 codes
   prism_candidate_readout(hidden, ...)           -> (logits, probs)
+  prism_quant_act_f16(x, inv_s)                  -> (codes as float16, a_scale)
+  prism_codes_to_f16(w)                          -> int8 codes as float16 (load time)
+  prism_w8a8_linear_f16(qh, a_scale, wh, w_scale, ...) -> out   codes given as float16
 """
 from __future__ import annotations
 
@@ -46,6 +49,7 @@ PRISM_DEV_ERR_COUNT = 2
 PRISM_DEV_ERR_ID_RANGE = 4
 PRISM_DEV_ERR_DUPLICATE = 8
 PRISM_DEV_ERR_ROW_RANGE = 16
+PRISM_DEVSTATUS_WAIT_TIMEOUT = 1
 
 # (restype, argtypes) of every symbol the header declares
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
@@ -59,6 +63,12 @@ SIGNATURES = {
     "prism_candidate_readout": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _P, _P,
                                        _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "prism_readout_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "prism_quant_act_f16": (_I32, [_P, _I64, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "prism_codes_to_f16": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P]),
+    "prism_w8a8_f16_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "prism_w8a8_linear_f16": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _P, _I64, _P,
+                                     _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "prism_debug_wait_expiry": (_I32, [ctypes.c_uint64]),
     "prism_smooth_requant": (_I32, [_P, _I64, _P, _I64, _P, _I64, _I64, _P, _I64, _P, _P]),
     "prism_quant_act_rows": (_I32, [_P, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
     "prism_w8a8_linear_rows": (_I32, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P,
@@ -556,3 +566,100 @@ def prism_candidate_readout(hidden, inv_s, lm_head, lm_scale, cand_offsets, cand
         _ptr(probs), _ptr(err), _ptr(workspace), ws_bytes, _stream(stream))
     _check("prism_candidate_readout", st)
     return logits, probs
+
+
+def prism_debug_wait_expiry(limit_ns: int) -> None:
+    """Arm (limit_ns > 0) or disarm (0) the test mode of the tensor-core
+    kernels' bounded waits: each CTA withholds one completion signal and the
+    wait for it expires after limit_ns (see include/prism.h)."""
+    _check("prism_debug_wait_expiry", lib().prism_debug_wait_expiry(int(limit_ns)))
+
+
+def prism_quant_act_f16(x, inv_s=None, qh=None, a_scale=None, stream=None):
+    """prism_quant_act with the codes stored as float16 values (exact integers
+    in [-127, 127]): bf16 ``x`` [M, K] -> (float16 qh [M, K], float32 a_scale [M])."""
+    import torch
+    _require(x, torch.bfloat16, "x", 2)
+    M, K = x.shape
+    if inv_s is not None:
+        _require(inv_s, torch.float32, "inv_s", 1)
+    if qh is None:
+        qh = torch.empty((M, K), dtype=torch.float16, device=x.device)
+    if a_scale is None:
+        a_scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _require(qh, torch.float16, "qh", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    if tuple(qh.shape) != (M, K) or a_scale.numel() != M:
+        raise ValueError("qh must be [M, K] and a_scale [M]")
+    st = lib().prism_quant_act_f16(_ptr(x), x.stride(0), _ptr(inv_s), M, K, _ptr(qh), qh.stride(0),
+                                   _ptr(a_scale), _stream(stream))
+    _check("prism_quant_act_f16", st)
+    return qh, a_scale
+
+
+def prism_codes_to_f16(w, wh=None, stream=None):
+    """int8 codes [N, K] -> the same codes as float16 [N, K] (exact; the weight
+    operand of prism_w8a8_linear_f16, made once at load time)."""
+    import torch
+    _require(w, torch.int8, "w", 2)
+    N, K = w.shape
+    if wh is None:
+        wh = torch.empty((N, K), dtype=torch.float16, device=w.device)
+    _require(wh, torch.float16, "wh", 2)
+    if tuple(wh.shape) != (N, K):
+        raise ValueError("wh must be [N, K]")
+    _check("prism_codes_to_f16", lib().prism_codes_to_f16(_ptr(w), w.stride(0), N, K, _ptr(wh), wh.stride(0),
+                                                          _stream(stream)))
+    return wh
+
+
+def prism_w8a8_f16_workspace_bytes(M: int, N: int, K: int, split_k: int = 0) -> int:
+    return int(lib().prism_w8a8_f16_workspace_bytes(M, N, K, split_k))
+
+
+def new_workspace_f16(M: int, N: int, K: int, split_k: int = 0, device=None):
+    """A zeroed workspace for prism_w8a8_linear_f16 (None when none is needed)."""
+    import torch
+    n = prism_w8a8_f16_workspace_bytes(M, N, K, split_k)
+    if n == 0:
+        return None
+    return torch.zeros((n,), dtype=torch.uint8, device=device)
+
+
+def prism_w8a8_linear_f16(qh, a_scale, wh, w_scale, residual=None, out=None, acc_out=None,
+                          split_k: int = 0, workspace=None, stream=None):
+    """prism_w8a8_linear with the codes given as float16 values: ``qh`` [M, K]
+    (prism_quant_act_f16) and ``wh`` [N, K] (prism_codes_to_f16).  Same
+    result, bit for bit; ``workspace`` as prism_w8a8_linear's, sized by
+    prism_w8a8_f16_workspace_bytes."""
+    import torch
+    _require(qh, torch.float16, "qh", 2)
+    _require(wh, torch.float16, "wh", 2)
+    _require(a_scale, torch.float32, "a_scale", 1)
+    _require(w_scale, torch.float32, "w_scale", 1)
+    M, K = qh.shape
+    N = wh.shape[0]
+    if wh.shape[1] != K or a_scale.numel() != M or w_scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if residual is not None:
+        _require(residual, torch.bfloat16, "residual", 2)
+        if tuple(residual.shape) != (M, N):
+            raise ValueError("residual must be [M, N]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=qh.device)
+    _require(out, torch.bfloat16, "out", 2)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N]")
+    if acc_out is not None:
+        _require(acc_out, torch.int32, "acc_out", 2)
+        if not acc_out.is_contiguous() or tuple(acc_out.shape) != (M, N):
+            raise ValueError("acc_out must be a contiguous [M, N] int32 tensor")
+    if workspace is None:
+        workspace = new_workspace_f16(M, N, K, split_k, qh.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().prism_w8a8_linear_f16(
+        _ptr(qh), qh.stride(0), _ptr(a_scale), _ptr(wh), wh.stride(0), _ptr(w_scale),
+        _ptr(residual), 0 if residual is None else residual.stride(0), _ptr(out), out.stride(0),
+        _ptr(acc_out), M, N, K, int(split_k), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("prism_w8a8_linear_f16", st)
+    return out

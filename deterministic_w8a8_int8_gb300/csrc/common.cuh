@@ -144,6 +144,8 @@ struct QuantCall {
   uint32_t* err;
   float* amax_out;
   const float* amax_in;
+  uint16_t* qh;     // non-null: the codes as binary16 values, row stride ldqh (plain mode only; q unused)
+  int64_t ldqh;
 };
 cudaError_t launch_quant(const QuantCall& c, cudaStream_t stream);
 cudaError_t launch_quant_act(const void* x, int64_t ldx, const float* inv_s, int64_t M, int64_t K, int8_t* q,
@@ -213,6 +215,36 @@ cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream);
 int sm_count();
 // Sticky device error bits raised by kernels (bounded waits that expired).
 cudaError_t read_and_clear_kernel_error(uint32_t* out);
+// Test mode of the tensor-core kernels' bounded waits: the pipeline waits'
+// limit, and whether each CTA withholds its first chunk-complete signal.
+cudaError_t set_tc_wait_expiry(unsigned long long limit_ns, int withhold);
+
+// The linear on binary16 codes (linear_f16.cu): the same contraction and
+// epilogue as launch_linear, with q and w given as binary16 values.
+struct LinearF16Args {
+  const uint16_t* qh;   // [M, K] activation codes, row stride ldq elements
+  int64_t ldq;
+  const float* a_scale;
+  const uint16_t* wh;   // [N, K] weight codes, row stride ldw elements
+  int64_t ldw;
+  const float* w_scale;
+  const uint16_t* residual;
+  int64_t ldr;
+  uint16_t* out;
+  int64_t ldo;
+  int32_t* acc_out;
+  int64_t M, N, K;
+  int split;            // 0: balanced schedule; >= 1: explicit split-K
+  void* ws;             // workspace (256-byte aligned, zero between calls)
+  size_t ws_bytes;
+};
+size_t linear_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
+cudaError_t launch_linear_f16(const LinearF16Args& a, cudaStream_t stream);
+// int8 codes [rows, K] -> binary16 codes (exact), K % 16 == 0.
+cudaError_t launch_codes_to_f16(const int8_t* w, int64_t ldw, int64_t rows, int64_t K, uint16_t* wh, int64_t ldwh,
+                                cudaStream_t stream);
+cudaError_t read_and_clear_f16_status(uint32_t* out);
+cudaError_t set_f16_wait_expiry(unsigned long long limit_ns, int withhold);
 
 // SmoothQuant requantisation of Q8_0 weights (requant.cu).
 cudaError_t launch_smooth_requant(const int8_t* q, int64_t ldq, const uint16_t* d, int64_t ldd, const float* s,

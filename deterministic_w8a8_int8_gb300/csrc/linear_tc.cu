@@ -48,6 +48,7 @@
 //                       128-row MMA.
 // Split-K reuses the integer-atomic / last-arriver protocol of the workspace.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstdlib>
@@ -57,10 +58,18 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "tc_common.cuh"
+#include "tc_sched.cuh"
 
 namespace prism {
 
 __device__ uint32_t g_kernel_error = 0;
+// Limit of the pipeline waits (tests shorten it to drive the expiry path);
+// the teardown waits always use kWaitLimitNs.
+__device__ unsigned long long g_tc_wait_limit_ns = 2000000000ull;
+// Test mode of the expiry path (prism_debug_wait_expiry): each CTA's MMA
+// issuer withholds its first chunk-complete signal.
+__device__ int g_tc_withhold = 0;
 
 namespace {
 
@@ -102,52 +111,45 @@ struct TcParams {
   int vec_io;    // vector epilogue loads/stores allowed (16-byte aligned out/residual, ldo/ldr % 8 == 0)
   int nst;       // f16 operand stages, each kSub slots of (128 + bpiece) x 128 bytes
   int nst8;      // int8 staging stages, each (128 + bpiece) x 64 kSub bytes
-  int sched;     // 0: one tile (K piece) per CTA; 1: balanced schedule (see get_item)
-  int gx;        // A blocks of 128 rows (tile index = ty * gx + tx)
-  int T;         // tiles
-  int S;         // K stages of 64 kSub
-  int W;         // balanced schedule: rounds of whole tiles per CTA
-  int R;         // balanced schedule: tiles whose K units are shared out
+  SchedParams sp;  // work schedule (tc_sched.cuh); S counts stages of 64 kSub
   uint32_t* cnt;   // balanced schedule: arrival counters of the shared tiles (zero between calls)
   int32_t* acc;    // balanced schedule: one int32 accumulator per shared tile (zero between calls)
   int slot_elems;  // int32 elements of one accumulator (128 * bpiece)
 };
 
 // ------------------------------------------------------------ PTX helpers --
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n selp.u32 %0, 1, 0, P;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: true when the phase completed; false on timeout or when
-// another thread of the CTA has already given up.
+using tc::fence_proxy_async;
+using tc::globaltimer;
+using tc::idesc_f16_f32;
+using tc::mbar_arrive;
+using tc::mbar_expect_tx;
+using tc::mbar_init;
+using tc::mbar_try_wait;
+using tc::smem_desc_sw128;
+using tc::tc_commit;
+using tc::tc_fence_after;
+using tc::tc_fence_before;
+using tc::tc_mma;
+using tc::tma_load_2d;
+using tc::tmem_ld16;
+using tc::tmem_st16;
+using tc::tmem_wait_ld;
+using tc::tmem_wait_st;
+
+// Bounded wait (g_tc_wait_limit_ns, 2 s unless a test shortened it); an
+// expiry raises kDevErrTimeout in g_kernel_error.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
+  return tc::mbar_wait_bounded(bar, parity, abort_flag, *reinterpret_cast<volatile unsigned long long*>(&g_tc_wait_limit_ns),
+                               &g_kernel_error, kDevErrTimeout);
+}
+// Teardown wait: bounded by kWaitLimitNs, blind to the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicOr(&g_kernel_error, kDevErrTimeout);
-        return false;
-      }
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(&g_kernel_error, kDevErrTimeout);
+      return;
     }
   }
 }
@@ -156,59 +158,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // never splits around a single polling lane.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
-// 1024 bytes (stride between atoms = 1024 B), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused here), 16 B
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;             // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
-  return d;
-}
-// Instruction descriptor: f16 x f16 -> f32, both K-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_f16_f32(int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 }
 
 // Exact int8 -> f16 widening of 4 packed bytes: bias to u = b + 128 in
@@ -223,17 +172,6 @@ __device__ __forceinline__ void widen4(uint32_t x, uint32_t& lo, uint32_t& hi) {
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(p1), "r"(0x64806480u));
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-// 2-D TMA tile load (x = K byte offset, a multiple of 64; y = first row).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
 // 16-byte shared-memory load when pred holds, else zeros (predicated, no branch).
 __device__ __forceinline__ uint4 ld_shared_v4_if(uint32_t addr, bool pred) {
   uint4 v;
@@ -496,78 +434,6 @@ __device__ __forceinline__ void readback_swap(const TcParams& p, const float* s_
 }
 
 // ------------------------------------------------------------------ kernel --
-// One unit of work of a CTA: output tile (tx, ty) -- A block tx of 128 rows,
-// B piece ty of bpiece rows -- over the K stages [k0, k1) of 64.
-//   kind 0: the whole K range; the epilogue is applied directly.
-//   kind 1: one of a.split equal K pieces (explicit split-K): int32 atomics
-//           into the workspace tile; the last piece's CTA applies the epilogue.
-//   kind 2: a K range of a tile that the balanced schedule shares between
-//           CTAs: the partial int32 sums are added (integer reductions) into
-//           the tile's accumulator; the last CTA to finish the tile reads it
-//           back, re-zeroes it and applies the epilogue.
-struct Item {
-  int tx, ty, k0, k1, kind, tile;
-};
-
-// Work item n of this CTA; every role of the CTA walks the same list.
-//   sched 0: one item: tile (blockIdx.x, blockIdx.y), K piece blockIdx.z of
-//            a.split.
-//   sched 1 (balanced, G = gridDim.x CTAs): CTA b first takes whole tiles
-//            b, b + G, ... (W rounds, indices below T), then the K units
-//            [b U / G, (b + 1) U / G) of the last R tiles, U = R * S units of
-//            64 K and shared tile st covering units [st S, (st + 1) S).
-__device__ __forceinline__ bool get_item(const TcParams& p, int n, Item& it) {
-  if (p.sched == 0) {
-    if (n > 0) return false;
-    const int per = (p.S + p.a.split - 1) / p.a.split;
-    it.tx = static_cast<int>(blockIdx.x);
-    it.ty = static_cast<int>(blockIdx.y);
-    const int k0 = static_cast<int>(blockIdx.z) * per;
-    it.k0 = k0 < p.S ? k0 : p.S;
-    it.k1 = it.k0 + per < p.S ? it.k0 + per : p.S;
-    it.kind = p.a.split > 1 ? 1 : 0;
-    it.tile = it.ty * p.gx + it.tx;
-    return true;
-  }
-  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-  if (n < p.W) {
-    const int t = n * G + b;
-    if (t >= p.T) return false;
-    it.tx = t % p.gx;
-    it.ty = t / p.gx;
-    it.k0 = 0;
-    it.k1 = p.S;
-    it.kind = 0;
-    it.tile = t;
-    return true;
-  }
-  if (p.R == 0) return false;
-  // U * G < 2^31: R < 2 G, S <= 2081 (K <= 133144) and G <= 512 (sm_count's cap)
-  const int j = n - p.W;
-  const int U = p.R * p.S;
-  const int u0 = b * U / G, u1 = (b + 1) * U / G;
-  const int st = u0 / p.S + j;
-  const int ts = st * p.S;
-  if (u0 >= u1 || ts >= u1) return false;
-  const int t = p.W * G + st;
-  it.tx = t % p.gx;
-  it.ty = t / p.gx;
-  it.k0 = (u0 > ts ? u0 : ts) - ts;
-  it.k1 = (u1 < ts + p.S ? u1 : ts + p.S) - ts;
-  it.kind = (it.k0 == 0 && it.k1 == p.S) ? 0 : 2;
-  it.tile = st;
-  return true;
-}
-
-// CTAs bf..bl of the balanced schedule whose K ranges meet shared tile st
-// (the CTA holding unit u is floor(((u + 1) G - 1) / U)).
-__device__ __forceinline__ void shared_tile_ctas(const TcParams& p, int st, int& bf, int& bl) {
-  const int G = static_cast<int>(gridDim.x);
-  const int U = p.R * p.S;
-  bf = ((st * p.S + 1) * G - 1) / U;
-  bl = ((st * p.S + p.S) * G - 1) / U;
-}
-
 
 // Worker wt's share of an item's epilogue scales: a_scale of token wt of the
 // tile (wt < 256) or w_scale of channel wt - 256 (0 beyond the tile or matrix).
@@ -666,13 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     // ======================= MMA issuer (one thread) =========================
     if (lane == 0) {
+      const bool withhold = *reinterpret_cast<volatile int*>(&g_tc_withhold) != 0;
       int s = 0;
       uint32_t ph = 0;  // stage slot and its phase parity, advanced incrementally
       int c = -1;       // chunk counter over all items
       uint32_t dcol = kColD, dbar = 0;
       bool ok = true, issued = false;
       Item itm;
-      for (int n = 0; ok && get_item(p, n, itm); ++n) {
+      for (int n = 0; ok && get_item(p.sp, n, itm); ++n) {
         const int nk = itm.k1 - itm.k0;
         const uint32_t idesc = idesc_f16_f32(tile_width(itm.ty));
         for (int it = 0; it < nk; ++it) {
@@ -708,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           issued = true;
           tc_commit(bar_empty + 8 * s);
-          if (cpos == kChunkL - 1 || it == nk - 1) tc_commit(bar_acc_full + 8 * dbar);
+          if ((cpos == kChunkL - 1 || it == nk - 1) && !(withhold && c == 0)) tc_commit(bar_acc_full + 8 * dbar);
           if (++s == nst) {
             s = 0;
             ph ^= 1u;
@@ -718,13 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issued) {
         // every MMA issued above has completed before TMEM is released
         tc_commit(bar_done);
-        const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(bar_done, 0)) {
-          if (globaltimer() - t0 > kWaitLimitNs) {
-            atomicOr(&g_kernel_error, kDevErrTimeout);
-            break;
-          }
-        }
+        mbar_wait_drain(bar_done, 0);
       }
     }
     __syncwarp();
@@ -734,9 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tx = static_cast<uint32_t>(kS8A + kBK8 * p.bpiece);
       int j = 0;
       uint32_t ph = 0;
+      int64_t issued = 0;
       bool ok = true;
       Item itm;
-      for (int n = 0; ok && get_item(p, n, itm); ++n) {
+      for (int n = 0; ok && get_item(p.sp, n, itm); ++n) {
         const int32_t ya = itm.tx * kBM, yb = itm.ty * p.bpiece;
         for (int it = itm.k0; it < itm.k1; ++it) {
           if (!mbar_wait(bar_s8_empty + 8 * j, ph ^ 1u, s_abort)) {
@@ -748,12 +610,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(bar_s8_full + 8 * j, tx);
           tma_load_2d(dst, &tmA, x, ya, bar_s8_full + 8 * j);
           tma_load_2d(dst + kS8A, &tmB, x, yb, bar_s8_full + 8 * j);
+          ++issued;
           if (++j == nst8) {
             j = 0;
             ph ^= 1u;
           }
         }
       }
+      // Before the CTA may exit, every load issued must have landed: after an
+      // expired wait the workers may stop consuming stages whose loads are
+      // still in flight.  Stage x completes phase x / nst8 of slot x % nst8;
+      // loads that were consumed pass at once.
+      for (int64_t x = issued > nst8 ? issued - nst8 : 0; x < issued; ++x)
+        mbar_wait_drain(bar_s8_full + 8 * static_cast<uint32_t>(x % nst8), static_cast<uint32_t>((x / nst8) & 1));
     }
     __syncwarp();
   } else {
@@ -853,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* s_scale = s_as;
     {
       Item first;
-      s_scale[wt] = get_item(p, 0, first) ? item_scale(p, first, tile_width(first.ty), wt) : 0.f;
+      s_scale[wt] = get_item(p.sp, 0, first) ? item_scale(p, first, tile_width(first.ty), wt) : 0.f;
     }
     for (int n = 0;; ++n) {
       int bn, nk;
@@ -861,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (only n stays live through the stage loop; the item is looked up
         // again for its output)
         Item itm;
-        if (!get_item(p, n, itm)) break;
+        if (!get_item(p.sp, n, itm)) break;
         // the previous item's output is finished and this item's scales are
         // in place
         asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
@@ -956,14 +825,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- the item's last chunk: drain straight into its output
       Item itm;
-      get_item(p, n, itm);
+      get_item(p.sp, n, itm);
       const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
       const float* sa = s_scale + (n & 1) * (2 * kBNMax);
       const float* sw = sa + kBNMax;
       float sc_next;  // loaded now, stored after the output (its latency overlaps)
       {
         Item nx;
-        sc_next = get_item(p, n + 1, nx) ? item_scale(p, nx, tile_width(nx.ty), wt) : 0.f;
+        sc_next = get_item(p.sp, n + 1, nx) ? item_scale(p, nx, tile_width(nx.ty), wt) : 0.f;
       }
       const bool have = ok && nchunks > 0;
       const int glast = gc + nchunks - 1;
@@ -991,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
         int bf = 0, bl = 0;
-        if (itm.kind == 2) shared_tile_ctas(p, itm.tile, bf, bl);
+        if (itm.kind == 2) shared_tile_ctas(p.sp, itm.tile, bf, bl);
         const unsigned target = itm.kind == 1 ? static_cast<unsigned>(a.split - 1) : static_cast<unsigned>(bl - bf);
         uint32_t* counter = itm.kind == 1 ? a.ws_count + itm.tile : p.cnt + itm.tile;
         // release: every worker's reductions reached thread 0 through the
@@ -1088,20 +957,6 @@ static TcPlan tc_plan(int64_t M, int64_t N, int64_t K) {
   return pl;
 }
 
-// The balanced schedule for T tiles of S K-stages on the device's SMs (see
-// get_item): whole tiles in W rounds over G CTAs, then the K units of the
-// last R tiles shared out evenly.  Shares below one 1024-K chunk per CTA are
-// not worth their partial-sum traffic: then one round fewer of whole tiles
-// is taken, or, with few tiles, fewer CTAs share them, or (little K) only
-// whole tiles are used.
-struct TcSched {
-  int G, W, R;
-};
-
-}  // namespace prism
-#include <atomic>
-namespace prism {
-
 // Streaming multiprocessors of the current device (152 on a GB300), queried
 // once per device; the balanced schedule runs one CTA per SM.  Without a
 // usable device (a host that only sizes workspaces) the GB300's count is
@@ -1126,29 +981,10 @@ int sm_count() {
   return n;
 }
 
+// The balanced schedule (tc_sched.cuh) over this device's SMs; a share of
+// less than one 1024-K chunk per CTA is not worth its partial sums.
 static TcSched tc_balanced(int64_t T, int64_t S, int sub) {
-  const int64_t kSMs = sm_count();
-  const int64_t kMinUnits = kChunkStages / sub;
-  TcSched sc{static_cast<int>(kSMs), 0, 0};
-  if (T % kSMs == 0) {
-    sc.W = static_cast<int>(T / kSMs);
-    return sc;
-  }
-  int64_t W = T / kSMs, R = T - W * kSMs;
-  if (R * S < kMinUnits * kSMs && W >= 1) {
-    W -= 1;
-    R += kSMs;
-  }
-  if (R * S >= kMinUnits * kSMs) {
-    sc.W = static_cast<int>(W);
-    sc.R = static_cast<int>(R);
-  } else if (W == 0) {
-    sc.G = static_cast<int>(std::max<int64_t>(R, std::min<int64_t>(kSMs, R * S / kMinUnits)));
-    sc.R = static_cast<int>(R);
-  } else {
-    sc.W = static_cast<int>(cdiv(T, kSMs));
-  }
-  return sc;
+  return tc_balanced_sched(T, S, kChunkStages / sub, sm_count());
 }
 
 // Workspace of the balanced schedule: tile counters, then one int32
@@ -1228,13 +1064,14 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   p.nst = pl.sub == 2 ? 2 : 3;
   p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * pl.sub * (kBM + pl.bpiece) * 128) /
                                     ((kBM + pl.bpiece) * kBK * pl.sub));
-  p.gx = static_cast<int>(pl.grid_x);
-  p.T = static_cast<int>(pl.grid_x * pl.grid_y);
-  p.S = static_cast<int>(cdiv(a.K, kBK * pl.sub));
+  p.sp.split = a.split;
+  p.sp.gx = static_cast<int>(pl.grid_x);
+  p.sp.T = static_cast<int>(pl.grid_x * pl.grid_y);
+  p.sp.S = static_cast<int>(cdiv(a.K, kBK * pl.sub));
   dim3 grid;
   if (a.split >= 1) {
     // explicit split-K: one CTA per tile and K piece; int32 atomics when split
-    p.sched = 0;
+    p.sp.sched = 0;
     if (a.split > 1) {
       p.a.ws_acc = static_cast<int32_t*>(a.ws);
       p.a.ws_count = reinterpret_cast<uint32_t*>(
@@ -1245,22 +1082,22 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   } else {
     // automatic: the balanced schedule, falling back to whole tiles in rounds
     // when the caller's workspace cannot hold the shared tiles' partials
-    p.sched = 1;
-    TcSched sc = tc_balanced(p.T, p.S, pl.sub);
+    p.sp.sched = 1;
+    TcSched sc = tc_balanced(p.sp.T, p.sp.S, pl.sub);
     size_t cb = 0;
     const size_t need = tc_balanced_bytes(a.M, a.N, a.K, &cb);
     if (need > 0 && need > a.ws_bytes) {
       const int g = sm_count();
-      sc = TcSched{g, static_cast<int>(cdiv(p.T, g)), 0};
+      sc = TcSched{g, static_cast<int>(cdiv(p.sp.T, g)), 0};
     }
     if (sc.R > 0 && need > 0) {
       p.cnt = static_cast<uint32_t*>(a.ws);
       p.acc = reinterpret_cast<int32_t*>(static_cast<char*>(a.ws) + cb);
     }
-    p.W = sc.W;
-    p.R = sc.R;
+    p.sp.W = sc.W;
+    p.sp.R = sc.R;
     p.slot_elems = kBM * pl.bpiece;
-    const int64_t ctas = sc.R > 0 ? sc.G : std::min<int64_t>(sc.G, p.T);
+    const int64_t ctas = sc.R > 0 ? sc.G : std::min<int64_t>(sc.G, p.sp.T);
     grid = dim3(static_cast<unsigned>(ctas), 1, 1);
   }
   CUtensorMap tmA, tmB;
@@ -1330,6 +1167,12 @@ cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream) {
         ((static_cast<size_t>(a.M) * static_cast<size_t>(a.N) * 4 + 255) & ~static_cast<size_t>(255)));
   }
   return launch_linear_mma(b, stream);
+}
+
+cudaError_t set_tc_wait_expiry(unsigned long long limit_ns, int withhold) {
+  cudaError_t e = cudaMemcpyToSymbol(g_tc_wait_limit_ns, &limit_ns, sizeof limit_ns);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_tc_withhold, &withhold, sizeof withhold);
+  return e;
 }
 
 cudaError_t read_and_clear_kernel_error(uint32_t* out) {

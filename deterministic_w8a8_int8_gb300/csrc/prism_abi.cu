@@ -279,7 +279,19 @@ int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K) { return prism::line
 
 int prism_device_status(uint32_t* flags) {
   if (flags == nullptr) return PRISM_ERR_INVALID_ARG;
-  return prism::record_cuda(prism::read_and_clear_kernel_error(flags));
+  uint32_t a = 0, b = 0;
+  int st = prism::record_cuda(prism::read_and_clear_kernel_error(&a));
+  if (st == PRISM_OK) st = prism::record_cuda(prism::read_and_clear_f16_status(&b));
+  *flags = a | b;
+  return st;
+}
+
+int prism_debug_wait_expiry(uint64_t limit_ns) {
+  const unsigned long long v = limit_ns == 0 ? 2000000000ull : static_cast<unsigned long long>(limit_ns);
+  const int withhold = limit_ns != 0 ? 1 : 0;
+  int st = prism::record_cuda(prism::set_tc_wait_expiry(v, withhold));
+  if (st == PRISM_OK) st = prism::record_cuda(prism::set_f16_wait_expiry(v, withhold));
+  return st;
 }
 
 int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K) { return prism::linear_auto_split(M, N, K); }
@@ -355,6 +367,101 @@ int prism_w8a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
                       void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return linear_impl(q, ldq, a_scale, w, ldw, w_scale, residual_bf16, ldr, out_bf16, ldo, acc_out, M, N, K, split_k,
                      workspace, workspace_bytes, nullptr, 0, nullptr, 0, cuda_stream);
+}
+
+int prism_quant_act_f16(const void* x_bf16, int64_t ldx, const float* inv_smooth, int64_t M, int64_t K,
+                        uint16_t* qh, int64_t ldqh, float* a_scale, void* cuda_stream) {
+  if (M < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (M == 0) return PRISM_OK;
+  if (x_bf16 == nullptr || qh == nullptr || a_scale == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldx < K || ldqh < K) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+  if (ldx % 8 != 0 || ldqh % 8 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(x_bf16, 16) || !aligned(qh, 16) || !aligned(a_scale, 4)) return PRISM_ERR_ALIGNMENT;
+  if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
+  if (M > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  prism::QuantCall c{};
+  c.x = x_bf16;
+  c.ldx = ldx;
+  c.inv_s = inv_smooth;
+  c.M = M;
+  c.K = K;
+  c.a_scale = a_scale;
+  c.M_x = M;
+  c.qh = qh;
+  c.ldqh = ldqh;
+  return prism::record_cuda(prism::launch_quant(c, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int prism_codes_to_f16(const int8_t* w, int64_t ldw, int64_t rows, int64_t K, uint16_t* wh, int64_t ldwh,
+                       void* cuda_stream) {
+  if (rows < 0 || K <= 0) return PRISM_ERR_INVALID_ARG;
+  if (rows == 0) return PRISM_OK;
+  if (w == nullptr || wh == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldw < K || ldwh < K) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0 || ldw % 16 != 0 || ldwh % 8 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(w, 16) || !aligned(wh, 16)) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_K || rows > (static_cast<int64_t>(1) << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  // the binary16 rows must not overlap the int8 rows they are made from
+  const uintptr_t w0 = reinterpret_cast<uintptr_t>(w), h0 = reinterpret_cast<uintptr_t>(wh);
+  const uintptr_t w1 = w0 + static_cast<uintptr_t>((rows - 1) * ldw + K);
+  const uintptr_t h1 = h0 + static_cast<uintptr_t>((rows - 1) * ldwh + K) * 2;
+  if (w0 < h1 && h0 < w1) return PRISM_ERR_INVALID_ARG;
+  return prism::record_cuda(prism::launch_codes_to_f16(w, ldw, rows, K, wh, ldwh,
+                                                       static_cast<cudaStream_t>(cuda_stream)));
+}
+
+size_t prism_w8a8_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+  if (M <= 0 || N <= 0 || K <= 0 || split_k < 0 || split_k > PRISM_MAX_SPLIT_K) return 0;
+  return prism::linear_f16_workspace_bytes(M, N, K, split_k);
+}
+
+int prism_w8a8_linear_f16(const uint16_t* qh, int64_t ldq, const float* a_scale, const uint16_t* wh, int64_t ldw,
+                          const float* w_scale, const void* residual_bf16, int64_t ldr, void* out_bf16, int64_t ldo,
+                          int32_t* acc_out, int64_t M, int64_t N, int64_t K, int split_k, void* workspace,
+                          size_t workspace_bytes, void* cuda_stream) {
+  if (M < 0 || N < 0 || K <= 0 || split_k < 0) return PRISM_ERR_INVALID_ARG;
+  if (split_k > PRISM_MAX_SPLIT_K) return PRISM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return PRISM_OK;
+  if (qh == nullptr || wh == nullptr || a_scale == nullptr || w_scale == nullptr || out_bf16 == nullptr)
+    return PRISM_ERR_INVALID_ARG;
+  if (ldq < K || ldw < K || ldo < N || (residual_bf16 != nullptr && ldr < N)) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_K) return PRISM_ERR_UNSUPPORTED;
+  if (ldq % 8 != 0 || ldw % 8 != 0) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(qh, 16) || !aligned(wh, 16) || !aligned(out_bf16, 2) || !aligned(a_scale, 4) ||
+      !aligned(w_scale, 4))
+    return PRISM_ERR_ALIGNMENT;
+  if (residual_bf16 != nullptr && !aligned(residual_bf16, 2)) return PRISM_ERR_ALIGNMENT;
+  if (acc_out != nullptr && !aligned(acc_out, 4)) return PRISM_ERR_ALIGNMENT;
+  // tile indices and grid dimensions stay within int32 and the launch limits
+  if (((M + 127) / 128) * ((N + 127) / 128) > (1LL << 31) - 1 || (N + 255) / 256 > 65535)
+    return PRISM_ERR_UNSUPPORTED;
+  const size_t need = prism::linear_f16_workspace_bytes(M, N, K, split_k);
+  prism::LinearF16Args a{};
+  a.qh = qh;
+  a.ldq = ldq;
+  a.a_scale = a_scale;
+  a.wh = wh;
+  a.ldw = ldw;
+  a.w_scale = w_scale;
+  a.residual = static_cast<const uint16_t*>(residual_bf16);
+  a.ldr = ldr;
+  a.out = static_cast<uint16_t*>(out_bf16);
+  a.ldo = ldo;
+  a.acc_out = acc_out;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.split = split_k;
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need) return PRISM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PRISM_ERR_ALIGNMENT;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+  }
+  return prism::record_cuda(prism::launch_linear_f16(a, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int prism_w8a8_linear_rows(const int8_t* q, int64_t ldq, const float* a_scale, const int8_t* w, int64_t ldw,

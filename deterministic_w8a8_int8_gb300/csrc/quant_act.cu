@@ -12,6 +12,8 @@
 // registers while they fit (CACHE vectors of 8 per thread), reduces amax with
 // warp shuffles, pass 2 quantises from registers (or re-reads the row from L2
 // when it is longer than the cache) and stores 8-byte int8 vectors.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace prism {
@@ -73,12 +75,28 @@ __device__ __forceinline__ float vmaxabs(const Vec8& r, float m) {
 // scale from the given maxima amax_io (the maximum over the ranks).
 enum QuantMode { kPlain = 0, kRows = 1, kAmaxOut = 2, kAmaxIn = 3 };
 
-template <int TEAM, int CACHE, int kMode>
+// The codes of 4 values (see quant4) as two packed binary16 pairs: integers
+// of at most 127 in magnitude, so the conversions are exact.
+__device__ __forceinline__ uint2 quant4_f16(float a, float b, float c, float d, float inv_a) {
+  const int qa = max(-127, min(127, __float2int_rn(__fmul_rn(a, inv_a))));
+  const int qb = max(-127, min(127, __float2int_rn(__fmul_rn(b, inv_a))));
+  const int qc = max(-127, min(127, __float2int_rn(__fmul_rn(c, inv_a))));
+  const int qd = max(-127, min(127, __float2int_rn(__fmul_rn(d, inv_a))));
+  const __half2 lo = __halves2half2(__int2half_rn(qa), __int2half_rn(qb));
+  const __half2 hi = __halves2half2(__int2half_rn(qc), __int2half_rn(qd));
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+// kHalf: the codes are stored as binary16 values (qh, row stride ldqh
+// elements) instead of int8 -- the operand form of the tensor-core kernel
+// that reads f16 codes (linear_f16.cu).  Only with kPlain.
+template <int TEAM, int CACHE, int kMode, bool kHalf>
 __global__ void __launch_bounds__(kBlock)
     quant_act_kernel(const uint16_t* __restrict__ x, int64_t ldx, const float* __restrict__ inv_s,
                      int64_t M, int64_t K, int8_t* __restrict__ q, int64_t ldq,
                      float* __restrict__ a_scale, const int32_t* __restrict__ rows, int64_t M_x,
-                     uint32_t* err, float* __restrict__ amax_io) {
+                     uint32_t* err, float* __restrict__ amax_io, uint16_t* __restrict__ qh, int64_t ldqh) {
+  static_assert(!kHalf || kMode == kPlain, "binary16 codes only for the plain quantiser");
   constexpr int kTeams = kBlock / TEAM;
   constexpr int kWarpsPerTeam = TEAM / 32;
   __shared__ float red[kBlock / 32];
@@ -139,25 +157,26 @@ __global__ void __launch_bounds__(kBlock)
   const bool zero_row = !(amax >= 0x1p-120f);
   const float inv_a = zero_row ? 0.0f : __fdiv_rn(127.0f, amax);
   if (lt == 0) a_scale[m] = zero_row ? 0.0f : __fdiv_rn(amax, 127.0f);
-
-#pragma unroll
-  for (int c = 0; c < CACHE; ++c) {
-    const int64_t v = lt + static_cast<int64_t>(c) * TEAM;
-    if (v < nvec) {
-      const Vec8& r = cache[c];
+  auto store8 = [&](const Vec8& r, int64_t v) {
+    if constexpr (kHalf) {
+      const uint2 lo = quant4_f16(r.v[0], r.v[1], r.v[2], r.v[3], inv_a);
+      const uint2 hi = quant4_f16(r.v[4], r.v[5], r.v[6], r.v[7], inv_a);
+      *reinterpret_cast<uint4*>(qh + m * ldqh + v * 8) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    } else {
       uint2 o;
       o.x = quant4(r.v[0], r.v[1], r.v[2], r.v[3], inv_a);
       o.y = quant4(r.v[4], r.v[5], r.v[6], r.v[7], inv_a);
       *reinterpret_cast<uint2*>(qr + v * 8) = o;
     }
+  };
+
+#pragma unroll
+  for (int c = 0; c < CACHE; ++c) {
+    const int64_t v = lt + static_cast<int64_t>(c) * TEAM;
+    if (v < nvec) store8(cache[c], v);
   }
-  for (int64_t v = lt + static_cast<int64_t>(CACHE) * TEAM; v < nvec; v += TEAM) {
-    const Vec8 r = load_smoothed(xr, inv_s, v * 8);
-    uint2 o;
-    o.x = quant4(r.v[0], r.v[1], r.v[2], r.v[3], inv_a);
-    o.y = quant4(r.v[4], r.v[5], r.v[6], r.v[7], inv_a);
-    *reinterpret_cast<uint2*>(qr + v * 8) = o;
-  }
+  for (int64_t v = lt + static_cast<int64_t>(CACHE) * TEAM; v < nvec; v += TEAM)
+    store8(load_smoothed(xr, inv_s, v * 8), v);
 }
 
 // ----------------------------------------------------------------------
@@ -190,6 +209,8 @@ struct PArgs {
   int64_t M_x;
   uint32_t* err;
   float* amax_io;
+  uint16_t* qh;      // binary16 codes out (kHalf), row stride ldqh elements
+  int64_t ldqh;
 };
 
 __device__ __forceinline__ float2 smooth2(uint32_t pair, float4 s, int half) {
@@ -197,9 +218,10 @@ __device__ __forceinline__ float2 smooth2(uint32_t pair, float4 s, int half) {
   return __fmul2_rn(v, half ? make_float2(s.z, s.w) : make_float2(s.x, s.y));
 }
 
-template <int C, int P, int kMode>
+template <int C, int P, int kMode, bool kHalf>
 __global__ void __launch_bounds__(kPMaxTeam)
     quant_persist_kernel(const __grid_constant__ PArgs a) {
+  static_assert(!kHalf || kMode == kPlain, "binary16 codes only for the plain quantiser");
   extern __shared__ float4 s_sm[];   // [2][K/8]
   __shared__ uint32_t red[2][kPMaxTeam / 32];
   pdl_trigger();
@@ -309,9 +331,26 @@ __global__ void __launch_bounds__(kPMaxTeam)
             b[2 * e] = __float_as_uint(__fadd_rn(lo, 12582912.0f));
             b[2 * e + 1] = __float_as_uint(__fadd_rn(hi, 12582912.0f));
           }
-          const uint32_t w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040u), __byte_perm(b[2], b[3], 0x0040u), 0x5410u);
-          const uint32_t w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040u), __byte_perm(b[6], b[7], 0x0040u), 0x5410u);
-          *reinterpret_cast<uint2*>(qr + 8 * static_cast<int64_t>(j)) = make_uint2(w0, w1);
+          if constexpr (kHalf) {
+            // the integer r = rint_even(t) back as a float (the subtraction of
+            // 1.5 * 2^23 is exact), then exactly to binary16
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __fsub_rn(__uint_as_float(b[2 * e]), 12582912.0f);
+              const float hi = __fsub_rn(__uint_as_float(b[2 * e + 1]), 12582912.0f);
+              const __half2 hv = __floats2half2_rn(lo, hi);
+              h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            *reinterpret_cast<uint4*>(a.qh + r * a.ldqh + 8 * static_cast<int64_t>(j)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
+          } else {
+            const uint32_t w0 =
+                __byte_perm(__byte_perm(b[0], b[1], 0x0040u), __byte_perm(b[2], b[3], 0x0040u), 0x5410u);
+            const uint32_t w1 =
+                __byte_perm(__byte_perm(b[4], b[5], 0x0040u), __byte_perm(b[6], b[7], 0x0040u), 0x5410u);
+            *reinterpret_cast<uint2*>(qr + 8 * static_cast<int64_t>(j)) = make_uint2(w0, w1);
+          }
         }
       }
     }
@@ -339,10 +378,13 @@ cudaError_t launch_persist(const QuantCall& c, int team, cudaStream_t stream) {
   p.M_x = c.rows != nullptr ? c.M_x : c.M;
   p.err = c.err;
   p.amax_io = c.amax_out != nullptr ? c.amax_out : const_cast<float*>(c.amax_in);
-  auto kernel = c.rows != nullptr      ? quant_persist_kernel<C, P, kRows>
-                : c.amax_out != nullptr ? quant_persist_kernel<C, P, kAmaxOut>
-                : c.amax_in != nullptr  ? quant_persist_kernel<C, P, kAmaxIn>
-                                        : quant_persist_kernel<C, P, kPlain>;
+  p.qh = c.qh;
+  p.ldqh = c.ldqh;
+  auto kernel = c.qh != nullptr         ? quant_persist_kernel<C, P, kPlain, true>
+                : c.rows != nullptr     ? quant_persist_kernel<C, P, kRows, false>
+                : c.amax_out != nullptr ? quant_persist_kernel<C, P, kAmaxOut, false>
+                : c.amax_in != nullptr  ? quant_persist_kernel<C, P, kAmaxIn, false>
+                                        : quant_persist_kernel<C, P, kPlain, false>;
   const size_t smem = static_cast<size_t>(c.K) * sizeof(float);
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), static_cast<int>(smem));
   int dev = 0, sms = 0, per_sm = 0;
@@ -360,14 +402,15 @@ template <int TEAM, int CACHE>
 cudaError_t launch_team(const QuantCall& c, cudaStream_t stream) {
   constexpr int kTeams = kBlock / TEAM;
   const int64_t blocks = (c.M + kTeams - 1) / kTeams;
-  auto kernel = c.rows != nullptr      ? quant_act_kernel<TEAM, CACHE, kRows>
-                : c.amax_out != nullptr ? quant_act_kernel<TEAM, CACHE, kAmaxOut>
-                : c.amax_in != nullptr  ? quant_act_kernel<TEAM, CACHE, kAmaxIn>
-                                        : quant_act_kernel<TEAM, CACHE, kPlain>;
+  auto kernel = c.qh != nullptr         ? quant_act_kernel<TEAM, CACHE, kPlain, true>
+                : c.rows != nullptr     ? quant_act_kernel<TEAM, CACHE, kRows, false>
+                : c.amax_out != nullptr ? quant_act_kernel<TEAM, CACHE, kAmaxOut, false>
+                : c.amax_in != nullptr  ? quant_act_kernel<TEAM, CACHE, kAmaxIn, false>
+                                        : quant_act_kernel<TEAM, CACHE, kPlain, false>;
   float* amax_io = c.amax_out != nullptr ? c.amax_out : const_cast<float*>(c.amax_in);
   return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kBlock), 0, stream, true,
                        static_cast<const uint16_t*>(c.x), c.ldx, c.inv_s, c.M, c.K, c.q, c.ldq, c.a_scale, c.rows,
-                       c.rows != nullptr ? c.M_x : c.M, c.err, amax_io);
+                       c.rows != nullptr ? c.M_x : c.M, c.err, amax_io, c.qh, c.ldqh);
 }
 
 }  // namespace

@@ -1,0 +1,129 @@
+// tc_sched.cuh -- the work schedule of the persistent tcgen05 contraction
+// kernels: which output tile and which range of K stages each CTA computes.
+//
+// Output tile (tx, ty) is A block tx (128 rows) by B piece ty; tile index
+// t = ty * gx + tx.  K is cut into S stages of 64 elements.
+//   sched 0: one item per CTA: tile (blockIdx.x, blockIdx.y), K piece
+//            blockIdx.z of `split` equal pieces (explicit split-K; the
+//            pieces' int32 partial sums are added with integer atomics).
+//   sched 1: the balanced schedule over G = gridDim.x CTAs: CTA b first
+//            takes whole tiles b, b + G, ... (W rounds, indices below T),
+//            then the K stages [b U / G, (b + 1) U / G) of the last R tiles,
+//            U = R * S, shared tile st covering stages [st S, (st + 1) S).
+//            Every CTA gets the same number of stages; a tile shared by
+//            several CTAs has their int32 partial sums added (integer
+//            reductions) into its accumulator slot, and the last CTA to
+//            finish the tile reads the slot back and applies the epilogue.
+// Integer addition is order-free, so no choice here changes a result bit.
+#pragma once
+
+#include <algorithm>
+#include <cstdint>
+
+namespace prism {
+
+struct SchedParams {
+  int sched;  // 0: one item per CTA (explicit split-K); 1: balanced
+  int split;  // explicit split-K factor (sched 0)
+  int gx;     // A blocks of 128 rows
+  int T;      // tiles
+  int S;      // K stages of 64 elements
+  int W;      // balanced: rounds of whole tiles per CTA
+  int R;      // balanced: tiles whose K stages are shared out
+};
+
+// One unit of work: tile (tx, ty) over K stages [k0, k1).
+//   kind 0: the whole K range; the epilogue is applied directly.
+//   kind 1: one of `split` equal K pieces (explicit split-K).
+//   kind 2: a K range of a tile the balanced schedule shares between CTAs.
+struct Item {
+  int tx, ty, k0, k1, kind, tile;
+};
+
+// Work item n of this CTA; every role of the CTA walks the same list.
+__device__ __forceinline__ bool get_item(const SchedParams& p, int n, Item& it) {
+  if (p.sched == 0) {
+    if (n > 0) return false;
+    const int per = (p.S + p.split - 1) / p.split;
+    it.tx = static_cast<int>(blockIdx.x);
+    it.ty = static_cast<int>(blockIdx.y);
+    const int k0 = static_cast<int>(blockIdx.z) * per;
+    it.k0 = k0 < p.S ? k0 : p.S;
+    it.k1 = it.k0 + per < p.S ? it.k0 + per : p.S;
+    it.kind = p.split > 1 ? 1 : 0;
+    it.tile = it.ty * p.gx + it.tx;
+    return true;
+  }
+  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  if (n < p.W) {
+    const int t = n * G + b;
+    if (t >= p.T) return false;
+    it.tx = t % p.gx;
+    it.ty = t / p.gx;
+    it.k0 = 0;
+    it.k1 = p.S;
+    it.kind = 0;
+    it.tile = t;
+    return true;
+  }
+  if (p.R == 0) return false;
+  // U * G < 2^31: R < 2 G, S <= 2081 (K <= 133144) and G <= 512 (sm_count's cap)
+  const int j = n - p.W;
+  const int U = p.R * p.S;
+  const int u0 = b * U / G, u1 = (b + 1) * U / G;
+  const int st = u0 / p.S + j;
+  const int ts = st * p.S;
+  if (u0 >= u1 || ts >= u1) return false;
+  const int t = p.W * G + st;
+  it.tx = t % p.gx;
+  it.ty = t / p.gx;
+  it.k0 = (u0 > ts ? u0 : ts) - ts;
+  it.k1 = (u1 < ts + p.S ? u1 : ts + p.S) - ts;
+  it.kind = (it.k0 == 0 && it.k1 == p.S) ? 0 : 2;
+  it.tile = st;
+  return true;
+}
+
+// CTAs bf..bl of the balanced schedule whose K ranges meet shared tile st
+// (the CTA holding unit u is floor(((u + 1) G - 1) / U)).
+__device__ __forceinline__ void shared_tile_ctas(const SchedParams& p, int st, int& bf, int& bl) {
+  const int G = static_cast<int>(gridDim.x);
+  const int U = p.R * p.S;
+  bf = ((st * p.S + 1) * G - 1) / U;
+  bl = ((st * p.S + p.S) * G - 1) / U;
+}
+
+// The balanced schedule for T tiles of S K-stages on `sms` CTAs: whole tiles
+// in W rounds, then the K stages of the last R tiles shared out evenly.
+// Shares below min_units stages (one exact 1024-K chunk) per CTA are not
+// worth their partial-sum traffic: then one round fewer of whole tiles is
+// taken, or, with few tiles, fewer CTAs share them, or (little K) only whole
+// tiles are used.
+struct TcSched {
+  int G, W, R;
+};
+
+inline TcSched tc_balanced_sched(int64_t T, int64_t S, int64_t min_units, int64_t sms) {
+  TcSched sc{static_cast<int>(sms), 0, 0};
+  if (T % sms == 0) {
+    sc.W = static_cast<int>(T / sms);
+    return sc;
+  }
+  int64_t W = T / sms, R = T - W * sms;
+  if (R * S < min_units * sms && W >= 1) {
+    W -= 1;
+    R += sms;
+  }
+  if (R * S >= min_units * sms) {
+    sc.W = static_cast<int>(W);
+    sc.R = static_cast<int>(R);
+  } else if (W == 0) {
+    sc.G = static_cast<int>(std::max<int64_t>(R, std::min<int64_t>(sms, R * S / min_units)));
+    sc.R = static_cast<int>(R);
+  } else {
+    sc.W = static_cast<int>((T + sms - 1) / sms);
+  }
+  return sc;
+}
+
+}  // namespace prism

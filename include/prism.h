@@ -284,6 +284,51 @@ int prism_w4a8_linear(const int8_t *q, int64_t ldq, const float *a_scale,
 int prism_unpack_w4(const uint8_t *w4, int64_t ldw4, int64_t N, int64_t K,
                     int8_t *w, int64_t ldw, void *cuda_stream);
 
+/*
+ * The linear with its codes held as binary16 values.  sm_103a's tensor cores
+ * have no integer MMA; their f16 MMA is exact on int8 codes (every code is
+ * exact in binary16, every product exact in the fp32 accumulator, and the
+ * kernel drains the accumulator into int32 every 1024 K, below 2^24).  Held
+ * as binary16 in memory, the codes go from global memory to the MMA by TMA
+ * alone, without the shared-memory widening pass of prism_w8a8_linear: the
+ * faster route for compute-bound calls (hundreds of token rows and more), at
+ * twice the operand bytes.  The results are prism_w8a8_linear's, bit for bit
+ * (StartLux-Prism, "Bitwise consistency is not lossless quantization").
+ *
+ * prism_quant_act_f16 -- prism_quant_act writing each code as a binary16
+ * value (exact integers in [-127, 127]).
+ *   qh, ldqh   [M, K] binary16 out (ldqh % 8 == 0, 16-byte aligned)
+ *   every other argument and rule as prism_quant_act.
+ */
+int prism_quant_act_f16(const void *x_bf16, int64_t ldx, const float *inv_smooth,
+                        int64_t M, int64_t K, uint16_t *qh, int64_t ldqh,
+                        float *a_scale, void *cuda_stream);
+
+/* int8 codes [rows, K] -> the same codes as binary16 [rows, K] (exact), the
+ * weight operand of prism_w8a8_linear_f16; a load-time step.  K % 16 == 0,
+ * ldw % 16 == 0, ldwh % 8 == 0, both 16-byte aligned, no overlap. */
+int prism_codes_to_f16(const int8_t *w, int64_t ldw, int64_t rows, int64_t K,
+                       uint16_t *wh, int64_t ldwh, void *cuda_stream);
+
+/* Workspace bytes prism_w8a8_linear_f16 needs (split_k as in that call). */
+size_t prism_w8a8_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+/*
+ * prism_w8a8_linear_f16 -- prism_w8a8_linear on binary16 codes:
+ *   qh, ldq    [M, K] activation codes (prism_quant_act_f16), ldq % 8 == 0
+ *   wh, ldw    [N, K] weight codes (prism_codes_to_f16), ldw % 8 == 0
+ *   every other argument, the workspace rules (sized by
+ *   prism_w8a8_f16_workspace_bytes) and the result as prism_w8a8_linear.
+ * Codes must be integers in [-127, 127]; other binary16 values void the
+ * exactness argument.
+ */
+int prism_w8a8_linear_f16(const uint16_t *qh, int64_t ldq, const float *a_scale,
+                          const uint16_t *wh, int64_t ldw, const float *w_scale,
+                          const void *residual_bf16, int64_t ldr, void *out_bf16,
+                          int64_t ldo, int32_t *acc_out, int64_t M, int64_t N,
+                          int64_t K, int split_k, void *workspace,
+                          size_t workspace_bytes, void *cuda_stream);
+
 /* Size of the fixed scratch array compiled into libprism.so for
  * prism_w8a8_linear_noalloc.  Every GPU that loads the library reserves it
  * until the process exits. */
@@ -422,6 +467,20 @@ int prism_w8a8_auto_split(int64_t M, int64_t N, int64_t K);
  * A nonzero value means some output of that period is invalid. */
 #define PRISM_DEVSTATUS_WAIT_TIMEOUT 1u /* a bounded on-chip wait expired */
 int prism_device_status(uint32_t *flags);
+
+/*
+ * Diagnostics for the bounded on-chip waits of the tensor-core kernels
+ * (prism_w8a8_linear's, prism_w8a8_linear_f16's) on the current device.
+ * limit_ns > 0 arms a test mode for the calls that follow: every pipeline
+ * wait is limited to limit_ns, and each CTA withholds its first
+ * chunk-complete signal, so the wait for it cannot complete and expires.
+ * The kernel then raises PRISM_DEVSTATUS_WAIT_TIMEOUT, lets every copy it
+ * started land and every MMA it issued complete, releases its tensor memory
+ * and returns.  limit_ns = 0 disarms the mode (the default: a 2 s limit,
+ * every signal sent).  The outputs of any call that raised the bit are
+ * invalid, and a workspace it used must be zeroed again before its next use.
+ */
+int prism_debug_wait_expiry(uint64_t limit_ns);
 
 #ifdef __cplusplus
 }
