@@ -90,7 +90,10 @@ constexpr int kGroups = kBNMax / 16 / 4; // 16-column groups per epilogue thread
 constexpr int kRing = 216 * 1024;
 constexpr int kMaxStages = 8;
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = 1024 + kRing + kBarBytes;
+// the epilogue scales of two items: per item kBNMax token scales (a_scale)
+// and kBNMax channel scales (w_scale)
+constexpr int kScaleBytes = 2 * 2 * kBNMax * 4;
+constexpr int kSmemBytes = 1024 + kRing + kBarBytes + kScaleBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr unsigned long long kDrainLimitNs = 2000000000ull;
@@ -111,7 +114,9 @@ struct HParams {
   int nst;                   // ring stages
   SchedParams sp;
   uint32_t* cnt;             // balanced: arrival counters of the shared tiles
-  int32_t* slots;            // balanced: one int32 accumulator per shared tile (128 x bpiece)
+  int32_t* slots;            // balanced: piece slots, one per (shared tile st, CTA b) pair at index st + b,
+                             // 128 x bpiece int32 each (st + b is unique: a CTA's tiles are consecutive
+                             // and the next CTA starts at or after its last one)
   int32_t* ws_acc;           // explicit split: [M, N] int32 accumulator
   uint32_t* ws_count;        // explicit split: per-tile arrival counters
 };
@@ -156,47 +161,61 @@ __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" :
 // normal orientation A rows are tokens and B rows channels, in the swapped
 // one the reverse.  Each element's residual is read before its output is
 // written by the same thread, so residual == out is safe.
-__device__ __forceinline__ void emit_group(const HParams& p, int64_t a0, int64_t b0, int trow, int cb,
-                                           const int32_t (&v)[16]) {
+// s_tok / s_ch: the item's token scales (a_scale of token t0 + i at i) and
+// channel scales (w_scale of channel c0 + i at i) in shared memory.
+__device__ __forceinline__ void emit_group(const HParams& p, const float* s_tok, const float* s_ch, int64_t a0,
+                                           int64_t b0, int trow, int cb, const int32_t (&v)[16]) {
+  // The group goes out in two halves of 8 elements, and the residual values
+  // of a half are loaded before its first output store: the stores may alias
+  // the residual, so a load placed after one would wait for a memory round
+  // trip of its own.  The scales come from shared memory.
   const bool res = p.residual != nullptr;
   if (p.swap) {
-    const int64_t n = a0 + trow, mb = b0 + cb * 16;
+    const int64_t n = a0 + trow;
     if (n >= p.N) return;
-    const float ws = __ldg(p.w_scale + n);
+    const float ws = s_ch[trow];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int64_t m = mb + j;
-      if (m < p.M) {
-        const float as = __ldg(p.a_scale + m);
-        const uint32_t o = res ? epilogue_bf16_res(v[j], as, ws, bf16_bits_to_float(p.residual[m * p.ldr + n]))
-                               : epilogue_bf16(v[j], as, ws);
-        p.out[m * p.ldo + n] = static_cast<uint16_t>(o);
-        if (p.acc_out != nullptr) p.acc_out[m * p.N + n] = v[j];
+    for (int h = 0; h < 2; ++h) {
+      const int64_t mb = b0 + cb * 16 + 8 * h;
+      uint32_t rb[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        rb[j] = res && mb + j < p.M ? static_cast<uint32_t>(p.residual[(mb + j) * p.ldr + n]) : 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t m = mb + j;
+        if (m < p.M) {
+          const int32_t x = v[8 * h + j];
+          const float as = s_tok[cb * 16 + 8 * h + j];
+          const uint32_t o = res ? epilogue_bf16_res(x, as, ws, bf16_bits_to_float(static_cast<uint16_t>(rb[j])))
+                                 : epilogue_bf16(x, as, ws);
+          p.out[m * p.ldo + n] = static_cast<uint16_t>(o);
+          if (p.acc_out != nullptr) p.acc_out[m * p.N + n] = x;
+        }
       }
     }
     return;
   }
   const int64_t m = a0 + trow, nb = b0 + cb * 16;
   if (m >= p.M) return;
-  const float as = __ldg(p.a_scale + m);
+  const float as = s_tok[trow];
+  const float* w = s_ch + cb * 16;
   if (p.vec_io && nb + 16 <= p.N) {
-    // two halves of 8 channels: scales as float4 pairs, residual and output
-    // as one 16-byte vector each
+    uint4 rv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    if (res) {
+      rv[0] = *reinterpret_cast<const uint4*>(p.residual + m * p.ldr + nb);
+      rv[1] = *reinterpret_cast<const uint4*>(p.residual + m * p.ldr + nb + 8);
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.w_scale + nb + 8 * h));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.w_scale + nb + 8 * h + 4));
-      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      uint4 rv = make_uint4(0u, 0u, 0u, 0u);
-      if (res) rv = *reinterpret_cast<const uint4*>(p.residual + m * p.ldr + nb + 8 * h);
-      const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+      const uint32_t rw[4] = {rv[h].x, rv[h].y, rv[h].z, rv[h].w};
       uint32_t o[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int j = 8 * h + 2 * i;
-        o[i] = res ? (epilogue_bf16_res(v[j], as, w[2 * i], bf16_lo(rw[i])) |
-                      (epilogue_bf16_res(v[j + 1], as, w[2 * i + 1], bf16_hi(rw[i])) << 16))
-                   : (epilogue_bf16(v[j], as, w[2 * i]) | (epilogue_bf16(v[j + 1], as, w[2 * i + 1]) << 16));
+        o[i] = res ? (epilogue_bf16_res(v[j], as, w[j], bf16_lo(rw[i])) |
+                      (epilogue_bf16_res(v[j + 1], as, w[j + 1], bf16_hi(rw[i])) << 16))
+                   : (epilogue_bf16(v[j], as, w[j]) | (epilogue_bf16(v[j + 1], as, w[j + 1]) << 16));
       }
       *reinterpret_cast<uint4*>(p.out + m * p.ldo + nb + 8 * h) = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -207,16 +226,37 @@ __device__ __forceinline__ void emit_group(const HParams& p, int64_t a0, int64_t
     return;
   }
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int64_t n = nb + j;
-    if (n < p.N) {
-      const float ws = __ldg(p.w_scale + n);
-      const uint32_t o = res ? epilogue_bf16_res(v[j], as, ws, bf16_bits_to_float(p.residual[m * p.ldr + n]))
-                             : epilogue_bf16(v[j], as, ws);
-      p.out[m * p.ldo + n] = static_cast<uint16_t>(o);
-      if (p.acc_out != nullptr) p.acc_out[m * p.N + n] = v[j];
+  for (int h = 0; h < 2; ++h) {
+    uint32_t rb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      rb[j] = res && nb + 8 * h + j < p.N ? static_cast<uint32_t>(p.residual[m * p.ldr + nb + 8 * h + j]) : 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t n = nb + 8 * h + j;
+      if (n < p.N) {
+        const int32_t x = v[8 * h + j];
+        const uint32_t o = res ? epilogue_bf16_res(x, as, w[8 * h + j], bf16_bits_to_float(static_cast<uint16_t>(rb[j])))
+                               : epilogue_bf16(x, as, w[8 * h + j]);
+        p.out[m * p.ldo + n] = static_cast<uint16_t>(o);
+        if (p.acc_out != nullptr) p.acc_out[m * p.N + n] = x;
+      }
     }
   }
+}
+
+// Epilogue thread et's share of an item's scales: the a_scale of the tile's
+// token et (et < kBNMax) or the w_scale of its channel et - kBNMax (0 past
+// the tile or the matrix).
+__device__ __forceinline__ float item_scale(const HParams& p, const Item& itm, int bn, int et) {
+  const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
+  if (et < kBNMax) {
+    const int64_t m = (p.swap ? b0 : a0) + et;
+    return et < (p.swap ? bn : kBM) && m < p.M ? __ldg(p.a_scale + m) : 0.f;
+  }
+  const int i = et - kBNMax;
+  const int64_t n = (p.swap ? a0 : b0) + i;
+  return i < (p.swap ? kBM : bn) && n < p.N ? __ldg(p.w_scale + n) : 0.f;
 }
 
 // (m, n) of element j of group cb, and whether it lies inside the matrix.
@@ -228,9 +268,11 @@ __device__ __forceinline__ bool group_elem(const HParams& p, int64_t a0, int64_t
   return m < p.M && n < p.N;
 }
 
-// A shared tile's slot holds element (trow, 16 cb + j) at word (16 cb + j) *
-// 128 + trow: a warp's 32 lanes touch 128 contiguous bytes.
-__device__ __forceinline__ int slot_index(int trow, int cb, int j) { return (cb * 16 + j) * kBM + trow; }
+// A piece slot holds a CTA's int32 partial sums of one shared tile: the 16
+// values of group cb of TMEM lane trow at words ((cb * 128) + trow) * 16 ..
+// + 15, so each thread moves its group as four 16-byte vectors and a warp's
+// vectors cover 2 KB contiguously.
+__device__ __forceinline__ int64_t piece_group(int trow, int cb) { return (static_cast<int64_t>(cb) * kBM + trow) * 16; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     linear_f16_kernel(const __grid_constant__ HParams p, const __grid_constant__ CUtensorMap tmA,
@@ -248,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acce = bar_accf + 16;               // 2 x 8 B: D[b] drained
   const uint32_t bar_done = bar_acce + 16;               // every MMA complete (teardown)
   uint8_t* scalars = smem + (bar_done + 8 - base);
+  float* s_scale = reinterpret_cast<float*>(smem + kRing + kBarBytes);   // [2][2 * kBNMax]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(scalars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(scalars + 4);
   int* s_last = reinterpret_cast<int*>(scalars + 8);
@@ -386,6 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = ew * 32 + lane;
     bool ok = true;
     int gc = 0;                                    // chunk counter over all items
+    {
+      // item 0's scales; item n + 1's are stored while item n finishes, and
+      // the barrier at item n + 1's output orders them before any read
+      Item first;
+      s_scale[et] = get_item(p.sp, 0, first) ? item_scale(p, first, tile_width(first.ty), et) : 0.f;
+    }
     for (int n = 0;; ++n) {
       int groups, nchunks;
       {
@@ -426,26 +475,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item itm;
       get_item(p.sp, n, itm);
       const int64_t a0 = static_cast<int64_t>(itm.tx) * kBM, b0 = static_cast<int64_t>(itm.ty) * p.bpiece;
+      // this item's scales are in place (and every thread is done with the
+      // previous item's, whose buffer takes item n + 1's below)
+      epi_barrier();
+      const float* s_tok = s_scale + (n & 1) * (2 * kBNMax);
+      const float* s_ch = s_tok + kBNMax;
+      {
+        Item nx;
+        const float sc = get_item(p.sp, n + 1, nx) ? item_scale(p, nx, tile_width(nx.ty), et) : 0.f;
+        s_scale[((n + 1) & 1) * (2 * kBNMax) + et] = sc;
+      }
       if (itm.kind == 0) {
         if (ok && nchunks > 0) {
 #pragma unroll
           for (int r = 0; r < kGroups; ++r)
-            if (slice + 4 * r < groups) emit_group(p, a0, b0, trow, slice + 4 * r, acc[r]);
+            if (slice + 4 * r < groups) emit_group(p, s_tok, s_ch, a0, b0, trow, slice + 4 * r, acc[r]);
         }
         continue;
       }
       // a K piece: the partial sums go to the workspace; the last CTA to finish
-      // the tile reads the total back and applies the epilogue
-      int32_t* slot = itm.kind == 2 ? p.slots + static_cast<int64_t>(itm.tile) * kBM * p.bpiece : nullptr;
+      // the tile adds the other pieces to its own and applies the epilogue.
+      // Balanced schedule: every piece has a slot of its own, written with
+      // plain 16-byte stores (no reductions, nothing to re-zero).  Explicit
+      // split-K: integer atomics into the [M, N] accumulator.
+      const int64_t slot_elems = static_cast<int64_t>(kBM) * p.bpiece;
       if (ok) {
+        if (itm.kind == 2) {
+          int32_t* mine = p.slots + (static_cast<int64_t>(itm.tile) + blockIdx.x) * slot_elems;
 #pragma unroll
-        for (int r = 0; r < kGroups; ++r) {
-          const int cb = slice + 4 * r;
-          if (cb >= groups) continue;
-          if (itm.kind == 2) {
+          for (int r = 0; r < kGroups; ++r) {
+            const int cb = slice + 4 * r;
+            if (cb >= groups) continue;
+            int4* dst = reinterpret_cast<int4*>(mine + piece_group(trow, cb));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) atomicAdd(slot + slot_index(trow, cb, j), acc[r][j]);
-          } else {
+            for (int q = 0; q < 4; ++q)
+              __stcg(dst + q, make_int4(acc[r][4 * q], acc[r][4 * q + 1], acc[r][4 * q + 2], acc[r][4 * q + 3]));
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kGroups; ++r) {
+            const int cb = slice + 4 * r;
+            if (cb >= groups) continue;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               int64_t m, nn;
@@ -459,16 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // could not finish (an expired wait) is not counted and not written
       const bool bad = epi_barrier_any(!ok);
       uint32_t* counter = itm.kind == 1 ? p.ws_count + itm.tile : p.cnt + itm.tile;
+      int bf = 0, bl = 0;
+      if (itm.kind == 2) shared_tile_ctas(p.sp, itm.tile, bf, bl);
       if (!bad && et == 0) {
-        unsigned target;
-        if (itm.kind == 1) {
-          target = static_cast<unsigned>(p.sp.split - 1);
-        } else {
-          int bf = 0, bl = 0;
-          shared_tile_ctas(p.sp, itm.tile, bf, bl);
-          target = static_cast<unsigned>(bl - bf);
-        }
-        // release: the reductions of every epilogue thread reached thread 0
+        const unsigned target = itm.kind == 1 ? static_cast<unsigned>(p.sp.split - 1) : static_cast<unsigned>(bl - bf);
+        // release: the stores of every epilogue thread reached thread 0
         // through the barrier; its fence orders them before the arrival.
         // acquire: the last arriver's fence orders the read-back after them.
         __threadfence();
@@ -479,36 +544,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_barrier();
       if (bad || !*s_last) continue;
       __threadfence();
-      // this thread's partial sums are in the workspace now: acc takes the totals
+      if (itm.kind == 2) {
+        // the other CTAs' pieces, added to this CTA's own sums in registers
+        for (int bo = bf; bo <= bl; ++bo) {
+          if (bo == static_cast<int>(blockIdx.x)) continue;
+          const int32_t* other = p.slots + (static_cast<int64_t>(itm.tile) + bo) * slot_elems;
 #pragma unroll
-      for (int r = 0; r < kGroups; ++r) {
-        const int cb = slice + 4 * r;
-        if (cb >= groups) continue;
+          for (int r = 0; r < kGroups; ++r) {
+            const int cb = slice + 4 * r;
+            if (cb >= groups) continue;
+            const int4* src = reinterpret_cast<const int4*>(other + piece_group(trow, cb));
+            int4 in[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (itm.kind == 2) {
-            acc[r][j] = __ldcg(slot + slot_index(trow, cb, j));
-          } else {
+            for (int q = 0; q < 4; ++q) in[q] = __ldcg(src + q);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[r][4 * q] += in[q].x;
+              acc[r][4 * q + 1] += in[q].y;
+              acc[r][4 * q + 2] += in[q].z;
+              acc[r][4 * q + 3] += in[q].w;
+            }
+          }
+        }
+      } else {
+        // explicit split-K: the total from the accumulator, which is re-zeroed
+#pragma unroll
+        for (int r = 0; r < kGroups; ++r) {
+          const int cb = slice + 4 * r;
+          if (cb >= groups) continue;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
             int64_t m, nn;
             acc[r][j] = group_elem(p, a0, b0, trow, cb, j, m, nn) ? __ldcg(p.ws_acc + m * p.N + nn) : 0;
           }
-        }
-      }
 #pragma unroll
-      for (int r = 0; r < kGroups; ++r) {
-        const int cb = slice + 4 * r;
-        if (cb >= groups) continue;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (itm.kind == 2) {
-            __stcg(slot + slot_index(trow, cb, j), 0);
-          } else {
+          for (int j = 0; j < 16; ++j) {
             int64_t m, nn;
             if (group_elem(p, a0, b0, trow, cb, j, m, nn)) __stcg(p.ws_acc + m * p.N + nn, 0);
           }
         }
-        emit_group(p, a0, b0, trow, cb, acc[r]);
       }
+#pragma unroll
+      for (int r = 0; r < kGroups; ++r)
+        if (slice + 4 * r < groups) emit_group(p, s_tok, s_ch, a0, b0, trow, slice + 4 * r, acc[r]);
       if (et == 0) *counter = 0u;
     }
   }
@@ -552,7 +630,9 @@ TcSched balanced(const HPlan& pl, int64_t K) { return tc_balanced_sched(pl.gx * 
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Balanced schedule: counters of the shared tiles, then one int32 slot each.
+// Balanced schedule: counters of the shared tiles, then the piece slots,
+// one per (shared tile st, CTA b) pair at index st + b: R + G - 1 slots of
+// 128 x bpiece int32.
 size_t balanced_bytes(int64_t M, int64_t N, int64_t K, size_t* counter_bytes) {
   const HPlan pl = plan(M, N);
   const TcSched sc = balanced(pl, K);
@@ -562,7 +642,7 @@ size_t balanced_bytes(int64_t M, int64_t N, int64_t K, size_t* counter_bytes) {
   }
   const size_t cb = round256(static_cast<size_t>(sc.R) * 4);
   if (counter_bytes != nullptr) *counter_bytes = cb;
-  return cb + static_cast<size_t>(sc.R) * kBM * pl.bpiece * 4;
+  return cb + static_cast<size_t>(sc.R + sc.G - 1) * kBM * pl.bpiece * 4;
 }
 
 // Explicit split-K: the [M, N] int32 accumulator, then one counter per tile.

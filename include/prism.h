@@ -317,8 +317,14 @@ size_t prism_w8a8_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int split
  * prism_w8a8_linear_f16 -- prism_w8a8_linear on binary16 codes:
  *   qh, ldq    [M, K] activation codes (prism_quant_act_f16), ldq % 8 == 0
  *   wh, ldw    [N, K] weight codes (prism_codes_to_f16), ldw % 8 == 0
- *   every other argument, the workspace rules (sized by
- *   prism_w8a8_f16_workspace_bytes) and the result as prism_w8a8_linear.
+ *   workspace  at least prism_w8a8_f16_workspace_bytes(M, N, K, split_k)
+ *              bytes, 256-byte aligned, zeroed by the caller before its first
+ *              use.  Every call leaves what must be zero at the next call
+ *              zero again (the automatic schedule's arrival counters, split-K's
+ *              accumulator); the automatic schedule's partial-sum slots are
+ *              scratch whose contents never reach a result.  Calls sharing a
+ *              workspace must not overlap in time.
+ *   every other argument and the result as prism_w8a8_linear.
  * Codes must be integers in [-127, 127]; other binary16 values void the
  * exactness argument.
  */

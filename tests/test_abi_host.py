@@ -180,6 +180,16 @@ def test_balanced_schedule_workspace_matches_its_statement(L, monkeypatch):
                 assert L.prism_w8a8_workspace_bytes(M, N, K, 0) == _balanced_workspace_bytes(M, N, K), (M, N, K)
 
 
+def test_f16_workspace_matches_its_statement(L):
+    """The binary16-code kernel's workspace: counters, then one slot per
+    (shared tile, CTA) piece (tests/sched_util.py restates the schedule)."""
+    from tests.sched_util import f16_workspace
+    for M in (1, 8, 37, 64, 128, 160, 192, 304, 511, 512, 600, 2048, 8192):
+        for N in (384, 640, 5120, 15360, 34816):
+            for K in (64, 128, 2064, 5120, 17408):
+                assert L.prism_w8a8_f16_workspace_bytes(M, N, K, 0) == f16_workspace(M, N, K)[1], (M, N, K)
+
+
 def ro(L, P=4, T=8, V=100, K=64, h=A, ldh=64, s=None, W=A, ldw=64, sc=A, off=A, ids=A,
        lg=A, pr=A, err=None):
     return L.prism_candidate_readout(h, ldh, s, W, ldw, sc, V, K, off, ids, P, T, lg, pr, err, None, 0, None)

@@ -19,6 +19,7 @@ import torch
 import oracle
 import workloads as wl
 from tests.gpu_util import dev, dev_bf16, host, host_bits, padded
+from tests.sched_util import f16_workspace
 
 import deterministic_w8a8_int8_gb300 as prism
 
@@ -162,14 +163,19 @@ def test_balanced_schedule_matches_single_piece(cuda_device, M, N, K):
     A, S, R = dev(a), dev(s), dev_bf16(rb)
     ref, ref_acc = run_f16(Q, A, W, S, R, split=1)
     ws_buf = prism.new_workspace_f16(M, N, K, 0, "cuda")
-    for _ in range(2):
+    counter_bytes, total = f16_workspace(M, N, K)
+    assert (0 if ws_buf is None else ws_buf.numel()) == total
+    for i in range(3):
         acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
         got = prism.prism_w8a8_linear_f16(Q, A, W, S, residual=R, split_k=0, workspace=ws_buf, acc_out=acc)
         torch.cuda.synchronize()
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
         assert torch.equal(acc, ref_acc)
-    if ws_buf is not None:
-        assert int(ws_buf.count_nonzero()) == 0
+        if ws_buf is not None:
+            # calls leave the arrival counters zero; the piece slots are
+            # scratch whose stale contents never reach a result
+            assert int(ws_buf[:counter_bytes].count_nonzero()) == 0
+            ws_buf[counter_bytes:].fill_(0x5A + i)
     # and the single-piece result is the oracle's (sampled rows)
     rows = np.unique(np.linspace(0, M - 1, 9).astype(int))
     outo, acco = oracle.w8a8_linear(q[rows], a[rows], w, s, rb[rows])
