@@ -274,6 +274,10 @@ __device__ __forceinline__ bool group_elem(const HParams& p, int64_t a0, int64_t
 // vectors cover 2 KB contiguously.
 __device__ __forceinline__ int64_t piece_group(int trow, int cb) { return (static_cast<int64_t>(cb) * kBM + trow) * 16; }
 
+// kExplicit: the explicit split-K instance (items of kind 0 and 1); the
+// other instance runs the balanced schedule (kinds 0 and 2).  Each carries
+// only its own protocol, which keeps the epilogue within its registers.
+template <bool kExplicit>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_f16_kernel(const __grid_constant__ HParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB) {
@@ -500,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // split-K: integer atomics into the [M, N] accumulator.
       const int64_t slot_elems = static_cast<int64_t>(kBM) * p.bpiece;
       if (ok) {
-        if (itm.kind == 2) {
+        if (!kExplicit) {
           int32_t* mine = p.slots + (static_cast<int64_t>(itm.tile) + blockIdx.x) * slot_elems;
 #pragma unroll
           for (int r = 0; r < kGroups; ++r) {
@@ -528,11 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every epilogue thread takes both barriers; a tile that any thread
       // could not finish (an expired wait) is not counted and not written
       const bool bad = epi_barrier_any(!ok);
-      uint32_t* counter = itm.kind == 1 ? p.ws_count + itm.tile : p.cnt + itm.tile;
+      uint32_t* counter = kExplicit ? p.ws_count + itm.tile : p.cnt + itm.tile;
       int bf = 0, bl = 0;
-      if (itm.kind == 2) shared_tile_ctas(p.sp, itm.tile, bf, bl);
+      if (!kExplicit) shared_tile_ctas(p.sp, itm.tile, bf, bl);
       if (!bad && et == 0) {
-        const unsigned target = itm.kind == 1 ? static_cast<unsigned>(p.sp.split - 1) : static_cast<unsigned>(bl - bf);
+        const unsigned target = kExplicit ? static_cast<unsigned>(p.sp.split - 1) : static_cast<unsigned>(bl - bf);
         // release: the stores of every epilogue thread reached thread 0
         // through the barrier; its fence orders them before the arrival.
         // acquire: the last arriver's fence orders the read-back after them.
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_barrier();
       if (bad || !*s_last) continue;
       __threadfence();
-      if (itm.kind == 2) {
+      if (!kExplicit) {
         // the other CTAs' pieces, added to this CTA's own sums in registers
         for (int bo = bf; bo <= bl; ++bo) {
           if (bo == static_cast<int>(blockIdx.x)) continue;
@@ -693,7 +697,8 @@ size_t linear_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
 
 cudaError_t launch_linear_f16(const LinearF16Args& a, cudaStream_t stream) {
   const HPlan pl = plan(a.M, a.N);
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(linear_f16_kernel), kSmemBytes);
+  auto kernel = a.split >= 1 ? linear_f16_kernel<true> : linear_f16_kernel<false>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   HParams p{};
   p.a_scale = a.a_scale;
@@ -747,7 +752,7 @@ cudaError_t launch_linear_f16(const LinearF16Args& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece);
   if (e != cudaSuccess) return e;
-  return launch_kernel(linear_f16_kernel, grid, dim3(kThreads), kSmemBytes, stream, true, p, tmA, tmB);
+  return launch_kernel(kernel, grid, dim3(kThreads), kSmemBytes, stream, true, p, tmA, tmB);
 }
 
 cudaError_t read_and_clear_f16_status(uint32_t* out) {
