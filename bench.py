@@ -1,33 +1,41 @@
 #!/usr/bin/env python
-"""Benchmark of the batch-invariant W8A8 hot path on one short-request bucket.
+"""Benchmark of the batch-invariant W8A8 hot path.
 
-Workload (synthetic, seeded): the StartLux-Prism short-request forest bucket,
-M = 304 token rows (256 evidence tokens + 3 questions x 16 tokens), hidden
-size 5120.  One step is one pass of the whole hot path:
-  1. prism_quant_act      X [304, 5120] bf16 -> int8 + scales (smoothing on)
-  2. prism_w8a8_linear    QKV projection, N = 15360, no residual
-  3. prism_quant_act      attention output stand-in [304, 5120]
-  4. prism_w8a8_linear    o_proj, N = 5120, + bf16 residual
-  5. prism_candidate_readout  the three answer positions (last token of each
-                          question) against a 248,000 x 5120 int8 LM head,
-                          2-10 candidates each, softmax over the candidates.
-The metric is int8 tensor operations per second (2*M*N*K per linear plus the
-read-out's candidate dot products) over the whole step.
+Headline workload (synthetic, seeded): the high-concurrency FFN block of
+the StartLux-Prism pages -- 64 clients x 32 tokens = 2048 token rows, hidden
+size 5120, FFN width 17408.  One step is one pass of the hot path over it:
+  1. prism_quant_act_f16   X [2048, 5120] bf16 -> codes + scales (smoothing on)
+  2. prism_w8a8_linear_f16 gate/up projection, N = 34816, no residual
+  3. prism_quant_act_f16   the down projection's input [2048, 17408]
+  4. prism_w8a8_linear_f16 down projection, N = 5120, + bf16 residual
+The weights are int8 codes with per-channel scales; they are converted once,
+at load time and outside the timed region, to binary16 codes
+(prism_codes_to_f16), the operand form of the tensor-core kernel on sm_103a,
+which has no integer MMA (the f16 MMA is exact on these codes).  The metric
+is int8 operations per second, 2*M*N*K per linear, over the whole step.
 
 Timing: W warm-up steps, then exactly K steps of direct C-ABI launches on one
-stream between CUDA events (device-resident inputs).  Three weight
-sets are rotated so every weight byte comes from HBM (3 x 105 MB > 2 x L2).
-CUDA events around every QKV launch give the dominant
-kernel's average duration for the roofline.  nvidia-smi samples SM clocks
-during the timed region.  The e2e figure repeats the step through the Python
-binding with the step's inputs copied from pinned host memory and the
-candidate probabilities copied back, inside the timed region; the next step's
-input copies run on a second stream while the current step computes (two
-device input buffers).
+stream between CUDA events (device-resident inputs; the step's weights, 534
+MB of codes, are larger than twice the L2).  Events around every gate/up
+launch give the dominant kernel's mean duration for the roofline.
+nvidia-smi samples SM clocks during the timed region.  The e2e figure
+repeats the step through the Python binding with the step's inputs copied
+from pinned host memory and the down projection's output copied back, all
+inside the timed region (the next step's input copies run on a second
+stream while the current step computes).
 
-`--impl reference` times the CPU oracle (the only other arm this method has)
-on a bounded sample of the same workload.  Multi-GPU (torchrun): each rank
-runs its own bucket, no collective on the data path (weak scaling).
+Sub-records in the same line (world size 1): the other configurations of the
+method, each timed alone -- the short-request forest bucket (quantise, QKV,
+quantise, o_proj, read-out of 3 answer positions), the decode-like weight
+stream at every row count and split-K factor (with the bit-identity check
+across all of them), the 8192-row long-evidence linear, the 192-position
+candidate read-out next to a plain gather of the same rows, and the
+quantiser.
+
+`--impl reference` times the CPU oracle (the only other implementation of
+this method) on a bounded sample of the same workload.  Multi-GPU
+(torchrun): each rank runs its own FFN block, no collective on the data path
+(weak scaling).
 """
 from __future__ import annotations
 
@@ -50,7 +58,10 @@ import workloads as wl
 
 METRIC = "W8A8 linear int8 TOPS & % of int8 peak / GB/s % HBM; bit-exact vs oracle"
 UNIT = "TOPS"
-M_ROWS = 304
+GATEUP, DOWN = "load_gateup_m2048_k5120_n34816", "load_down_m2048_k17408_n5120"
+WORKLOAD = ("ffn_block_m2048: quant + gate_up(k5120,n34816) + quant + down(k17408,n5120,+res), "
+            "64 clients x 32 tokens")
+M_ROWS = 304                        # forest bucket rows (sub-record)
 ANSWER_ROWS = (271, 287, 303)       # last token of each 16-token question
 N_ROTATE = 3
 
@@ -69,9 +80,27 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-# ------------------------------------------------------------- workload ----
-class Workload:
-    """Host-side inputs of one forest bucket (numpy)."""
+# ------------------------------------------------------------- workloads ---
+class FfnWorkload:
+    """Host-side inputs of the headline FFN block (numpy)."""
+
+    def __init__(self):
+        self.gu = wl.make_linear(GATEUP)
+        self.dn = wl.make_linear(DOWN)
+        self.M = self.gu.M
+        self.ops_gu = 2 * self.M * self.gu.N * self.gu.K
+        self.ops_dn = 2 * self.M * self.dn.N * self.dn.K
+        self.ops = self.ops_gu + self.ops_dn
+        # algorithmic HBM bytes (int8 codes read once, outputs written once)
+        self.bytes_gu = self.M * self.gu.K + self.gu.N * self.gu.K + 4 * self.gu.N + 4 * self.M + 2 * self.M * self.gu.N
+        self.bytes_dn = (self.M * self.dn.K + self.dn.N * self.dn.K + 4 * self.dn.N + 4 * self.M
+                         + 2 * self.M * self.dn.N * 2)
+        self.bytes_quant = sum(3 * self.M * k + 4 * self.M + 4 * k for k in (self.gu.K, self.dn.K))
+        self.bytes = self.bytes_gu + self.bytes_dn + self.bytes_quant
+
+
+class ForestWorkload:
+    """Host-side inputs of one short-request forest bucket (numpy)."""
 
     def __init__(self):
         self.qkv = wl.make_linear("forest_qkv_m304_k5120_n15360")
@@ -84,14 +113,6 @@ class Workload:
         self.ops_linear_o = 2 * M * self.o.N * K
         self.ops_readout = 2 * int(self.ro.cand_ids.size) * K
         self.ops = self.ops_linear_qkv + self.ops_linear_o + self.ops_readout
-        T = int(self.ro.cand_ids.size)
-        # algorithmic HBM bytes of one step (inputs read once, outputs written once)
-        self.bytes_qkv = M * K + self.qkv.N * K + 4 * self.qkv.N + 4 * M + 2 * M * self.qkv.N
-        self.bytes_o = M * K + self.o.N * K + 4 * self.o.N + 4 * M + 2 * M * self.o.N * 2
-        self.bytes_quant = 2 * (3 * M * K + 4 * M + 4 * K)
-        self.bytes_readout = (2 * len(ANSWER_ROWS) * K + T * (K + 4) + 4 * (len(ANSWER_ROWS) + 1)
-                              + 4 * T + 8 * T)
-        self.bytes = self.bytes_qkv + self.bytes_o + self.bytes_quant + self.bytes_readout
 
 
 def reduce_max(value: float, device) -> float:
@@ -107,7 +128,7 @@ def reduce_max(value: float, device) -> float:
 
 
 def weak_scaling_value(ops_per_step: float, steps: int, world: int, t_ms: float) -> float:
-    """Whole-job TOPS: every rank runs ``steps`` steps of its own bucket; the
+    """Whole-job TOPS: every rank runs ``steps`` steps of its own block; the
     job time is the slowest rank's."""
     return ops_per_step * steps * world / (t_ms / 1e3) / 1e12
 
@@ -119,6 +140,13 @@ def load_peaks():
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def load_sustained_bf16():
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops_sustained"])
+    except Exception:
+        return None
 
 
 def kernel_traffic(kernel_file: str, workload: str):
@@ -191,53 +219,44 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------- CPU oracle ----
-def cpu_oracle_step(work: Workload, rows: np.ndarray):
-    """The oracle on ``rows`` of the bucket (both linears and the read-out of
-    the answer rows among them).  Returns (ops, outputs)."""
+def ffn_sample_rows(n: int) -> np.ndarray:
+    """n token rows of the FFN block, always including the first and last."""
+    M = wl.LINEAR_CONFIGS[GATEUP][0]
+    pick = np.random.default_rng(0).choice(np.arange(1, M - 1), size=max(0, n - 2), replace=False)
+    return np.sort(np.concatenate([[0, M - 1], pick])).astype(np.int64)
+
+
+def cpu_oracle_ffn(work: FfnWorkload, rows: np.ndarray):
+    """The oracle on ``rows`` of the FFN block (both linears).  Returns
+    (ops, (gate/up output rows, down output rows))."""
     import oracle
-    q1, a1 = oracle.quant_act(work.qkv.x_bits[rows], work.qkv.inv_s)
-    y, _ = oracle.w8a8_linear(q1, a1, work.qkv.w, work.qkv.w_scale, None)
-    q2, a2 = oracle.quant_act(work.o.x_bits[rows], work.o.inv_s)
-    h, _ = oracle.w8a8_linear(q2, a2, work.o.w, work.o.w_scale, work.o.residual_bits[rows])
-    ops = 2 * rows.size * wl.HIDDEN * (work.qkv.N + work.o.N)
-    ans = [i for i, r in enumerate(rows.tolist()) if r in ANSWER_ROWS]
-    ro = None
-    if len(ans) == len(ANSWER_ROWS):
-        remap = np.searchsorted(work.cand_unique, work.ro.cand_ids).astype(np.int32)
-        rc, lg, pr = oracle.candidate_readout(h[ans], None, work.cand_rows,
-                                              work.ro.lm_scale[work.cand_unique],
-                                              work.ro.cand_offsets, remap)
-        assert rc == 0
-        ops += work.ops_readout
-        ro = (lg, pr)
-    return ops, (y, h, ro)
+    q1, a1 = oracle.quant_act(work.gu.x_bits[rows], work.gu.inv_s)
+    y, _ = oracle.w8a8_linear(q1, a1, work.gu.w, work.gu.w_scale, None)
+    q2, a2 = oracle.quant_act(work.dn.x_bits[rows], work.dn.inv_s)
+    h, _ = oracle.w8a8_linear(q2, a2, work.dn.w, work.dn.w_scale, work.dn.residual_bits[rows])
+    ops = 2 * rows.size * (work.gu.N * work.gu.K + work.dn.N * work.dn.K)
+    return ops, (y, h)
 
 
-def sample_rows(n: int) -> np.ndarray:
-    rest = [r for r in range(M_ROWS) if r not in ANSWER_ROWS]
-    pick = np.random.default_rng(0).choice(rest, size=max(0, n - len(ANSWER_ROWS)), replace=False)
-    return np.sort(np.concatenate([pick, np.array(ANSWER_ROWS)])).astype(np.int64)
-
-
-def run_cpu_baseline(work: Workload, budget_s: float = 12.0):
+def run_cpu_baseline(work: FfnWorkload, budget_s: float = 12.0):
     import oracle
     cores = host_cores()
     oracle.set_threads(cores)
-    rows = sample_rows(96)
+    rows = ffn_sample_rows(32)
     t0 = time.perf_counter()
-    ops, outs = cpu_oracle_step(work, rows)
+    ops, outs = cpu_oracle_ffn(work, rows)
     dt = time.perf_counter() - t0
     reps, total_ops, total_t = 1, ops, dt
     while total_t < budget_s and reps < 50:
         t0 = time.perf_counter()
-        o, _ = cpu_oracle_step(work, rows)
+        o, _ = cpu_oracle_ffn(work, rows)
         total_t += time.perf_counter() - t0
         total_ops += o
         reps += 1
     return {"value": total_ops / total_t / 1e12, "unit": UNIT, "cores": int(oracle.get_threads()),
             "kind": "oracle",
-            "sample": f"{rows.size} of {M_ROWS} token rows (incl. the 3 answer rows) through both "
-                      f"linears and the read-out, {reps} repetitions, {total_t:.1f} s"}, rows, outs
+            "sample": f"{rows.size} of {work.M} token rows (first and last included) through both "
+                      f"linears, {reps} repetitions, {total_t:.1f} s"}, rows, outs
 
 
 def run_reference(args):
@@ -245,16 +264,16 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    work = Workload()
+    work = FfnWorkload()
     cores = host_cores()
     oracle.set_threads(cores)
-    rows = sample_rows(16)
+    rows = ffn_sample_rows(8)
     for _ in range(args.warmup):
-        cpu_oracle_step(work, rows)
+        cpu_oracle_ffn(work, rows)
     t0 = time.perf_counter()
     ops = 0
     for _ in range(args.steps):
-        o, _ = cpu_oracle_step(work, rows)
+        o, _ = cpu_oracle_ffn(work, rows)
         ops += o
     dt = time.perf_counter() - t0
     value = ops / dt / 1e12
@@ -263,10 +282,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic",
-        "config": {"workload": "forest_bucket_m304_k5120: quant + qkv(n15360) + quant + o_proj(n5120,+res) "
-                               "+ candidate readout(3 pos, v248000)", "sample_rows": int(rows.size)},
+        "config": {"workload": WORKLOAD, "sample_rows": int(rows.size)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(oracle.get_threads()), "kind": "oracle",
-                         "sample": f"{rows.size} of {M_ROWS} token rows (incl. the 3 answer rows) per step"},
+                         "sample": f"{rows.size} of {work.M} token rows of both linears per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -274,7 +292,26 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU ----
+def _timed(stream, fn, n, warm=3):
+    """Mean and all per-call device times (us) of fn(i), i = 0..n-1, each
+    bracketed by CUDA events on ``stream``."""
+    import torch
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        evs[i][0].record(stream)
+        fn(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    return statistics.mean(us), us
+
+
 def run_gpu(args):
+    import ctypes
+
     import torch
     import torch.distributed as dist
 
@@ -285,10 +322,10 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    prism.lib()
+    L = prism.lib()
 
-    work = Workload()
-    M, K = M_ROWS, wl.HIDDEN
+    work = FfnWorkload()
+    gu, dn, M = work.gu, work.dn, work.M
 
     def bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -296,67 +333,38 @@ def run_gpu(args):
     def t(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    # device-resident model state: N_ROTATE copies of every weight set
-    sets = []
-    for _ in range(N_ROTATE):
-        sets.append(dict(wq=t(work.qkv.w), sq=t(work.qkv.w_scale), iq=t(work.qkv.inv_s),
-                         wo=t(work.o.w), so=t(work.o.w_scale), io=t(work.o.inv_s)))
-    g = torch.Generator(device=dev)
-    g.manual_seed(1234)
-    lm_head = torch.randint(-127, 128, (wl.VOCAB, K), dtype=torch.int8, device=dev, generator=g)
-    lm_head[t(work.cand_unique.astype(np.int64))] = t(work.cand_rows)
-    lm_scale = t(work.ro.lm_scale)
-
+    # model state, made once at load time: binary16 codes of the int8 weights
+    Wgu = prism.prism_codes_to_f16(t(gu.w))
+    Wdn = prism.prism_codes_to_f16(t(dn.w))
+    Sgu, Sdn, Igu, Idn = t(gu.w_scale), t(dn.w_scale), t(gu.inv_s), t(dn.inv_s)
     # per-step inputs and outputs (preallocated)
-    X = bf16(work.qkv.x_bits)
-    Xo = bf16(work.o.x_bits)
-    Res = bf16(work.o.residual_bits)
-    off = t(work.ro.cand_offsets)
-    ids = t(work.ro.cand_ids)
-    T = ids.numel()
-    q1 = torch.empty((M, K), dtype=torch.int8, device=dev)
-    q2 = torch.empty_like(q1)
+    X, Xd, Res = bf16(gu.x_bits), bf16(dn.x_bits), bf16(dn.residual_bits)
+    q1 = torch.empty((M, gu.K), dtype=torch.float16, device=dev)
+    q2 = torch.empty((M, dn.K), dtype=torch.float16, device=dev)
     a1 = torch.empty((M,), dtype=torch.float32, device=dev)
     a2 = torch.empty_like(a1)
-    Y = torch.empty((M, work.qkv.N), dtype=torch.bfloat16, device=dev)
-    H = torch.empty((M, work.o.N), dtype=torch.bfloat16, device=dev)
-    logits = torch.empty((T,), dtype=torch.float32, device=dev)
-    probs = torch.empty((T,), dtype=torch.float32, device=dev)
-    err = torch.zeros((1,), dtype=torch.int32, device=dev)
-    split_q = prism.prism_w8a8_auto_split(M, work.qkv.N, K)
-    split_o = prism.prism_w8a8_auto_split(M, work.o.N, K)
-    ws_q = prism.new_workspace(M, work.qkv.N, K, 0, dev)
-    ws_o = prism.new_workspace(M, work.o.N, K, 0, dev)
-    hid = H[ANSWER_ROWS[0]::16]
-    assert hid.shape[0] == len(ANSWER_ROWS)
+    Y = torch.empty((M, gu.N), dtype=torch.bfloat16, device=dev)
+    H = torch.empty((M, dn.N), dtype=torch.bfloat16, device=dev)
+    ws_gu = prism.new_workspace_f16(M, gu.N, gu.K, 0, dev)
+    ws_dn = prism.new_workspace_f16(M, dn.N, dn.K, 0, dev)
+    torch.cuda.synchronize()
 
-    import ctypes
-    L = prism.lib()
     vp = lambda x: ctypes.c_void_p(x.data_ptr()) if x is not None else None
     stream = torch.cuda.Stream(device=dev)
     st = ctypes.c_void_p(stream.cuda_stream)
-    wsq_b = 0 if ws_q is None else ws_q.numel()
-    wso_b = 0 if ws_o is None else ws_o.numel()
-    Nq, No, T_ = work.qkv.N, work.o.N, int(T)
-
-    def calls_for(s):
-        """The five C-ABI calls of one step, arguments marshalled once."""
-        return [
-            (L.prism_quant_act, (vp(X), K, vp(s["iq"]), M, K, vp(q1), K, vp(a1), st)),
-            (L.prism_w8a8_linear, (vp(q1), K, vp(a1), vp(s["wq"]), K, vp(s["sq"]), None, 0, vp(Y), Nq,
-                                   None, M, Nq, K, 0, vp(ws_q), wsq_b, st)),
-            (L.prism_quant_act, (vp(Xo), K, vp(s["io"]), M, K, vp(q2), K, vp(a2), st)),
-            (L.prism_w8a8_linear, (vp(q2), K, vp(a2), vp(s["wo"]), K, vp(s["so"]), vp(Res), No, vp(H), No,
-                                   None, M, No, K, 0, vp(ws_o), wso_b, st)),
-            (L.prism_candidate_readout, (vp(hid), hid.stride(0), None, vp(lm_head), K, vp(lm_scale),
-                                         wl.VOCAB, K, vp(off), vp(ids), len(ANSWER_ROWS), T_, vp(logits),
-                                         vp(probs), vp(err), None, 0, st)),
-        ]
-
-    rot_calls = [calls_for(s) for s in sets]
+    nb = lambda w: 0 if w is None else w.numel()
+    calls = [
+        (L.prism_quant_act_f16, (vp(X), gu.K, vp(Igu), M, gu.K, vp(q1), gu.K, vp(a1), st)),
+        (L.prism_w8a8_linear_f16, (vp(q1), gu.K, vp(a1), vp(Wgu), gu.K, vp(Sgu), None, 0, vp(Y), gu.N, None,
+                                   M, gu.N, gu.K, 0, vp(ws_gu), nb(ws_gu), st)),
+        (L.prism_quant_act_f16, (vp(Xd), dn.K, vp(Idn), M, dn.K, vp(q2), dn.K, vp(a2), st)),
+        (L.prism_w8a8_linear_f16, (vp(q2), dn.K, vp(a2), vp(Wdn), dn.K, vp(Sdn), vp(Res), dn.N, vp(H), dn.N,
+                                   None, M, dn.N, dn.K, 0, vp(ws_dn), nb(ws_dn), st)),
+    ]
+    launches_per_step = len(calls)
 
     def step(i, ev=None):
-        for j, (fn, a) in enumerate(rot_calls[i % N_ROTATE]):
+        for j, (fn, a) in enumerate(calls):
             if ev is not None and j == 1:
                 ev[0].record(stream)
             rc = fn(*a)
@@ -365,12 +373,10 @@ def run_gpu(args):
             if ev is not None and j == 1:
                 ev[1].record(stream)
 
-    launches_per_step = 5
     torch.cuda.synchronize()
-    for i in range(max(args.warmup, N_ROTATE)):
+    for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -386,60 +392,46 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     elapsed_ms = start.elapsed_time(end)
-    qkv_ms = [a.elapsed_time(b) for a, b in evs]
-    if int(err.item()) != 0:
-        raise RuntimeError(f"read-out device error word {int(err.item())}")
-
+    gu_us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    if prism.prism_device_status() != 0:
+        raise RuntimeError("a kernel raised a device status bit during the timed steps")
     t_max = reduce_max(elapsed_ms, dev)
     secs = t_max / 1e3
     value = weak_scaling_value(work.ops, args.steps, world, t_max)
 
     # ---- end to end through the binding, host buffers, copies inside timing
     pin = lambda a: a.pin_memory()
-    hX = pin(torch.from_numpy(work.qkv.x_bits.view(np.int16)).view(torch.bfloat16))
-    hXo = pin(torch.from_numpy(work.o.x_bits.view(np.int16)).view(torch.bfloat16))
-    hRes = pin(torch.from_numpy(work.o.residual_bits.view(np.int16)).view(torch.bfloat16))
-    hoff = pin(torch.from_numpy(work.ro.cand_offsets))
-    hids = pin(torch.from_numpy(work.ro.cand_ids))
-    hlog = torch.empty((T,), dtype=torch.float32).pin_memory()
-    hpro = torch.empty((T,), dtype=torch.float32).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hX, hXo, hRes, hoff, hids))
-    d2h = hlog.numel() * 4 + hpro.numel() * 4
-
-    # Two device input sets: the copies of step i + 1 run on a copy stream
-    # while step i computes; every copy stays inside the timed region (the
-    # copy stream starts after e0, and e1 follows the last step, which waits
-    # for its own copies).
-    dX, dXo, dRes = [X, torch.empty_like(X)], [Xo, torch.empty_like(Xo)], [Res, torch.empty_like(Res)]
-    doff, dids = [off, torch.empty_like(off)], [ids, torch.empty_like(ids)]
+    hX = pin(torch.from_numpy(gu.x_bits.view(np.int16)).view(torch.bfloat16))
+    hXd = pin(torch.from_numpy(dn.x_bits.view(np.int16)).view(torch.bfloat16))
+    hRes = pin(torch.from_numpy(dn.residual_bits.view(np.int16)).view(torch.bfloat16))
+    hH = torch.empty((M, dn.N), dtype=torch.bfloat16).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hX, hXd, hRes))
+    d2h = hH.numel() * hH.element_size()
+    # two device input sets: the copies of step i + 1 run on a copy stream
+    # while step i computes; every copy is inside the timed region
+    dX, dXd, dRes = [X, torch.empty_like(X)], [Xd, torch.empty_like(Xd)], [Res, torch.empty_like(Res)]
     copy_stream = torch.cuda.Stream(device=dev)
-    ready = [torch.cuda.Event() for _ in range(2)]   # buffer b holds its step's inputs
-    free = [torch.cuda.Event() for _ in range(2)]    # buffer b's step has consumed it
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_copy(i):
         b = i % 2
         copy_stream.wait_event(free[b])
         with torch.cuda.stream(copy_stream):
             dX[b].copy_(hX, non_blocking=True)
-            dXo[b].copy_(hXo, non_blocking=True)
+            dXd[b].copy_(hXd, non_blocking=True)
             dRes[b].copy_(hRes, non_blocking=True)
-            doff[b].copy_(hoff, non_blocking=True)
-            dids[b].copy_(hids, non_blocking=True)
             ready[b].record(copy_stream)
 
     def e2e_compute(i):
         b = i % 2
-        sset = sets[i % N_ROTATE]
         stream.wait_event(ready[b])
         with torch.cuda.stream(stream):
-            prism.prism_quant_act(dX[b], sset["iq"], q=q1, a_scale=a1)
-            prism.prism_w8a8_linear(q1, a1, sset["wq"], sset["sq"], out=Y, workspace=ws_q)
-            prism.prism_quant_act(dXo[b], sset["io"], q=q2, a_scale=a2)
-            prism.prism_w8a8_linear(q2, a2, sset["wo"], sset["so"], residual=dRes[b], out=H, workspace=ws_o)
-            prism.prism_candidate_readout(hid, None, lm_head, lm_scale, doff[b], dids[b], logits=logits,
-                                          probs=probs, err=err)
-            hlog.copy_(logits, non_blocking=True)
-            hpro.copy_(probs, non_blocking=True)
+            prism.prism_quant_act_f16(dX[b], Igu, qh=q1, a_scale=a1)
+            prism.prism_w8a8_linear_f16(q1, a1, Wgu, Sgu, out=Y, workspace=ws_gu)
+            prism.prism_quant_act_f16(dXd[b], Idn, qh=q2, a_scale=a2)
+            prism.prism_w8a8_linear_f16(q2, a2, Wdn, Sdn, residual=dRes[b], out=H, workspace=ws_dn)
+            hH.copy_(H, non_blocking=True)
             free[b].record(stream)
 
     def e2e_run(n):
@@ -462,30 +454,31 @@ def run_gpu(args):
     e2e_ms = reduce_max(e0.elapsed_time(e1), dev)
     e2e_value = weak_scaling_value(work.ops, args.steps, world, e2e_ms)
 
-    # ---- roofline of the dominant kernel (the QKV linear)
+    # ---- roofline of the dominant kernel (the gate/up linear)
     hbm_gbs, bf16_tflops, peak_src = load_peaks()
-    qkv_avg_s = statistics.mean(qkv_ms) / 1e3
-    achieved = work.ops_linear_qkv / qkv_avg_s / 1e12
-    traffic = kernel_traffic("linear_tc.cu", "linear_qkv_m304_k5120_n15360")
-    roofline = {"kernel": "prism_w8a8_linear (QKV, M=304 K=5120 N=15360)", "bound": "tensor",
+    sustained = load_sustained_bf16()
+    gu_avg_s = statistics.mean(gu_us) / 1e6
+    achieved = work.ops_gu / gu_avg_s / 1e12
+    traffic = kernel_traffic("linear_f16.cu", "linear_f16_gateup_m2048_k5120_n34816")
+    roofline = {"kernel": "prism_w8a8_linear_f16 (gate/up, M=2048 K=5120 N=34816)", "bound": "tensor",
                 "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
                 "frac": achieved / bf16_tflops, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 dense (burst): exact int8 contraction's best pipe on sm_103a",
-                "algorithmic_ops_per_launch": work.ops_linear_qkv,
-                "algorithmic_bytes_per_launch": work.bytes_qkv,
-                "achieved_gbs": work.bytes_qkv / qkv_avg_s / 1e9, "hbm_peak_gbs": hbm_gbs,
-                "avg_launch_us": qkv_avg_s * 1e6}
+                "peak_source": f"{peak_src} bf16 dense burst (the exact int8 contraction runs on the f16 "
+                               f"tensor pipe: sm_103a has no integer MMA)",
+                "frac_of_sustained": None if sustained is None else achieved / sustained,
+                "algorithmic_ops_per_launch": work.ops_gu,
+                "algorithmic_bytes_per_launch": work.bytes_gu,
+                "achieved_gbs": work.bytes_gu / gu_avg_s / 1e9, "hbm_peak_gbs": hbm_gbs,
+                "avg_launch_us": gu_avg_s * 1e6}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": "forest_bucket_m304_k5120: quant + qkv(n15360) + quant + o_proj(n5120,+res) "
-                               "+ candidate readout(3 pos, v248000)",
-                   "global_batch_rows": M * world, "schedule": {"qkv": "balanced" if split_q == 0 else f"split_k={split_q}",
-                                "o_proj": "balanced" if split_o == 0 else f"split_k={split_o}"},
-                   "l2": f"inputs larger than L2: {N_ROTATE} rotated weight sets "
-                         f"({N_ROTATE * (work.qkv.N + work.o.N) * K / 1e6:.0f} MB) + 1.27 GB LM head",
+        "config": {"workload": WORKLOAD, "global_batch_rows": M * world,
+                   "operands": "int8 codes held as binary16 (weights converted once at load time)",
+                   "schedule": "balanced persistent schedule, one CTA per SM",
+                   "l2": "inputs larger than L2: 534 MB of weight codes per step",
                    "launch": "direct C-ABI calls, arguments marshalled once",
                    "step_gbs": work.bytes * args.steps * world / secs / 1e9},
         "roofline": roofline,
@@ -496,22 +489,258 @@ def run_gpu(args):
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, rows, outs = run_cpu_baseline(work)
-        # the oracle's outputs for the sampled rows must match the GPU bit for bit
-        y_o, h_o, ro_o = outs
+        y_o, h_o = outs
         yb = Y.cpu().view(torch.int16).numpy().view(np.uint16)
         hb = H.cpu().view(torch.int16).numpy().view(np.uint16)
-        ok = np.array_equal(yb[rows], y_o) and np.array_equal(hb[rows], h_o)
-        if ro_o is not None:
-            ok = ok and np.array_equal(logits.cpu().numpy().view(np.uint32), ro_o[0].view(np.uint32))
-            ok = ok and np.array_equal(probs.cpu().numpy().view(np.uint32), ro_o[1].view(np.uint32))
-        cpu["matches_gpu_bitwise"] = bool(ok)
+        cpu["matches_gpu_bitwise"] = bool(np.array_equal(yb[rows], y_o) and np.array_equal(hb[rows], h_o))
         line["cpu_baseline"] = cpu
+    del Wgu, Wdn, Y
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_subrecords:
+        line["configs"] = run_subrecords(prism, L, dev)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_subrecords(prism, L, dev):
+    """Every other configuration of the method, timed alone on this GPU."""
+    import torch
+    out = {}
+    for name, fn in (("forest_bucket_m304", sub_forest), ("decode_m1_64_k17408_n5120", sub_decode),
+                     ("long_m8192_k5120_n5120", sub_long), ("readout_p192_v248000", sub_readout)):
+        try:
+            out[name] = fn(prism, L, dev)
+        except Exception as e:   # a sub-record never hides the headline
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    return out
+
+
+def _linear_record(ops, byts, us, hbm, bf16):
+    return {"us": us, "tops": ops / us / 1e6, "frac_bf16_peak": ops / us / 1e6 / bf16,
+            "gbs": byts / us / 1e3, "frac_hbm": byts / us / 1e3 / hbm}
+
+
+def sub_forest(prism, L, dev):
+    """Short-request forest bucket: quantise X [304, 5120] -> QKV (N 15360) ->
+    quantise -> o_proj (N 5120, +residual) -> read-out of the 3 answer
+    positions against a 248,000 x 5120 LM head.  Each linear takes the faster
+    of the two contraction kernels for its shape (binary16 codes for QKV, int8
+    operands for o_proj); three weight sets are rotated so that weights come
+    from HBM.  Per-linear times are events around that linear's launches."""
+    import ctypes
+    import torch
+    work = ForestWorkload()
+    M, K = M_ROWS, wl.HIDDEN
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf16 = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    sets = [dict(wq=prism.prism_codes_to_f16(t(work.qkv.w)), sq=t(work.qkv.w_scale), iq=t(work.qkv.inv_s),
+                 wo=t(work.o.w), so=t(work.o.w_scale), io=t(work.o.inv_s)) for _ in range(N_ROTATE)]
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    lm_head = torch.randint(-127, 128, (wl.VOCAB, K), dtype=torch.int8, device=dev, generator=g)
+    lm_head[t(work.cand_unique.astype(np.int64))] = t(work.cand_rows)
+    lm_scale = t(work.ro.lm_scale)
+    X, Xo, Res = bf16(work.qkv.x_bits), bf16(work.o.x_bits), bf16(work.o.residual_bits)
+    off, ids = t(work.ro.cand_offsets), t(work.ro.cand_ids)
+    T = int(ids.numel())
+    q1 = torch.empty((M, K), dtype=torch.float16, device=dev)
+    q2 = torch.empty((M, K), dtype=torch.int8, device=dev)
+    a1 = torch.empty((M,), dtype=torch.float32, device=dev)
+    a2 = torch.empty_like(a1)
+    Y = torch.empty((M, work.qkv.N), dtype=torch.bfloat16, device=dev)
+    H = torch.empty((M, work.o.N), dtype=torch.bfloat16, device=dev)
+    logits = torch.empty((T,), dtype=torch.float32, device=dev)
+    probs = torch.empty((T,), dtype=torch.float32, device=dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ws_q = prism.new_workspace_f16(M, work.qkv.N, K, 0, dev)
+    ws_o = prism.new_workspace(M, work.o.N, K, 0, dev)
+    hid = H[ANSWER_ROWS[0]::16]
+    vp = lambda x: ctypes.c_void_p(x.data_ptr()) if x is not None else None
+    stream = torch.cuda.Stream(device=dev)
+    st = ctypes.c_void_p(stream.cuda_stream)
+    nb = lambda w: 0 if w is None else w.numel()
+    Nq, No = work.qkv.N, work.o.N
+
+    def calls_for(s):
+        return [
+            (L.prism_quant_act_f16, (vp(X), K, vp(s["iq"]), M, K, vp(q1), K, vp(a1), st)),
+            (L.prism_w8a8_linear_f16, (vp(q1), K, vp(a1), vp(s["wq"]), K, vp(s["sq"]), None, 0, vp(Y), Nq,
+                                       None, M, Nq, K, 0, vp(ws_q), nb(ws_q), st)),
+            (L.prism_quant_act, (vp(Xo), K, vp(s["io"]), M, K, vp(q2), K, vp(a2), st)),
+            (L.prism_w8a8_linear, (vp(q2), K, vp(a2), vp(s["wo"]), K, vp(s["so"]), vp(Res), No, vp(H), No,
+                                   None, M, No, K, 0, vp(ws_o), nb(ws_o), st)),
+            (L.prism_candidate_readout, (vp(hid), hid.stride(0), None, vp(lm_head), K, vp(lm_scale),
+                                         wl.VOCAB, K, vp(off), vp(ids), len(ANSWER_ROWS), T, vp(logits),
+                                         vp(probs), vp(err), None, 0, st)),
+        ]
+
+    rot = [calls_for(s) for s in sets]
+    ev = {j: [] for j in (1, 3, 4)}
+
+    def step(i, record=False):
+        for j, (fn, a) in enumerate(rot[i % N_ROTATE]):
+            if record and j in ev:
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                e[0].record(stream)
+            assert fn(*a) == 0
+            if record and j in ev:
+                e[1].record(stream)
+                ev[j].append(e)
+
+    for i in range(5):
+        step(i)
+    torch.cuda.synchronize()
+    n = 30
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for i in range(n):
+        step(i)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    step_us = s0.elapsed_time(s1) * 1e3 / n
+    for i in range(n):
+        step(i, record=True)
+    torch.cuda.synchronize()
+    us = {j: statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev[j]) for j in ev}
+    assert int(err.item()) == 0
+    hbm, bf16p, _ = load_peaks()
+    bq = M * K + Nq * K + 4 * Nq + 4 * M + 2 * M * Nq
+    bo = M * K + No * K + 4 * No + 4 * M + 2 * M * No * 2
+    br = 2 * 3 * K + T * (K + 4) + 16 + 12 * T
+    return {"step_us": step_us, "step_tops": work.ops / step_us / 1e6, "launches_per_step": 5,
+            "qkv_m304_k5120_n15360": dict(_linear_record(work.ops_linear_qkv, bq, us[1], hbm, bf16p),
+                                          kernel="binary16 codes"),
+            "oproj_m304_k5120_n5120": dict(_linear_record(work.ops_linear_o, bo, us[3], hbm, bf16p),
+                                           kernel="int8 operands"),
+            "readout_p3": {"us": us[4], "gbs": br / us[4] / 1e3, "frac_hbm": br / us[4] / 1e3 / hbm},
+            "timing": "back-to-back steps on one stream, 3 rotated weight sets; per-call events in a second pass"}
+
+
+def sub_decode(prism, L, dev):
+    """Decode-like weight stream: M in {1, 8, 16, 64} rows of a 5120 x 17408
+    weight (+ residual) at split-K in {1, 4, 8, 16}: device time per call (a
+    CUDA graph of back-to-back calls, four weight copies rotated so each call
+    reads its weight from HBM), GB/s of the int8 weight stream, and the bit
+    identity of every row across all 16 runs."""
+    import torch
+    c = wl.make_linear("decode_m64_k17408_n5120")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    X = torch.from_numpy(c.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    q, a = prism.prism_quant_act(X, t(c.inv_s))
+    n_rot = 4
+    Ws = [t(c.w) for _ in range(n_rot)]
+    S = t(c.w_scale)
+    R = torch.from_numpy(c.residual_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    hbm, bf16p, _ = load_peaks()
+    recs, ref = {}, None
+    identical = True
+    for M in wl.DECODE_M:
+        best = None
+        for split in wl.DECODE_SPLITS:
+            ws = prism.new_workspace(M, c.N, c.K, split, dev)
+            out = torch.empty((M, c.N), dtype=torch.bfloat16, device=dev)
+            fn = lambda i: prism.prism_w8a8_linear(q[:M], a[:M], Ws[i % n_rot], S, residual=R[:M], out=out,
+                                                   split_k=split, workspace=ws)
+            us = graph_time_us([lambda i=i: fn(i) for i in range(2 * n_rot)])
+            bits = out.view(torch.int16)
+            if ref is None:
+                ref = torch.empty((64, c.N), dtype=torch.int16, device=dev)
+                ref[:M] = bits
+                filled = M
+            elif M > filled:
+                ref[filled:M] = bits[filled:M]
+                filled = M
+            identical = identical and torch.equal(bits, ref[:M])
+            byts = M * c.K + c.N * c.K + 4 * c.N + 4 * M + 2 * M * c.N * 2
+            r = dict(_linear_record(2 * M * c.N * c.K, byts, us, hbm, bf16p),
+                     kind=prism.prism_w8a8_kernel_kind(M, c.N, c.K))
+            recs[f"m{M}_split{split}"] = r
+            if best is None or us < best[1]:
+                best = (split, us, r["frac_hbm"])
+        recs[f"m{M}_best"] = {"split": best[0], "us": best[1], "frac_hbm": best[2]}
+    torch.cuda.synchronize()
+    recs["all_rows_bit_identical_across_m_and_split"] = bool(identical)
+    return recs
+
+
+def sub_long(prism, L, dev):
+    """Long-evidence linear: M = 8192, K = N = 5120, + residual, binary16
+    codes (four weight copies rotated)."""
+    import torch
+    c = wl.make_linear("long_m8192_k5120_n5120")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    X = torch.from_numpy(c.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    qh, a = prism.prism_quant_act_f16(X, t(c.inv_s))
+    w8 = t(c.w)
+    Ws = [prism.prism_codes_to_f16(w8) for _ in range(4)]
+    S = t(c.w_scale)
+    R = torch.from_numpy(c.residual_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev)
+    ws = prism.new_workspace_f16(c.M, c.N, c.K, 0, dev)
+    fn = lambda i: prism.prism_w8a8_linear_f16(qh, a, Ws[i % 4], S, residual=R, out=out, workspace=ws)
+    us, _ = _timed(torch.cuda.current_stream(), fn, 20)
+    hbm, bf16p, _ = load_peaks()
+    byts = c.M * c.K + c.N * c.K + 4 * c.N + 4 * c.M + 2 * c.M * c.N * 2
+    return dict(_linear_record(2 * c.M * c.N * c.K, byts, us, hbm, bf16p), kernel="binary16 codes")
+
+
+def sub_readout(prism, L, dev):
+    """Candidate read-out of 192 answer positions (2-10 candidates each)
+    against a 248,000 x 5120 LM head, next to a plain gather of the same
+    candidate rows (torch.index_select, the rows' bytes copied once): the
+    gather is the measured ceiling of a read-out that must fetch those rows.
+    Several candidate sets and two heads are rotated so that rows come from
+    HBM; both are CUDA graphs of back-to-back calls."""
+    import torch
+    P, K = 192, wl.HIDDEN
+    case = wl.readout_case("readout", P=P, K=K, V=wl.VOCAB, seed=7)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    uniq = np.unique(case.cand_ids)
+    rows = torch.from_numpy(case.lm_rows(uniq)).to(dev)
+    heads = []
+    for _ in range(2):
+        W = torch.randint(-127, 128, (case.V, K), dtype=torch.int8, device=dev, generator=g)
+        W[torch.from_numpy(uniq.astype(np.int64)).to(dev)] = rows
+        heads.append(W)
+    n_sets = max(8, int(np.ceil(2 * 129e6 / (P * 6 * (K + 4)))))
+    sets = []
+    for r in range(n_sets):
+        cs = wl.readout_case("readout", P=P, K=K, V=wl.VOCAB, seed=100 + r)
+        sets.append((torch.from_numpy(cs.h_bits.view(np.int16)).view(torch.bfloat16).to(dev),
+                     torch.from_numpy(cs.cand_offsets).to(dev), torch.from_numpy(cs.cand_ids).to(dev),
+                     int(cs.cand_ids.size)))
+    ls = torch.from_numpy(case.lm_scale).to(dev)
+    Tmax = max(x[3] for x in sets)
+    lg = torch.empty((Tmax,), dtype=torch.float32, device=dev)
+    pr = torch.empty((Tmax,), dtype=torch.float32, device=dev)
+    gath = torch.empty((Tmax, K), dtype=torch.int8, device=dev)
+
+    def call(i):
+        h, off, ids, T = sets[i % n_sets]
+        prism.prism_candidate_readout(h, None, heads[i % 2], ls, off, ids, logits=lg[:T], probs=pr[:T])
+
+    def gather(i):
+        h, off, ids, T = sets[i % n_sets]
+        torch.index_select(heads[i % 2], 0, ids.long(), out=gath[:T])
+
+    n = 2 * n_sets
+    us = graph_time_us([lambda i=i: call(i) for i in range(n)])
+    gus = graph_time_us([lambda i=i: gather(i) for i in range(n)])
+    T = statistics.mean(x[3] for x in sets)
+    byts = 2 * P * K + T * (K + 4) + 4 * (P + 1) + 4 * T + 8 * T
+    gbytes = 2 * T * K   # the gather reads and writes every row once
+    hbm, _, _ = load_peaks()
+    return {"P": P, "T_avg": T, "us": us, "gbs": byts / us / 1e3, "frac_hbm": byts / us / 1e3 / hbm,
+            "gather_ceiling": {"us": gus, "row_bytes_gbs": T * K / gus / 1e3,
+                               "copy_gbs": gbytes / gus / 1e3, "frac_hbm": gbytes / gus / 1e3 / hbm},
+            "frac_of_gather_ceiling": gus / us,
+            "timing": f"CUDA graphs of back-to-back calls, {n_sets} candidate sets x 2 heads"}
 
 
 def run_kernel(args):
@@ -947,6 +1176,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-subrecords", action="store_true", help="headline line only (no per-config sub-records)")
     ap.add_argument("--kernel", choices=["linear", "linear_f16", "quant", "readout", "requant", "restricted", "tp",
                                          "w4a8", "int8_peak"],
                     help="time one call type alone")
