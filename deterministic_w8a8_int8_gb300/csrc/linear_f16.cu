@@ -135,13 +135,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 }
 // Teardown wait: bounded by kDrainLimitNs, blind to the abort flag.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-  const unsigned long long t0 = tc::globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (tc::globaltimer() - t0 > kDrainLimitNs) {
-      atomicOr(&g_f16_status, kStatusTimeout);
-      return;
-    }
-  }
+  tc::mbar_wait_drain_bounded(bar, parity, kDrainLimitNs, &g_f16_status, kStatusTimeout);
 }
 // Named barrier 1 over the epilogue warps, returning whether any thread
 // passed `pred` (the same answer in every thread).

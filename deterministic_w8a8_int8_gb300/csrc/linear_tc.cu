@@ -119,7 +119,6 @@ struct TcParams {
 
 // ------------------------------------------------------------ PTX helpers --
 using tc::fence_proxy_async;
-using tc::globaltimer;
 using tc::idesc_f16_f32;
 using tc::mbar_arrive;
 using tc::mbar_expect_tx;
@@ -145,13 +144,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 // Teardown wait: bounded by kWaitLimitNs, blind to the abort flag.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      atomicOr(&g_kernel_error, kDevErrTimeout);
-      return;
-    }
-  }
+  tc::mbar_wait_drain_bounded(bar, parity, kWaitLimitNs, &g_kernel_error, kDevErrTimeout);
 }
 // The same wait made by every lane of a warp: all lanes poll (one broadcast
 // shared-memory read per poll) and the warp agrees on the outcome, so the warp

@@ -31,6 +31,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Elapsed-time test of a bounded wait on the global nanosecond timer.  That
+// timer is not promised to be monotonic: it can step backwards when it is
+// re-synchronised with the host clock.  An unsigned difference taken across
+// such a step wraps to about 2^64 ns and would end, as "expired", a wait that
+// had barely started -- the kernel would then wind down and leave wrong
+// outputs behind a status bit.  So a backward step restarts the measurement
+// from the new reading, and expiry also needs kMinPolls polls, which no
+// completed handshake of these kernels comes near.
+constexpr uint32_t kMinPolls = 4096;
+__device__ __forceinline__ bool wait_expired(unsigned long long& t0, uint32_t polls, unsigned long long limit_ns) {
+  const unsigned long long now = globaltimer();
+  if (now < t0) {
+    t0 = now;
+    return false;
+  }
+  return polls >= kMinPolls && now - t0 > limit_ns;
+}
 // Bounded wait for the phase of the given parity: true when it completed;
 // false when *abort_flag was set by another thread of the CTA, or when
 // limit_ns of global time passed (then the flag is set and status_bit is
@@ -39,16 +56,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned long long limit_ns, uint32_t* status,
                                                   uint32_t status_bit) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
+  unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > limit_ns) {
+      if (wait_expired(t0, i, limit_ns)) {
         *abort_flag = 1;
         atomicOr(status, status_bit);
         return false;
       }
+    }
+  }
+}
+// Teardown wait (for copies and MMAs already issued): bounded by limit_ns,
+// blind to any abort flag; expiry only ORs status_bit into *status.
+__device__ __forceinline__ void mbar_wait_drain_bounded(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
+                                                        uint32_t* status, uint32_t status_bit) {
+  unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1; !mbar_try_wait(bar, parity); ++i) {
+    if ((i & 255u) == 0u && wait_expired(t0, i, limit_ns)) {
+      atomicOr(status, status_bit);
+      return;
     }
   }
 }

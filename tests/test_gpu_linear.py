@@ -176,22 +176,25 @@ def test_decode_rows_invariant_across_m_and_split(cuda_device):
 @pytest.mark.parametrize("name", ["forest_qkv_m304_k5120_n15360", "forest_oproj_m304_k5120_n5120",
                                   "load_gateup_m2048_k5120_n34816", "load_down_m2048_k17408_n5120",
                                   "long_m8192_k5120_n5120"])
-def test_full_size_sampled_parity(cuda_device, name):
+def test_full_size_every_tile(cuda_device, name):
     """Full-size call in the benchmark's launch configuration (automatic
-    split-K); sampled rows and output channels checked against the oracle,
-    which computes them one by one."""
+    schedule, so shared tiles and their read-back are included): one row of
+    every 128-row block (plus the first and last rows) checked against the
+    oracle across ALL output channels, accumulators and outputs -- every
+    output tile of either orientation holds some of the checked elements."""
     c = wl.make_linear(name)
     q, a = prism.prism_quant_act(dev_bf16(c.x_bits), dev(c.inv_s))
     R = None if c.residual_bits is None else dev_bf16(c.residual_bits)
-    out, _ = gpu_linear(q, a, dev(c.w), dev(c.w_scale), R, acc=False)
+    out, acc = gpu_linear(q, a, dev(c.w), dev(c.w_scale), R, acc=True)
     rng = np.random.default_rng(7)
-    rows = np.unique(np.concatenate([[0, c.M - 1], rng.choice(c.M, 6, replace=False)]))
-    cols = np.unique(np.concatenate([[0, c.N - 1], rng.choice(c.N, 250, replace=False)]))
+    rows = [0, c.M - 1] + [b * 128 + int(rng.integers(0, min(128, c.M - b * 128))) for b in range((c.M + 127) // 128)]
+    rows = np.unique(np.array(rows))
     qo, ao = oracle.quant_act(c.x_bits[rows], c.inv_s)
     assert np.array_equal(host(q)[rows], qo) and np.array_equal(host(a)[rows], ao)
-    rr = None if c.residual_bits is None else c.residual_bits[rows][:, cols]
-    outo, _ = oracle.w8a8_linear(qo, ao, c.w[cols], c.w_scale[cols], rr)
-    assert np.array_equal(host_bits(out)[rows][:, cols], outo)
+    rr = None if c.residual_bits is None else c.residual_bits[rows]
+    outo, acco = oracle.w8a8_linear(qo, ao, c.w, c.w_scale, rr)
+    assert np.array_equal(host(acc)[rows], acco)
+    assert np.array_equal(host_bits(out)[rows], outo)
 
 
 def _with_path(path, fn):

@@ -6,8 +6,9 @@ fixed memory budget).  For them the library keeps a fixed scratch array of
 its own.  These tests call that entry point through the C ABI and check that
 its outputs equal prism_w8a8_linear's bit for bit -- the tolerance every
 linear test here uses -- on two calls in a row (the second call reuses the
-shared array the first one left behind), and that shapes whose scratch would
-not fit are refused.  This file is named to be collected last.
+shared array the first one left behind), that on a shape with shared tiles
+they also equal the CPU oracle's on their own, and that shapes whose scratch
+would not fit are refused.  This file is named to be collected last.
 """
 import ctypes
 
@@ -15,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 
 import deterministic_w8a8_int8_gb300 as prism
@@ -60,6 +62,31 @@ def test_noalloc_matches_workspace_entry_point(cuda_device, M, N, K, split):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
         assert torch.equal(acc, ref_acc)
+
+
+def test_noalloc_matches_oracle(cuda_device):
+    """A shape whose automatic schedule shares tiles between CTAs (so the
+    scratch array is used), checked against the oracle directly, twice."""
+    M, N, K = 70, 520, 2064
+    assert prism.prism_w8a8_workspace_bytes(M, N, K, 0) > 0
+    rng = np.random.default_rng(5)
+    xb = wl.bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    w = wl.draw_weights(rng, (N, K), "normal")
+    ws = rng.uniform(0.001, 0.02, N).astype(np.float32)
+    rb = wl.bf16_bits(rng.standard_normal((M, N), dtype=np.float32))
+    qo, ao = oracle.quant_act(xb, None)
+    outo, acco = oracle.w8a8_linear(qo, ao, w, ws, rb)
+    q = torch.from_numpy(qo).cuda()
+    a = torch.from_numpy(ao).cuda()
+    W, S = torch.from_numpy(w).cuda(), torch.from_numpy(ws).cuda()
+    R = torch.from_numpy(rb.view(np.int16)).view(torch.bfloat16).cuda()
+    for _ in range(2):
+        out = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+        acc = torch.full((M, N), -1, dtype=torch.int32, device="cuda")
+        assert _noalloc(q, a, W, S, R, out, acc, 0) == prism.PRISM_OK
+        torch.cuda.synchronize()
+        assert np.array_equal(acc.cpu().numpy(), acco)
+        assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), outo)
 
 
 def test_noalloc_refuses_scratch_beyond_its_array(cuda_device):
