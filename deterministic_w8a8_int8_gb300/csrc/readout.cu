@@ -11,14 +11,15 @@
 //   3. each warp takes candidates round-robin and streams the candidate's
 //      LM-head row with 16-byte non-allocating loads, dp4a into exact int32,
 //      warp-reduces, and forms logit = (float(acc) * a_scale) * lm_scale[c];
-//   4. one thread forms the softmax in list order: e_c = exp(logit_c - max),
-//      s = e_1 + ... + e_n, prob_c = e_c / s, every step binary32 RN.
+//   4. warp 0 forms the softmax: max over the logits, e_c = exp(logit_c -
+//      max) and prob_c = e_c / s one candidate per lane, s = e_1 + ... + e_n
+//      added in list order; every step binary32 RN.
 // Bytes: 2K (hidden row) + count * (K + 4) (candidate rows and scales) per
 // position, plus 12 bytes per candidate (id, logit, prob) -- HBM- and
-// latency-bound; nothing is written to global memory but the outputs.  For K
-// up to 8192 each warp starts streaming its first candidate row right after
-// the offsets are checked (the id is range-checked first), and the hidden
-// row is read once into registers.
+// latency-bound (a chain of dependent reads: offsets, ids, rows); nothing is
+// written to global memory but the outputs.  The hidden row's loads and the
+// candidate rows' copies into shared memory go out as early as their
+// addresses are known, so the chain is three memory round trips long.
 #include "common.cuh"
 
 namespace prism {
@@ -71,15 +72,21 @@ __device__ __forceinline__ float smooth(float v, const float* inv_s, int64_t k) 
   return inv_s != nullptr ? __fmul_rn(v, __ldg(inv_s + k)) : v;
 }
 
-// Hidden rows of up to kRegK elements are read once into registers; the
-// first 5 KB of each warp's first candidate row (all of a 5120-wide row) are
-// fetched into registers as soon as its id is known to be in range, so that
-// their memory latency overlaps the quantisation of the hidden row (any rest
-// of a longer row is read when the dot product reaches it).  Two CTAs fit on an SM (at most 128
-// registers), so 192 answer positions run in one wave on 152 SMs.
+// Hidden rows of up to kRegK elements are read once into registers, with
+// loads issued before anything else (they depend on p alone).  The first
+// pre_rows candidates of a position (pre_rows set by the launcher from the
+// shared memory that two CTAs per SM leave: 16 rows of a 5120-wide head)
+// are copied into shared memory with cp.async as soon as each id has passed
+// its range check, together with their lm_scale values, so that all of the
+// position's gathers are in flight while the list is validated and the
+// hidden row quantised; candidates beyond pre_rows are streamed when the dot
+// product reaches them.  Two CTAs fit on an SM (at most 128 registers), so
+// 192 answer positions run in one wave on 152 SMs.
 constexpr int kRegK = 8192;
 constexpr int kHidVec = kRegK / 8 / kThreads;   // uint4 (8 bf16) per thread: 4
-constexpr int kRowVec = 10;                     // uint4 (16 int8) per lane: 5 KB of the row per warp
+constexpr int kPreMax = 16;                     // staged candidate rows at most
+constexpr int kPrePerWarp = kPreMax / kWarps;   // 2
+constexpr int kSmemBudget = 110 * 1024;         // dynamic shared memory per CTA (two per SM)
 
 template <bool kReg>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -87,54 +94,86 @@ __global__ void __launch_bounds__(kThreads, 2)
                    const int8_t* __restrict__ W, int64_t ldw, const float* __restrict__ lm_scale,
                    int64_t V, int64_t K, const int32_t* __restrict__ off,
                    const int32_t* __restrict__ ids, int64_t T, float* __restrict__ logits,
-                   float* __restrict__ probs, uint32_t* __restrict__ err) {
-  extern __shared__ __align__(16) int8_t sq[];
+                   float* __restrict__ probs, uint32_t* __restrict__ err, int pre_rows) {
+  extern __shared__ __align__(16) int8_t smem[];
+  int8_t* sq = smem;          // [K] the quantised hidden row
+  int8_t* srow = smem + K;    // [pre_rows][K] staged candidate rows
   pdl_trigger();
   pdl_wait();
   __shared__ float s_logit[PRISM_MAX_CANDIDATES];
-  __shared__ float s_prob[PRISM_MAX_CANDIDATES];
   __shared__ float s_red[kWarps];
   __shared__ unsigned s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t p = blockIdx.x;
   const int64_t nchunk = K >> 4;   // 16-byte chunks of a row
 
-  // ---- 1. validate this position's candidate list
-  if (tid == 0) s_bad = 0u;
-  __syncthreads();
+  // the hidden row depends on nothing but p: its loads go out first
+  const uint16_t* hr = h + p * ldh;
+  uint4 hv[kReg ? kHidVec : 1];
+  if (kReg) {
+#pragma unroll
+    for (int i = 0; i < kHidVec; ++i) {
+      const int64_t k = (static_cast<int64_t>(tid) + static_cast<int64_t>(i) * kThreads) * 8;
+      hv[i] = k < K ? __ldg(reinterpret_cast<const uint4*>(hr + k)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  // ---- 1. stage the first candidate rows, validate the candidate list
   const int64_t b = off[p], e = off[p + 1];
   const bool off_ok = b >= 0 && e <= T && b <= e;
   const int64_t cnt = off_ok ? e - b : 0;
   const bool cnt_ok = off_ok && cnt >= 1 && cnt <= PRISM_MAX_CANDIDATES;
-  // this warp's first candidate row, fetched early when its id is in range
-  uint4 row[kReg ? kRowVec : 1];
-  int32_t id0 = -1;
-  if (kReg && cnt_ok && warp < cnt) {
-    const int32_t id = ids[b + warp];
-    if (id >= 0 && id < V) {
-      id0 = id;
-      const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
+  // the position's ids, held by every warp: candidate c is lane c % 32 of
+  // id_l (c < 32) or id_h (two coalesced loads; L1 serves the other warps)
+  int32_t id_l = -1, id_h = -1;
+  if (cnt_ok) {
+    if (lane < cnt) id_l = ids[b + lane];
+    if (lane + 32 < cnt) id_h = ids[b + lane + 32];
+  }
+  auto id_of = [&](int64_t c) {   // c is the same in every lane
+    return __shfl_sync(0xffffffffu, c < 32 ? id_l : id_h, static_cast<int>(c & 31));
+  };
+  const int nstage = cnt_ok ? static_cast<int>(cnt < pre_rows ? cnt : pre_rows) : 0;
+  int32_t pre_id[kPrePerWarp];
+  float pre_ls[kPrePerWarp];
 #pragma unroll
-      for (int i = 0; i < kRowVec; ++i) {
-        const int64_t c = lane + 32 * i;
-        row[i] = c < nchunk ? ld_stream_16(wr + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+  for (int j = 0; j < kPrePerWarp; ++j) {
+    const int c = warp + j * kWarps;
+    pre_id[j] = -1;
+    pre_ls[j] = 0.0f;
+    if (c < nstage) {
+      const int32_t id = id_of(c);
+      if (id >= 0 && id < V) {   // out-of-range ids are never dereferenced
+        pre_id[j] = id;
+        pre_ls[j] = __ldg(lm_scale + id);
+        const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
+        const uint32_t dst = smem_u32(srow + static_cast<int64_t>(c) * K);
+        for (int64_t ch = lane; ch < nchunk; ch += 32) cp_async_16(dst + static_cast<uint32_t>(ch * 16), wr + ch * 16, 16);
       }
     }
   }
-  unsigned bad = 0u;
-  if (!off_ok) {
-    bad = PRISM_DEV_ERR_OFFSETS;
-  } else if (!cnt_ok) {
-    bad = PRISM_DEV_ERR_COUNT;
-  } else if (tid < cnt) {
-    const int32_t id = ids[b + tid];
-    if (id < 0 || id >= V) bad |= PRISM_DEV_ERR_ID_RANGE;
-    for (int j = 0; j < tid; ++j)
-      if (ids[b + j] == id) bad |= PRISM_DEV_ERR_DUPLICATE;
+  cp_async_commit();
+  // warp 0 validates: offsets, count, every id in range, no id twice
+  if (warp == 0) {
+    unsigned bad = 0u;
+    if (!off_ok) {
+      bad = PRISM_DEV_ERR_OFFSETS;
+    } else if (!cnt_ok) {
+      bad = PRISM_DEV_ERR_COUNT;
+    } else {
+      const bool has_l = lane < cnt, has_h = lane + 32 < cnt;
+      if ((has_l && (id_l < 0 || id_l >= V)) || (has_h && (id_h < 0 || id_h >= V))) bad |= PRISM_DEV_ERR_ID_RANGE;
+      for (int64_t i = 0; i < cnt; ++i) {
+        const int32_t o = id_of(i);
+        if ((has_l && i < lane && o == id_l) || (has_h && i < lane + 32 && o == id_h)) bad |= PRISM_DEV_ERR_DUPLICATE;
+      }
+    }
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (lane == 0) s_bad = bad;
   }
-  if (bad) atomicOr(&s_bad, bad);
   __syncthreads();
   if (s_bad) {
+    cp_async_wait<0>();   // no copy may land in shared memory after the CTA is gone
     if (tid == 0 && err != nullptr) atomicOr(err, s_bad);
     if (off_ok) {
       const float nan = __uint_as_float(0x7fc00000u);
@@ -147,15 +186,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // ---- 2. quantise the hidden row into shared memory
-  const uint16_t* hr = h + p * ldh;
-  uint4 hv[kReg ? kHidVec : 1];
   float amax = 0.0f;
   if (kReg) {
-#pragma unroll
-    for (int i = 0; i < kHidVec; ++i) {
-      const int64_t k = (static_cast<int64_t>(tid) + static_cast<int64_t>(i) * kThreads) * 8;
-      hv[i] = k < K ? __ldg(reinterpret_cast<const uint4*>(hr + k)) : make_uint4(0u, 0u, 0u, 0u);
-    }
 #pragma unroll
     for (int i = 0; i < kHidVec; ++i) {
       const int64_t k = (static_cast<int64_t>(tid) + static_cast<int64_t>(i) * kThreads) * 8;
@@ -211,22 +243,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int64_t k = static_cast<int64_t>(tid) * 8; k < K; k += kThreads * 8)
       quant8(__ldg(reinterpret_cast<const uint4*>(hr + k)), k);
   }
-  __syncthreads();
+  cp_async_wait<0>();
+  __syncthreads();   // the quantised row and every staged candidate row are visible
 
   // ---- 3. one warp per candidate: exact int32 dot against the gathered row
   for (int64_t i = warp; i < cnt; i += kWarps) {
-    const int32_t id = ids[b + i];
-    const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
     int acc = 0;
-    if (kReg && i == warp && id == id0) {
+    int32_t id;
+    float ls;
+    if (i < nstage) {
+      const int j = static_cast<int>(i) / kWarps;
+      id = pre_id[0];
 #pragma unroll
-      for (int j = 0; j < kRowVec; ++j) {
-        const int64_t c = lane + 32 * j;
-        if (c < nchunk) acc = dot16(row[j], *reinterpret_cast<const uint4*>(sq + c * 16), acc);
-      }
-      for (int64_t c = lane + 32 * kRowVec; c < nchunk; c += 32)
-        acc = dot16(ld_stream_16(wr + c * 16), *reinterpret_cast<const uint4*>(sq + c * 16), acc);
+      for (int jj = 1; jj < kPrePerWarp; ++jj)
+        if (j == jj) id = pre_id[jj];
+      ls = pre_ls[0];
+#pragma unroll
+      for (int jj = 1; jj < kPrePerWarp; ++jj)
+        if (j == jj) ls = pre_ls[jj];
+      const int8_t* rs = srow + i * K;
+      for (int64_t c = lane; c < nchunk; c += 32)
+        acc = dot16(*reinterpret_cast<const uint4*>(rs + c * 16), *reinterpret_cast<const uint4*>(sq + c * 16), acc);
     } else {
+      id = id_of(i);
+      ls = __ldg(lm_scale + id);
+      const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
       int64_t c = lane;
       for (; c + 32 * 3 < nchunk; c += 32 * 4) {
         const uint4 w0 = ld_stream_16(wr + (c)*16);
@@ -246,28 +287,36 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       float t = __int2float_rn(acc);
       t = __fmul_rn(t, a_scale);
-      t = __fmul_rn(t, __ldg(lm_scale + id));
+      t = __fmul_rn(t, ls);
       s_logit[i] = t;
     }
   }
   __syncthreads();
 
-  // ---- 4. softmax over the candidates, fixed order
-  if (tid == 0) {
-    float mx = s_logit[0];
-    for (int i = 1; i < cnt; ++i) mx = fmaxf(mx, s_logit[i]);
+  // ---- 4. softmax over the candidates, fixed order, in warp 0: the maximum
+  // (exact, any order), e_c = exp(logit_c - max) and prob_c = e_c / s one
+  // candidate per lane, and s = e_1 + ... + e_n added in list order (every
+  // lane forms the same sum from shuffled values)
+  if (warp == 0) {
+    const float l0 = lane < cnt ? s_logit[lane] : -INFINITY;
+    const float l1 = lane + 32 < cnt ? s_logit[lane + 32] : -INFINITY;
+    float mx = fmaxf(l0, l1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float e0 = lane < cnt ? cw_exp(__fsub_rn(l0, mx)) : 0.0f;
+    const float e1 = lane + 32 < cnt ? cw_exp(__fsub_rn(l1, mx)) : 0.0f;
     float s = 0.0f;
-    for (int i = 0; i < cnt; ++i) {
-      const float ev = cw_exp(__fsub_rn(s_logit[i], mx));
-      s_prob[i] = ev;
-      s = __fadd_rn(s, ev);
+    const int n0 = static_cast<int>(cnt < 32 ? cnt : 32);
+    for (int i = 0; i < n0; ++i) s = __fadd_rn(s, __shfl_sync(0xffffffffu, e0, i));
+    for (int i = 32; i < cnt; ++i) s = __fadd_rn(s, __shfl_sync(0xffffffffu, e1, i - 32));
+    if (lane < cnt) {
+      logits[b + lane] = l0;
+      probs[b + lane] = __fdiv_rn(e0, s);
     }
-    for (int i = 0; i < cnt; ++i) s_prob[i] = __fdiv_rn(s_prob[i], s);
-  }
-  __syncthreads();
-  if (tid < cnt) {
-    logits[b + tid] = s_logit[tid];
-    probs[b + tid] = s_prob[tid];
+    if (lane + 32 < cnt) {
+      logits[b + lane + 32] = l1;
+      probs[b + lane + 32] = __fdiv_rn(e1, s);
+    }
   }
 }
 
@@ -277,19 +326,23 @@ cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const
                            int64_t ldw, const float* lm_scale, int64_t V, int64_t K,
                            const int32_t* off, const int32_t* ids, int64_t P, int64_t T,
                            float* logits, float* probs, uint32_t* err, cudaStream_t stream) {
-  const int smem = static_cast<int>((K + 15) & ~static_cast<int64_t>(15));
+  // staged rows: as many as fit beside the quantised row in kSmemBudget, at most kPreMax
+  const int64_t fit = K < kSmemBudget ? (kSmemBudget - K) / K : 0;
+  const int pre = static_cast<int>(std::min<int64_t>(kPreMax, fit));
+  const size_t smem = static_cast<size_t>(K) * static_cast<size_t>(1 + pre);
   if (K <= kRegK) {
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<true>), kRegK);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<true>), kSmemBudget);
     if (e != cudaSuccess) return e;
-    return launch_kernel(readout_kernel<true>, dim3(static_cast<unsigned>(P)), dim3(kThreads),
-                         static_cast<size_t>(smem), stream, true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw,
-                         lm_scale, V, K, off, ids, T, logits, probs, err);
+    return launch_kernel(readout_kernel<true>, dim3(static_cast<unsigned>(P)), dim3(kThreads), smem, stream, true,
+                         static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, K, off, ids, T, logits,
+                         probs, err, pre);
   }
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<false>), PRISM_MAX_READOUT_K);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<false>),
+                                   std::max<int>(kSmemBudget, PRISM_MAX_READOUT_K));
   if (e != cudaSuccess) return e;
-  return launch_kernel(readout_kernel<false>, dim3(static_cast<unsigned>(P)), dim3(kThreads),
-                       static_cast<size_t>(smem), stream, true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw,
-                       lm_scale, V, K, off, ids, T, logits, probs, err);
+  return launch_kernel(readout_kernel<false>, dim3(static_cast<unsigned>(P)), dim3(kThreads), smem, stream, true,
+                       static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, K, off, ids, T, logits,
+                       probs, err, pre);
 }
 
 }  // namespace prism
