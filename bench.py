@@ -623,10 +623,11 @@ def sub_forest(prism, L, dev):
 
 def sub_decode(prism, L, dev):
     """Decode-like weight stream: M in {1, 8, 16, 64} rows of a 5120 x 17408
-    weight (+ residual) at split-K in {1, 4, 8, 16}: device time per call (a
-    CUDA graph of back-to-back calls, four weight copies rotated so each call
-    reads its weight from HBM), GB/s of the int8 weight stream, and the bit
-    identity of every row across all 16 runs."""
+    weight (+ residual) at split-K in {1, 4, 8, 16} and the library's
+    automatic choice (0): device time per call (a CUDA graph of back-to-back
+    calls, four weight copies rotated so each call reads its weight from
+    HBM), GB/s of the int8 weight stream, and the bit identity of every row
+    across all 20 runs."""
     import torch
     c = wl.make_linear("decode_m64_k17408_n5120")
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -641,7 +642,7 @@ def sub_decode(prism, L, dev):
     identical = True
     for M in wl.DECODE_M:
         best = None
-        for split in wl.DECODE_SPLITS:
+        for split in (0,) + tuple(wl.DECODE_SPLITS):
             ws = prism.new_workspace(M, c.N, c.K, split, dev)
             out = torch.empty((M, c.N), dtype=torch.bfloat16, device=dev)
             fn = lambda i: prism.prism_w8a8_linear(q[:M], a[:M], Ws[i % n_rot], S, residual=R[:M], out=out,
@@ -801,14 +802,22 @@ def run_kernel(args):
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
-    avg = statistics.mean(us)
+    # device time per call without host gaps: a CUDA graph of back-to-back
+    # calls on the capturing stream (per-call events above also time the
+    # host's enqueue when a call is shorter than it)
+    def gcall(i):
+        cs = torch.cuda.current_stream().cuda_stream
+        assert fn(*calls[i % n_rot][:-1], ctypes.c_void_p(cs)) == 0
+
+    avg = graph_time_us([lambda i=i: gcall(i) for i in range(2 * n_rot)])
     ops = 2 * rows * N * K
     byts = rows * K + N * K + 4 * N + 4 * rows + 2 * rows * N * (2 if R is not None else 1)
     hbm, bf16, src = load_peaks()
     print(json.dumps({"kernel": "prism_w8a8_linear_f16" if f16 else "prism_w8a8_linear", "case": args.case,
                       "M": rows, "N": N, "K": K,
                       "split": split, "kind": "f16 codes" if f16 else prism.prism_w8a8_kernel_kind(rows, N, K),
-                      "avg_us": avg, "min_us": min(us), "tflops": ops / avg / 1e6,
+                      "avg_us": avg, "events_avg_us": statistics.mean(us), "min_us": min(us),
+                      "timing": "CUDA graph of back-to-back calls", "tflops": ops / avg / 1e6,
                       "frac_bf16_peak": ops / avg / 1e6 / bf16, "gbs": byts / avg / 1e3,
                       "frac_hbm": byts / avg / 1e3 / hbm, "weight_copies": n_rot,
                       "status": prism.prism_device_status()}), flush=True)

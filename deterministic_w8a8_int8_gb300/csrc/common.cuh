@@ -197,9 +197,12 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
 // Leading bytes of the workspace that must be zero when a call starts, for a
 // workspace of cap bytes (SIZE_MAX: the call cannot run within cap).
 size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, size_t cap);
-// Dispatch between the two contraction kernels (linear_tc.cu): the tcgen05
-// kernel by default; PRISM_LINEAR_PATH=mma selects the mma.sync s8 kernel.
+// Dispatch between the contraction kernels (linear_tc.cu): by token rows the
+// dp4a weight stream, the mma.sync weight stream or the tcgen05 kernel;
+// PRISM_LINEAR_PATH forces one (diagnostics).  linear_w4_packed: whether a
+// W4A8 call streams its packed weights through the dp4a kernel.
 int linear_kernel_kind(int64_t M, int64_t N, int64_t K);
+bool linear_w4_packed(int64_t M);
 int linear_auto_split(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream);
 int mma_auto_split(int64_t M, int64_t N, int64_t K);
@@ -211,6 +214,10 @@ cudaError_t launch_linear_gemv_w4(const LinearArgs& a, cudaStream_t stream);
 cudaError_t launch_unpack_w4(const uint8_t* w4, int64_t ldw4, int64_t N, int64_t K, int8_t* w8, int64_t ldw8,
                              cudaStream_t stream);
 cudaError_t launch_linear_mma(const LinearArgs& a, cudaStream_t stream);
+// The mma.sync weight-streaming kernel for calls of up to 16 token rows
+// (linear_stream.cu) and its workspace bytes.
+cudaError_t launch_linear_stream(const LinearArgs& a, cudaStream_t stream);
+size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int split);
 // Streaming multiprocessors of the current device (one persistent CTA each).
 int sm_count();
 // Sticky device error bits raised by kernels (bounded waits that expired).

@@ -52,6 +52,8 @@
 // be zeroed again before its next use.
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -608,9 +610,20 @@ struct HPlan {
   int64_t gx, gy;
 };
 
+// PRISM_F16_ORIENT=rows / =cols forces the tokens onto the MMA's rows / its
+// N side whatever M (a diagnostic: both orientations give the same bits).
+int orient_override() {
+  const char* e = std::getenv("PRISM_F16_ORIENT");
+  if (e == nullptr) return -1;
+  if (std::strcmp(e, "rows") == 0) return 0;
+  if (std::strcmp(e, "cols") == 0) return 1;
+  return -1;
+}
+
 HPlan plan(int64_t M, int64_t N) {
   HPlan pl{};
-  pl.swap = M < 512 ? 1 : 0;
+  const int forced = orient_override();
+  pl.swap = forced >= 0 ? forced : (M < 512 ? 1 : 0);
   if (pl.swap) {
     const int64_t pieces = cdiv(M, kBNMax);
     pl.bpiece = static_cast<int>(cdiv(cdiv(M, pieces), 32) * 32);
@@ -714,6 +727,8 @@ cudaError_t launch_linear_f16(const LinearF16Args& a, cudaStream_t stream) {
   p.nst = std::min(kMaxStages, kRing / ((kBM + pl.bpiece) * 128));
   p.sp.split = a.split;
   p.sp.gx = static_cast<int>(pl.gx);
+  p.sp.gy = static_cast<int>(pl.gy);
+  p.sp.a_w = pl.swap ? 1 : 0;
   p.sp.T = static_cast<int>(pl.gx * pl.gy);
   p.sp.S = static_cast<int>(cdiv(a.K, kBK));
   dim3 grid;

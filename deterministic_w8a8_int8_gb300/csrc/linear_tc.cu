@@ -1059,6 +1059,8 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
                                     ((kBM + pl.bpiece) * kBK * pl.sub));
   p.sp.split = a.split;
   p.sp.gx = static_cast<int>(pl.grid_x);
+  p.sp.gy = static_cast<int>(pl.grid_y);
+  p.sp.a_w = pl.swap ? 1 : 0;
   p.sp.T = static_cast<int>(pl.grid_x * pl.grid_y);
   p.sp.S = static_cast<int>(cdiv(a.K, kBK * pl.sub));
   dim3 grid;
@@ -1111,17 +1113,38 @@ static bool path_is(const char* name) {
   return s != nullptr && std::strcmp(s, name) == 0;
 }
 static bool use_mma_path() { return path_is("mma"); }
-// Calls of at most this many token rows stream the weights through the
-// dp4a kernel (linear_gemv.cu) unless the tcgen05 kernel is forced.
-constexpr int64_t kGemvMaxM = 8;
-static bool use_gemv_path(int64_t M) { return M <= kGemvMaxM && !path_is("tc") && !path_is("mma"); }
+// Calls of at most kGemvMaxM token rows stream the weights through the dp4a
+// kernel (linear_gemv.cu), calls of up to kStreamMaxM rows through the
+// mma.sync weight-streaming kernel (linear_stream.cu), more rows run on the
+// tcgen05 kernel.  PRISM_LINEAR_PATH names a kernel instead (diagnostics;
+// every kernel gives the same bits): "tc" or "mma" for every shape,
+// "gemv" for calls of up to kGemvPathMaxM rows, "stream" for calls of up to
+// kStreamMaxM rows.
+constexpr int64_t kGemvMaxM = 2;
+constexpr int64_t kGemvPathMaxM = 8;
+constexpr int64_t kStreamMaxM = 16;
+static bool use_gemv_path(int64_t M) {
+  if (path_is("tc") || path_is("mma") || path_is("stream")) return false;
+  return M <= (path_is("gemv") ? kGemvPathMaxM : kGemvMaxM);
+}
+static bool use_stream_path(int64_t M) {
+  if (M > kStreamMaxM || path_is("tc") || path_is("mma") || use_gemv_path(M)) return false;
+  return true;
+}
 
 int linear_kernel_kind(int64_t M, int64_t N, int64_t K) {
   (void)K;
   if (M <= 0 || N <= 0) return 0;
   if (use_mma_path()) return 1;
   if (use_gemv_path(M)) return 4;
+  if (use_stream_path(M)) return 5;
   return tc_plan(M, N, K).swap ? 3 : 2;
+}
+
+// The packed 4-bit weights of W4A8 stream through the dp4a kernel for calls
+// of up to kGemvPathMaxM rows unless another kernel is forced.
+bool linear_w4_packed(int64_t M) {
+  return M <= kGemvPathMaxM && !path_is("tc") && !path_is("mma") && !path_is("stream");
 }
 
 int linear_auto_split(int64_t M, int64_t N, int64_t K) {
@@ -1131,6 +1154,7 @@ int linear_auto_split(int64_t M, int64_t N, int64_t K) {
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (use_gemv_path(M)) return 0;
+  if (use_stream_path(M)) return stream_workspace_bytes(M, N, K, split);
   if (use_mma_path() && split == 0) split = mma_auto_split(M, N, K);
   if (split == 0) return tc_balanced_bytes(M, N, K, nullptr);
   return split > 1 ? atomic_bytes(M, N) : 0;
@@ -1139,6 +1163,11 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
 size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, size_t cap) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (use_gemv_path(M)) return 0;
+  if (use_stream_path(M)) {
+    const size_t need = stream_workspace_bytes(M, N, K, split);
+    if (split == 0) return need <= cap ? need : 0;  // beyond cap: whole K per CTA
+    return need <= cap ? need : SIZE_MAX;
+  }
   if (use_mma_path() && split == 0) split = mma_auto_split(M, N, K);
   if (split == 0) {
     const size_t need = tc_balanced_bytes(M, N, K, nullptr);
@@ -1150,6 +1179,7 @@ size_t linear_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int split, s
 
 cudaError_t launch_linear(const LinearArgs& a, cudaStream_t stream) {
   if (use_gemv_path(a.M)) return launch_linear_gemv(a, stream);
+  if (use_stream_path(a.M)) return launch_linear_stream(a, stream);
   if (!use_mma_path()) return launch_linear_tc(a, stream);
   LinearArgs b = a;
   if (b.split == 0) b.split = mma_auto_split(a.M, a.N, a.K);

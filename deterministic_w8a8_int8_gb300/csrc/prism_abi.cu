@@ -117,7 +117,7 @@ static size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255);
 
 size_t prism_w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
   if (M <= 0 || N <= 0 || K <= 0 || split_k < 0 || split_k > PRISM_MAX_SPLIT_K) return 0;
-  if (prism::linear_kernel_kind(M, N, K) == 4) return 0;   // few rows: packed weights streamed directly
+  if (prism::linear_w4_packed(M)) return 0;   // few rows: packed weights streamed directly
   return align256(static_cast<size_t>(N) * static_cast<size_t>(K)) + prism::linear_workspace_bytes(M, N, K, split_k);
 }
 
@@ -144,7 +144,7 @@ int prism_w4a8_linear(const int8_t* q, int64_t ldq, const float* a_scale, const 
   if (ldw4 < K / 2) return PRISM_ERR_INVALID_ARG;
   if (ldw4 % 16 != 0 || !aligned(w4, 16)) return PRISM_ERR_ALIGNMENT;
   const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  if (prism::linear_kernel_kind(M, N, K) == 4) {
+  if (prism::linear_w4_packed(M)) {
     // few rows: the dp4a kernel streams the packed codes (the W8A8 call's
     // argument rules, with the packed row as the weight)
     if (q == nullptr || a_scale == nullptr || w_scale == nullptr || out_bf16 == nullptr) return PRISM_ERR_INVALID_ARG;

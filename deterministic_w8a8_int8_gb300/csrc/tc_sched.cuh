@@ -1,8 +1,13 @@
 // tc_sched.cuh -- the work schedule of the persistent tcgen05 contraction
 // kernels: which output tile and which range of K stages each CTA computes.
 //
-// Output tile (tx, ty) is A block tx (128 rows) by B piece ty; tile index
-// t = ty * gx + tx.  K is cut into S stages of 64 elements.
+// Output tile (tx, ty) is A block tx (128 rows) by B piece ty.  The balanced
+// schedule numbers tiles so that consecutive indices share the weight
+// operand: t = ty * gx + tx when the weights are B (tokens on the MMA rows),
+// t = tx * gy + ty when they are A (output channels on the MMA rows), so the
+// CTAs that run side by side read the same weight stages and all but the
+// first of them find those stages in L2.  K is cut into S stages of 64
+// elements.
 //   sched 0: one item per CTA: tile (blockIdx.x, blockIdx.y), K piece
 //            blockIdx.z of `split` equal pieces (explicit split-K; the
 //            pieces' int32 partial sums are added with integer atomics).
@@ -26,6 +31,8 @@ struct SchedParams {
   int sched;  // 0: one item per CTA (explicit split-K); 1: balanced
   int split;  // explicit split-K factor (sched 0)
   int gx;     // A blocks of 128 rows
+  int gy;     // B pieces
+  int a_w;    // 1: the weights are the A operand (tile index runs over B pieces fastest)
   int T;      // tiles
   int S;      // K stages of 64 elements
   int W;      // balanced: rounds of whole tiles per CTA
@@ -39,6 +46,17 @@ struct SchedParams {
 struct Item {
   int tx, ty, k0, k1, kind, tile;
 };
+
+// Tile index t of the balanced schedule -> (tx, ty).
+__device__ __forceinline__ void tile_coords(const SchedParams& p, int t, Item& it) {
+  if (p.a_w) {
+    it.tx = t / p.gy;
+    it.ty = t % p.gy;
+  } else {
+    it.tx = t % p.gx;
+    it.ty = t / p.gx;
+  }
+}
 
 // Work item n of this CTA; every role of the CTA walks the same list.
 __device__ __forceinline__ bool get_item(const SchedParams& p, int n, Item& it) {
@@ -58,8 +76,7 @@ __device__ __forceinline__ bool get_item(const SchedParams& p, int n, Item& it) 
   if (n < p.W) {
     const int t = n * G + b;
     if (t >= p.T) return false;
-    it.tx = t % p.gx;
-    it.ty = t / p.gx;
+    tile_coords(p, t, it);
     it.k0 = 0;
     it.k1 = p.S;
     it.kind = 0;
@@ -75,8 +92,7 @@ __device__ __forceinline__ bool get_item(const SchedParams& p, int n, Item& it) 
   const int ts = st * p.S;
   if (u0 >= u1 || ts >= u1) return false;
   const int t = p.W * G + st;
-  it.tx = t % p.gx;
-  it.ty = t / p.gx;
+  tile_coords(p, t, it);
   it.k0 = (u0 > ts ? u0 : ts) - ts;
   it.k1 = (u1 < ts + p.S ? u1 : ts + p.S) - ts;
   it.kind = (it.k0 == 0 && it.k1 == p.S) ? 0 : 2;

@@ -456,10 +456,13 @@ int prism_last_cuda_error(char *buf, size_t buf_bytes);
  * 0 = none (empty); 1 = warp-level mma.sync s8 kernel; 2 = tcgen05 kernel,
  * tokens on the 128-row MMA side; 3 = tcgen05 kernel, output channels on the
  * 128-row side and tokens on the N side; 4 = weight-streaming dp4a kernel
- * (calls of at most 8 token rows: decode steps, answer rows).  Kinds 2-4 are
- * the default; the environment variable PRISM_LINEAR_PATH=mma selects the
- * mma.sync kernel and PRISM_LINEAR_PATH=tc keeps few-row calls on tcgen05
- * (diagnostics; results are bit-identical on every kernel).
+ * (calls of at most 2 token rows); 5 = weight-streaming mma.sync kernel
+ * (calls of 3 to 16 token rows: decode steps, answer rows).  Kinds 2-5 are
+ * the default.  The environment variable PRISM_LINEAR_PATH overrides the
+ * choice (diagnostics; results are bit-identical on every kernel): "mma" the
+ * mma.sync s8 kernel, "tc" tcgen05 for every shape, "gemv" the dp4a kernel
+ * for calls of up to 8 rows, "stream" the mma.sync weight stream for calls of
+ * up to 16 rows.
  */
 int prism_w8a8_kernel_kind(int64_t M, int64_t N, int64_t K);
 

@@ -124,13 +124,20 @@ def test_workspace_and_dispatch_queries(L):
         assert 0 <= s <= 64   # 0: the balanced schedule of the tensor-core kernel
         if s > 0:
             assert L.prism_w8a8_workspace_bytes(M, N, K, 0) == L.prism_w8a8_workspace_bytes(M, N, K, s)
-        assert L.prism_w8a8_kernel_kind(M, N, K) in (1, 2, 3, 4)
-    # calls of at most 8 token rows stream the weights (kind 4), need no workspace
-    for M in (1, 3, 8):
+        assert L.prism_w8a8_kernel_kind(M, N, K) in (1, 2, 3, 4, 5)
+    # calls of at most 2 token rows stream the weights through dp4a (kind 4),
+    # with no workspace
+    for M in (1, 2):
         assert L.prism_w8a8_kernel_kind(M, 5120, 17408) == 4
         assert L.prism_w8a8_workspace_bytes(M, 5120, 17408, 0) == 0
         assert L.prism_w8a8_workspace_bytes(M, 5120, 17408, 16) == 0
-    assert L.prism_w8a8_kernel_kind(9, 5120, 17408) in (2, 3)
+    # 3 to 16 rows: the mma.sync weight stream (kind 5), whole K per CTA on
+    # a wide weight; more rows: tcgen05
+    for M in (3, 8, 9, 16):
+        assert L.prism_w8a8_kernel_kind(M, 5120, 17408) == 5
+        assert L.prism_w8a8_workspace_bytes(M, 5120, 17408, 0) == 0
+    assert L.prism_w8a8_workspace_bytes(16, 5120, 17408, 4) == ((16 * 5120 * 4 + 255) & ~255) + 1280
+    assert L.prism_w8a8_kernel_kind(17, 5120, 17408) in (2, 3)
     # the balanced schedule keeps partial tiles only when it shares tiles
     assert L.prism_w8a8_workspace_bytes(37, 384, 256, 0) == 0
     assert L.prism_w8a8_workspace_bytes(304, 15360, 5120, 0) > 0
@@ -142,12 +149,23 @@ def _cdiv(x, y):
 
 
 def _balanced_workspace_bytes(M, N, K):
-    """The tensor-core kernel's automatic schedule restated: orientation and
+    """The automatic schedule restated: calls of 3 to 16 rows on the
+    weight-streaming kernel (whole K per 16-channel CTA, unless the weight has
+    too few tiles to fill the SMs: then [M, N] int32 partial sums and one
+    counter per tile); more rows on the tensor-core kernel: orientation and
     token-piece width, 64- or 128-K stages, W rounds of whole tiles on the
     152 SMs and R tiles whose K stages are shared (shares of at least one
     1024-K chunk), then the bytes of R arrival counters and R int32 tiles."""
-    if M <= 8:                                  # the dp4a weight stream
+    if M <= 2:                                  # the dp4a weight stream
         return 0
+    if M <= 16:                                 # the mma.sync weight stream
+        tiles = _cdiv(N, 16)
+        if 2 * tiles >= 2 * 152:                 # the tiles fill the SMs twice: whole K per CTA
+            return 0
+        pieces = min(_cdiv(2 * 152, tiles), max(1, _cdiv(K, 128) // 64))
+        if pieces <= 1:
+            return 0
+        return ((M * N * 4 + 255) & ~255) + ((tiles * 4 + 255) & ~255)
     if M < 512:                                 # tokens on the MMA's N side
         bpiece = _cdiv(_cdiv(M, _cdiv(M, 256)), 32) * 32
         T = _cdiv(N, 128) * _cdiv(M, bpiece)

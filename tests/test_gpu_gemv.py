@@ -1,6 +1,7 @@
-"""The weight-streaming dp4a kernel that runs W8A8 linear calls of at most 8
-token rows (decode steps, answer rows of a restricted last layer): bit for
-bit against the oracle and against the tcgen05 and mma.sync kernels
+"""The weight-streaming dp4a kernel that runs W8A8 linear calls of at most 2
+token rows by default and of up to 8 under PRISM_LINEAR_PATH=gemv (decode
+steps, answer rows of a restricted last layer): bit for bit against the
+oracle and against the tcgen05 and mma.sync kernels
 (StartLux-Prism, "Bitwise consistency is not lossless quantization": exact
 int32 accumulation, fixed epilogue -- so every kernel gives the same bits).
 
@@ -35,7 +36,7 @@ def _problem(M, N, K, seed, residual=True):
 
 def _with_path(path, fn):
     old = os.environ.get("PRISM_LINEAR_PATH")
-    if path in ("mma", "tc"):
+    if path in ("mma", "tc", "gemv", "stream"):
         os.environ["PRISM_LINEAR_PATH"] = path
     else:
         os.environ.pop("PRISM_LINEAR_PATH", None)
@@ -50,7 +51,8 @@ def _with_path(path, fn):
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])
 @pytest.mark.parametrize("N,K", [(1027, 5120), (6, 16), (130, 528), (64, 17408)])
-def test_gemv_matches_oracle(cuda_device, M, N, K):
+def test_gemv_matches_oracle(cuda_device, monkeypatch, M, N, K):
+    monkeypatch.setenv("PRISM_LINEAR_PATH", "gemv")   # the library's own choice is dp4a up to 2 rows
     x, w, ws, r = _problem(M, N, K, 100 * M + N)
     q, a = prism.prism_quant_act(dev_bf16(x))
     assert prism.prism_w8a8_kernel_kind(M, N, K) == 4
@@ -75,7 +77,8 @@ def test_three_kernels_agree_on_few_rows(cuda_device, M, N, K):
     assert torch.equal(outs["gemv"].view(torch.int16), outs["mma"].view(torch.int16))
 
 
-def test_gemv_strided_and_in_place(cuda_device):
+def test_gemv_strided_and_in_place(cuda_device, monkeypatch):
+    monkeypatch.setenv("PRISM_LINEAR_PATH", "gemv")
     M, N, K = 5, 300, 1040
     x, w, ws, r = _problem(M, N, K, 9)
     q0, a = prism.prism_quant_act(dev_bf16(x))
@@ -91,7 +94,8 @@ def test_gemv_strided_and_in_place(cuda_device):
     assert np.array_equal(host_bits(O), out_o)
 
 
-def test_gemv_int32_extremes_at_max_k(cuda_device):
+def test_gemv_int32_extremes_at_max_k(cuda_device, monkeypatch):
+    monkeypatch.setenv("PRISM_LINEAR_PATH", "gemv")
     M, N, K = 2, 8, 133136
     q = torch.full((M, K), 127, dtype=torch.int8, device="cuda")
     q[1] = -127

@@ -200,7 +200,7 @@ def test_full_size_every_tile(cuda_device, name):
 def _with_path(path, fn):
     import os
     old = os.environ.get("PRISM_LINEAR_PATH")
-    if path in ("mma", "tc"):
+    if path in ("mma", "tc", "gemv", "stream"):
         os.environ["PRISM_LINEAR_PATH"] = path
     else:                      # the library's own choice
         os.environ.pop("PRISM_LINEAR_PATH", None)

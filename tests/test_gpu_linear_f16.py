@@ -97,7 +97,12 @@ def test_codes_to_f16_every_byte(cuda_device):
                                    (130, 257, 528), (255, 136, 1040), (600, 520, 2064), (1000, 300, 1024),
                                    (513, 272, 1088)])
 @pytest.mark.parametrize("residual", [True, False])
-def test_ragged_shapes(cuda_device, M, N, K, residual):
+@pytest.mark.parametrize("orient", ["auto", "rows", "cols"])
+def test_ragged_shapes(cuda_device, monkeypatch, M, N, K, residual, orient):
+    """Both MMA orientations on every shape (PRISM_F16_ORIENT: tokens on the
+    128 MMA rows, or on the N side in pieces), and the library's choice."""
+    if orient != "auto":
+        monkeypatch.setenv("PRISM_F16_ORIENT", orient)
     xb, w, w_scale, rb = problem(M, N, K, M * 131 + N * 7 + K, residual)
     qo, ao = oracle.quant_act(xb, None)
     outo, acco = oracle.w8a8_linear(qo, ao, w, w_scale, rb)

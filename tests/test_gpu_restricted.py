@@ -41,7 +41,7 @@ def _inputs(M_x, K, N, seed):
 
 def _with_path(path, fn):
     old = os.environ.get("PRISM_LINEAR_PATH")
-    if path in ("mma", "tc"):
+    if path in ("mma", "tc", "gemv", "stream"):
         os.environ["PRISM_LINEAR_PATH"] = path
     else:                      # the library's own choice
         os.environ.pop("PRISM_LINEAR_PATH", None)
@@ -83,8 +83,11 @@ def test_quant_rows_match_oracle(cuda_device, M_x, K, n):
     (600, 1024, 640, 300, 0, "tc"),       # enough rows for the token-side orientation
     (304, 2048, 1536, 3, 4, "tc"),        # explicit split-K
     (300, 1024, 640, 40, 0, "mma"),       # the mma.sync kernel
-    (304, 5120, 5120, 3, 0, "gemv"),      # the library's choice for 3 rows: the dp4a weight stream
+    (304, 5120, 5120, 3, 0, "auto"),      # the library's choice for 3 rows: the mma.sync weight stream
+    (304, 5120, 5120, 3, 0, "gemv"),      # the dp4a weight stream
     (2048, 17408, 5120, 8, 0, "gemv"),
+    (2048, 17408, 5120, 8, 0, "stream"),
+    (2048, 5120, 5120, 2, 0, "auto"),     # the library's choice for 2 rows: the dp4a weight stream
 ])
 def test_restricted_layer_matches_oracle_and_full_rows(cuda_device, M_x, K, N, n, split, path):
     rng, x, inv_s, w, ws, res = _inputs(M_x, K, N, 3 * M_x + N)

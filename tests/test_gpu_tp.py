@@ -39,7 +39,7 @@ def _inputs(M, K, N, seed):
 
 def _with_path(path, fn):
     old = os.environ.get("PRISM_LINEAR_PATH")
-    if path in ("mma", "tc"):
+    if path in ("mma", "tc", "gemv", "stream"):
         os.environ["PRISM_LINEAR_PATH"] = path
     else:
         os.environ.pop("PRISM_LINEAR_PATH", None)
@@ -57,7 +57,8 @@ def _with_path(path, fn):
     (600, 2048, 1536, [0, 512, 2048], 0, "auto"),     # tokens on the 128-row side, uneven shards
     (304, 2048, 1536, [0, 1024, 2048], 4, "auto"),    # explicit split-K
     (1, 17408, 5120, [0, 4352, 8704, 13056, 17408], 0, "auto"),   # a decode row over four ranks: dp4a kernel
-    (8, 5120, 640, [0, 2048, 5120], 0, "auto"),
+    (8, 5120, 640, [0, 2048, 5120], 0, "auto"),      # mma.sync weight stream, accumulator-only mode
+    (8, 5120, 640, [0, 2048, 5120], 0, "gemv"),      # the dp4a kernel's accumulator-only mode
     (40, 5120, 1536, [0, 2048, 5120], 0, "auto"),     # tcgen05 accumulator-only mode on 128-K stages
     (8, 2048, 640, [0, 1024, 2048], 3, "tc"),         # the same, explicit split-K
     (300, 1024, 640, [0, 512, 1024], 0, "mma"),

@@ -34,7 +34,7 @@ def _problem(M, N, K, seed):
 
 def _with_path(path, fn):
     old = os.environ.get("PRISM_LINEAR_PATH")
-    if path in ("mma", "tc"):
+    if path in ("mma", "tc", "gemv", "stream"):
         os.environ["PRISM_LINEAR_PATH"] = path
     else:
         os.environ.pop("PRISM_LINEAR_PATH", None)
@@ -73,6 +73,7 @@ def test_w4a8_few_rows_match_oracle(cuda_device, M, N, K):
     (37, 384, 256, 0, "auto"),
     (600, 1024, 2048, 4, "auto"),       # explicit split-K
     (8, 1536, 5120, 0, "tc"),           # few rows forced onto unpack + tcgen05
+    (5, 1536, 5120, 0, "stream"),       # few rows forced onto unpack + the mma.sync weight stream
     (300, 640, 1024, 0, "mma"),
 ])
 def test_w4a8_more_rows_match_w8a8_and_oracle(cuda_device, M, N, K, split, path):
