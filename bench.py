@@ -1178,6 +1178,83 @@ def run_kernel_int8_peak(args):
     return 0
 
 
+_MMA_RATE_SRC = r"""
+#include <torch/extension.h>
+#include <cstdint>
+// Register-resident loops of the warp-level MMAs (independent accumulators):
+// the issue rate of mma.sync m16n8k16 f16 -> f32 and m16n8k32 s8 -> s32.
+template <int kAcc>
+__global__ void f16_loop(float* out, int iters) {
+  uint32_t a0 = threadIdx.x, a1 = a0 * 3, a2 = a0 * 5, a3 = a0 * 7, b0 = a0 + 1, b1 = a0 + 2;
+  float c[kAcc][4] = {};
+  for (int i = 0; i < iters; ++i)
+#pragma unroll
+    for (int j = 0; j < kAcc; ++j)
+      asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                   : "+f"(c[j][0]), "+f"(c[j][1]), "+f"(c[j][2]), "+f"(c[j][3])
+                   : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  float s = 0.f;
+  for (int j = 0; j < kAcc; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+template <int kAcc>
+__global__ void s8_loop(float* out, int iters) {
+  uint32_t a0 = threadIdx.x, a1 = a0 * 3, a2 = a0 * 5, a3 = a0 * 7, b0 = a0 + 1, b1 = a0 + 2;
+  int c[kAcc][4] = {};
+  for (int i = 0; i < iters; ++i)
+#pragma unroll
+    for (int j = 0; j < kAcc; ++j)
+      asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                   : "+r"(c[j][0]), "+r"(c[j][1]), "+r"(c[j][2]), "+r"(c[j][3])
+                   : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  int s = 0;
+  for (int j = 0; j < kAcc; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = static_cast<float>(s);
+}
+void launch(torch::Tensor out, int64_t which, int64_t blocks, int64_t threads, int64_t iters) {
+  auto st = at::cuda::getCurrentCUDAStream();
+  if (which == 0) f16_loop<8><<<blocks, threads, 0, st>>>(out.data_ptr<float>(), static_cast<int>(iters));
+  else s8_loop<8><<<blocks, threads, 0, st>>>(out.data_ptr<float>(), static_cast<int>(iters));
+}
+"""
+
+
+def run_kernel_mma_rate(args):
+    """Issue rate of the warp-level tensor-core MMAs that the weight-streaming
+    kernel uses (mma.sync m16n8k16 f16 -> f32 and m16n8k32 s8 -> s32): each
+    warp loops over 8 independent accumulators in registers, 4 to 16 warps per
+    CTA, one or two CTAs per SM, timed with CUDA events (a probe compiled at
+    run time for sm_103a)."""
+    import torch
+    from torch.utils.cpp_extension import load_inline
+
+    ext = load_inline("prism_mma_rate_probe", cpp_sources="void launch(torch::Tensor, int64_t, int64_t, int64_t, int64_t);",
+                      cuda_sources="#include <ATen/cuda/CUDAContext.h>\n" + _MMA_RATE_SRC, functions=["launch"],
+                      extra_cuda_cflags=["-gencode", "arch=compute_103a,code=sm_103a", "-O3"], verbose=False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = torch.empty(sms * 2 * 512, dtype=torch.float32, device="cuda")
+    iters = 20000
+    res = {}
+    for which, name, ops_per in ((0, "f16_m16n8k16_tflops", 2 * 16 * 8 * 16), (1, "s8_m16n8k32_tops", 2 * 16 * 8 * 32)):
+        best = 0.0
+        for warps in (4, 8, 16):
+            for per_sm in (1, 2):
+                blocks, threads = sms * per_sm, warps * 32
+                ext.launch(out, which, blocks, threads, 100)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                ext.launch(out, which, blocks, threads, iters)
+                e1.record()
+                torch.cuda.synchronize()
+                rate = ops_per * 8.0 * iters * blocks * warps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+                res[f"{name}_w{warps}_b{per_sm}"] = rate
+                best = max(best, rate)
+        res[name] = best
+    print(json.dumps({"kernel": "warp-level mma.sync issue rate", **res,
+                      "gpu": torch.cuda.get_device_name(0)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1187,7 +1264,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-subrecords", action="store_true", help="headline line only (no per-config sub-records)")
     ap.add_argument("--kernel", choices=["linear", "linear_f16", "quant", "readout", "requant", "restricted", "tp",
-                                         "w4a8", "int8_peak"],
+                                         "w4a8", "int8_peak", "mma_rate"],
                     help="time one call type alone")
     ap.add_argument("--case", default=None, choices=sorted(wl.LINEAR_CONFIGS) + sorted(wl.REQUANT_CONFIGS),
                     help="workload of --kernel (a linear case; for requant a weight as loaded)")
@@ -1220,6 +1297,8 @@ def main():
         return run_kernel_w4a8(args)
     if args.kernel == "readout":
         return run_kernel_readout(args)
+    if args.kernel == "mma_rate":
+        return run_kernel_mma_rate(args)
     if args.kernel:
         return run_kernel(args)
     return run_gpu(args)

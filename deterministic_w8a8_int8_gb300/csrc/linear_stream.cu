@@ -24,12 +24,12 @@
 // and 2j + 1 of each as the fragment's K groups 4t .. 4t + 3 and
 // 16 + 4t .. 16 + 4t + 3, in both operands alike.
 //
-// CTA (256 threads, eight warps): 16 output channels against all token rows
-// (NT tiles of 8); the warps take the CTA's 128-K steps in turn, each
-// copying its next steps into its own two-step cp.async ring in shared memory
-// (48 or 64 KB per CTA, so that every CTA of a 5120-channel weight is
-// resident at once), and add their int32 sums through shared memory at the
-// end.  The grid is one CTA per 16 channels (and per K piece when split).  A
+// CTA: 16 output channels against all token rows (NT tiles of 8); its warps
+// take the CTA's 128-K steps in turn, each copying its next steps into its
+// own cp.async ring in shared memory -- eight warps with two-step rings for
+// one token tile, four warps with four-step rings for two (48 or 64 KB per
+// CTA, so that every CTA of a 5120-channel weight is resident at once) --
+// and add their int32 sums through shared memory at the end.  The grid is one CTA per 16 channels (and per K piece when split).  A
 // split K range has each piece add its int32 partial sums into the workspace
 // accumulator with integer reductions; the last piece to arrive (an integer
 // counter per channel tile) reads the sums back, zeroes them and applies the
@@ -363,11 +363,11 @@ cudaError_t launch_nt(const LinearArgs& a, cudaStream_t stream) {
   return launch_kernel(kernel, grid, dim3(kWarps * 32), static_cast<size_t>(smem), stream, a.no_pdl == 0, p);
 }
 
-template <int NT>
+template <int NT, int U, int W>
 cudaError_t launch_modes(const LinearArgs& a, cudaStream_t stream) {
-  if (a.acc_only) return launch_nt<NT, 2, kRing, kWarps>(a, stream);
-  if (a.res_rows != nullptr) return launch_nt<NT, 1, kRing, kWarps>(a, stream);
-  return launch_nt<NT, 0, kRing, kWarps>(a, stream);
+  if (a.acc_only) return launch_nt<NT, 2, U, W>(a, stream);
+  if (a.res_rows != nullptr) return launch_nt<NT, 1, U, W>(a, stream);
+  return launch_nt<NT, 0, U, W>(a, stream);
 }
 
 }  // namespace
@@ -383,7 +383,9 @@ size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int split) {
 }
 
 cudaError_t launch_linear_stream(const LinearArgs& a, cudaStream_t stream) {
-  return a.M <= 8 ? launch_modes<1>(a, stream) : launch_modes<2>(a, stream);
+  // up to 8 rows: eight warps with two-step rings; 9-16 rows (the f16 MMA,
+  // more registers per step): four warps with four-step rings
+  return a.M <= 8 ? launch_modes<1, kRing, kWarps>(a, stream) : launch_modes<2, 4, 4>(a, stream);
 }
 
 }  // namespace prism
