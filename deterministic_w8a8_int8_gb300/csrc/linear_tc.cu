@@ -446,7 +446,14 @@ __device__ __forceinline__ float item_scale(const TcParams& p, const Item& itm, 
 // kSub: f16 operand slots (64 K each) per stage.  Stages of 128 K (kSub = 2,
 // narrow tiles) halve the barrier round trips, MMA-issue loop turns and TMA
 // boxes per K (the boxes then carry 128-byte rows).
-template <int kMode, int kSub>
+// kTA (swapped orientation, 128-K stages, narrow token tiles): the widened
+// weight rows go to tensor memory instead of shared memory and the MMA reads
+// its A operand from there.  Each worker thread then widens its own TMEM
+// lane's row (the int8 A box arrives 128-byte swizzled, so a warp's 32 rows
+// are read without bank conflicts) and only the token rows take the
+// shared-memory round trip; per 128-K stage that removes 64 of the ~144 KB
+// of shared-memory traffic of a 64-token tile.
+template <int kMode, int kSub, bool kTA>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB) {
@@ -459,7 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
   const int nst = p.nst, nst8 = p.nst8;
-  const uint32_t kStageBytes = static_cast<uint32_t>((kBM + p.bpiece) * 128);
+  // f16 operand slot: A tile then B tile (kTA: the B tile alone)
+  constexpr uint32_t kSlotB = kTA ? 0u : static_cast<uint32_t>(kStageA);
+  const uint32_t kStageBytes = static_cast<uint32_t>(((kTA ? 0 : kBM) + p.bpiece) * 128);
   const uint32_t kS8Bytes = static_cast<uint32_t>((kBM + p.bpiece) * kBK8);
   const uint32_t sStage = base;                               // nst x kSub x (A tile | B tile), f16
   const uint32_t sS8 = sStage + nst * kSub * kStageBytes;     // nst8 x (A box | B box), int8
@@ -484,6 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM layout: double-buffered D[0] | D[1] | I when three widths fit, else D | I
   const bool dbuf = 3 * p.bpiece <= static_cast<int>(kTmemCols);
   const uint32_t col_i = dbuf ? 2u * static_cast<uint32_t>(p.bpiece) : kColI;
+  // kTA: the widened A slots, 32 columns (64 f16 of K) per 64-K slot, after I
+  const uint32_t col_a = col_i + static_cast<uint32_t>(p.bpiece);
   // B rows of piece ty that exist, rounded up to 32 (the MMA's N)
   auto tile_width = [&](int ty) -> int {
     const int64_t left = (p.swap ? a.M : a.N) - static_cast<int64_t>(ty) * p.bpiece;
@@ -560,11 +571,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int h = 0; h < kSub; ++h) {
-            const uint64_t ad = smem_desc_sw128(sStage + (s * kSub + h) * kStageBytes);
-            const uint64_t bd = smem_desc_sw128(sStage + (s * kSub + h) * kStageBytes + kStageA);
+            const uint64_t bd = smem_desc_sw128(sStage + (s * kSub + h) * kStageBytes + kSlotB);
+            if constexpr (kTA) {
+              // K = 16 is 8 columns of the slot's A rows in TMEM
+              const uint32_t at = tmem + col_a + static_cast<uint32_t>(s * kSub + h) * 32u;
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              tc_mma(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc, (cpos | h | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < kBK / 16; ++k)
+                tc::tc_mma_ta(tmem + dcol, at + 8u * k, bd + 2 * k, idesc, (cpos | h | k) != 0 ? 1u : 0u);
+            } else {
+              const uint64_t ad = smem_desc_sw128(sStage + (s * kSub + h) * kStageBytes);
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                tc_mma(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc, (cpos | h | k) != 0 ? 1u : 0u);
+            }
           }
           issued = true;
           tc_commit(bar_empty + 8 * s);
@@ -669,6 +688,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_shared_v4_if(addr ^ 16u, w[4], w[5], w[6], w[7], valid);
       }
     };
+    // kTA widening of the stage in staging slot j8 into operand slot s8op:
+    // the group's two warps of a TMEM lane quadrant take the two 64-K halves
+    // of their 32 weight rows (a thread its own lane's row: 64 bytes read
+    // from the swizzled box, 32 columns stored); the group's 256 threads
+    // share the token rows' 16-byte pieces (chunk u = row u / 8, K bytes
+    // 16 (u % 8) ..), which go to the swizzled f16 B slot as before.
+    auto widen_ta = [&](int j8, int s8op, uint32_t phase8, uint32_t phase, int bn) -> bool {
+      constexpr int kTaB = 3;   // B pieces a thread: 96 rows x 8 pieces / 256 threads
+      if (!mbar_wait_warp(bar_s8_full + 8 * j8, phase8, s_abort)) return false;
+      const uint32_t s8 = sS8 + j8 * kS8Bytes;
+      const int half = slice >> 1;
+      uint4 av[4], bv[kTaB];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c = static_cast<uint32_t>(4 * half + i);
+        av[i] = ld_shared_v4_if(s8 + trow * 128u + ((c ^ static_cast<uint32_t>(trow & 7)) << 4), true);
+      }
+#pragma unroll
+      for (int i = 0; i < kTaB; ++i) {
+        const int u = gt + 256 * i;
+        bv[i] = ld_shared_v4_if(s8 + kS8A + static_cast<uint32_t>(u) * 16u, (u >> 3) < bn);
+      }
+      // the operand slot's previous MMAs have completed
+      if (!mbar_wait_warp(bar_empty + 8 * s8op, phase ^ 1u, s_abort)) return false;
+      {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          widen4(av[i].x, w[8 * i], w[8 * i + 1]);
+          widen4(av[i].y, w[8 * i + 2], w[8 * i + 3]);
+          widen4(av[i].z, w[8 * i + 4], w[8 * i + 5]);
+          widen4(av[i].w, w[8 * i + 6], w[8 * i + 7]);
+        }
+        tc::tmem_st32(tmem + lane_base + col_a + static_cast<uint32_t>(s8op * kSub + half) * 32u, w);
+      }
+#pragma unroll
+      for (int i = 0; i < kTaB; ++i) {
+        const int u = gt + 256 * i;
+        const int row = u >> 3, c = u & 7;
+        uint32_t w[8];
+        widen4(bv[i].x, w[0], w[1]);
+        widen4(bv[i].y, w[2], w[3]);
+        widen4(bv[i].z, w[4], w[5]);
+        widen4(bv[i].w, w[6], w[7]);
+        // 16 int8 K values of 64-K slot c / 4 become its f16 chunks 2 (c % 4)
+        // and 2 (c % 4) + 1 of the row, 128-byte swizzled
+        const uint32_t rb = sStage + static_cast<uint32_t>(s8op * kSub + (c >> 2)) * kStageBytes +
+                            static_cast<uint32_t>(row) * 128u;
+        const uint32_t f = static_cast<uint32_t>(2 * (c & 3)), sw = static_cast<uint32_t>(row & 7);
+        st_shared_v4_if(rb + ((f ^ sw) << 4), w[0], w[1], w[2], w[3], row < bn);
+        st_shared_v4_if(rb + (((f + 1u) ^ sw) << 4), w[4], w[5], w[6], w[7], row < bn);
+      }
+      tc::tmem_wait_st();
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_full + 8 * s8op);
+      if (lane == 0) mbar_arrive(bar_s8_empty + 8 * j8);
+      return true;
+    };
     // Drain this warp's share of chunk gc (chunk lc of its item): I += int(D),
     // or, for the item's last chunk (out != nullptr), hand each round of final
     // int32 sums to out(cb, v).  Either way the D buffer is then handed back.
@@ -770,7 +849,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           next_trigger += kChunkL;
           if (!ok) break;
         }
-        if (((gst + it) & 1) == grp) {
+        if constexpr (kTA) {
+          if (((gst + it) & 1) == grp) {
+            ok = widen_ta(j, s, ph8, ph, bn);
+            if (!ok) break;
+          }
+        } else if (((gst + it) & 1) == grp) {
           // this group's stage: widen it while the other group waits for
           // the next one
           ok = mbar_wait_warp(bar_s8_full + 8 * j, ph8, s_abort);
@@ -1021,9 +1105,10 @@ static EncodeTiledFn encode_fn() {
 }
 
 // Row-major int8 [rows, K] matrix with row stride ld bytes, read in boxes of
-// box_k K-bytes x box_rows rows; out-of-range rows and K read as zero.
+// box_k K-bytes x box_rows rows (128-byte swizzled when swz, which needs
+// box_k = 128); out-of-range rows and K read as zero.
 static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int64_t K, int64_t ld, int box_rows,
-                            int box_k) {
+                            int box_k, bool swz = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
@@ -1031,19 +1116,36 @@ static cudaError_t make_map(CUtensorMap* m, const int8_t* ptr, int64_t rows, int
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Operand stages of the tensor-memory A variant: as many as the TMEM columns
+// beside D[0] | D[1] | I hold (32 a 64-K slot), at most 4; 0 where the
+// variant does not apply (the normal orientation, 64-K stages, tiles too
+// wide for a double-buffered D).  PRISM_TC_A=smem keeps every call on the
+// shared-memory A operand (a diagnostic: both give the same bits).
+static int ta_stages(const TcPlan& pl) {
+  if (!pl.swap || pl.sub != 2 || 3 * pl.bpiece > static_cast<int>(kTmemCols)) return 0;
+  const char* e = std::getenv("PRISM_TC_A");
+  if (e != nullptr && std::strcmp(e, "smem") == 0) return 0;
+  const int cols = (static_cast<int>(kTmemCols) - 3 * pl.bpiece) / (32 * pl.sub);
+  return cols >= 2 ? std::min(cols, 4) : 0;
+}
+
 static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const TcPlan pl = tc_plan(a.M, a.N, a.K);
-  auto kernel = pl.sub == 2 ? (a.acc_only                ? linear_tc_kernel<kTcAccOnly, 2>
-                               : a.res_rows != nullptr ? linear_tc_kernel<kTcRows, 2>
-                                                       : linear_tc_kernel<kTcPlain, 2>)
-                            : (a.acc_only                ? linear_tc_kernel<kTcAccOnly, 1>
-                               : a.res_rows != nullptr ? linear_tc_kernel<kTcRows, 1>
-                                                       : linear_tc_kernel<kTcPlain, 1>);
+  const int ta = ta_stages(pl);
+  auto kernel = ta > 0 ? (a.acc_only                ? linear_tc_kernel<kTcAccOnly, 2, true>
+                          : a.res_rows != nullptr ? linear_tc_kernel<kTcRows, 2, true>
+                                                  : linear_tc_kernel<kTcPlain, 2, true>)
+                : pl.sub == 2 ? (a.acc_only                ? linear_tc_kernel<kTcAccOnly, 2, false>
+                                 : a.res_rows != nullptr ? linear_tc_kernel<kTcRows, 2, false>
+                                                         : linear_tc_kernel<kTcPlain, 2, false>)
+                              : (a.acc_only                ? linear_tc_kernel<kTcAccOnly, 1, false>
+                                 : a.res_rows != nullptr ? linear_tc_kernel<kTcRows, 1, false>
+                                                         : linear_tc_kernel<kTcPlain, 1, false>);
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel), kSmemBytes);
   if (e != cudaSuccess) return e;
   TcParams p{};
@@ -1054,9 +1156,15 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const uintptr_t wb = reinterpret_cast<uintptr_t>(a.w_scale);
   p.vec_io = (ob % 16 == 0) && (a.ldo % 8 == 0) && (wb % 16 == 0) &&
              (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
-  p.nst = pl.sub == 2 ? 2 : 3;
-  p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * pl.sub * (kBM + pl.bpiece) * 128) /
-                                    ((kBM + pl.bpiece) * kBK * pl.sub));
+  // f16 operand stages: 3 at 64 K; at 128 K a third one where three int8
+  // stages still fit beside it (tiles of 32 and 64 tokens: 2-4 % faster than
+  // two; sweeping 64-K stages with 3-6 operand stages was 12-20 % slower)
+  const int f16_stage = pl.sub * ((ta > 0 ? 0 : kBM) + pl.bpiece) * 128, s8_stage = (kBM + pl.bpiece) * kBK * pl.sub;
+  if (ta > 0)
+    p.nst = ta;
+  else
+    p.nst = pl.sub == 2 ? ((kRingRegion - 3 * f16_stage) / s8_stage >= 3 ? 3 : 2) : 3;
+  p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * f16_stage) / s8_stage);
   p.sp.split = a.split;
   p.sp.gx = static_cast<int>(pl.grid_x);
   p.sp.gy = static_cast<int>(pl.grid_y);
@@ -1098,7 +1206,7 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   CUtensorMap tmA, tmB;
   const int8_t* Am = pl.swap ? a.w : a.q;
   const int8_t* Bm = pl.swap ? a.q : a.w;
-  e = make_map(&tmA, Am, pl.swap ? a.N : a.M, a.K, pl.swap ? a.ldw : a.ldq, kBM, kBK * pl.sub);
+  e = make_map(&tmA, Am, pl.swap ? a.N : a.M, a.K, pl.swap ? a.ldw : a.ldq, kBM, kBK * pl.sub, ta > 0);
   if (e != cudaSuccess) return e;
   e = make_map(&tmB, Bm, pl.swap ? a.M : a.N, a.K, pl.swap ? a.ldq : a.ldw, pl.bpiece, kBK * pl.sub);
   if (e != cudaSuccess) return e;
