@@ -29,12 +29,17 @@ def f16_plan(M, N):
     return 256, cdiv(M, 128) * cdiv(N, 256)
 
 
-def f16_workspace(M, N, K):
-    """(counter bytes, total bytes) of the binary16-code kernel's balanced
-    schedule: arrival counters of the R shared tiles, then one piece slot per
-    (shared tile, CTA) pair, R + G - 1 slots of 128 x bpiece int32."""
+def f16_workspace(M, N, K, sms=152):
+    """(counter bytes, total bytes) of the binary16-code kernel's automatic
+    schedule: none when it runs whole tiles in rounds (at least half the SMs'
+    worth of tiles and a last round of at least a fifth of them), else the
+    balanced schedule's arrival counters of the R shared tiles, then one
+    piece slot per (shared tile, CTA) pair, R + G - 1 slots of 128 x bpiece
+    int32."""
     bpiece, T = f16_plan(M, N)
-    G, W, R = balanced(T, cdiv(K, 64), 16)
+    if T >= sms // 2 and T % sms >= sms // 5:
+        return 0, 0
+    G, W, R = balanced(T, cdiv(K, 64), 16, sms)
     if R == 0 or G == R:
         return 0, 0
     cb = (R * 4 + 255) & ~255

@@ -148,9 +148,10 @@ def test_split_k_bit_identical(cuda_device, M):
     (1024, 4864, 512),    # 152 tiles: whole tiles only, one round
     (304, 1536, 5120),    # few tiles, K ranges shared out
     (600, 2560, 2048),    # K units shared over all CTAs
-    (304, 15360, 1024),   # one round of whole tiles, the rest shared
+    (304, 15360, 1024),   # whole tiles in two rounds (the last 88 of 152)
+    (1024, 5120, 1024),   # 160 tiles (a round would leave 8): every tile shared
     (37, 384, 256),       # one CTA per tile
-    (640, 25600, 256),    # whole tiles in rounds (little K)
+    (640, 25600, 256),    # whole tiles in four rounds
     (96, 640, 17408),     # few tiles of many K stages
     (2048, 5120, 5120),   # one round of whole tiles, then shared tiles
 ])
@@ -293,7 +294,7 @@ def test_argument_checks(cuda_device):
     assert call(split=65) == prism.PRISM_ERR_UNSUPPORTED
     assert call(K=133152, ldq=133152, ldw=133152) == prism.PRISM_ERR_UNSUPPORTED
     assert call(M=0) == prism.PRISM_OK
-    M, N, K = 304, 15360, 1024
+    M, N, K = 304, 1536, 5120
     assert prism.prism_w8a8_f16_workspace_bytes(M, N, K, 0) > 0
     assert L.prism_w8a8_linear_f16(P(z.data_ptr()), K, P(s.data_ptr()), P(z.data_ptr()), K, P(s.data_ptr()), None, 0,
                                    P(o.data_ptr()), N, None, M, N, K, 0, None, 0, st) == prism.PRISM_ERR_WORKSPACE

@@ -8,7 +8,7 @@ hang, no fault, the context usable -- with PRISM_DEVSTATUS_WAIT_TIMEOUT
 raised for the host; and after the mode is disarmed and the workspace zeroed
 again, the next call must give the oracle's bits.  Both contraction kernels
 (int8 operands; binary16 codes), each with shared tiles in both MMA
-orientations and with whole tiles only."""
+orientations, with one CTA per tile, and with whole tiles in rounds."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +25,7 @@ LIMIT_NS = 20_000_000   # 20 ms
 
 
 @pytest.mark.parametrize("kernel", ["int8", "f16"])
-@pytest.mark.parametrize("M,N,K", [(600, 2560, 2048), (304, 5120, 5120), (37, 384, 256)])
+@pytest.mark.parametrize("M,N,K", [(600, 2560, 2048), (304, 1536, 5120), (37, 384, 256), (304, 15360, 1024)])
 def test_expired_wait_returns_reports_and_recovers(cuda_device, monkeypatch, kernel, M, N, K):
     monkeypatch.delenv("PRISM_LINEAR_PATH", raising=False)
     rng = np.random.default_rng(M + N + K)
