@@ -21,14 +21,15 @@
 //
 // CTA roles (576 threads = 18 warps, one CTA per SM):
 //   warp 17       lane 0 streams the raw int8 A and B tiles into a
-//                 shared-memory staging ring (3 stages at width 256, up to 8
+//                 shared-memory staging ring (5 stages at width 256, up to 8
 //                 for narrow tiles) with 2-D TMA loads;
 //   warp 4        TMEM allocator; lane 0 issues every tcgen05.mma;
 //   16 workers    (the other warps, four per TMEM lane quadrant) do all the
 //                 rest: exact int8->f16 widening from the staging ring into
-//                 128-byte-swizzled K-major f16 tiles (3 stages), in two
-//                 groups of 8 warps that take alternate stages, so that one
-//                 group's widening overlaps the other's wait for its data;
+//                 128-byte-swizzled K-major f16 tiles (2 stages: one per
+//                 group), in two groups of 8 warps that take alternate
+//                 stages, so that one group's widening overlaps the other's
+//                 wait for its data;
 //                 at each 1024-K chunk boundary each warp drains its quarter
 //                 of its quadrant's accumulator columns; at the end all 512
 //                 threads write the tile out.
@@ -1131,7 +1132,7 @@ static int ta_stages(const TcPlan& pl) {
   const char* e = std::getenv("PRISM_TC_A");
   if (e != nullptr && std::strcmp(e, "smem") == 0) return 0;
   const int cols = (static_cast<int>(kTmemCols) - 3 * pl.bpiece) / (32 * pl.sub);
-  return cols >= 2 ? std::min(cols, 4) : 0;
+  return cols >= 2 ? std::min(cols, 4) & ~1 : 0;   // an even number of slots (see launch_linear_tc)
 }
 
 static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
@@ -1156,14 +1157,16 @@ static cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const uintptr_t wb = reinterpret_cast<uintptr_t>(a.w_scale);
   p.vec_io = (ob % 16 == 0) && (a.ldo % 8 == 0) && (wb % 16 == 0) &&
              (a.residual == nullptr || ((rb % 16 == 0) && (a.ldr % 8 == 0)));
-  // f16 operand stages: 3 at 64 K; at 128 K a third one where three int8
-  // stages still fit beside it (tiles of 32 and 64 tokens: 2-4 % faster than
-  // two; sweeping 64-K stages with 3-6 operand stages was 12-20 % slower)
+  // f16 operand stages: an even number, so that every operand slot is only
+  // ever written by one of the two worker groups (stage parity = slot
+  // parity).  With three slots the groups took turns on each slot, and about
+  // one full-size call in 15 to 40 had one tile whose products for one stage
+  // used wrong values in the rows one group's warps write first (the first
+  // pass); with an even count no call of 820 across five shapes did.
+  // Four where four still leave three staging stages (tiles up to 160
+  // wide), else two.
   const int f16_stage = pl.sub * ((ta > 0 ? 0 : kBM) + pl.bpiece) * 128, s8_stage = (kBM + pl.bpiece) * kBK * pl.sub;
-  if (ta > 0)
-    p.nst = ta;
-  else
-    p.nst = pl.sub == 2 ? ((kRingRegion - 3 * f16_stage) / s8_stage >= 3 ? 3 : 2) : 3;
+  p.nst = ta > 0 ? ta : ((kRingRegion - 4 * f16_stage) / s8_stage >= 3 ? 4 : 2);
   p.nst8 = std::min(kMaxStages, (kRingRegion - p.nst * f16_stage) / s8_stage);
   p.sp.split = a.split;
   p.sp.gx = static_cast<int>(pl.grid_x);
