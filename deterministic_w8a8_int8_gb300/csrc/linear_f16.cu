@@ -499,9 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // plain 16-byte stores (no reductions, nothing to re-zero).  Explicit
       // split-K: integer atomics into the [M, N] accumulator.
       const int64_t slot_elems = static_cast<int64_t>(kBM) * p.bpiece;
+      int sfirst = 0, sn = 0, smine = 0;
+      if (!kExplicit) shared_tile_slots(p.sp, itm.tile, sfirst, sn, smine);
       if (ok) {
         if (!kExplicit) {
-          int32_t* mine = p.slots + (static_cast<int64_t>(itm.tile) + blockIdx.x) * slot_elems;
+          int32_t* mine = p.slots + static_cast<int64_t>(smine) * slot_elems;
 #pragma unroll
           for (int r = 0; r < kGroups; ++r) {
             const int cb = slice + 4 * r;
@@ -529,10 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // could not finish (an expired wait) is not counted and not written
       const bool bad = epi_barrier_any(!ok);
       uint32_t* counter = kExplicit ? p.ws_count + itm.tile : p.cnt + itm.tile;
-      int bf = 0, bl = 0;
-      if (!kExplicit) shared_tile_ctas(p.sp, itm.tile, bf, bl);
       if (!bad && et == 0) {
-        const unsigned target = kExplicit ? static_cast<unsigned>(p.sp.split - 1) : static_cast<unsigned>(bl - bf);
+        const unsigned target = kExplicit ? static_cast<unsigned>(p.sp.split - 1) : static_cast<unsigned>(sn - 1);
         // release: the stores of every epilogue thread reached thread 0
         // through the barrier; its fence orders them before the arrival.
         // acquire: the last arriver's fence orders the read-back after them.
@@ -546,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __threadfence();
       if (!kExplicit) {
         // the other CTAs' pieces, added to this CTA's own sums in registers
-        for (int bo = bf; bo <= bl; ++bo) {
-          if (bo == static_cast<int>(blockIdx.x)) continue;
-          const int32_t* other = p.slots + (static_cast<int64_t>(itm.tile) + bo) * slot_elems;
+        for (int so = sfirst; so < sfirst + sn; ++so) {
+          if (so == smine) continue;
+          const int32_t* other = p.slots + static_cast<int64_t>(so) * slot_elems;
 #pragma unroll
           for (int r = 0; r < kGroups; ++r) {
             const int cb = slice + 4 * r;
@@ -637,37 +637,65 @@ HPlan plan(int64_t M, int64_t N) {
   return pl;
 }
 
-// The automatic schedule.  Whole tiles in rounds (tile b, b + G, ... on CTA
-// b) unless that leaves the last round nearly empty: the balanced schedule's
-// shared tiles cost this kernel more than an uneven last round -- their
-// private slots (128 x width int32 each) written and read back, and the
-// weight tile no longer read by the CTAs beside it at the same time -- so
-// it only serves shapes whose whole-tile rounds would leave most SMs idle at
-// the end: fewer tiles than half the SMs, or a last round under a fifth of
-// them.  (Measured, per call: gate/up 480 -> 453 us, QKV 72 -> 63, o_proj
-// 50 -> 40, 8192 rows 332 -> 311 with whole tiles; the 2048 x 17408 down
-// projection, 2 rounds and 16 tiles, 292 balanced against 308.)
-TcSched balanced(const HPlan& pl, int64_t K) {
-  const int64_t T = pl.gx * pl.gy, g = sm_count();
-  if (T >= g / 2 && T % g >= g / 5) return TcSched{static_cast<int>(g), static_cast<int>(cdiv(T, g)), 0};
-  return tc_balanced_sched(T, cdiv(K, kBK), kChunk, g);
+// The automatic schedule (tc_sched.cuh).  Whole tiles in rounds (tile b,
+// b + G, ... on CTA b) unless the last round would leave most SMs idle:
+// then the rounds with the last one split in lockstep (each remainder tile
+// cut into P equal K pieces on P CTAs, the pieces of tiles that share a
+// weight operand running side by side), or, where no such split fits, the
+// balanced schedule.  The balanced schedule's arbitrary cuts cost this
+// kernel more than they gain -- each shared tile's private slots (128 x
+// width int32) written and read back, and the weight tiles no longer read
+// by neighbouring CTAs at the same time.  Measured per call (whole /
+// balanced / lockstep, us): gate/up 458 / 481 / 463; 8192 rows 313 / 334 /
+// 313; down (2 rounds and 16 tiles) 311 / 295 / 275; QKV 64.8 whole against
+// 72 balanced; o_proj 40.5 against 50.  PRISM_F16_SCHED = whole, balanced or
+// lock forces one (a diagnostic: every schedule gives the same bits).
+struct F16Sched {
+  int sched, G, W, R, P;
+};
+
+F16Sched schedule(const HPlan& pl, int64_t K) {
+  const int64_t T = pl.gx * pl.gy, g = sm_count(), S = cdiv(K, kBK);
+  auto whole = [&] { return F16Sched{1, static_cast<int>(g), static_cast<int>(cdiv(T, g)), 0, 1}; };
+  auto bal = [&] {
+    const TcSched sc = tc_balanced_sched(T, S, kChunk, g);
+    return F16Sched{1, sc.G, sc.W, sc.R, 1};
+  };
+  auto lock = [&] {
+    const int64_t W = T / g, R = T % g;
+    const int64_t P = R == 0 ? 1 : std::min<int64_t>(g / R, S / kChunk);
+    if (P <= 1) return whole();
+    return F16Sched{2, static_cast<int>(W > 0 ? g : R * P), static_cast<int>(W), static_cast<int>(R),
+                    static_cast<int>(P)};
+  };
+  if (const char* e = std::getenv("PRISM_F16_SCHED")) {
+    if (std::strcmp(e, "whole") == 0) return whole();
+    if (std::strcmp(e, "balanced") == 0) return bal();
+    if (std::strcmp(e, "lock") == 0) return lock();
+  }
+  if (T >= g / 2 && T % g >= g / 5) return whole();
+  const F16Sched l = lock();
+  return l.sched == 2 ? l : bal();
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Balanced schedule: counters of the shared tiles, then the piece slots,
-// one per (shared tile st, CTA b) pair at index st + b: R + G - 1 slots of
-// 128 x bpiece int32.
+// Automatic schedule's workspace: counters of the shared tiles, then the
+// piece slots of 128 x bpiece int32 -- balanced: one per (shared tile st,
+// CTA b) pair at index st + b, R + G - 1 slots; lockstep rounds: P per
+// remainder tile.
 size_t balanced_bytes(int64_t M, int64_t N, int64_t K, size_t* counter_bytes) {
   const HPlan pl = plan(M, N);
-  const TcSched sc = balanced(pl, K);
-  if (sc.R == 0 || sc.G == sc.R) {   // no tile shared between CTAs
+  const F16Sched sc = schedule(pl, K);
+  const size_t slots = sc.sched == 2 ? static_cast<size_t>(sc.R) * sc.P
+                                     : (sc.R == 0 || sc.G == sc.R ? 0 : static_cast<size_t>(sc.R + sc.G - 1));
+  if (slots == 0) {   // no tile shared between CTAs
     if (counter_bytes != nullptr) *counter_bytes = 0;
     return 0;
   }
   const size_t cb = round256(static_cast<size_t>(sc.R) * 4);
   if (counter_bytes != nullptr) *counter_bytes = cb;
-  return cb + static_cast<size_t>(sc.R + sc.G - 1) * kBM * pl.bpiece * 4;
+  return cb + slots * kBM * pl.bpiece * 4;
 }
 
 // Explicit split-K: the [M, N] int32 accumulator, then one counter per tile.
@@ -755,8 +783,8 @@ cudaError_t launch_linear_f16(const LinearF16Args& a, cudaStream_t stream) {
     }
     grid = dim3(static_cast<unsigned>(pl.gx), static_cast<unsigned>(pl.gy), static_cast<unsigned>(a.split));
   } else {
-    p.sp.sched = 1;
-    const TcSched sc = balanced(pl, a.K);
+    const F16Sched sc = schedule(pl, a.K);
+    p.sp.sched = sc.sched;
     size_t cb = 0;
     const size_t need = balanced_bytes(a.M, a.N, a.K, &cb);
     if (need > 0) {
@@ -765,7 +793,8 @@ cudaError_t launch_linear_f16(const LinearF16Args& a, cudaStream_t stream) {
     }
     p.sp.W = sc.W;
     p.sp.R = sc.R;
-    const int64_t ctas = sc.R > 0 ? sc.G : std::min<int64_t>(sc.G, p.sp.T);
+    p.sp.P = sc.P;
+    const int64_t ctas = sc.sched == 2 || sc.R > 0 ? sc.G : std::min<int64_t>(sc.G, p.sp.T);
     grid = dim3(static_cast<unsigned>(ctas), 1, 1);
   }
   CUtensorMap tmA, tmB;

@@ -19,6 +19,12 @@
 //            several CTAs has their int32 partial sums added (integer
 //            reductions) into its accumulator slot, and the last CTA to
 //            finish the tile reads the slot back and applies the epilogue.
+//   sched 2: rounds with the last one split in lockstep: CTA b takes whole
+//            tiles b, b + G, ... (W rounds), then, when b < R * P, K piece
+//            b / R of the P equal pieces of remainder tile b % R, so that the
+//            pieces of tiles that share a weight operand run side by side
+//            and start together; the last piece of a tile to finish adds
+//            the others' partial sums.
 // Integer addition is order-free, so no choice here changes a result bit.
 #pragma once
 
@@ -37,6 +43,7 @@ struct SchedParams {
   int S;      // K stages of 64 elements
   int W;      // balanced: rounds of whole tiles per CTA
   int R;      // balanced: tiles whose K stages are shared out
+  int P;      // sched 2: K pieces of each remainder tile
 };
 
 // One unit of work: tile (tx, ty) over K stages [k0, k1).
@@ -73,6 +80,26 @@ __device__ __forceinline__ bool get_item(const SchedParams& p, int n, Item& it) 
     return true;
   }
   const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  if (p.sched == 2) {
+    if (n < p.W) {
+      const int t = n * G + b;
+      if (t >= p.T) return false;
+      tile_coords(p, t, it);
+      it.k0 = 0;
+      it.k1 = p.S;
+      it.kind = 0;
+      it.tile = t;
+      return true;
+    }
+    if (n > p.W || b >= p.R * p.P) return false;
+    const int r = b % p.R, kp = b / p.R;
+    tile_coords(p, p.W * G + r, it);
+    it.k0 = kp * p.S / p.P;
+    it.k1 = (kp + 1) * p.S / p.P;
+    it.kind = p.P > 1 ? 2 : 0;
+    it.tile = r;
+    return true;
+  }
   if (n < p.W) {
     const int t = n * G + b;
     if (t >= p.T) return false;
@@ -107,6 +134,24 @@ __device__ __forceinline__ void shared_tile_ctas(const SchedParams& p, int st, i
   const int U = p.R * p.S;
   bf = ((st * p.S + 1) * G - 1) / U;
   bl = ((st * p.S + p.S) * G - 1) / U;
+}
+
+// The partial-sum slots of shared tile st: this CTA's (mine) and the tile's
+// ns slots first, first + 1, ... (one per CTA sharing the tile: the sched-1
+// pair index st + b over the tile's CTAs bf..bl, or st * P + piece).
+__device__ __forceinline__ void shared_tile_slots(const SchedParams& p, int st, int& first, int& ns, int& mine) {
+  const int b = static_cast<int>(blockIdx.x);
+  if (p.sched == 2) {
+    first = st * p.P;
+    ns = p.P;
+    mine = first + b / p.R;
+    return;
+  }
+  int bf, bl;
+  shared_tile_ctas(p, st, bf, bl);
+  first = st + bf;
+  ns = bl - bf + 1;
+  mine = st + b;
 }
 
 // The balanced schedule for T tiles of S K-stages on `sms` CTAs: whole tiles

@@ -29,17 +29,39 @@ def f16_plan(M, N):
     return 256, cdiv(M, 128) * cdiv(N, 256)
 
 
-def f16_workspace(M, N, K, sms=152):
-    """(counter bytes, total bytes) of the binary16-code kernel's automatic
-    schedule: none when it runs whole tiles in rounds (at least half the SMs'
-    worth of tiles and a last round of at least a fifth of them), else the
-    balanced schedule's arrival counters of the R shared tiles, then one
-    piece slot per (shared tile, CTA) pair, R + G - 1 slots of 128 x bpiece
-    int32."""
-    bpiece, T = f16_plan(M, N)
+def f16_schedule(M, N, K, sms=152):
+    """The binary16-code kernel's automatic schedule: ("whole",), ("lock", W,
+    R, P) or ("balanced", G, W, R).  Whole tiles in rounds when there are at
+    least half the SMs' worth of tiles and the last round holds at least a
+    fifth of them; else the rounds with the R remainder tiles cut into P =
+    min(SMs // R, K stages // 16) K pieces when P >= 2; else the balanced
+    schedule."""
+    _, T = f16_plan(M, N)
+    S = cdiv(K, 64)
     if T >= sms // 2 and T % sms >= sms // 5:
+        return ("whole",)
+    W, R = T // sms, T % sms
+    P = min(sms // R, S // 16) if R else 1
+    if P >= 2:
+        return ("lock", W, R, P)
+    G, W, R = balanced(T, S, 16, sms)
+    return ("balanced", G, W, R)
+
+
+def f16_workspace(M, N, K, sms=152):
+    """(counter bytes, total bytes) of that schedule's workspace: arrival
+    counters of the R shared tiles, then the piece slots of 128 x bpiece
+    int32 -- P per remainder tile in lockstep rounds, one per (shared tile,
+    CTA) pair (R + G - 1) in the balanced schedule; none for whole tiles."""
+    bpiece, T = f16_plan(M, N)
+    sc = f16_schedule(M, N, K, sms)
+    if sc[0] == "whole":
         return 0, 0
-    G, W, R = balanced(T, cdiv(K, 64), 16, sms)
+    if sc[0] == "lock":
+        _, W, R, P = sc
+        cb = (R * 4 + 255) & ~255
+        return cb, cb + R * P * 128 * bpiece * 4
+    G, W, R = sc[1], sc[2], sc[3]
     if R == 0 or G == R:
         return 0, 0
     cb = (R * 4 + 255) & ~255

@@ -19,7 +19,7 @@ import torch
 import oracle
 import workloads as wl
 from tests.gpu_util import dev, dev_bf16, host, host_bits, padded
-from tests.sched_util import f16_workspace
+from tests.sched_util import balanced, f16_plan, f16_workspace
 
 import deterministic_w8a8_int8_gb300 as prism
 
@@ -145,15 +145,15 @@ def test_split_k_bit_identical(cuda_device, M):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (1024, 4864, 512),    # 152 tiles: whole tiles only, one round
-    (304, 1536, 5120),    # few tiles, K ranges shared out
-    (600, 2560, 2048),    # K units shared over all CTAs
+    (1024, 4864, 512),    # 152 tiles: one round of whole tiles
+    (304, 1536, 5120),    # 24 tiles, each cut into 5 K pieces (lockstep)
+    (600, 2560, 2048),    # 50 tiles, 2 pieces each
     (304, 15360, 1024),   # whole tiles in two rounds (the last 88 of 152)
-    (1024, 5120, 1024),   # 160 tiles (a round would leave 8): every tile shared
     (37, 384, 256),       # one CTA per tile
     (640, 25600, 256),    # whole tiles in four rounds
-    (96, 640, 17408),     # few tiles of many K stages
-    (2048, 5120, 5120),   # one round of whole tiles, then shared tiles
+    (96, 640, 17408),     # 5 tiles of 272 K stages, 17 pieces each
+    (2048, 5120, 5120),   # two rounds, then 16 tiles in 5 pieces
+    (1024, 5120, 1024),   # 160 tiles of 16 stages: the balanced schedule shares them all
 ])
 def test_balanced_schedule_matches_single_piece(cuda_device, M, N, K):
     """Every branch of the balanced schedule gives the bits of one K piece
@@ -187,6 +187,37 @@ def test_balanced_schedule_matches_single_piece(cuda_device, M, N, K):
     outo, acco = oracle.w8a8_linear(q[rows], a[rows], w, s, rb[rows])
     assert np.array_equal(host(ref_acc)[rows], acco)
     assert np.array_equal(host_bits(ref)[rows], outo)
+
+
+@pytest.mark.parametrize("sched", ["whole", "balanced", "lock"])
+@pytest.mark.parametrize("M,N,K", [(304, 1536, 5120), (2048, 5120, 2048), (300, 2600, 1040)])
+def test_every_schedule_matches_oracle(cuda_device, monkeypatch, sched, M, N, K):
+    """Each automatic schedule forced on the same shapes (PRISM_F16_SCHED):
+    whole tiles in rounds, the balanced schedule's shared K ranges, and the
+    rounds with the remainder tiles split in lockstep -- every one bit-exact
+    against the oracle, with the workspace sized for it."""
+    monkeypatch.setenv("PRISM_F16_SCHED", sched)
+    xb, w, w_scale, rb = problem(M, N, K, 3 * M + N)
+    rows = np.unique(np.linspace(0, M - 1, 11).astype(int))
+    qo, ao = oracle.quant_act(xb[rows], None)
+    outo, acco = oracle.w8a8_linear(qo, ao, w, w_scale, rb[rows])
+    qh, a = prism.prism_quant_act_f16(dev_bf16(xb))
+    W = prism.prism_codes_to_f16(dev(w))
+    ws_buf = prism.new_workspace_f16(M, N, K, 0, "cuda")
+    for i in range(2):
+        acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        out = prism.prism_w8a8_linear_f16(qh, a, W, dev(w_scale), residual=dev_bf16(rb), acc_out=acc,
+                                          workspace=ws_buf)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(acc)[rows], acco), i
+        assert np.array_equal(host_bits(out)[rows], outo), i
+        if ws_buf is not None:
+            # slots are scratch; the counters (one per shared tile, first) stay zero
+            T = f16_plan(M, N)[1]
+            R = T % 152 if sched == "lock" else balanced(T, (K + 63) // 64, 16)[2]
+            cb = (R * 4 + 255) & ~255
+            assert int(ws_buf[:cb].count_nonzero()) == 0
+            ws_buf[cb:].fill_(0x3C + i)
 
 
 @pytest.mark.parametrize("M", [5, 40, 130, 600])
