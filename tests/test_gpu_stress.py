@@ -126,3 +126,31 @@ def test_full_layer_rows_equal_restricted_rows_repeatedly(cuda_device, problem, 
     bad = sum(0 if torch.equal(o.view(torch.int16)[idx], p["out_o"]) else 1 for o in outs)
     assert bad == 0
     assert int(ws_buf.count_nonzero()) == 0
+
+
+def test_full_size_gateup_repeated_calls_identical(cuda_device, monkeypatch):
+    """60 full-size gate/up calls (2048 x 34816 x 5120, int8 operands: 2176
+    tiles of 80 widened stages a call) give identical accumulators, and the
+    first one is the oracle's on one row of every 128-row block.  With an odd
+    number of operand slots, shared by the two widening groups, about one
+    call in 15 to 40 had a wrong tile; this repeats enough calls to see it."""
+    monkeypatch.delenv("PRISM_LINEAR_PATH", raising=False)
+    c = wl.make_linear("load_gateup_m2048_k5120_n34816")
+    q, a = prism.prism_quant_act(dev_bf16(c.x_bits), dev(c.inv_s))
+    W, S = dev(c.w), dev(c.w_scale)
+    ws_buf = prism.new_workspace(c.M, c.N, c.K, 0, "cuda")
+    ref = torch.empty((c.M, c.N), dtype=torch.int32, device="cuda")
+    prism.prism_w8a8_linear(q, a, W, S, acc_out=ref, workspace=ws_buf)
+    torch.cuda.synchronize()
+    rows = np.unique(np.array([0, c.M - 1] + [b * 128 + 37 for b in range(c.M // 128)]))
+    qo, ao = oracle.quant_act(c.x_bits[rows], c.inv_s)
+    _, acco = oracle.w8a8_linear(qo, ao, c.w, c.w_scale, None)
+    assert np.array_equal(ref.cpu().numpy()[rows], acco)
+    acc = torch.empty_like(ref)
+    bad = 0
+    for _ in range(60):
+        prism.prism_w8a8_linear(q, a, W, S, acc_out=acc, workspace=ws_buf)
+        torch.cuda.synchronize()
+        bad += 0 if torch.equal(acc, ref) else 1
+    assert prism.prism_device_status() == 0
+    assert bad == 0
