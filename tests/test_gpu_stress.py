@@ -154,3 +154,28 @@ def test_full_size_gateup_repeated_calls_identical(cuda_device, monkeypatch):
         bad += 0 if torch.equal(acc, ref) else 1
     assert prism.prism_device_status() == 0
     assert bad == 0
+
+
+def test_full_size_gateup_f16_repeated_calls_identical(cuda_device):
+    """The same for the binary16-code kernel (whole tiles in rounds): 40
+    calls, identical accumulators, the first one the oracle's."""
+    c = wl.make_linear("load_gateup_m2048_k5120_n34816")
+    qh, a = prism.prism_quant_act_f16(dev_bf16(c.x_bits), dev(c.inv_s))
+    W = prism.prism_codes_to_f16(dev(c.w))
+    S = dev(c.w_scale)
+    ws_buf = prism.new_workspace_f16(c.M, c.N, c.K, 0, "cuda")
+    ref = torch.empty((c.M, c.N), dtype=torch.int32, device="cuda")
+    prism.prism_w8a8_linear_f16(qh, a, W, S, acc_out=ref, workspace=ws_buf)
+    torch.cuda.synchronize()
+    rows = np.unique(np.array([0, c.M - 1] + [b * 128 + 91 for b in range(c.M // 128)]))
+    qo, ao = oracle.quant_act(c.x_bits[rows], c.inv_s)
+    _, acco = oracle.w8a8_linear(qo, ao, c.w, c.w_scale, None)
+    assert np.array_equal(ref.cpu().numpy()[rows], acco)
+    acc = torch.empty_like(ref)
+    bad = 0
+    for _ in range(40):
+        prism.prism_w8a8_linear_f16(qh, a, W, S, acc_out=acc, workspace=ws_buf)
+        torch.cuda.synchronize()
+        bad += 0 if torch.equal(acc, ref) else 1
+    assert prism.prism_device_status() == 0
+    assert bad == 0
