@@ -608,17 +608,31 @@ def sub_forest(prism, L, dev):
     torch.cuda.synchronize()
     us = {j: statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev[j]) for j in ev}
     assert int(err.item()) == 0
+
+    def isolated(j):
+        # launch j of every weight set, back to back in one CUDA graph on the
+        # capturing stream (events around single calls also time launch gaps)
+        calls = []
+        for r in rot:
+            fn, a = r[j]
+            calls.append(lambda fn=fn, a=a: fn(*[ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+                                                 if x is st else x for x in a]))
+        return graph_time_us(calls * 4)
+
+    gq, go = isolated(1), isolated(3)
     hbm, bf16p, _ = load_peaks()
     bq = M * K + Nq * K + 4 * Nq + 4 * M + 2 * M * Nq
     bo = M * K + No * K + 4 * No + 4 * M + 2 * M * No * 2
     br = 2 * 3 * K + T * (K + 4) + 16 + 12 * T
     return {"step_us": step_us, "step_tops": work.ops / step_us / 1e6, "launches_per_step": 5,
-            "qkv_m304_k5120_n15360": dict(_linear_record(work.ops_linear_qkv, bq, us[1], hbm, bf16p),
-                                          kernel="binary16 codes"),
-            "oproj_m304_k5120_n5120": dict(_linear_record(work.ops_linear_o, bo, us[3], hbm, bf16p),
-                                           kernel="int8 operands"),
+            "qkv_m304_k5120_n15360": dict(_linear_record(work.ops_linear_qkv, bq, gq, hbm, bf16p),
+                                          kernel="binary16 codes", events_us=us[1]),
+            "oproj_m304_k5120_n5120": dict(_linear_record(work.ops_linear_o, bo, go, hbm, bf16p),
+                                           kernel="int8 operands", events_us=us[3]),
             "readout_p3": {"us": us[4], "gbs": br / us[4] / 1e3, "frac_hbm": br / us[4] / 1e3 / hbm},
-            "timing": "back-to-back steps on one stream, 3 rotated weight sets; per-call events in a second pass"}
+            "timing": ("step: back-to-back steps on one stream, 3 rotated weight sets; QKV and o_proj us: "
+                       "each alone, a CUDA graph of back-to-back calls over the weight sets (events_us: "
+                       "events around the call inside the step); read-out: events")}
 
 
 def sub_decode(prism, L, dev):
