@@ -115,10 +115,10 @@ struct HParams {
   int vec_io;                // out / residual rows and w_scale 16-byte aligned, ld % 8 == 0
   int nst;                   // ring stages
   SchedParams sp;
-  uint32_t* cnt;             // balanced: arrival counters of the shared tiles
-  int32_t* slots;            // balanced: piece slots, one per (shared tile st, CTA b) pair at index st + b,
-                             // 128 x bpiece int32 each (st + b is unique: a CTA's tiles are consecutive
-                             // and the next CTA starts at or after its last one)
+  uint32_t* cnt;             // automatic: arrival counters of the shared tiles
+  int32_t* slots;            // automatic: piece slots of 128 x bpiece int32 (shared_tile_slots in
+                             // tc_sched.cuh: balanced, one per (shared tile st, CTA b) pair at index st + b;
+                             // lockstep rounds, P per remainder tile)
   int32_t* ws_acc;           // explicit split: [M, N] int32 accumulator
   uint32_t* ws_count;        // explicit split: per-tile arrival counters
 };
@@ -271,7 +271,7 @@ __device__ __forceinline__ bool group_elem(const HParams& p, int64_t a0, int64_t
 __device__ __forceinline__ int64_t piece_group(int trow, int cb) { return (static_cast<int64_t>(cb) * kBM + trow) * 16; }
 
 // kExplicit: the explicit split-K instance (items of kind 0 and 1); the
-// other instance runs the balanced schedule (kinds 0 and 2).  Each carries
+// other instance runs the automatic schedules (kinds 0 and 2).  Each carries
 // only its own protocol, which keeps the epilogue within its registers.
 template <bool kExplicit>
 __global__ void __launch_bounds__(kThreads, 1)

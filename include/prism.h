@@ -310,7 +310,12 @@ int prism_quant_act_f16(const void *x_bf16, int64_t ldx, const float *inv_smooth
 int prism_codes_to_f16(const int8_t *w, int64_t ldw, int64_t rows, int64_t K,
                        uint16_t *wh, int64_t ldwh, void *cuda_stream);
 
-/* Workspace bytes prism_w8a8_linear_f16 needs (split_k as in that call). */
+/* Workspace bytes prism_w8a8_linear_f16 needs (split_k as in that call).
+ * Its automatic schedule (split_k = 0) runs whole tiles in rounds and needs
+ * none, unless the last round would leave most SMs idle: then the rounds with
+ * the remainder tiles cut into equal K pieces side by side (or, for many
+ * tiles of little K, the balanced schedule), whose arrival counters and
+ * partial-sum slots this counts. */
 size_t prism_w8a8_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
 
 /*
