@@ -20,6 +20,9 @@ Entry points (same names as the C ABI):
   prism_w4a8_linear(q, a_scale, w4, w_scale, ...) -> out   packed 4-bit weights
   prism_unpack_w4(w4, K)                         -> int8 codes
   prism_candidate_readout(hidden, ...)           -> (logits, probs)
+  prism_candidate_logits(hidden, ..., shard)     -> logits of one vocabulary shard
+  prism_candidate_softmax(logits, cand_offsets)  -> probs
+  readout_column_parallel(hidden, ..., shard)    those two around torch.distributed
   prism_quant_act_f16(x, inv_s)                  -> (codes as float16, a_scale)
   prism_codes_to_f16(w)                          -> int8 codes as float16 (load time)
   prism_w8a8_linear_f16(qh, a_scale, wh, w_scale, ...) -> out   codes given as float16
@@ -63,6 +66,9 @@ SIGNATURES = {
     "prism_candidate_readout": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _P, _P,
                                        _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "prism_readout_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "prism_candidate_logits": (_I32, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P,
+                                      _I64, _I64, _P, _P, _P]),
+    "prism_candidate_softmax": (_I32, [_P, _P, _I64, _I64, _P, _P, _P]),
     "prism_quant_act_f16": (_I32, [_P, _I64, _P, _I64, _I64, _P, _I64, _P, _P]),
     "prism_codes_to_f16": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P]),
     "prism_w8a8_f16_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
@@ -566,6 +572,83 @@ def prism_candidate_readout(hidden, inv_s, lm_head, lm_scale, cand_offsets, cand
         _ptr(probs), _ptr(err), _ptr(workspace), ws_bytes, _stream(stream))
     _check("prism_candidate_readout", st)
     return logits, probs
+
+
+def prism_candidate_logits(hidden, inv_s, lm_shard, lm_scale_shard, v0: int, V: int, cand_offsets, cand_ids,
+                           logits=None, err=None, stream=None):
+    """Logits float32 [T] of the candidates held by one vocabulary shard
+    (``lm_shard`` [V_shard, K] int8 = rows v0 .. v0 + V_shard - 1 of a V-row
+    head, ``lm_scale_shard`` [V_shard]); -0.0 for the other candidates, so
+    that the SUM over the shards is the one-device read-out's logits."""
+    import torch
+    _require(hidden, torch.bfloat16, "hidden", 2)
+    _require(lm_shard, torch.int8, "lm_shard", 2)
+    _require(lm_scale_shard, torch.float32, "lm_scale_shard", 1)
+    _require(cand_offsets, torch.int32, "cand_offsets", 1)
+    _require(cand_ids, torch.int32, "cand_ids", 1)
+    if inv_s is not None:
+        _require(inv_s, torch.float32, "inv_s", 1)
+    P, K = hidden.shape
+    Vs = lm_shard.shape[0]
+    T = cand_ids.numel()
+    if lm_shard.shape[1] != K or lm_scale_shard.numel() != Vs or cand_offsets.numel() != P + 1:
+        raise ValueError("shape mismatch")
+    if logits is None:
+        logits = torch.empty((T,), dtype=torch.float32, device=hidden.device)
+    _require(logits, torch.float32, "logits", 1)
+    if logits.numel() != T:
+        raise ValueError("logits must hold T values")
+    if err is not None:
+        _require(err, torch.int32, "err", 1)
+    st = lib().prism_candidate_logits(
+        _ptr(hidden), hidden.stride(0), _ptr(inv_s), _ptr(lm_shard), lm_shard.stride(0), _ptr(lm_scale_shard),
+        int(v0), Vs, int(V), K, _ptr(cand_offsets), _ptr(cand_ids), P, T, _ptr(logits), _ptr(err),
+        _stream(stream))
+    _check("prism_candidate_logits", st)
+    return logits
+
+
+def prism_candidate_softmax(logits, cand_offsets, probs=None, err=None, stream=None):
+    """The read-out's candidate softmax on given logits -> probs float32 [T]."""
+    import torch
+    _require(logits, torch.float32, "logits", 1)
+    _require(cand_offsets, torch.int32, "cand_offsets", 1)
+    P, T = cand_offsets.numel() - 1, logits.numel()
+    if probs is None:
+        probs = torch.empty((T,), dtype=torch.float32, device=logits.device)
+    _require(probs, torch.float32, "probs", 1)
+    if probs.numel() != T:
+        raise ValueError("probs must hold T values")
+    if err is not None:
+        _require(err, torch.int32, "err", 1)
+    st = lib().prism_candidate_softmax(_ptr(logits), _ptr(cand_offsets), P, T, _ptr(probs), _ptr(err),
+                                       _stream(stream))
+    _check("prism_candidate_softmax", st)
+    return probs
+
+
+class ReadoutKernelOps:
+    """The per-rank steps of readout_column_parallel on this library's kernels."""
+    candidate_logits = staticmethod(lambda hidden, inv_s, lm_shard, lm_scale_shard, v0, V, off, ids, err:
+                                    prism_candidate_logits(hidden, inv_s, lm_shard, lm_scale_shard, v0, V, off,
+                                                           ids, err=err))
+    candidate_softmax = staticmethod(lambda logits, off, err: prism_candidate_softmax(logits, off, err=err))
+
+
+def readout_column_parallel(hidden, inv_s, lm_shard, lm_scale_shard, v0: int, V: int, cand_offsets, cand_ids,
+                            err=None, group=None, ops=ReadoutKernelOps):
+    """One rank of the column-parallel candidate read-out: this rank holds
+    rows v0 .. v0 + V_shard - 1 of the V-row LM head; ``hidden`` and the
+    candidate lists are replicated.  Each rank forms its candidates' logits
+    (-0.0 for the others), the ranks add them (SUM all-reduce: one rank owns
+    each candidate and x + -0.0 == x, so the sum is exact in any order), and
+    every rank applies the candidate softmax -- returning the one-device
+    read-out's (logits, probs) bit for bit.  ``ops`` holds the per-rank
+    steps (candidate_logits, candidate_softmax)."""
+    import torch.distributed as dist
+    logits = ops.candidate_logits(hidden, inv_s, lm_shard, lm_scale_shard, v0, V, cand_offsets, cand_ids, err)
+    dist.all_reduce(logits, op=dist.ReduceOp.SUM, group=group)
+    return logits, ops.candidate_softmax(logits, cand_offsets, err)
 
 
 def prism_debug_wait_expiry(limit_ns: int) -> None:

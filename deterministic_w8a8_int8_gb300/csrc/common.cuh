@@ -267,4 +267,12 @@ cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const
                            int64_t ldw, const float* lm_scale, int64_t V, int64_t K,
                            const int32_t* off, const int32_t* ids, int64_t P, int64_t T,
                            float* logits, float* probs, uint32_t* err, cudaStream_t stream);
+// A vocabulary shard's logits (rows [v0, v0 + Vs) of the V-row head; -0.0 for
+// other shards' candidates) and the softmax on combined logits (readout.cu).
+cudaError_t launch_readout_logits(const void* h, int64_t ldh, const float* inv_s, const int8_t* W_shard,
+                                  int64_t ldw, const float* lm_scale_shard, int64_t v0, int64_t Vs, int64_t V,
+                                  int64_t K, const int32_t* off, const int32_t* ids, int64_t P, int64_t T,
+                                  float* logits, uint32_t* err, cudaStream_t stream);
+cudaError_t launch_candidate_softmax(const float* logits, const int32_t* off, int64_t P, int64_t T, float* probs,
+                                     uint32_t* err, cudaStream_t stream);
 }  // namespace prism

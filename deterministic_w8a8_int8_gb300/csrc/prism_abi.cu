@@ -515,6 +515,45 @@ int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* i
                                                    static_cast<cudaStream_t>(cuda_stream)));
 }
 
+int prism_candidate_logits(const void* hidden_bf16, int64_t ldh, const float* inv_smooth,
+                           const int8_t* lm_head_shard, int64_t ldw, const float* lm_scale_shard, int64_t v0,
+                           int64_t V_shard, int64_t V, int64_t K, const int32_t* cand_offsets,
+                           const int32_t* cand_ids, int64_t P, int64_t T, float* logits, int32_t* dev_error_word,
+                           void* cuda_stream) {
+  if (P < 0 || T < 0 || V <= 0 || K <= 0 || v0 < 0 || V_shard < 0 || v0 + V_shard > V)
+    return PRISM_ERR_INVALID_ARG;
+  if (P == 0) return T == 0 ? PRISM_OK : PRISM_ERR_INVALID_ARG;
+  if (hidden_bf16 == nullptr || cand_offsets == nullptr || logits == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (V_shard > 0 && (lm_head_shard == nullptr || lm_scale_shard == nullptr)) return PRISM_ERR_INVALID_ARG;
+  if (T > 0 && cand_ids == nullptr) return PRISM_ERR_INVALID_ARG;
+  if (ldh < K || (V_shard > 0 && ldw < K)) return PRISM_ERR_INVALID_ARG;
+  if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
+  if (K > PRISM_MAX_READOUT_K || T > P * PRISM_MAX_CANDIDATES || V > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  if (ldh % 8 != 0 || (V_shard > 0 && ldw % 16 != 0)) return PRISM_ERR_ALIGNMENT;
+  if (!aligned(hidden_bf16, 16) || !aligned(lm_head_shard, 16) || !aligned(lm_scale_shard, 4) ||
+      !aligned(cand_offsets, 4) || !aligned(cand_ids, 4) || !aligned(logits, 4))
+    return PRISM_ERR_ALIGNMENT;
+  if (inv_smooth != nullptr && !aligned(inv_smooth, 16)) return PRISM_ERR_ALIGNMENT;
+  if (dev_error_word != nullptr && !aligned(dev_error_word, 4)) return PRISM_ERR_ALIGNMENT;
+  if (P > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  return prism::record_cuda(prism::launch_readout_logits(
+      hidden_bf16, ldh, inv_smooth, lm_head_shard, ldw, lm_scale_shard, v0, V_shard, V, K, cand_offsets, cand_ids, P,
+      T, logits, reinterpret_cast<uint32_t*>(dev_error_word), static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int prism_candidate_softmax(const float* logits, const int32_t* cand_offsets, int64_t P, int64_t T, float* probs,
+                            int32_t* dev_error_word, void* cuda_stream) {
+  if (P < 0 || T < 0) return PRISM_ERR_INVALID_ARG;
+  if (P == 0) return T == 0 ? PRISM_OK : PRISM_ERR_INVALID_ARG;
+  if (cand_offsets == nullptr || probs == nullptr || (T > 0 && logits == nullptr)) return PRISM_ERR_INVALID_ARG;
+  if (T > P * PRISM_MAX_CANDIDATES || P > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  if (!aligned(logits, 4) || !aligned(cand_offsets, 4) || !aligned(probs, 4)) return PRISM_ERR_ALIGNMENT;
+  if (dev_error_word != nullptr && !aligned(dev_error_word, 4)) return PRISM_ERR_ALIGNMENT;
+  return prism::record_cuda(prism::launch_candidate_softmax(logits, cand_offsets, P, T, probs,
+                                                            reinterpret_cast<uint32_t*>(dev_error_word),
+                                                            static_cast<cudaStream_t>(cuda_stream)));
+}
+
 size_t prism_readout_workspace_bytes(int64_t P, int64_t T, int64_t K) {
   (void)P;
   (void)T;

@@ -14,6 +14,12 @@
 //   4. warp 0 forms the softmax: max over the logits, e_c = exp(logit_c -
 //      max) and prob_c = e_c / s one candidate per lane, s = e_1 + ... + e_n
 //      added in list order; every step binary32 RN.
+// A vocabulary shard (the column-parallel read-out): the same kernel with
+// the LM head's rows [v0, v0 + Vs) only computes the logits of the
+// candidates it holds and writes -0.0 for the others (x + -0.0 == x for every
+// x, so a SUM over the shards' outputs gives each logit bit for bit), and a
+// separate kernel applies the softmax of step 4 to the combined logits with
+// the same arithmetic (candidate_softmax below).
 // Bytes: 2K (hidden row) + count * (K + 4) (candidate rows and scales) per
 // position, plus 12 bytes per candidate (id, logit, prob) -- HBM- and
 // latency-bound (a chain of dependent reads: offsets, ids, rows); nothing is
@@ -72,6 +78,25 @@ __device__ __forceinline__ float smooth(float v, const float* inv_s, int64_t k) 
   return inv_s != nullptr ? __fmul_rn(v, __ldg(inv_s + k)) : v;
 }
 
+// Step 4 in one warp: lane i holds candidates i and 32 + i (l0, l1; lanes
+// past the count hold -inf).  The maximum (exact, any order), e_c =
+// exp(logit_c - max) and prob_c = e_c / s per lane, s = e_1 + ... + e_n added
+// in list order (every lane forms the same sum from shuffled values); every
+// step binary32 RN.
+__device__ __forceinline__ void candidate_softmax(float l0, float l1, int64_t cnt, int lane, float& p0, float& p1) {
+  float mx = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float e0 = lane < cnt ? cw_exp(__fsub_rn(l0, mx)) : 0.0f;
+  const float e1 = lane + 32 < cnt ? cw_exp(__fsub_rn(l1, mx)) : 0.0f;
+  float s = 0.0f;
+  const int n0 = static_cast<int>(cnt < 32 ? cnt : 32);
+  for (int i = 0; i < n0; ++i) s = __fadd_rn(s, __shfl_sync(0xffffffffu, e0, i));
+  for (int i = 32; i < cnt; ++i) s = __fadd_rn(s, __shfl_sync(0xffffffffu, e1, i - 32));
+  p0 = __fdiv_rn(e0, s);
+  p1 = __fdiv_rn(e1, s);
+}
+
 // Hidden rows of up to kRegK elements are read once into registers, with
 // loads issued before anything else (they depend on p alone).  The first
 // pre_rows candidates of a position (pre_rows set by the launcher from the
@@ -88,11 +113,14 @@ constexpr int kPreMax = 16;                     // staged candidate rows at most
 constexpr int kPrePerWarp = kPreMax / kWarps;   // 2
 constexpr int kSmemBudget = 110 * 1024;         // dynamic shared memory per CTA (two per SM)
 
-template <bool kReg>
+// kLogits: logits only (a vocabulary shard, probs unused); W and lm_scale
+// hold the rows [v0, v0 + Vs) of the V-row head (the whole head: v0 = 0,
+// Vs = V).
+template <bool kReg, bool kLogits>
 __global__ void __launch_bounds__(kThreads, 2)
     readout_kernel(const uint16_t* __restrict__ h, int64_t ldh, const float* __restrict__ inv_s,
                    const int8_t* __restrict__ W, int64_t ldw, const float* __restrict__ lm_scale,
-                   int64_t V, int64_t K, const int32_t* __restrict__ off,
+                   int64_t V, int64_t v0, int64_t Vs, int64_t K, const int32_t* __restrict__ off,
                    const int32_t* __restrict__ ids, int64_t T, float* __restrict__ logits,
                    float* __restrict__ probs, uint32_t* __restrict__ err, int pre_rows) {
   extern __shared__ __align__(16) int8_t smem[];
@@ -143,10 +171,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     pre_ls[j] = 0.0f;
     if (c < nstage) {
       const int32_t id = id_of(c);
-      if (id >= 0 && id < V) {   // out-of-range ids are never dereferenced
+      // out-of-range ids are never dereferenced, nor ids of another shard
+      if (id >= 0 && id < V && id >= v0 && id - v0 < Vs) {
         pre_id[j] = id;
-        pre_ls[j] = __ldg(lm_scale + id);
-        const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
+        pre_ls[j] = __ldg(lm_scale + (id - v0));
+        const int8_t* wr = W + static_cast<int64_t>(id - v0) * ldw;
         const uint32_t dst = smem_u32(srow + static_cast<int64_t>(c) * K);
         for (int64_t ch = lane; ch < nchunk; ch += 32) cp_async_16(dst + static_cast<uint32_t>(ch * 16), wr + ch * 16, 16);
       }
@@ -179,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float nan = __uint_as_float(0x7fc00000u);
       for (int64_t i = b + tid; i < e; i += kThreads) {
         logits[i] = nan;
-        probs[i] = nan;
+        if (!kLogits) probs[i] = nan;
       }
     }
     return;
@@ -251,6 +280,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     int acc = 0;
     int32_t id;
     float ls;
+    if (kLogits) {
+      const int32_t ic = id_of(i);
+      if (ic < v0 || ic - v0 >= Vs) {   // another shard's candidate
+        if (lane == 0) s_logit[i] = -0.0f;
+        continue;
+      }
+    }
     if (i < nstage) {
       const int j = static_cast<int>(i) / kWarps;
       id = pre_id[0];
@@ -266,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         acc = dot16(*reinterpret_cast<const uint4*>(rs + c * 16), *reinterpret_cast<const uint4*>(sq + c * 16), acc);
     } else {
       id = id_of(i);
-      ls = __ldg(lm_scale + id);
-      const int8_t* wr = W + static_cast<int64_t>(id) * ldw;
+      ls = __ldg(lm_scale + (id - v0));
+      const int8_t* wr = W + static_cast<int64_t>(id - v0) * ldw;
       int64_t c = lane;
       for (; c + 32 * 3 < nchunk; c += 32 * 4) {
         const uint4 w0 = ld_stream_16(wr + (c)*16);
@@ -293,56 +329,105 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
 
-  // ---- 4. softmax over the candidates, fixed order, in warp 0: the maximum
-  // (exact, any order), e_c = exp(logit_c - max) and prob_c = e_c / s one
-  // candidate per lane, and s = e_1 + ... + e_n added in list order (every
-  // lane forms the same sum from shuffled values)
+  // ---- 4. softmax over the candidates in warp 0 (candidate_softmax), or
+  // for a shard its logits only
   if (warp == 0) {
     const float l0 = lane < cnt ? s_logit[lane] : -INFINITY;
     const float l1 = lane + 32 < cnt ? s_logit[lane + 32] : -INFINITY;
-    float mx = fmaxf(l0, l1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float e0 = lane < cnt ? cw_exp(__fsub_rn(l0, mx)) : 0.0f;
-    const float e1 = lane + 32 < cnt ? cw_exp(__fsub_rn(l1, mx)) : 0.0f;
-    float s = 0.0f;
-    const int n0 = static_cast<int>(cnt < 32 ? cnt : 32);
-    for (int i = 0; i < n0; ++i) s = __fadd_rn(s, __shfl_sync(0xffffffffu, e0, i));
-    for (int i = 32; i < cnt; ++i) s = __fadd_rn(s, __shfl_sync(0xffffffffu, e1, i - 32));
-    if (lane < cnt) {
-      logits[b + lane] = l0;
-      probs[b + lane] = __fdiv_rn(e0, s);
-    }
-    if (lane + 32 < cnt) {
-      logits[b + lane + 32] = l1;
-      probs[b + lane + 32] = __fdiv_rn(e1, s);
+    if (lane < cnt) logits[b + lane] = l0;
+    if (lane + 32 < cnt) logits[b + lane + 32] = l1;
+    if (!kLogits) {
+      float p0, p1;
+      candidate_softmax(l0, l1, cnt, lane, p0, p1);
+      if (lane < cnt) probs[b + lane] = p0;
+      if (lane + 32 < cnt) probs[b + lane + 32] = p1;
     }
   }
 }
 
+// The softmax of step 4 on logits combined from the vocabulary shards: one
+// warp per position checks the CSR slice like the read-out (bad offsets or
+// count: the error bit, NaN probabilities) and treats a position with a NaN
+// logit (a shard found its list invalid and said so in the error word) as
+// invalid too; the others get candidate_softmax, bit for bit the fused
+// read-out's probabilities.
+__global__ void __launch_bounds__(128)
+    softmax_kernel(const float* __restrict__ logits, const int32_t* __restrict__ off, int64_t P, int64_t T,
+                   float* __restrict__ probs, uint32_t* __restrict__ err) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (p >= P) return;
+  const int64_t b = off[p], e = off[p + 1];
+  const bool off_ok = b >= 0 && e <= T && b <= e;
+  const int64_t cnt = off_ok ? e - b : 0;
+  const bool cnt_ok = off_ok && cnt >= 1 && cnt <= PRISM_MAX_CANDIDATES;
+  const float l0 = cnt_ok && lane < cnt ? logits[b + lane] : -INFINITY;
+  const float l1 = cnt_ok && lane + 32 < cnt ? logits[b + lane + 32] : -INFINITY;
+  const bool has_nan = __any_sync(0xffffffffu, l0 != l0 || l1 != l1);
+  if (!cnt_ok || has_nan) {
+    if (lane == 0 && err != nullptr && !cnt_ok) atomicOr(err, off_ok ? PRISM_DEV_ERR_COUNT : PRISM_DEV_ERR_OFFSETS);
+    if (off_ok) {
+      const float nan = __uint_as_float(0x7fc00000u);
+      for (int64_t i = b + lane; i < e; i += 32) probs[i] = nan;
+    }
+    return;
+  }
+  float p0, p1;
+  candidate_softmax(l0, l1, cnt, lane, p0, p1);
+  if (lane < cnt) probs[b + lane] = p0;
+  if (lane + 32 < cnt) probs[b + lane + 32] = p1;
+}
+
+}  // namespace
+
+namespace {
+template <bool kLogits>
+cudaError_t launch_readout_impl(const void* h, int64_t ldh, const float* inv_s, const int8_t* W, int64_t ldw,
+                                const float* lm_scale, int64_t V, int64_t v0, int64_t Vs, int64_t K,
+                                const int32_t* off, const int32_t* ids, int64_t P, int64_t T, float* logits,
+                                float* probs, uint32_t* err, cudaStream_t stream) {
+  // staged rows: as many as fit beside the quantised row in kSmemBudget, at most kPreMax
+  const int64_t fit = K < kSmemBudget ? (kSmemBudget - K) / K : 0;
+  const int pre = static_cast<int>(std::min<int64_t>(kPreMax, fit));
+  const size_t smem = static_cast<size_t>(K) * static_cast<size_t>(1 + pre);
+  if (K <= kRegK) {
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<true, kLogits>), kSmemBudget);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(readout_kernel<true, kLogits>, dim3(static_cast<unsigned>(P)), dim3(kThreads), smem,
+                         stream, true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, v0, Vs, K,
+                         off, ids, T, logits, probs, err, pre);
+  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<false, kLogits>),
+                                   std::max<int>(kSmemBudget, PRISM_MAX_READOUT_K));
+  if (e != cudaSuccess) return e;
+  return launch_kernel(readout_kernel<false, kLogits>, dim3(static_cast<unsigned>(P)), dim3(kThreads), smem, stream,
+                       true, static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, v0, Vs, K, off, ids,
+                       T, logits, probs, err, pre);
+}
 }  // namespace
 
 cudaError_t launch_readout(const void* h, int64_t ldh, const float* inv_s, const int8_t* W,
                            int64_t ldw, const float* lm_scale, int64_t V, int64_t K,
                            const int32_t* off, const int32_t* ids, int64_t P, int64_t T,
                            float* logits, float* probs, uint32_t* err, cudaStream_t stream) {
-  // staged rows: as many as fit beside the quantised row in kSmemBudget, at most kPreMax
-  const int64_t fit = K < kSmemBudget ? (kSmemBudget - K) / K : 0;
-  const int pre = static_cast<int>(std::min<int64_t>(kPreMax, fit));
-  const size_t smem = static_cast<size_t>(K) * static_cast<size_t>(1 + pre);
-  if (K <= kRegK) {
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<true>), kSmemBudget);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(readout_kernel<true>, dim3(static_cast<unsigned>(P)), dim3(kThreads), smem, stream, true,
-                         static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, K, off, ids, T, logits,
-                         probs, err, pre);
-  }
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(readout_kernel<false>),
-                                   std::max<int>(kSmemBudget, PRISM_MAX_READOUT_K));
-  if (e != cudaSuccess) return e;
-  return launch_kernel(readout_kernel<false>, dim3(static_cast<unsigned>(P)), dim3(kThreads), smem, stream, true,
-                       static_cast<const uint16_t*>(h), ldh, inv_s, W, ldw, lm_scale, V, K, off, ids, T, logits,
-                       probs, err, pre);
+  return launch_readout_impl<false>(h, ldh, inv_s, W, ldw, lm_scale, V, 0, V, K, off, ids, P, T, logits, probs, err,
+                                    stream);
+}
+
+cudaError_t launch_readout_logits(const void* h, int64_t ldh, const float* inv_s, const int8_t* W_shard,
+                                  int64_t ldw, const float* lm_scale_shard, int64_t v0, int64_t Vs, int64_t V,
+                                  int64_t K, const int32_t* off, const int32_t* ids, int64_t P, int64_t T,
+                                  float* logits, uint32_t* err, cudaStream_t stream) {
+  return launch_readout_impl<true>(h, ldh, inv_s, W_shard, ldw, lm_scale_shard, V, v0, Vs, K, off, ids, P, T, logits,
+                                   nullptr, err, stream);
+}
+
+cudaError_t launch_candidate_softmax(const float* logits, const int32_t* off, int64_t P, int64_t T, float* probs,
+                                     uint32_t* err, cudaStream_t stream) {
+  return launch_kernel(softmax_kernel, dim3(static_cast<unsigned>((P + 3) / 4)), dim3(128), 0, stream, true, logits,
+                       off, P, T, probs, err);
 }
 
 }  // namespace prism

@@ -441,6 +441,44 @@ int prism_candidate_readout(const void *hidden_bf16, int64_t ldh,
                             int32_t *dev_error_word, void *workspace,
                             size_t workspace_bytes, void *cuda_stream);
 
+/*
+ * The column-parallel read-out: the LM head split by vocabulary rows over
+ * ranks, each holding rows [v0, v0 + V_shard) of the V-row head; the
+ * candidate softmax needs only the candidates' logits, so the ranks exchange
+ * T floats, not vocabulary-sized rows (post "把决策模型推理从 vLLM 换到 Prism",
+ * sections 方案 and 实现要点).
+ *
+ * prism_candidate_logits -- prism_candidate_readout's logits for the
+ * candidates this shard holds, and -0.0 for every other candidate:
+ *   lm_head_shard, ldw   [V_shard, K] int8 rows v0 .. v0 + V_shard - 1 of the head
+ *   lm_scale_shard       [V_shard] float32 their scales
+ *   v0, V_shard, V       0 <= v0, v0 + V_shard <= V (the whole head's rows)
+ *   every other argument as prism_candidate_readout (ids are whole-head ids,
+ *   validated against V; an invalid position gets the error bits and NaN
+ *   logits on every shard).
+ * Since x + -0.0 == x for every binary32 x, the element-wise SUM of the
+ * shards' logits (any order; one shard owns each candidate) is the one-device
+ * read-out's logits bit for bit.
+ *
+ * prism_candidate_softmax -- the read-out's candidate softmax on those
+ * combined logits:
+ *   logits        [T] float32 in CSR order
+ *   probs         [T] float32 out, bit for bit prism_candidate_readout's
+ *   cand_offsets, P, T, dev_error_word as in prism_candidate_readout; a
+ *   position with malformed offsets or a count outside [1, 64] gets the
+ *   error bit and NaN probabilities, one with a NaN logit NaN probabilities.
+ */
+int prism_candidate_logits(const void *hidden_bf16, int64_t ldh,
+                           const float *inv_smooth, const int8_t *lm_head_shard,
+                           int64_t ldw, const float *lm_scale_shard, int64_t v0,
+                           int64_t V_shard, int64_t V, int64_t K,
+                           const int32_t *cand_offsets, const int32_t *cand_ids,
+                           int64_t P, int64_t T, float *logits,
+                           int32_t *dev_error_word, void *cuda_stream);
+int prism_candidate_softmax(const float *logits, const int32_t *cand_offsets,
+                            int64_t P, int64_t T, float *probs,
+                            int32_t *dev_error_word, void *cuda_stream);
+
 /* Bytes of workspace prism_candidate_readout needs for P positions, T
  * candidates and hidden size K: 0 for every shape in this implementation. */
 size_t prism_readout_workspace_bytes(int64_t P, int64_t T, int64_t K);

@@ -76,6 +76,8 @@ def _load():
             "oracle_exp": (F, [F]),
             "oracle_exp_batch": (None, [P, I64, P]),
             "oracle_candidate_readout": (I32, [P, I64, P, P, I64, P, I64, I64, P, P, I64, I64, P, P]),
+            "oracle_candidate_logits_shard": (I32, [P, I64, P, P, I64, P, I64, I64, I64, I64, P, P, I64, I64, P]),
+            "oracle_candidate_softmax": (I32, [P, P, I64, I64, P]),
             "oracle_bf16_to_float": (None, [P, I64, P]),
             "oracle_f16_to_float": (None, [P, I64, P]),
             "oracle_smooth_requant": (None, [P, I64, P, I64, P, I64, I64, P, I64, P]),
@@ -354,6 +356,36 @@ def candidate_readout(h_bits, inv_s, lm_head, lm_scale, cand_offsets, cand_ids):
     rc = _load().oracle_candidate_readout(_p(h), K, _p(s), _p(W), K, _p(ls), V, K,
                                           _p(off), _p(ids), P, T, _p(logits), _p(probs))
     return int(rc), logits, probs
+
+
+def candidate_logits_shard(h_bits, inv_s, lm_shard, lm_scale_shard, v0, V, cand_offsets, cand_ids):
+    """Logits of the candidates held by rows v0 .. v0 + V_shard - 1 of a
+    V-row head (``lm_shard`` int8 [V_shard, K]); -0.0 for the others.
+    Returns (status, logits float32 [T])."""
+    h = _c(h_bits, np.uint16)
+    P, K = h.shape
+    W = _c(lm_shard, np.int8).reshape(-1, K)
+    Vs = W.shape[0]
+    s = None if inv_s is None else _c(inv_s, np.float32)
+    ls = _c(lm_scale_shard, np.float32)
+    off = _c(cand_offsets, np.int32)
+    ids = _c(cand_ids, np.int32)
+    T = ids.size
+    logits = np.empty((T,), np.float32)
+    rc = _load().oracle_candidate_logits_shard(_p(h), K, _p(s), _p(W), K, _p(ls), int(v0), Vs, int(V), K,
+                                               _p(off), _p(ids), P, T, _p(logits))
+    return int(rc), logits
+
+
+def candidate_softmax(logits, cand_offsets):
+    """The read-out's candidate softmax on given logits.  Returns (status,
+    probs float32 [T])."""
+    lg = _c(logits, np.float32)
+    off = _c(cand_offsets, np.int32)
+    P, T = off.size - 1, lg.size
+    probs = np.empty((T,), np.float32)
+    rc = _load().oracle_candidate_softmax(_p(lg), _p(off), P, T, _p(probs))
+    return int(rc), probs
 
 
 def bf16_bits_to_float(h) -> np.ndarray:

@@ -589,6 +589,109 @@ int oracle_candidate_readout(const uint16_t *h, int64_t ldh, const float *inv_s,
     return status;
 }
 
+/*
+ * Column-parallel read-out (the LM head split by vocabulary rows; a reading
+ * of [P4-plan]: the candidate softmax needs only the candidates' logits).
+ *
+ * oracle_candidate_logits_shard: the logits of oracle_candidate_readout for
+ * the candidates whose id lies in [v0, v0 + Vs), from the shard's rows
+ * (lm_shard row id - v0, lm_scale_shard[id - v0]); -0.0 for every other
+ * candidate of a valid position.  Validation and return codes as
+ * oracle_candidate_readout (ids checked against the whole head's V);
+ * invalid positions get NaN logits.
+ */
+int oracle_candidate_logits_shard(const uint16_t *h, int64_t ldh, const float *inv_s,
+                                  const int8_t *lm_shard, int64_t ldw,
+                                  const float *lm_scale_shard, int64_t v0, int64_t Vs,
+                                  int64_t V, int64_t K, const int32_t *cand_offsets,
+                                  const int32_t *cand_ids, int64_t P, int64_t T,
+                                  float *logits)
+{
+    const float qnan = nanf("");
+    int status = 0;
+    if (cand_offsets[0] != 0 || cand_offsets[P] != T) return -1;
+    for (int64_t p = 0; p < P; ++p) {
+        int64_t b = cand_offsets[p], e = cand_offsets[p + 1];
+        int64_t cnt = e - b;
+        int err = 0;
+        if (b < 0 || e > T || cnt < 0) err = -1;
+        else if (cnt < 1 || cnt > ORACLE_MAX_CANDIDATES) err = -2;
+        else {
+            for (int64_t i = b; i < e && !err; ++i) {
+                if (cand_ids[i] < 0 || cand_ids[i] >= V) err = -3;
+                for (int64_t j = b; j < i && !err; ++j)
+                    if (cand_ids[j] == cand_ids[i]) err = -4;
+            }
+        }
+        if (err) {
+            if (b >= 0 && e <= T)
+                for (int64_t i = b; i < e; ++i) logits[i] = qnan;
+            if (err < status) status = err;
+            continue;
+        }
+        int8_t qrow[ORACLE_MAX_K];
+        float a_scale;
+        oracle_quant_act(h + p * ldh, ldh, inv_s, 1, K, qrow, K, &a_scale);
+        for (int64_t i = b; i < e; ++i) {
+            const int64_t id = cand_ids[i];
+            if (id < v0 || id >= v0 + Vs) {
+                logits[i] = -0.0f;
+                continue;
+            }
+            const int8_t *wr = lm_shard + (id - v0) * ldw;
+            int64_t s = 0;
+            for (int64_t k = 0; k < K; ++k) s += (int64_t)qrow[k] * (int64_t)wr[k];
+            float t = (float)(int32_t)s;
+            t = t * a_scale;
+            t = t * lm_scale_shard[id - v0];
+            logits[i] = t;
+        }
+    }
+    return status;
+}
+
+/*
+ * oracle_candidate_softmax: step 4 of oracle_candidate_readout on given
+ * logits -- mx = max logit; e_c = oracle_exp(logit_c - mx); s = sum of e_c
+ * in list order; prob_c = e_c / s.  Returns -1 / -2 for malformed offsets or
+ * a count outside [1, 64] (NaN probabilities); a position with a NaN logit
+ * gets NaN probabilities (its error was reported where the logits were made).
+ */
+int oracle_candidate_softmax(const float *logits, const int32_t *cand_offsets, int64_t P,
+                             int64_t T, float *probs)
+{
+    const float qnan = nanf("");
+    int status = 0;
+    if (cand_offsets[0] != 0 || cand_offsets[P] != T) return -1;
+    for (int64_t p = 0; p < P; ++p) {
+        int64_t b = cand_offsets[p], e = cand_offsets[p + 1];
+        int64_t cnt = e - b;
+        int err = 0;
+        if (b < 0 || e > T || cnt < 0) err = -1;
+        else if (cnt < 1 || cnt > ORACLE_MAX_CANDIDATES) err = -2;
+        int has_nan = 0;
+        if (!err)
+            for (int64_t i = b; i < e; ++i) has_nan |= logits[i] != logits[i];
+        if (err || has_nan) {
+            if (b >= 0 && e <= T)
+                for (int64_t i = b; i < e; ++i) probs[i] = qnan;
+            if (err < status) status = err;
+            continue;
+        }
+        float mx = -INFINITY;
+        for (int64_t i = b; i < e; ++i)
+            if (logits[i] > mx) mx = logits[i];
+        float e_val[ORACLE_MAX_CANDIDATES];
+        float sum = 0.0f;
+        for (int64_t i = b; i < e; ++i) {
+            e_val[i - b] = oracle_exp(logits[i] - mx);
+            sum = sum + e_val[i - b];
+        }
+        for (int64_t i = b; i < e; ++i) probs[i] = e_val[i - b] / sum;
+    }
+    return status;
+}
+
 /* ------------------------------------------------ bf16 helpers, exported -- */
 void oracle_bf16_to_float(const uint16_t *h, int64_t n, float *f)
 {

@@ -744,3 +744,68 @@ def test_w4a8_extremes_at_max_k():
     w4[1] = 0x77                                              # every code 7
     _, acc = oracle.w4a8_linear(q, np.ones(2, np.float32), w4, np.ones(2, np.float32))
     assert acc.tolist() == [[-K * 127 * 8, K * 127 * 7], [K * 127 * 8, -K * 127 * 7]]
+
+
+# ------------------------------------------- column-parallel read-out ----
+def _shard_bounds(V, n, rng):
+    cuts = np.sort(rng.choice(np.arange(1, V), size=n - 1, replace=False))
+    return [0] + [int(c) for c in cuts] + [V]
+
+
+def test_shard_logits_whole_head_is_the_readout():
+    """The shard function over the whole head gives the (pinned) read-out's
+    logits bit for bit, invalid positions included."""
+    rng = np.random.default_rng(21)
+    K, V = 128, 40
+    W = rng.integers(-127, 128, size=(V, K), dtype=np.int8)
+    sc = rng.uniform(0.001, 0.02, V).astype(np.float32)
+    h = bits(rng.standard_normal((5, K)).astype(np.float32))
+    off = np.array([0, 3, 5, 8, 10, 12], np.int32)
+    ids = np.array([4, 9, 31, 2, 2, 7, 40, 1, 39, 0, 17, 23], np.int32)   # dup in p1, range in p2
+    rc0, lg0, _ = oracle.candidate_readout(h, None, W, sc, off, ids)
+    rc1, lg1 = oracle.candidate_logits_shard(h, None, W, sc, 0, V, off, ids)
+    assert rc0 == rc1 < 0
+    assert np.array_equal(lg0.view(np.uint32), lg1.view(np.uint32))
+
+
+@pytest.mark.parametrize("n", [2, 3, 5])
+def test_shard_logits_sum_to_the_readout(n):
+    """Every candidate belongs to exactly one shard and the others write
+    -0.0, so adding the shards' outputs in any order reproduces the one-head
+    logits bit for bit (signs of zero included); the softmax of the sum is
+    the read-out's probabilities bit for bit."""
+    rng = np.random.default_rng(30 + n)
+    case = wl.make_readout("readout_p192_v248000", P=12)
+    uniq = np.unique(case.cand_ids)
+    rows = case.lm_rows(uniq)
+    ids = np.searchsorted(uniq, case.cand_ids).astype(np.int32)
+    V = rows.shape[0]
+    sc = case.lm_scale[uniq]
+    rc, lg, pr = oracle.candidate_readout(case.h_bits, None, rows, sc, case.cand_offsets, ids)
+    assert rc == 0
+    bounds = _shard_bounds(V, n, rng)
+    parts = []
+    for r in range(n):
+        v0, v1 = bounds[r], bounds[r + 1]
+        rc_r, lg_r = oracle.candidate_logits_shard(case.h_bits, None, rows[v0:v1], sc[v0:v1], v0, V,
+                                                   case.cand_offsets, ids)
+        assert rc_r == 0
+        owned = (ids >= v0) & (ids < v1)
+        assert np.array_equal(lg_r[owned].view(np.uint32), lg[owned].view(np.uint32))
+        assert np.all(lg_r[~owned].view(np.uint32) == np.float32(-0.0).view(np.uint32))
+        parts.append(lg_r)
+    for order in (range(n), reversed(range(n))):
+        tot = np.full_like(lg, -0.0)
+        for r in order:
+            tot = (tot + parts[r]).astype(np.float32)
+        assert np.array_equal(tot.view(np.uint32), lg.view(np.uint32))
+    rc_s, pr_s = oracle.candidate_softmax(lg, case.cand_offsets)
+    assert rc_s == 0 and np.array_equal(pr_s.view(np.uint32), pr.view(np.uint32))
+
+
+def test_candidate_softmax_invalid_positions():
+    lg = np.array([0.5, np.nan, 1.0, 2.0, 3.0], np.float32)
+    rc, pr = oracle.candidate_softmax(lg, np.array([0, 2, 5], np.int32))
+    assert rc == 0 and np.isnan(pr[:2]).all() and np.isfinite(pr[2:]).all()
+    rc, pr = oracle.candidate_softmax(lg[2:], np.array([0, 0, 3], np.int32))
+    assert rc == -2 and np.isfinite(pr).all()
