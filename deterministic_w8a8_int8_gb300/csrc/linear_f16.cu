@@ -643,9 +643,9 @@ HPlan plan(int64_t M, int64_t N) {
 // cut into P equal K pieces on P CTAs, the pieces of tiles that share a
 // weight operand running side by side), or, where no such split fits, the
 // balanced schedule.  The balanced schedule's arbitrary cuts cost this
-// kernel more than they gain -- each shared tile's private slots (128 x
-// width int32) written and read back, and the weight tiles no longer read
-// by neighbouring CTAs at the same time.  Measured per call (whole /
+// kernel more than they gain -- each shared piece's private slot (128 x
+// width int32) written, counted and read back; keeping the pieces of a
+// weight tile side by side did not recover it.  Measured per call (whole /
 // balanced / lockstep, us): gate/up 458 / 481 / 463; 8192 rows 313 / 334 /
 // 313; down (2 rounds and 16 tiles) 311 / 295 / 275; QKV 64.8 whole against
 // 72 balanced; o_proj 40.5 against 50.  PRISM_F16_SCHED = whole, balanced or
