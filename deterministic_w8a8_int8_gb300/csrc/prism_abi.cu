@@ -500,7 +500,7 @@ int prism_candidate_readout(const void* hidden_bf16, int64_t ldh, const float* i
   if (T > 0 && cand_ids == nullptr) return PRISM_ERR_INVALID_ARG;
   if (ldh < K || ldw < K) return PRISM_ERR_INVALID_ARG;
   if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
-  if (K > PRISM_MAX_READOUT_K || T > P * PRISM_MAX_CANDIDATES || V > (1LL << 31) - 1)
+  if (P > (1LL << 31) - 1 || K > PRISM_MAX_READOUT_K || T > P * PRISM_MAX_CANDIDATES || V > (1LL << 31) - 1)
     return PRISM_ERR_UNSUPPORTED;
   if (ldh % 8 != 0 || ldw % 16 != 0) return PRISM_ERR_ALIGNMENT;
   if (!aligned(hidden_bf16, 16) || !aligned(lm_head, 16) || !aligned(lm_scale, 4) ||
@@ -528,7 +528,8 @@ int prism_candidate_logits(const void* hidden_bf16, int64_t ldh, const float* in
   if (T > 0 && cand_ids == nullptr) return PRISM_ERR_INVALID_ARG;
   if (ldh < K || (V_shard > 0 && ldw < K)) return PRISM_ERR_INVALID_ARG;
   if (K % 16 != 0) return PRISM_ERR_ALIGNMENT;
-  if (K > PRISM_MAX_READOUT_K || T > P * PRISM_MAX_CANDIDATES || V > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  if (P > (1LL << 31) - 1 || K > PRISM_MAX_READOUT_K || T > P * PRISM_MAX_CANDIDATES || V > (1LL << 31) - 1)
+    return PRISM_ERR_UNSUPPORTED;
   if (ldh % 8 != 0 || (V_shard > 0 && ldw % 16 != 0)) return PRISM_ERR_ALIGNMENT;
   if (!aligned(hidden_bf16, 16) || !aligned(lm_head_shard, 16) || !aligned(lm_scale_shard, 4) ||
       !aligned(cand_offsets, 4) || !aligned(cand_ids, 4) || !aligned(logits, 4))
@@ -546,7 +547,7 @@ int prism_candidate_softmax(const float* logits, const int32_t* cand_offsets, in
   if (P < 0 || T < 0) return PRISM_ERR_INVALID_ARG;
   if (P == 0) return T == 0 ? PRISM_OK : PRISM_ERR_INVALID_ARG;
   if (cand_offsets == nullptr || probs == nullptr || (T > 0 && logits == nullptr)) return PRISM_ERR_INVALID_ARG;
-  if (T > P * PRISM_MAX_CANDIDATES || P > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
+  if (P > (1LL << 31) - 1 || T > P * PRISM_MAX_CANDIDATES) return PRISM_ERR_UNSUPPORTED;
   if (!aligned(logits, 4) || !aligned(cand_offsets, 4) || !aligned(probs, 4)) return PRISM_ERR_ALIGNMENT;
   if (dev_error_word != nullptr && !aligned(dev_error_word, 4)) return PRISM_ERR_ALIGNMENT;
   return prism::record_cuda(prism::launch_candidate_softmax(logits, cand_offsets, P, T, probs,

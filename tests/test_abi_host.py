@@ -231,6 +231,45 @@ def test_readout_validation(L):
     assert L.prism_readout_workspace_bytes(192, 1152, 5120) == 0 and L.prism_readout_workspace_bytes(0, 0, 16) == 0
 
 
+def lo(L, P=4, T=8, V=100, K=64, h=A, ldh=64, s=None, W=A, ldw=64, sc=A, v0=0, Vs=50, off=A, ids=A, lg=A,
+       err=None):
+    return L.prism_candidate_logits(h, ldh, s, W, ldw, sc, v0, Vs, V, K, off, ids, P, T, lg, err, None)
+
+
+def test_shard_logits_validation(L):
+    """prism_candidate_logits: the shard must lie inside the head; an empty
+    shard needs no rows; the read-out's own limits and alignments apply."""
+    assert lo(L, P=0, T=0) == 0 and lo(L, P=0, T=3) == -1
+    assert lo(L, P=-1) == -1 and lo(L, T=-1) == -1 and lo(L, V=0) == -1 and lo(L, K=0) == -1
+    assert lo(L, v0=-1) == -1 and lo(L, Vs=-1) == -1
+    assert lo(L, v0=60, Vs=50) == -1                     # past the head's last row
+    # a shard ending at the head's last row, and an empty shard without rows,
+    # pass the range checks (K = 72 then stops them before any launch)
+    assert lo(L, v0=50, Vs=50, K=72, ldh=80, ldw=80) == -2
+    assert lo(L, v0=100, Vs=0, W=None, sc=None, K=72, ldh=80, ldw=80) == -2
+    assert lo(L, W=None) == -1 and lo(L, sc=None) == -1
+    assert lo(L, h=None) == -1 and lo(L, off=None) == -1 and lo(L, lg=None) == -1 and lo(L, ids=None) == -1
+    assert lo(L, ldh=32) == -1 and lo(L, ldw=32) == -1
+    assert lo(L, K=72, ldh=80, ldw=80) == -2
+    assert lo(L, T=4 * 64 + 1) == -3
+    assert lo(L, P=1 << 62, T=1) == -3                   # refused before P * cap is formed
+    assert lo(L, K=65536 + 16, ldh=65552, ldw=65552) == -3
+    assert lo(L, ldh=68) == -2 and lo(L, ldw=72) == -2
+    assert lo(L, h=A + 8) == -2 and lo(L, W=A + 8) == -2 and lo(L, off=A + 2) == -2 and lo(L, lg=A + 2) == -2
+    assert lo(L, s=A + 4) == -2 and lo(L, err=A + 2) == -2
+
+
+def test_candidate_softmax_validation(L):
+    def sm(P=4, T=8, lg=A, off=A, pr=A, err=None):
+        return L.prism_candidate_softmax(lg, off, P, T, pr, err, None)
+    assert sm(P=0, T=0) == 0 and sm(P=0, T=2) == -1
+    assert sm(P=-1) == -1 and sm(T=-1) == -1
+    assert sm(off=None) == -1 and sm(pr=None) == -1 and sm(lg=None) == -1
+    assert sm(T=4 * 64 + 1) == -3 and sm(P=1 << 62, T=1) == -3 and sm(P=1 << 31, T=1) == -3
+    assert sm(lg=A + 2) == -2 and sm(off=A + 1) == -2 and sm(pr=A + 2) == -2 and sm(err=A + 2) == -2
+    assert ro(L, P=1 << 62, T=1) == -3
+
+
 def test_linear_operand_checks_before_any_launch():
     """The binding refuses mis-shaped or mis-typed outputs and residuals of a
     linear call (the W8A8 linear and its no-workspace variant share these
